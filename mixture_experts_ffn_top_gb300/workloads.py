@@ -1,0 +1,183 @@
+"""Seeded synthetic workloads for the batched routed-MoE FFN layer.
+
+This is the one module that both the CUDA path and the CPU oracle consume.
+It draws random numbers and packs them into the layer's input formats; it
+holds none of the layer's own arithmetic (no router, no activation
+quantiser, no expert FFN, no combine).
+
+Input recipe (numpy ``default_rng``, platform independent; float32
+``standard_normal`` draws scaled to the stated standard deviation).  Each
+tensor family has its own seeded stream, so expert weights do not depend on N
+and can be drawn in parallel:
+
+1. stream ``[seed, 0]``: hidden ``[N, D]`` ~ N(0, 1)
+2. stream ``[seed, 1]``: routerW ``[E, D]`` ~ N(0, 1/sqrt(D)) (router logits
+   ~N(0, 1)), then the shared-expert gate vector ``[D]`` ~ N(0, 1/sqrt(D))
+   (shared expert only), then the skew permutation (skewed routing only)
+3. stream ``[seed, 2, e]`` for expert e: gate ``[F, D]``, up ``[F, D]``,
+   down ``[D, F]``, each ~ N(0, 0.02), stored as Q8_0 blocks
+4. stream ``[seed, 3]``: shared expert gate ``[Fs, D]``, up ``[Fs, D]``,
+   down ``[D, Fs]`` ~ N(0, 0.02), Q8_0
+5. skewed routing: expert e gets the logit bias
+   1.5 * ln(Zipf_{s=1.2} pmf(rank_e)) = -1.8 ln(rank_e) + const with
+   rank_e = perm[e] + 1.  The bias is folded into the data (hidden[:, D-1] = 1,
+   routerW[:, D-1] = bias) so the layer's arguments stay as the pages state
+   them; the constant cancels in the softmax.
+
+Expert weights arrive in the GGUF Q8_0 block format, as a quantised model file
+would deliver them: per 32-block an fp16 scale d = fp16(amax/127) followed by
+32 int8 quants round(w/d) (half away from zero), 34 bytes per block, blocks
+row-major along the reduction dimension.  Packing the weights is how the
+synthetic *inputs* are manufactured; both the oracle and the CUDA path take
+the resulting bytes as given.
+
+The pages ("batched int8-MMQ trunk prefill gated off for MoE", #406; "Carnice
+prefill toward llama.cpp 676 t/s", #388) benchmark whole models (OLMoE-1B-7B,
+a 35B-A3B hybrid) whose trained weights are not used here: these synthetic
+layers stand in for them with the same shapes.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, replace
+from functools import lru_cache
+
+import numpy as np
+
+QK = 32
+Q8_0_BYTES = 34
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    N: int          # tokens
+    D: int          # hidden size (embDim)
+    E: int          # routed experts
+    top_k: int      # active experts per token (na)
+    F: int          # routed expert intermediate size
+    Fs: int         # shared expert intermediate size (0 = none)
+    norm_topk_prob: bool
+    seed: int
+    skew: bool = False
+
+    @property
+    def has_shared(self) -> bool:
+        return self.Fs > 0
+
+    def with_tokens(self, N: int) -> "Workload":
+        return replace(self, N=N, name=f"{self.name.split('_n')[0]}_n{N}")
+
+    def describe(self) -> str:
+        s = (f"N={self.N} D={self.D} E={self.E} top_k={self.top_k} F={self.F}"
+             f" norm_topk_prob={int(self.norm_topk_prob)}")
+        if self.Fs:
+            s += f" shared_Fs={self.Fs}"
+        if self.skew:
+            s += " zipf_skew=1.2"
+        return s + f" seed={self.seed}"
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", N=64, D=256, E=8, top_k=2, F=128, Fs=0, norm_topk_prob=False, seed=0),
+    "olmoe": Workload("olmoe", N=2048, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False, seed=1),
+    "decode_n1": Workload("decode_n1", N=1, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False, seed=2),
+    "decode_n4": Workload("decode_n4", N=4, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False, seed=2),
+    "decode_n8": Workload("decode_n8", N=8, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False, seed=2),
+    "qwen3moe_shared": Workload("qwen3moe_shared", N=512, D=2048, E=256, top_k=8, F=512, Fs=512,
+                                norm_topk_prob=True, seed=3),
+    "skewed": Workload("skewed", N=4096, D=2048, E=128, top_k=8, F=768, Fs=0, norm_topk_prob=True,
+                       seed=4, skew=True),
+}
+
+
+def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    return (rng.standard_normal(shape, dtype=np.float32) * np.float32(std)).astype(np.float32)
+
+
+def pack_q8_0(w: np.ndarray) -> np.ndarray:
+    """Pack fp32 weights ``[rows, K]`` into GGUF Q8_0 blocks ``uint8[rows, K/32*34]``."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, K = w.shape
+    assert K % QK == 0
+    b = w.reshape(rows, K // QK, QK)
+    amax = np.abs(b).max(axis=2)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    inv = np.zeros_like(d)
+    nz = d != 0
+    inv[nz] = (np.float32(1.0) / d[nz]).astype(np.float32)
+    v = (b * inv[..., None]).astype(np.float32)
+    q = np.sign(v) * np.floor(np.abs(v).astype(np.float64) + 0.5)
+    out = np.empty((rows, K // QK, Q8_0_BYTES), np.uint8)
+    out[..., 0:2] = d.astype(np.float16).view(np.uint8).reshape(rows, K // QK, 2)
+    out[..., 2:] = q.astype(np.int8).view(np.uint8)
+    return out.reshape(rows, (K // QK) * Q8_0_BYTES)
+
+
+def _expert(seed: int, e: int, D: int, F: int):
+    rng = np.random.default_rng([seed, 2, e])
+    g = pack_q8_0(_normal(rng, (F, D), 0.02))
+    u = pack_q8_0(_normal(rng, (F, D), 0.02))
+    d = pack_q8_0(_normal(rng, (D, F), 0.02))
+    return g, u, d
+
+
+@lru_cache(maxsize=2)
+def _experts(seed: int, E: int, D: int, F: int):
+    gate = np.empty((E, F, (D // QK) * Q8_0_BYTES), np.uint8)
+    up = np.empty_like(gate)
+    down = np.empty((E, D, (F // QK) * Q8_0_BYTES), np.uint8)
+
+    def one(e):
+        gate[e], up[e], down[e] = _expert(seed, e, D, F)
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(one, range(E)))
+    for a in (gate, up, down):
+        a.setflags(write=False)
+    return gate, up, down
+
+
+def make_inputs(wl: Workload) -> dict:
+    """Draw one workload's inputs.  Returns numpy arrays:
+
+    hidden f32[N,D], routerW f32[E,D], shexp_gate f32[D] or None,
+    gate/up u8[E,F,D/32*34], down u8[E,D,F/32*34],
+    sh_gate/sh_up u8[Fs,D/32*34], sh_down u8[D,Fs/32*34] (or None).
+    The expert arrays are shared read-only between calls with equal shapes.
+    """
+    N, D, E, F, Fs = wl.N, wl.D, wl.E, wl.F, wl.Fs
+    assert D % QK == 0 and F % QK == 0 and Fs % QK == 0
+    hidden = _normal(np.random.default_rng([wl.seed, 0]), (N, D), 1.0)
+    rng = np.random.default_rng([wl.seed, 1])
+    routerW = _normal(rng, (E, D), 1.0 / np.sqrt(D))
+    shexp_gate = _normal(rng, (D,), 1.0 / np.sqrt(D)) if Fs else None
+    gate, up, down = _experts(wl.seed, E, D, F)
+    sh_gate = sh_up = sh_down = None
+    if Fs:
+        srng = np.random.default_rng([wl.seed, 3])
+        sh_gate = pack_q8_0(_normal(srng, (Fs, D), 0.02))
+        sh_up = pack_q8_0(_normal(srng, (Fs, D), 0.02))
+        sh_down = pack_q8_0(_normal(srng, (D, Fs), 0.02))
+    if wl.skew:
+        perm = rng.permutation(E)
+        bias = (1.5 * -1.2 * np.log(perm + 1.0)).astype(np.float32)
+        hidden[:, D - 1] = 1.0
+        routerW[:, D - 1] = bias
+    return dict(hidden=hidden, routerW=routerW, shexp_gate=shexp_gate,
+                gate=gate, up=up, down=down, sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down)
+
+
+def make_hidden(wl: Workload, seed_offset: int = 0) -> np.ndarray:
+    """A fresh hidden batch of the workload's shape (used to vary inputs between steps)."""
+    rng = np.random.default_rng([wl.seed, 4, seed_offset])
+    h = _normal(rng, (wl.N, wl.D), 1.0)
+    if wl.skew:
+        h[:, wl.D - 1] = 1.0
+    return h
+
+
+def expert_weight_bytes(wl: Workload) -> int:
+    """Q8_0 bytes of one routed expert (gate + up + down)."""
+    return 3 * wl.F * wl.D // QK * Q8_0_BYTES
