@@ -1,0 +1,396 @@
+"""Benchmark of the batched routed-MoE FFN layer on GB300.
+
+One step = one pass of the whole layer (router + softmax/top-k + Q8_1 of x,
+CSR bucketing, grouped gate/up/down experts, combine) over one batch of N
+synthetic tokens of the OLMoE-shaped layer (N=2048, D=2048, E=64, top_k=8,
+F=1024, norm_topk_prob off).  Metric: MoE-FFN prefill tokens/s per layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K steps between a barrier and a
+device synchronise on both sides; every step is bracketed by CUDA events on
+the launching stream with events between the stages, and the L2 is flushed
+(a 512 MB write) between steps outside the events.  Under torchrun each rank
+runs its own token batch (replicas, weak scaling) and rank 0 prints the line
+with the maximum time over ranks.  --impl reference times the CPU oracle on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_ffn_top_gb300.workloads import QK, Q8_0_BYTES, WORKLOADS, make_hidden, make_inputs  # noqa: E402
+
+METRIC = "MoE-FFN prefill tokens/s/layer, OLMoE shape N=2048; % of int8 tensor peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "olmoe"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_work(wl, topk_idx: np.ndarray | None):
+    """Algorithmic bytes and int8 ops of one layer pass: touched experts' Q8_0 weights, hidden read
+    once, routerW, (shared expert weights and gate), output written once; ops = 2 * MACs."""
+    N, D, E, F, Fs, k = wl.N, wl.D, wl.E, wl.F, wl.Fs, wl.top_k
+    per_expert = 3 * F * D // QK * Q8_0_BYTES
+    touched = E if topk_idx is None else int(np.unique(topk_idx).size)
+    wbytes = touched * per_expert + (3 * Fs * D // QK * Q8_0_BYTES if Fs else 0)
+    bytes_ = wbytes + N * D * 4 + E * D * 4 + (D * 4 if Fs else 0) + N * D * 4
+    ops = 2 * N * k * 3 * F * D + (2 * N * 3 * Fs * D if Fs else 0)
+    return dict(bytes=bytes_, weight_bytes=wbytes, touched_experts=touched, int8_ops=ops)
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(wl, inp, sample_tokens: int):
+    """The oracle, as it stands, on the first `sample_tokens` tokens of the workload (host cores)."""
+    import oracle
+
+    oracle.build()
+    sub = dict(inp)
+    sub["hidden"] = np.ascontiguousarray(inp["hidden"][:sample_tokens])
+    t0 = time.perf_counter()
+    oracle.moe_ffn_inputs(sub, wl.top_k, wl.norm_topk_prob, keep=False)
+    dt = time.perf_counter() - t0
+    return dict(value=sample_tokens / dt, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
+                sample=f"first {sample_tokens} of {wl.N} tokens of the {wl.name} layer ({wl.describe()}), "
+                       f"whole layer, {dt:.2f} s wall")
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl)
+    sample = args.ref_tokens
+    times = []
+    import oracle
+
+    oracle.build()
+    for i in range(args.warmup + args.steps):
+        sub = dict(inp)
+        sub["hidden"] = np.ascontiguousarray(inp["hidden"][:sample])
+        t0 = time.perf_counter()
+        oracle.moe_ffn_inputs(sub, wl.top_k, wl.norm_topk_prob, keep=False)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = sample / (ms / 1e3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {wl.describe()}", "sample_tokens": sample},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"first {sample} of {wl.N} tokens per step, whole layer"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_ffn_top_gb300 import ops
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl)
+    if rank != 0 or world > 1:
+        inp["hidden"] = make_hidden(wl, seed_offset=rank)  # each rank its own token batch
+    layer = ops.MoeLayer.from_numpy(inp, device=device, top_k=wl.top_k, max_tokens=wl.N)
+    w = layer.w
+    stream = torch.cuda.current_stream()
+    hidden = torch.from_numpy(inp["hidden"]).to(device)
+    routerW = layer.routerW
+    shg = layer.shexp_gate
+    out = torch.empty((wl.N, wl.D), dtype=torch.float32, device=device)
+    ws = layer.ws
+    N, D, E, F, k, Fs = wl.N, wl.D, wl.E, wl.F, wl.top_k, wl.Fs
+    path = args.path
+    resolved_path = path
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    v = layer.views(N)
+    # staged calls: the same kernels moe_ffn_prefill launches, with events between the stages
+    stages = ["router", "bucket", "experts", "combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+
+        mark(0)
+        rc = ops.lib().moe_router_topk(ops._P(hidden.data_ptr()), ops._P(routerW.data_ptr()),
+                                       ops._P(shg.data_ptr()) if shg is not None else None, N, D, E, k,
+                                       int(wl.norm_topk_prob), ops._P(v["topk_idx"].data_ptr()),
+                                       ops._P(v["topk_w"].data_ptr()),
+                                       ops._P(v["shexp_scale"].data_ptr()) if shg is not None else None,
+                                       ops._P(v["x_q"].data_ptr()), ops._P(v["x_d"].data_ptr()), None,
+                                       ops._P(ws.data_ptr()), ws.numel(), ops._P(stream.cuda_stream))
+        ops._check(rc, "moe_router_topk")
+        mark(1)
+        rc = ops.lib().moe_bucket(ops._P(v["topk_idx"].data_ptr()), N, k, E, ops._P(v["expStart"].data_ptr()),
+                                  ops._P(v["expTokI"].data_ptr()), ops._P(v["expTokK"].data_ptr()),
+                                  ops._P(ws.data_ptr()), ws.numel(), ops._P(stream.cuda_stream))
+        ops._check(rc, "moe_bucket")
+        mark(2)
+        rc = ops.lib().moe_grouped_ffn_ex(w.handle, ops._P(v["x_q"].data_ptr()), ops._P(v["x_d"].data_ptr()),
+                                          ops._P(v["expStart"].data_ptr()), ops._P(v["expTokI"].data_ptr()),
+                                          ops._P(v["expTokK"].data_ptr()), N, k,
+                                          ops._P(v["shexp_scale"].data_ptr()) if shg is not None else None,
+                                          ops._P(v["partials"].data_ptr()),
+                                          ops._P(v["shared_out"].data_ptr()) if shg is not None else None, path,
+                                          ops._P(ws.data_ptr()), ws.numel(), ops._P(stream.cuda_stream))
+        ops._check(rc, "moe_grouped_ffn")
+        mark(3)
+        ops.moe_combine(v["partials"], v["topk_w"], v["shared_out"] if shg is not None else None, out=out)
+        mark(4)
+
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    status = layer.status()
+    if status:
+        raise RuntimeError(f"device status {status} after warm-up")
+    # which expert path AUTO chose is visible in the kernel count: derive it from the rules
+    if path == ops.MOE_PATH_AUTO:
+        avg_rows = N * k // E
+        tensor = (D % 128 == 0 and F % 64 == 0 and (Fs == 0 or Fs % 64 == 0) and N >= 64 and avg_rows >= 8
+                  and _tensor_available(ops, layer))
+        resolved_path = ops.MOE_PATH_TENSOR if tensor else ops.MOE_PATH_MATVEC
+    topk_idx = v["topk_idx"].cpu().numpy()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    gpu_index = int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].strip().isdigit() else local_rank
+    clocks = ClockSampler(gpu_index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step(evs[i])
+        flush.fill_(1)  # outside the step's events: the next step starts with a cold L2
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    status = layer.status()
+    if status:
+        raise RuntimeError(f"device status {status} after the timed steps")
+    stage_ms = {s: [] for s in stages}
+    step_ms = []
+    for e in evs:
+        for j, s in enumerate(stages):
+            stage_ms[s].append(e[j].elapsed_time(e[j + 1]))
+        step_ms.append(e[0].elapsed_time(e[4]))
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * N / (ms / 1e3)
+
+    # e2e: the public one-call API with pinned host buffers, H2D + D2H inside the timed region
+    h_host = torch.from_numpy(inp["hidden"]).pin_memory()
+    o_host = torch.empty((N, D), dtype=torch.float32).pin_memory()
+    h_dev = torch.empty_like(hidden)
+
+    def e2e_step():
+        h_dev.copy_(h_host, non_blocking=True)
+        ops.moe_ffn_prefill(w, h_dev, routerW, shg, k, wl.norm_topk_prob, ws, out=out, path=path)
+        o_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_mean = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_mean], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+    if layer.status():
+        raise RuntimeError("device status set during the e2e steps")
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    work = algorithmic_work(wl, topk_idx)
+    exp_ms = statistics.mean(stage_ms["experts"])
+    if resolved_path == ops.MOE_PATH_TENSOR:
+        tflops = work["int8_ops"] / (exp_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                    "traffic": TRAFFIC.get(("experts", resolved_path))}
+        roof_kernel = "grouped expert GEMM (tcgen05 kind::f16 on exact fp16 integers)"
+    else:
+        gbs = work["weight_bytes"] / (exp_ms / 1e3) / 1e9
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                    "traffic": TRAFFIC.get(("experts", resolved_path))}
+        roof_kernel = "grouped expert matvec (dp4a)"
+    roofline["kernel"] = roof_kernel
+    roofline["peak_source"] = peak_src
+    layer_roof_s = max(work["int8_ops"] / (peaks.get("bf16_tflops", 1900.0) * 1e12),
+                       work["bytes"] / (peaks.get("hbm_gbs", 6800.0) * 1e9))
+    launches_per_step = 2 + 1 + (4 if resolved_path == ops.MOE_PATH_TENSOR else 2) * (2 if Fs else 1) + 1
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.describe()}", "tokens_per_rank": N,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "expert_path": {1: "matvec", 2: "tensor"}[resolved_path],
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write); expert weights exceed L2"},
+        "stage_ms": {s: statistics.mean(vv) for s, vv in stage_ms.items()},
+        "layer_roofline_us": layer_roof_s * 1e6,
+        "layer_roofline_frac": layer_roof_s / (ms / 1e3),
+        "algorithmic": work,
+        "roofline": roofline,
+        "e2e": {"value": world * N / (e2e_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
+                "d2h_bytes_per_step": N * D * 4, "ms_per_step": e2e_mean},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
+    print(json.dumps(line), flush=True)
+
+
+# ncu dram bytes (read + write) per launch of the dominant stage, keyed by (stage, path);
+# filled from the committed profiles/ summaries, None when not measured for the current kernels
+TRAFFIC = {}
+
+
+def _tensor_available(ops, layer) -> bool:
+    try:
+        return bool(ops.tensor_path_available(layer.w))
+    except AttributeError:
+        return False
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 matvec, 2 tensor")
+    ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=64, help="oracle sample per step for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

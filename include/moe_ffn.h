@@ -1,0 +1,269 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) batched routed-MoE FFN library.
+ *
+ * The layer (one call, moe_ffn_prefill) follows the SharpInference issue pages:
+ *   router matvec over all N tokens, softmax + top-k (norm_topk_prob on/off)
+ *   and shared-expert gate   -- "Carnice prefill toward llama.cpp 676 t/s"
+ *                               (#388), breakdown table "router" row and
+ *                               "Remaining levers" item 1;
+ *   GPU-side expert bucketing into the expStart/expTokI/expTokK CSR
+ *                             -- #388 "Remaining levers" item 1 ("Hard part");
+ *   gather tokens per expert -> grouped expert GEMM -> scatter
+ *                             -- "batched int8-MMQ trunk prefill gated off for
+ *                               MoE" (#406), "The work" item 2; #388 lever 3;
+ *   Q8_0 weights x Q8_1 activations (int8 block dot products)
+ *                             -- #406 references (Q8_0 MMQ), "full-offload MoE
+ *                               decode" (#408) lever 2 (Q8_1 / dp4a);
+ *   weighted scatter-reduce in top-k slot order k = 0..na-1, then the shared
+ *   expert row             -- issue #129, "Scope".
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers (CUDA global memory of the
+ *     current device) unless a comment says otherwise.  Arrays are dense,
+ *     row-major, C order.  The caller owns every buffer it passes; the library
+ *     owns only what moe_weights_create allocates.
+ *   - Calls are asynchronous on `stream`: they enqueue kernels and return.
+ *     Only moe_weights_create/destroy and moe_workspace_status synchronise.
+ *     No call on the hot path allocates memory or copies to/from the host.
+ *   - Return value: MOE_OK (0) or a negative moe_status code for an error the
+ *     host can see before launching (bad argument, unsupported shape, small
+ *     workspace, launch failure).  Errors found by the kernels (an expert
+ *     index out of range, a token that selects an expert twice, a malformed
+ *     CSR, a device wait that timed out) are OR-ed into the status word at the
+ *     start of the workspace; read them with moe_workspace_status.  A kernel
+ *     that finds such an error writes a safe result (empty segments, zero
+ *     rows) instead of reading out of bounds.
+ *   - Shapes: D (hidden), F (routed expert intermediate) and Fs (shared
+ *     expert intermediate) are multiples of 32 (the Q8 block).  The tensor-
+ *     core path also needs D % 128 == 0, F % 64 == 0 and Fs % 64 == 0; other
+ *     shapes run on the matvec path.  1 <= top_k <= min(E, 32), E <= 1024, N >= 1.
+ *
+ * Block formats
+ *   Q8_0 (weights, GGUF): per 32 values one 34-byte block: fp16 scale d
+ *     (little-endian) followed by 32 int8 quants q; value = d * q.
+ *   Q8_1 (activations, produced on the device): per 32 values
+ *     d = amax/127 (fp32), q = roundf(x * (1/d)) (int8), stored scale fp16(d).
+ *     This library stores the quants as int8 and the stored scale widened to
+ *     fp32 (exactly the fp16 value); the Q8_1 sum field d*sum(q) is only
+ *     consumed by weight formats with an offset, so it is not produced.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_FFN_ABI_VERSION 1
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,        /* null required pointer, N < 1, top_k > E, ... */
+    MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* D/F/Fs not a multiple of 32, E > 1024, sizes overflow */
+    MOE_ERR_WORKSPACE_TOO_SMALL = -3,
+    MOE_ERR_CUDA = -4,               /* a CUDA call or launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = -5,     /* a bounded device-side wait gave up */
+    MOE_ERR_UNSUPPORTED_DEVICE = -6, /* not compute capability 10.3 */
+    MOE_ERR_BAD_ROUTING = -7,        /* expert index out of range / selected twice */
+    MOE_ERR_BAD_CSR = -8             /* CSR offsets or token indices out of range */
+};
+
+/* Device status word bits (moe_workspace_status returns the word; a nonzero
+ * word maps to the first matching moe_status in this order). */
+#define MOE_DEV_BAD_ROUTING 0x1u
+#define MOE_DEV_BAD_CSR 0x2u
+#define MOE_DEV_TIMEOUT 0x4u
+
+/* Human-readable name of a moe_status code (static string, never NULL). */
+const char *moe_status_string(int status);
+
+/* MOE_FFN_ABI_VERSION of the loaded library. */
+int moe_abi_version(void);
+
+/* Path selection for moe_grouped_ffn_ex / moe_ffn_prefill_ex. */
+enum moe_path {
+    MOE_PATH_AUTO = 0,   /* tensor-core grouped GEMM for prefill batches, matvec for small N */
+    MOE_PATH_MATVEC = 1, /* fused gather-matvec (dp4a int8 dots), any N */
+    MOE_PATH_TENSOR = 2  /* tcgen05 grouped GEMM (needs the shapes above) */
+};
+
+/* ---------------------------------------------------------------------------
+ * Expert weights.  moe_weights_create copies the caller's Q8_0 tensors into a
+ * library-owned device copy laid out for the kernels (int8 quants and fp32
+ * scales split apart; a second copy of the quants as exact fp16 integers in
+ * 128-row tiles for the tensor cores).  It allocates device memory and
+ * synchronises `stream`.  The caller's buffers may be freed afterwards.
+ *   gate_q8_0, up_q8_0 : device, Q8_0 blocks [E][F][D/32]  (row f reduces over D)
+ *   down_q8_0          : device, Q8_0 blocks [E][D][F/32]
+ *   sh_gate, sh_up     : device, Q8_0 blocks [Fs][D/32], or NULL when Fs == 0
+ *   sh_down            : device, Q8_0 blocks [D][Fs/32], or NULL when Fs == 0
+ * Returns MOE_ERR_UNSUPPORTED_DEVICE on anything but compute capability 10.3.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_weights_s *moe_weights_t;
+
+int moe_weights_create(moe_weights_t *out, int E, int D, int F,
+                       const void *gate_q8_0, const void *up_q8_0, const void *down_q8_0,
+                       int Fs, const void *sh_gate_q8_0, const void *sh_up_q8_0,
+                       const void *sh_down_q8_0, cudaStream_t stream);
+int moe_weights_destroy(moe_weights_t w);
+/* Shape of a weights handle (any output pointer may be NULL; host pointers). */
+int moe_weights_shape(moe_weights_t w, int *E, int *D, int *F, int *Fs);
+/* Library-owned device bytes held by the handle. */
+size_t moe_weights_device_bytes(moe_weights_t w);
+/* 1 when the tensor-core path can run on these weights (shapes and build), else 0. */
+int moe_weights_tensor_path(moe_weights_t w);
+
+/* ---------------------------------------------------------------------------
+ * Workspace: one caller-owned device buffer per concurrent call chain.  The
+ * first 256 bytes hold the device status word.  moe_workspace_init zeroes
+ * the status word (asynchronously); moe_workspace_status synchronises the
+ * stream, returns the status word (host int, MOE_DEV_* bits) and, when
+ * clear != 0, zeroes it.  Two call chains must not share a workspace.
+ * moe_ffn_workspace_size covers every entry point below for that shape.
+ * ------------------------------------------------------------------------- */
+size_t moe_ffn_workspace_size(int N, int D, int E, int F, int top_k, int Fs);
+int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+int moe_workspace_status(void *ws, int clear, cudaStream_t stream);
+/* Map a status word to the moe_status code of its first error (MOE_OK if 0). */
+int moe_status_from_word(int word);
+
+/* ---------------------------------------------------------------------------
+ * moe_router_topk -- router, softmax, top-k, shared gate, Q8_1 of x (#388
+ * breakdown table "router" row: matvec + softmax + top-k + shexp-gate;
+ * levers item 1: norm[N x embDim] x routerW[numExperts x embDim]).
+ *   hidden     [N][D] fp32          routerW [E][D] fp32
+ *   shexp_gate [D] fp32 or NULL     (shared-expert gate vector)
+ *   topk_idx   [N][top_k] int32 out: experts by decreasing logit, ties to
+ *              the lower index (slot 0 = largest)
+ *   topk_w     [N][top_k] fp32 out: softmax over all E experts at the
+ *              selected experts; divided by their sum when norm_topk_prob
+ *   shexp_scale [N] fp32 out, sigmoid(hidden[t] . shexp_gate); NULL iff
+ *              shexp_gate is NULL
+ *   x_q [N][D] int8 out, x_d [N][D/32] fp32 out: Q8_1 of hidden
+ *   logits_out [N][E] fp32 out or NULL (the router logits)
+ *   ws: workspace (split-K partial logits).
+ * ------------------------------------------------------------------------- */
+int moe_router_topk(const float *hidden, const float *routerW, const float *shexp_gate,
+                    int N, int D, int E, int top_k, int norm_topk_prob,
+                    int32_t *topk_idx, float *topk_w, float *shexp_scale,
+                    int8_t *x_q, float *x_d, float *logits_out,
+                    void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Softmax + top-k alone, from given logits [N][E] (same outputs as above).
+ * Lets a caller check routing against logits computed elsewhere. */
+int moe_topk_from_logits(const float *logits, int N, int E, int top_k, int norm_topk_prob,
+                         int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
+/* Q8_1 quantisation of n_blocks consecutive 32-value blocks: q [n_blocks*32]
+ * int8, d [n_blocks] fp32 (the fp16 stored scale, widened).  The same rule
+ * moe_router_topk applies to hidden. */
+int moe_quantize_q8_1(const float *x, int64_t n_blocks, int8_t *q, float *d, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_bucket -- expert bucketing into a CSR on the device (#388 levers item 1:
+ * expStart/expTokI/expTokK).  A counting sort of the N*top_k (token, slot)
+ * pairs by expert, stable in token order:
+ *   expStart [E+1] int32 out: segment offsets, expStart[0] = 0,
+ *            expStart[E] = N*top_k
+ *   expTokI  [N*top_k] int32 out: token of each entry (ascending per segment)
+ *   expTokK  [N*top_k] int32 out: top-k slot of that token for this expert
+ * A bad index or a repeated expert within a token sets MOE_DEV_BAD_ROUTING
+ * and leaves every segment empty.  One kernel: histogram, scan and scatter.
+ * ------------------------------------------------------------------------- */
+int moe_bucket(const int32_t *topk_idx, int N, int top_k, int E,
+               int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
+               void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_grouped_ffn -- every routed expert over its CSR segment, plus the shared
+ * expert over all tokens (#406 "The work" item 2: gather -> grouped GEMM ->
+ * scatter; #129 intro: gate/up/down grouped by expert; #129 "Scope": the
+ * optionally batched shared expert):
+ *   for entry j of expert e (t = expTokI[j], s = expTokK[j]):
+ *     h_j = Q8_1( SiLU(W_g[e] x_t) * (W_u[e] x_t) )      (x_t = Q8_1 row t)
+ *     partials[t*top_k + s][0..D) = W_d[e] h_j            (fp32, unweighted)
+ *   shared (when the weights have Fs > 0 and shared_out != NULL):
+ *     shared_out[t][0..D) = shexp_scale[t] * W_sd Q8_1(SiLU(W_sg x_t) * (W_su x_t))
+ *   x_q [N][D] int8, x_d [N][D/32] fp32: Q8_1 rows (moe_router_topk output)
+ *   partials [N*top_k][D] fp32 out; shared_out [N][D] fp32 out or NULL.
+ * Every dot product is a sum over 32-blocks of fp16(d_w)*d_x*isum with isum
+ * the exact int32 dot of the block's quants.
+ * ------------------------------------------------------------------------- */
+int moe_grouped_ffn(moe_weights_t w, const int8_t *x_q, const float *x_d,
+                    const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
+                    int N, int top_k, const float *shexp_scale, float *partials, float *shared_out,
+                    void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* As moe_grouped_ffn with an explicit path (enum moe_path). */
+int moe_grouped_ffn_ex(moe_weights_t w, const int8_t *x_q, const float *x_d,
+                       const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
+                       int N, int top_k, const float *shexp_scale, float *partials, float *shared_out,
+                       int path, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The two halves of moe_grouped_ffn, for checking each on its own.
+ * moe_expert_gate_up writes the requantised activations of every entry in
+ * segment order: h_q [N*top_k][F] int8, h_d [N*top_k][F/32] fp32.
+ * moe_expert_down consumes them (from any source) and writes partials. */
+int moe_expert_gate_up(moe_weights_t w, const int8_t *x_q, const float *x_d,
+                       const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
+                       int8_t *h_q, float *h_d, int path, void *ws, size_t ws_bytes,
+                       cudaStream_t stream);
+int moe_expert_down(moe_weights_t w, const int8_t *h_q, const float *h_d,
+                    const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
+                    int N, int top_k, float *partials, int path, void *ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* Raw int32 block dot products of the gate/up GEMM for one 32-block `block`
+ * of the reduction dimension: dots [N*top_k][2][F] int32, entry j in segment
+ * order, [.][0][f] = isum(W_g[e][f], x_t), [.][1][f] = isum(W_u[e][f], x_t),
+ * as computed inside the selected path's kernel. */
+int moe_debug_gate_up_block_dots(moe_weights_t w, const int8_t *x_q, const float *x_d,
+                                 const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
+                                 int block, int32_t *dots, int path, void *ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine -- batched weighted scatter-reduce (#129 "Scope"), one launch
+ * over N x D: for every token t and column c
+ *   acc = +0.0f;
+ *   for s = 0..top_k-1: acc = fmaf(topk_w[t][s], partials[t*top_k+s][c], acc);
+ *   if (shared) acc = acc + shared[t][c];
+ *   out[t][c] = acc;
+ * in exactly this order and rounding (bit-reproducible).
+ *   partials [N*top_k][D] fp32, topk_w [N][top_k] fp32, shared [N][D] or NULL,
+ *   out [N][D] fp32 (may not alias the inputs).
+ * ------------------------------------------------------------------------- */
+int moe_combine(const float *partials, const float *topk_w, const float *shared,
+                int N, int top_k, int D, float *out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_ffn_prefill -- the whole layer in one call (all of the above, on one
+ * stream, with no host round trip): the pages' batched routed-MoE FFN over
+ * N prompt tokens.
+ *   hidden [N][D] fp32, routerW [E][D] fp32, shexp_gate [D] fp32 or NULL
+ *   (NULL: no shared expert even if the weights carry one; non-NULL needs
+ *   weights with Fs > 0), out [N][D] fp32 (the FFN output; no residual).
+ * ------------------------------------------------------------------------- */
+int moe_ffn_prefill(moe_weights_t w, const float *hidden, const float *routerW,
+                    const float *shexp_gate, int N, int top_k, int norm_topk_prob, float *out,
+                    void *ws, size_t ws_bytes, cudaStream_t stream);
+int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *routerW,
+                       const float *shexp_gate, int N, int top_k, int norm_topk_prob, float *out,
+                       int path, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Device pointers to the intermediates moe_ffn_prefill leaves in `ws`
+ * (valid after it ran on that workspace with the same shape); any output
+ * pointer may be NULL.  Host pointers to receive device addresses. */
+int moe_workspace_views(void *ws, int N, int D, int E, int F, int top_k, int Fs,
+                        int32_t **topk_idx, float **topk_w, float **shexp_scale,
+                        int8_t **x_q, float **x_d, int32_t **expStart, int32_t **expTokI,
+                        int32_t **expTokK, float **partials, float **shared_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FFN_H */

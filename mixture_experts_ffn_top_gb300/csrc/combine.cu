@@ -1,0 +1,59 @@
+// combine.cu -- batched weighted scatter-reduce (issue #129, "Scope"): for each
+// token row, sum the top_k unweighted down-partials in slot order k = 0..na-1
+// with the per-(token, slot) weights, then add the shared-expert row, in one
+// launch over N x D.  The per-element order and rounding are fixed (one fused
+// multiply-add per slot, then one add), so the result is bit-reproducible:
+//   acc = +0; for s: acc = fma(w[t,s], partial[t*k+s], acc); acc += shared.
+// HBM-bound: each thread owns 4 consecutive columns (16-byte loads/stores);
+// partial rows are streamed once (evict-first loads), the output is written once.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
+               const float4 *__restrict__ shared, int N, int k, int D4, float4 *__restrict__ out) {
+    const int64_t total = (int64_t)N * D4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / D4;
+        const int64_t c = i - t * D4;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s = 0; s < k; ++s) {
+            const float ws = w[t * k + s];
+            const float4 p = __ldcs(partials + (t * k + s) * D4 + c);
+            acc.x = __fmaf_rn(ws, p.x, acc.x);
+            acc.y = __fmaf_rn(ws, p.y, acc.y);
+            acc.z = __fmaf_rn(ws, p.z, acc.z);
+            acc.w = __fmaf_rn(ws, p.w, acc.w);
+        }
+        if (shared != nullptr) {
+            const float4 sv = __ldcs(shared + t * D4 + c);
+            acc.x = __fadd_rn(acc.x, sv.x);
+            acc.y = __fadd_rn(acc.y, sv.y);
+            acc.z = __fadd_rn(acc.z, sv.z);
+            acc.w = __fadd_rn(acc.w, sv.w);
+        }
+        out[i] = acc;
+    }
+}
+
+}  // namespace
+
+int launch_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k,
+                   int D, float *out, cudaStream_t s) {
+    const int D4 = D / 4;
+    const int64_t total = (int64_t)N * D4;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = 152 * 8;  // 8 resident CTAs of 256 threads per SM
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(partials), topk_w,
+                                                    reinterpret_cast<const float4 *>(shared), N, top_k, D4,
+                                                    reinterpret_cast<float4 *>(out));
+    return launch_status();
+}
+
+}  // namespace moe

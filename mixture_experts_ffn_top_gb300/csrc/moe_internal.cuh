@@ -1,0 +1,161 @@
+// moe_internal.cuh -- shared declarations of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_ffn.h"
+
+namespace moe {
+
+constexpr int QK = 32;          // values per Q8 block
+constexpr int Q8_0_BYTES = 34;  // fp16 scale + 32 int8
+constexpr int MAX_E = 1024;
+constexpr int SEG_ALIGN = 16;   // padded segment start (rows) in the tensor-core row space
+constexpr int TILE_M = 128;     // weight rows per tensor-core tile
+constexpr int TILE_N = 128;     // token rows per tensor-core tile (max)
+
+// ---------------------------------------------------------------- weights --
+// Library-owned device copy of the expert weights (see moe_weights_create).
+struct WeightSet {
+    int rows_gu = 0;  // 2*F (gate and up, tile-interleaved for the tensor path)
+    int F = 0;        // intermediate size of this set
+    // int8 quants + fp32 scales, row-major, for the matvec path
+    int8_t *gate_q = nullptr, *up_q = nullptr;  // [nexp][F][D]
+    float *gate_d = nullptr, *up_d = nullptr;   // [nexp][F][D/32]
+    int8_t *down_q = nullptr;                   // [nexp][D][F]
+    float *down_d = nullptr;                    // [nexp][D][F/32]
+    // tensor path: exact fp16 integers in tile-interleaved order + transposed scales
+    __half *gu16 = nullptr;   // [nexp][2F][D]: 128-row tile mt = 64 gate rows then 64 up rows
+    float *gu_dT = nullptr;   // [nexp][D/32][2F] (same row order)
+    __half *dn16 = nullptr;   // [nexp][D][F]
+    float *dn_dT = nullptr;   // [nexp][F/32][D]
+};
+
+}  // namespace moe
+
+struct moe_weights_s {
+    int E = 0, D = 0, F = 0, Fs = 0;
+    int device = -1;
+    bool tensor_ok = false;  // shapes fit the tensor-core path
+    moe::WeightSet routed;   // E experts
+    moe::WeightSet shared;   // 1 expert (Fs > 0)
+    size_t bytes = 0;
+    char *routed_arena_ = nullptr;  // one device allocation holding both weight sets
+    void *tmaps = nullptr;   // host copy of the TMA descriptors (tensor path), owned
+};
+
+namespace moe {
+
+// ------------------------------------------------------------- workspace --
+struct WsLayout {
+    size_t status, topk_idx, topk_w, shexp_scale, x_q, x_d, expStart, expTokI, expTokK;
+    size_t partials, shared_out, part_logits, total;
+    // tensor path
+    size_t plan, tiles, rowinfo, xg16, xg_dT, h16, h_dT;
+    // matvec path
+    size_t hq8, hd8;
+    int nsplit;      // router split-K factor
+    int rows_max;    // padded row space of the tensor path
+    int tiles_max;   // token tiles of the tensor path
+};
+
+WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs);
+
+template <typename T>
+inline T *ws_ptr(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
+
+// Plan header written by the planning kernel (tensor path), at ws + plan.
+struct PlanHeader {
+    int n_tiles;        // token tiles (routed + shared)
+    int n_rows;         // padded rows used
+    int shared_row0;    // first padded row of the shared segment (-1: none)
+    int pad;
+};
+// One token tile: padded row start, valid rows, expert (E = shared), segment entry start.
+struct TileDesc {
+    int row0, nrows, expert, entry0;
+};
+
+// ----------------------------------------------------------- launchers --
+// router.cu
+int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
+                  int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
+                  int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
+                  cudaStream_t s);
+int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,
+                            float *w, cudaStream_t s);
+int launch_quantize_q8_1(const float *x, int64_t nblk, int8_t *q, float *d, cudaStream_t s);
+// bucket.cu
+int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart,
+                  int32_t *expTokI, int32_t *expTokK, unsigned *status, cudaStream_t s);
+// expert_matvec.cu
+int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
+                          const int8_t *x_q, const float *x_d, const int32_t *expStart,
+                          const int32_t *expTokI, int N, int top_k, int8_t *h_q, float *h_d,
+                          int32_t *dbg_dots, int dbg_block, unsigned *status, cudaStream_t s);
+int launch_matvec_down(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
+                       const int8_t *h_q, const float *h_d, const int32_t *expStart,
+                       const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
+                       const float *shexp_scale, float *out, unsigned *status, cudaStream_t s);
+// combine.cu
+int launch_combine(const float *partials, const float *topk_w, const float *shared, int N,
+                   int top_k, int D, float *out, cudaStream_t s);
+// weights.cu
+int repack_weights(moe_weights_s *w, const void *gate, const void *up, const void *down,
+                   const void *sh_gate, const void *sh_up, const void *sh_down, cudaStream_t s);
+void free_weights(moe_weights_s *w);
+// expert_gemm.cu (tensor path)
+bool tensor_path_supported(const moe_weights_s *w);
+int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const float *x_d,
+                           const int32_t *expStart, const int32_t *expTokI,
+                           const int32_t *expTokK, int N, int top_k, bool with_shared,
+                           void *ws, const WsLayout &L, cudaStream_t s);
+int launch_gemm_gate_up(const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws,
+                        const WsLayout &L, int32_t *dbg_dots, int dbg_block, cudaStream_t s);
+int launch_gemm_down(const moe_weights_s *w, int N, int top_k, bool with_shared,
+                     const float *shexp_scale, float *partials, float *shared_out, void *ws,
+                     const WsLayout &L, cudaStream_t s);
+int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
+                     int8_t *h_q, float *h_d, cudaStream_t s);
+int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
+                     const int8_t *h_q, const float *h_d, cudaStream_t s);
+int prepare_tensor_maps(moe_weights_s *w);
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+inline int launch_status() { return cuda_status(cudaGetLastError()); }
+
+// ----------------------------------------------------- device helpers --
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Q8_1 quantisation of one 32-value block held one value per lane:
+//   d = amax/127 (IEEE fp32 division), q = roundf(x * (1/d)), stored scale fp16(d).
+// Returns q; *d16f receives the stored scale widened to fp32.
+__device__ __forceinline__ int q8_quantize_lane(float x, float *d16f) {
+    float a = fabsf(x);
+    // |x| bit patterns order like the values for non-negative floats
+    unsigned amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(a));
+    float amax = __uint_as_float(amax_bits);
+    float d = __fdiv_rn(amax, 127.0f);
+    float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+    *d16f = __half2float(__float2half_rn(d));
+    return (int)roundf(__fmul_rn(x, id));
+}
+
+}  // namespace moe

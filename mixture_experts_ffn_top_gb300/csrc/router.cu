@@ -1,0 +1,259 @@
+// router.cu -- router logits, softmax + top-k, shared-expert gate and the Q8_1
+// quantisation of the hidden rows ("Carnice prefill toward llama.cpp 676 t/s",
+// #388: breakdown table "router" row -- matvec + softmax + top-k + shexp-gate,
+// per token -- and "Remaining levers" item 1, which moves it onto the GPU).
+//
+// Two kernels:
+//   router_logits_kernel: split-K fp32 SIMT GEMM  logits = hidden . routerW^T
+//     (routerW extended by the shared gate vector as row E).  The CTAs of
+//     expert tile 0 also quantise the hidden rows they stage (each 32-wide K
+//     chunk is exactly one Q8_1 block), so hidden is read from HBM once.
+//   softmax_topk_kernel: one warp per token; sums the split-K partials in a
+//     fixed order, softmax over all E, top-k by repeated warp argmax (ties to
+//     the lower expert index), weights, sigmoid gate.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int RB_M = 64;   // tokens per tile
+constexpr int RB_N = 64;   // experts per tile
+constexpr int RB_K = 32;   // K chunk = one Q8 block
+constexpr int R_THREADS = 256;
+
+__global__ void __launch_bounds__(R_THREADS)
+router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__ routerW,
+                     const float *__restrict__ shexp_gate, int N, int D, int E, int Eext, int ksplit,
+                     float *__restrict__ part, int8_t *__restrict__ x_q, float *__restrict__ x_d) {
+    __shared__ __align__(16) float Xs[RB_K][RB_M + 4];
+    __shared__ __align__(16) float Ws[RB_K][RB_N + 4];
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * RB_M;
+    const int e0 = blockIdx.y * RB_N;
+    const int split = blockIdx.z;
+    const int k_begin = split * ksplit;
+    const int k_end = min(D, k_begin + ksplit);
+    const bool quantise = (blockIdx.y == 0);
+    const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4x4 outputs each
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+    for (int k0 = k_begin; k0 < k_end; k0 += RB_K) {
+        // stage hidden[t0..t0+64)[k0..k0+32) and W[e0..e0+64)[k0..k0+32), transposed (k-major)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            int i = tid + r * R_THREADS;  // 0..511 float4 slots
+            int row = i >> 3, c4 = (i & 7) * 4;
+            int t = t0 + row;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < N) v = *reinterpret_cast<const float4 *>(hidden + (size_t)t * D + k0 + c4);
+            Xs[c4 + 0][row] = v.x;
+            Xs[c4 + 1][row] = v.y;
+            Xs[c4 + 2][row] = v.z;
+            Xs[c4 + 3][row] = v.w;
+            int e = e0 + row;
+            float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < E)
+                wv = *reinterpret_cast<const float4 *>(routerW + (size_t)e * D + k0 + c4);
+            else if (e == E && shexp_gate != nullptr)
+                wv = *reinterpret_cast<const float4 *>(shexp_gate + k0 + c4);
+            Ws[c4 + 0][row] = wv.x;
+            Ws[c4 + 1][row] = wv.y;
+            Ws[c4 + 2][row] = wv.z;
+            Ws[c4 + 3][row] = wv.w;
+        }
+        __syncthreads();
+        if (quantise) {
+            // Q8_1 of this K chunk for the tile's 64 tokens: warp w takes 8 tokens, lane = element
+            const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+            for (int r = 0; r < RB_M / 8; ++r) {
+                int row = warp * (RB_M / 8) + r;
+                int t = t0 + row;
+                float d16f;
+                int q = q8_quantize_lane(Xs[lane][row], &d16f);
+                if (t < N) {
+                    x_q[(size_t)t * D + k0 + lane] = (int8_t)q;
+                    if (lane == 0) x_d[(size_t)t * (D / QK) + k0 / QK] = d16f;
+                }
+            }
+        }
+#pragma unroll 8
+        for (int kk = 0; kk < RB_K; ++kk) {
+            float4 a = *reinterpret_cast<const float4 *>(&Xs[kk][ty * 4]);
+            float4 b = *reinterpret_cast<const float4 *>(&Ws[kk][tx * 4]);
+            float av[4] = {a.x, a.y, a.z, a.w};
+            float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int t = t0 + ty * 4 + i;
+        if (t >= N) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int e = e0 + tx * 4 + j;
+            if (e < Eext) part[((size_t)split * N + t) * Eext + e] = acc[i][j];
+        }
+    }
+}
+
+// One warp per token.  EPL = experts per lane (power of two, EPL*32 >= E).
+template <int EPL>
+__global__ void __launch_bounds__(256)
+softmax_topk_kernel(const float *__restrict__ part, int nsplit, int N, int E, int Eext, int top_k,
+                    int norm, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                    float *__restrict__ shexp_scale, float *__restrict__ logits_out) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= N) return;
+    float l[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        int e = lane + 32 * i;
+        float v = -INFINITY;
+        if (e < E) {
+            v = part[(size_t)t * Eext + e];
+            for (int s = 1; s < nsplit; ++s) v = __fadd_rn(v, part[((size_t)s * N + t) * Eext + e]);
+            if (logits_out) logits_out[(size_t)t * E + e] = v;
+        }
+        l[i] = v;
+    }
+    if (shexp_scale != nullptr && lane == 0) {
+        float g = part[(size_t)t * Eext + E];
+        for (int s = 1; s < nsplit; ++s) g = __fadd_rn(g, part[((size_t)s * N + t) * Eext + E]);
+        shexp_scale[t] = __fdiv_rn(1.0f, 1.0f + expf(-g));
+    }
+    // softmax over all E experts
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) m = fmaxf(m, l[i]);
+    m = warp_max(m);
+    float p[EPL];
+    float z = 0.0f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        p[i] = (lane + 32 * i < E) ? expf(l[i] - m) : 0.0f;
+        z += p[i];
+    }
+    z = warp_sum(z);
+    // top-k (top_k <= 32): repeated warp argmax on the logits, ties to the lower index;
+    // lane s keeps slot s's probability
+    float psel_sum = 0.0f;
+    float my_w = 0.0f;
+    for (int s = 0; s < top_k; ++s) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            bool cand = e < E && p[i] >= 0.0f;  // p = -1 marks a taken expert
+            if (cand && (bi == 0x7fffffff || l[i] > bv || (l[i] == bv && e < bi))) {
+                bv = l[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        float pw = 0.0f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (lane + 32 * i == bi) {
+                pw = __fdiv_rn(p[i], z);
+                p[i] = -1.0f;
+            }
+        pw = __shfl_sync(0xffffffffu, pw, bi & 31);
+        psel_sum = __fadd_rn(psel_sum, pw);
+        if (lane == s) my_w = pw;
+        if (lane == 0) topk_idx[(size_t)t * top_k + s] = bi;
+    }
+    if (lane < top_k)
+        topk_w[(size_t)t * top_k + lane] = norm ? __fdiv_rn(my_w, psel_sum) : my_w;
+}
+
+__global__ void quantize_q8_1_kernel(const float *__restrict__ x, int64_t nblk, int8_t *__restrict__ q,
+                                     float *__restrict__ d) {
+    const int lane = threadIdx.x & 31;
+    int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= nblk) return;
+    float d16f;
+    int qi = q8_quantize_lane(x[b * QK + lane], &d16f);
+    q[b * QK + lane] = (int8_t)qi;
+    if (lane == 0) d[b] = d16f;
+}
+
+int launch_softmax(const float *part, int nsplit, int N, int E, int Eext, int top_k, int norm,
+                   int32_t *idx, float *w, float *sh, float *logits_out, cudaStream_t s) {
+    dim3 grid((N + 7) / 8), block(256);
+    int epl = (E + 31) / 32;
+    if (epl <= 1)
+        softmax_topk_kernel<1><<<grid, block, 0, s>>>(part, nsplit, N, E, Eext, top_k, norm, idx, w, sh, logits_out);
+    else if (epl <= 2)
+        softmax_topk_kernel<2><<<grid, block, 0, s>>>(part, nsplit, N, E, Eext, top_k, norm, idx, w, sh, logits_out);
+    else if (epl <= 4)
+        softmax_topk_kernel<4><<<grid, block, 0, s>>>(part, nsplit, N, E, Eext, top_k, norm, idx, w, sh, logits_out);
+    else if (epl <= 8)
+        softmax_topk_kernel<8><<<grid, block, 0, s>>>(part, nsplit, N, E, Eext, top_k, norm, idx, w, sh, logits_out);
+    else if (epl <= 16)
+        softmax_topk_kernel<16><<<grid, block, 0, s>>>(part, nsplit, N, E, Eext, top_k, norm, idx, w, sh, logits_out);
+    else
+        softmax_topk_kernel<32><<<grid, block, 0, s>>>(part, nsplit, N, E, Eext, top_k, norm, idx, w, sh, logits_out);
+    return launch_status();
+}
+
+}  // namespace
+
+int router_nsplit(int N, int D, int E) {
+    // enough CTAs to cover the SMs about twice, each split at least 256 deep
+    int tiles = ((N + RB_M - 1) / RB_M) * ((E + 1 + RB_N - 1) / RB_N);
+    int want = (2 * 152 + tiles - 1) / tiles;
+    int maxs = D / 256 > 0 ? D / 256 : 1;
+    int s = want < 1 ? 1 : (want > maxs ? maxs : want);
+    while (s > 1 && (D / QK) % s != 0) --s;  // equal splits on block boundaries
+    return s;
+}
+
+int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
+                  int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
+                  int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
+                  cudaStream_t s) {
+    int Eext = E + (shexp_gate ? 1 : 0);
+    int ksplit = D / nsplit;
+    dim3 grid((N + RB_M - 1) / RB_M, (Eext + RB_N - 1) / RB_N, nsplit);
+    router_logits_kernel<<<grid, R_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, ksplit,
+                                                   part_logits, x_q, x_d);
+    int rc = launch_status();
+    if (rc) return rc;
+    return launch_softmax(part_logits, nsplit, N, E, Eext, top_k, norm, topk_idx, topk_w,
+                          shexp_gate ? shexp_scale : nullptr, logits_out, s);
+}
+
+int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,
+                            float *w, cudaStream_t s) {
+    return launch_softmax(logits, 1, N, E, E, top_k, norm, idx, w, nullptr, nullptr, s);
+}
+
+int launch_quantize_q8_1(const float *x, int64_t nblk, int8_t *q, float *d, cudaStream_t s) {
+    if (nblk <= 0) return MOE_OK;
+    int64_t grid = (nblk + 7) / 8;
+    quantize_q8_1_kernel<<<(unsigned)grid, 256, 0, s>>>(x, nblk, q, d);
+    return launch_status();
+}
+
+}  // namespace moe

@@ -1,0 +1,136 @@
+// weights.cu -- one-time repack of the caller's Q8_0 expert tensors into the
+// library-owned layouts the kernels read (load time, not on the hot path).
+//
+// GGUF Q8_0 stores each 32-block as 34 bytes (fp16 scale + 32 int8), which
+// leaves the quants misaligned for vector loads and interleaves them with the
+// scales.  Following the SoA repack idea of the pages' int8 MMQ work (#406
+// references: "split-K + better-tiled int8 MMQ GEMM ... (SoA repack)"), the
+// repack splits every matrix into
+//   - int8 quants [rows][K] (16-byte aligned rows) and fp32 scales [rows][K/32]
+//     (the fp16 scale widened exactly), read by the matvec path;
+//   - for the tensor-core path: the quants again as exact fp16 integers
+//     (|q| <= 127 is exact in fp16), gate and up interleaved per 128-row tile
+//     (rows 0-63 gate f0..f0+63, rows 64-127 up f0..f0+63) so one MMA tile
+//     yields gate and up of the same 64 features; scales transposed to
+//     [K/32][rows] so a TMA box of 128 rows x 2 blocks is one copy.
+#include "moe_internal.cuh"
+
+#include <vector>
+
+namespace moe {
+
+namespace {
+
+// One thread per 32-block.  src: [nmat][rows][nblk] AoS blocks.
+__global__ void repack_kernel(const uint8_t *__restrict__ src, int nmat, int rows, int nblk,
+                              int8_t *__restrict__ q, float *__restrict__ d, __half *__restrict__ h16,
+                              float *__restrict__ dT, int interleave_gu, int up_half) {
+    const int64_t total = (int64_t)nmat * rows * nblk;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t mr = i / nblk;  // matrix * rows + row
+        const int b = (int)(i - mr * nblk);
+        const int m = (int)(mr / rows);
+        const int r = (int)(mr - (int64_t)m * rows);
+        const uint8_t *blk = src + i * Q8_0_BYTES;
+        const __half dh = __ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8)));
+        const float df = __half2float(dh);
+        alignas(16) int8_t vals[QK];
+#pragma unroll
+        for (int j = 0; j < QK; ++j) vals[j] = (int8_t)blk[2 + j];
+        const int K = nblk * QK;
+        if (q != nullptr) {
+            int4 *dst = reinterpret_cast<int4 *>(q + mr * K + (int64_t)b * QK);
+            dst[0] = *reinterpret_cast<const int4 *>(vals);
+            dst[1] = *reinterpret_cast<const int4 *>(vals + 16);
+            d[mr * nblk + b] = df;
+        }
+        if (h16 != nullptr) {
+            // row inside the tensor-core operand of this matrix
+            int64_t rr = r;
+            int64_t rows_out = rows;
+            if (interleave_gu) {  // gate/up pair: [2*rows] rows, 64-row halves per 128-row tile
+                rows_out = 2 * (int64_t)rows;
+                rr = (int64_t)(r / 64) * 128 + (up_half ? 64 : 0) + (r % 64);
+            }
+            __half *dst = h16 + ((int64_t)m * rows_out + rr) * K + (int64_t)b * QK;
+#pragma unroll
+            for (int j = 0; j < QK; j += 2)
+                *reinterpret_cast<__half2 *>(dst + j) = __halves2half2(__int2half_rn(vals[j]), __int2half_rn(vals[j + 1]));
+            dT[((int64_t)m * nblk + b) * rows_out + rr] = df;
+        }
+    }
+}
+
+int repack(const void *src, int nmat, int rows, int K, int8_t *q, float *d, __half *h16, float *dT,
+           int interleave, int up_half, cudaStream_t s) {
+    int64_t total = (int64_t)nmat * rows * (K / QK);
+    if (total == 0) return MOE_OK;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    repack_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
+                                                   h16, dT, interleave, up_half);
+    return launch_status();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+// Sizes of one weight set's arrays; carve == true assigns pointers from base.
+static size_t layout_set(WeightSet &ws, int nexp, int D, int F, bool tensor, char *base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align256(bytes);
+        return base ? base + o : nullptr;
+    };
+    const size_t gu = (size_t)nexp * F * D, dn = (size_t)nexp * D * F;
+    ws.F = F;
+    ws.rows_gu = 2 * F;
+    ws.gate_q = (int8_t *)take(gu);
+    ws.up_q = (int8_t *)take(gu);
+    ws.gate_d = (float *)take(gu / QK * sizeof(float));
+    ws.up_d = (float *)take(gu / QK * sizeof(float));
+    ws.down_q = (int8_t *)take(dn);
+    ws.down_d = (float *)take(dn / QK * sizeof(float));
+    if (tensor) {
+        ws.gu16 = (__half *)take(2 * gu * sizeof(__half));
+        ws.gu_dT = (float *)take(2 * gu / QK * sizeof(float));
+        ws.dn16 = (__half *)take(dn * sizeof(__half));
+        ws.dn_dT = (float *)take(dn / QK * sizeof(float));
+    }
+    return off;
+}
+
+int repack_weights(moe_weights_s *w, const void *gate, const void *up, const void *down, const void *sh_gate,
+                   const void *sh_up, const void *sh_down, cudaStream_t s) {
+    const int E = w->E, D = w->D, F = w->F, Fs = w->Fs;
+    const bool tensor = w->tensor_ok;
+    size_t r_bytes = layout_set(w->routed, E, D, F, tensor, nullptr);
+    size_t s_bytes = Fs ? layout_set(w->shared, 1, D, Fs, tensor, nullptr) : 0;
+    char *arena = nullptr;
+    if (cudaMalloc(&arena, r_bytes + s_bytes) != cudaSuccess) return MOE_ERR_CUDA;
+    w->bytes = r_bytes + s_bytes;
+    layout_set(w->routed, E, D, F, tensor, arena);
+    if (Fs) layout_set(w->shared, 1, D, Fs, tensor, arena + r_bytes);
+    // the arena start doubles as the handle's allocation
+    w->routed_arena_ = arena;
+    auto sets = [&](WeightSet &ws, int nexp, int Fx, const void *g, const void *u, const void *dn) {
+        int rc = repack(g, nexp, Fx, D, ws.gate_q, ws.gate_d, ws.gu16, ws.gu_dT, 1, 0, s);
+        if (!rc) rc = repack(u, nexp, Fx, D, ws.up_q, ws.up_d, ws.gu16, ws.gu_dT, 1, 1, s);
+        if (!rc) rc = repack(dn, nexp, D, Fx, ws.down_q, ws.down_d, ws.dn16, ws.dn_dT, 0, 0, s);
+        return rc;
+    };
+    int rc = sets(w->routed, E, F, gate, up, down);
+    if (!rc && Fs) rc = sets(w->shared, 1, Fs, sh_gate, sh_up, sh_down);
+    if (!rc) rc = cuda_status(cudaStreamSynchronize(s));
+    return rc;
+}
+
+void free_weights(moe_weights_s *w) {
+    if (w->routed_arena_) cudaFree(w->routed_arena_);
+    w->routed_arena_ = nullptr;
+}
+
+}  // namespace moe

@@ -123,7 +123,7 @@ def _expert(seed: int, e: int, D: int, F: int):
     return g, u, d
 
 
-@lru_cache(maxsize=2)
+@lru_cache(maxsize=8)
 def _experts(seed: int, E: int, D: int, F: int):
     gate = np.empty((E, F, (D // QK) * Q8_0_BYTES), np.uint8)
     up = np.empty_like(gate)

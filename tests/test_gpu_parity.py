@@ -1,0 +1,357 @@
+"""GPU parity: every step of the CUDA path, called through the C ABI, against
+the CPU oracle on the same seeded inputs.
+
+Bars (from the layer's contract):
+  - routing indices, CSR arrays, Q8_1 codes of x and the int32 block dot
+    products: bit-exact (routing given the same logits, or on tokens whose
+    k-th/(k+1)-th logit gap exceeds twice the logit tolerance);
+  - router logits: |dl| <= 1e-4 * max(|l_ref|_max, rms(l_ref)) per token row;
+  - FFN outputs: relative L2 <= 2e-3 and max-abs <= 1e-2 of the oracle;
+  - the combine, given identical partials and weights: bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from mixture_experts_ffn_top_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+LOGIT_RTOL = 1e-4
+OUT_REL_L2 = 2e-3
+OUT_MAX_ABS = 1e-2
+W_RTOL = 2e-5
+
+CONFIGS = ["tiny", "olmoe", "decode_n1", "decode_n4", "decode_n8", "qwen3moe_shared", "skewed"]
+SMALL = ["tiny", "decode_n4", "qwen3moe_shared"]
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_ffn_top_gb300 import build, ops as _ops
+
+    build.build()
+    torch.cuda.set_device(0)
+    return _ops
+
+
+_cache = {}
+
+
+def case(name, full=True):
+    """(workload, inputs, oracle results) for a named workload, cached for the module."""
+    key = (name, full)
+    if key not in _cache:
+        wl = WORKLOADS[name]
+        inp = make_inputs(wl)
+        ref = O.moe_ffn_inputs(inp, wl.top_k, wl.norm_topk_prob)
+        _cache[key] = (wl, inp, ref)
+    return _cache[key]
+
+
+def dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return t if dtype is None else t.to(dtype)
+
+
+def logit_tol(ref_logits):
+    row_max = np.abs(ref_logits).max(axis=1)
+    row_rms = np.sqrt((ref_logits.astype(np.float64) ** 2).mean(axis=1))
+    return LOGIT_RTOL * np.maximum(row_max, row_rms)
+
+
+def clear_tokens(ref_logits, k):
+    """Tokens whose routing is decided by more than twice the logit tolerance."""
+    E = ref_logits.shape[1]
+    if k >= E:
+        return np.ones(ref_logits.shape[0], bool)
+    srt = np.sort(ref_logits, axis=1)[:, ::-1]
+    gap = srt[:, k - 1] - srt[:, k]
+    return gap > 2 * logit_tol(ref_logits)
+
+
+def assert_out_close(got, ref, mask=None, what="output"):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if mask is not None:
+        got, ref = got[mask], ref[mask]
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    assert rel <= OUT_REL_L2 and mx <= OUT_MAX_ABS, f"{what}: rel L2 {rel:.3e}, max abs {mx:.3e}"
+    return rel, mx
+
+
+def new_ws(ops, wl, N=None):
+    return ops.new_workspace(N or wl.N, wl.D, wl.E, wl.F, wl.top_k, wl.Fs)
+
+
+def layer_for(ops, inp, wl):
+    return ops.MoeLayer.from_numpy(inp, device="cuda:0", top_k=wl.top_k, max_tokens=wl.N)
+
+
+# -------------------------------------------------------------- router ----
+@pytest.mark.parametrize("name", CONFIGS)
+def test_router_parity(ops, name):
+    wl, inp, ref = case(name)
+    ws = new_ws(ops, wl)
+    r = ops.moe_router_topk(dev(inp["hidden"]), dev(inp["routerW"]),
+                            None if inp["shexp_gate"] is None else dev(inp["shexp_gate"]),
+                            wl.top_k, wl.norm_topk_prob, ws, want_logits=True)
+    assert ops.moe_workspace_status(ws) == 0
+    logits = r["logits"].cpu().numpy()
+    tol = logit_tol(ref["logits"])
+    assert np.all(np.abs(logits - ref["logits"]) <= tol[:, None])
+    clear = clear_tokens(ref["logits"], wl.top_k)
+    idx = r["topk_idx"].cpu().numpy()
+    np.testing.assert_array_equal(idx[clear], ref["topk_idx"][clear])
+    np.testing.assert_allclose(r["topk_w"].cpu().numpy()[clear], ref["topk_w"][clear], rtol=W_RTOL, atol=1e-7)
+    # Q8_1 of x: the same fp32 inputs give the same codes and scales
+    np.testing.assert_array_equal(r["x_q"].cpu().numpy(), ref["x_q"])
+    np.testing.assert_array_equal(r["x_d"].cpu().numpy(), O.halves(ref["x_d16"]))
+    if wl.has_shared:
+        np.testing.assert_allclose(r["shexp_scale"].cpu().numpy(), ref["shexp_scale"], rtol=1e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared", "skewed"])
+def test_topk_from_oracle_logits_bit_exact(ops, name):
+    """Given the oracle's logits, every token's routing is identical (ties to the lower index)."""
+    wl, inp, ref = case(name)
+    idx, w = ops.moe_topk_from_logits(dev(ref["logits"]), wl.top_k, wl.norm_topk_prob)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_allclose(w.cpu().numpy(), ref["topk_w"], rtol=W_RTOL, atol=1e-7)
+
+
+def test_topk_ties_and_norm(ops):
+    rng = np.random.default_rng(20)
+    for E, k in [(8, 2), (64, 8), (256, 8), (16, 16), (1024, 32)]:
+        logits = rng.integers(-2, 3, (300, E)).astype(np.float32)
+        for norm in (False, True):
+            ridx, rw, _ = O.softmax_topk(logits, k, norm)
+            idx, w = ops.moe_topk_from_logits(dev(logits), k, norm)
+            np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+            np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=W_RTOL, atol=1e-7)
+
+
+def test_quantize_bit_exact(ops):
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((4096, 64)) * np.exp(rng.uniform(-10, 10, (4096, 1)))).astype(np.float32)
+    x[0] = 0.0
+    x[1, :32] = np.arange(32)
+    x[2, 0] = 127.0
+    x[2, 1:9] = [2.5, -2.5, 0.5, -0.5, 1.5, 126.5, -3.5, 0.49999997]
+    x[3, 0] = 127.0 * (1.0 + 2.0 ** -12)
+    x[3, 1] = 63.5
+    q, d = ops.moe_quantize_q8_1(dev(x))
+    rq, rd16, _ = O.quantize_q8_1(x)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(d.cpu().numpy(), O.halves(rd16))
+
+
+# ------------------------------------------------------------- bucketing ---
+@pytest.mark.parametrize("name", CONFIGS)
+def test_bucket_bit_exact(ops, name):
+    wl, inp, ref = case(name)
+    ws = new_ws(ops, wl)
+    es, ti, tk = ops.moe_bucket(dev(ref["topk_idx"]), wl.E, ws)
+    assert ops.moe_workspace_status(ws) == 0
+    np.testing.assert_array_equal(es.cpu().numpy(), ref["expStart"])
+    np.testing.assert_array_equal(ti.cpu().numpy(), ref["expTokI"])
+    np.testing.assert_array_equal(tk.cpu().numpy(), ref["expTokK"])
+
+
+@pytest.mark.parametrize("N,E,k", [(1, 8, 2), (3, 8, 8), (1025, 64, 8), (4096, 128, 8), (2500, 1024, 32),
+                                   (7, 1, 1)])
+def test_bucket_random_shapes(ops, N, E, k):
+    rng = np.random.default_rng(N + E + k)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    ws = ops.new_workspace(N, 64, E, 64, k)
+    es, ti, tk = ops.moe_bucket(dev(idx), E, ws)
+    assert ops.moe_workspace_status(ws) == 0
+    res, rti, rtk = O.bucket(idx, E)
+    np.testing.assert_array_equal(es.cpu().numpy(), res)
+    np.testing.assert_array_equal(ti.cpu().numpy(), rti)
+    np.testing.assert_array_equal(tk.cpu().numpy(), rtk)
+
+
+@pytest.mark.parametrize("bad", ["out_of_range", "negative", "repeated"])
+def test_bucket_flags_bad_routing(ops, bad):
+    idx = np.array([[0, 1], [2, 3], [4, 5]], np.int32)
+    if bad == "out_of_range":
+        idx[1, 1] = 8
+    elif bad == "negative":
+        idx[2, 0] = -1
+    else:
+        idx[0, 1] = 0
+    ws = ops.new_workspace(3, 64, 8, 64, 2)
+    es, ti, tk = ops.moe_bucket(dev(idx), 8, ws)
+    word = ops.moe_workspace_status(ws)
+    assert word & 0x1
+    assert np.all(es.cpu().numpy() == 0)  # every segment left empty
+    assert ops.moe_workspace_status(ws) == 0  # cleared
+
+
+# ------------------------------------------------------ grouped experts ---
+def _csr(ref):
+    return dev(ref["expStart"]), dev(ref["expTokI"]), dev(ref["expTokK"])
+
+
+@pytest.mark.parametrize("name", SMALL + ["olmoe"])
+@pytest.mark.parametrize("path", [1])
+def test_gate_up_block_dots_bit_exact(ops, name, path):
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    ws = layer.ws
+    es, ti, tk = _csr(ref)
+    xq, xd = dev(ref["x_q"]), dev(O.halves(ref["x_d16"]))
+    nblk = wl.D // 32
+    rows = np.arange(ref["expStart"][-1])
+    rng = np.random.default_rng(0)
+    sample = rng.choice(rows, size=min(64, len(rows)), replace=False)
+    for block in sorted({0, nblk // 2 + 1, nblk - 1}):
+        dots = ops.moe_debug_gate_up_block_dots(layer.w, xq, xd, es, ti, wl.top_k, block, ws, path=path)
+        assert ops.moe_workspace_status(ws) == 0
+        dots = dots.cpu().numpy()
+        for j in sample:
+            e = int(np.searchsorted(ref["expStart"], j, side="right") - 1)
+            t = int(ref["expTokI"][j])
+            for mat, W in ((0, inp["gate"]), (1, inp["up"])):
+                for f in (0, wl.F // 2 + 3, wl.F - 1):
+                    ref_dot = O.block_dots(W[e, f], ref["x_q"][t])[block]
+                    assert dots[j, mat, f] == ref_dot, (j, mat, f, block)
+
+
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
+@pytest.mark.parametrize("path", [1])
+def test_gate_up_requantised_activations(ops, name, path):
+    """h_q from the oracle's x_q and CSR: codes within +-1 (fp32 vs double accumulation can
+    move a value across a rounding boundary), at most 1% of them different."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    es, ti, tk = _csr(ref)
+    hq, hd = ops.moe_expert_gate_up(layer.w, dev(ref["x_q"]), dev(O.halves(ref["x_d16"])), es, ti, wl.top_k,
+                                    layer.ws, path=path)
+    assert ops.moe_workspace_status(layer.ws) == 0
+    total = int(ref["expStart"][-1])
+    hq = hq.cpu().numpy()[:total].astype(np.int32)
+    hd = hd.cpu().numpy()[:total]
+    rq = ref["h_q"].astype(np.int32)
+    diff = np.abs(hq - rq)
+    assert diff.max() <= 1
+    assert (diff > 0).mean() <= 0.01
+    rd = O.halves(ref["h_d16"])
+    np.testing.assert_allclose(hd, rd, rtol=1e-3, atol=1e-30)
+
+
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
+@pytest.mark.parametrize("path", [1])
+def test_down_given_oracle_h(ops, name, path):
+    """The down half on the oracle's own h_q: partials to fp32 accumulation accuracy."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    es, ti, tk = _csr(ref)
+    total = int(ref["expStart"][-1])
+    hq = np.zeros((wl.N * wl.top_k, wl.F), np.int8)
+    hd = np.zeros((wl.N * wl.top_k, wl.F // 32), np.float32)
+    hq[:total] = ref["h_q"]
+    hd[:total] = O.halves(ref["h_d16"])
+    part = ops.moe_expert_down(layer.w, dev(hq), dev(hd), es, ti, tk, wl.N, wl.top_k, layer.ws, path=path)
+    assert ops.moe_workspace_status(layer.ws) == 0
+    got = part.cpu().numpy().astype(np.float64)
+    r = ref["partials"].astype(np.float64)
+    rel = np.linalg.norm(got - r) / np.linalg.norm(r)
+    assert rel <= 1e-5, rel
+
+
+@pytest.mark.parametrize("name", SMALL + ["olmoe"])
+@pytest.mark.parametrize("path", [1])
+def test_grouped_ffn_partials(ops, name, path):
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    es, ti, tk = _csr(ref)
+    sh = dev(ref["shexp_scale"]) if wl.has_shared else None
+    part, shared = ops.moe_grouped_ffn(layer.w, dev(ref["x_q"]), dev(O.halves(ref["x_d16"])), es, ti, tk,
+                                       wl.top_k, layer.ws, shexp_scale=sh, path=path)
+    assert ops.moe_workspace_status(layer.ws) == 0
+    assert_out_close(part.cpu().numpy(), ref["partials"], what="partials")
+    if wl.has_shared:
+        assert_out_close(shared.cpu().numpy(), ref["shared_out"], what="shared expert")
+
+
+# -------------------------------------------------------------- combine ---
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared"])
+def test_combine_bit_exact(ops, name):
+    wl, inp, ref = case(name)
+    S = dev(ref["shared_out"]) if wl.has_shared else None
+    out = ops.moe_combine(dev(ref["partials"]), dev(ref["topk_w"]), S)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref["out"])
+
+
+def test_combine_order_sensitive_values(ops):
+    """Values where the slot order, the fma and the shared-last order each change the bits."""
+    p = np.zeros((4 * 3, 4), np.float32)
+    w = np.ones((4, 3), np.float32)
+    S = np.zeros((4, 4), np.float32)
+    p[0:3, 0] = [2.0 ** 24, 1.0, 1.0]                       # slot order
+    a = np.float32(1.0 + 2.0 ** -12)
+    p[3:6, 0] = [-1.0, a, 0.0]
+    w[1] = [1.0, a, 1.0]                                   # fma
+    p[6:9, 0] = [1.0, 2.0 ** 24, 0.0]
+    S[2, 0] = 1.0                                          # shared last
+    rng = np.random.default_rng(3)
+    p[9:12] = rng.standard_normal((3, 4)).astype(np.float32)
+    w[3] = rng.standard_normal(3).astype(np.float32)
+    out = ops.moe_combine(dev(p), dev(w), dev(S)).cpu().numpy()
+    np.testing.assert_array_equal(out, O.combine(p, w, S))
+    assert out[0, 0] == 2.0 ** 24 and out[1, 0] == 2.0 ** -11 + 2.0 ** -24 and out[2, 0] == 2.0 ** 24
+
+
+# ---------------------------------------------------------- whole layer ---
+@pytest.mark.parametrize("name", CONFIGS)
+@pytest.mark.parametrize("path", [0, 1])
+def test_layer_parity(ops, name, path):
+    """moe_ffn_prefill (the call bench.py times, path 0 = its launch configuration)."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    out = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=path)
+    assert layer.status() == 0
+    clear = clear_tokens(ref["logits"], wl.top_k)
+    v = layer.views(wl.N)
+    np.testing.assert_array_equal(v["topk_idx"].cpu().numpy()[clear], ref["topk_idx"][clear])
+    rel, mx = assert_out_close(out.cpu().numpy(), ref["out"], clear, what=f"{name} layer output")
+    assert clear.mean() > 0.98
+
+
+def _random_layer(N, D, E, k, F, Fs, norm, seed):
+    wl = Workload(f"rand{seed}", N=N, D=D, E=E, top_k=k, F=F, Fs=Fs, norm_topk_prob=norm, seed=seed)
+    return wl, make_inputs(wl)
+
+
+@pytest.mark.parametrize("N,D,E,k,F,Fs,norm", [
+    (1, 256, 8, 2, 128, 0, False),      # a single token
+    (3, 256, 8, 8, 128, 0, True),       # k = E: every expert selected
+    (130, 256, 16, 4, 192, 64, True),   # ragged N and F, shared expert
+    (77, 512, 32, 1, 64, 0, False),     # top-1
+    (5, 64, 4, 2, 32, 32, False),       # minimal blocks
+])
+def test_layer_edge_shapes(ops, N, D, E, k, F, Fs, norm):
+    wl, inp = _random_layer(N, D, E, k, F, Fs, norm, seed=N * 31 + E)
+    ref = O.moe_ffn_inputs(inp, k, norm)
+    layer = layer_for(ops, inp, wl)
+    for path in (0, 1):
+        out = layer.prefill(dev(inp["hidden"]), k, norm, path=path)
+        assert layer.status() == 0
+        clear = clear_tokens(ref["logits"], k)
+        assert_out_close(out.cpu().numpy(), ref["out"], clear, what=f"edge N={N} E={E} k={k}")
+
+
+def test_zero_hidden_gives_zero(ops):
+    wl, inp = _random_layer(16, 256, 8, 2, 128, 64, False, seed=5)
+    inp["hidden"][:] = 0.0
+    layer = layer_for(ops, inp, wl)
+    out = layer.prefill(dev(inp["hidden"]), 2, False)
+    assert layer.status() == 0
+    assert torch.count_nonzero(out).item() == 0
