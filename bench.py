@@ -77,7 +77,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -189,53 +189,57 @@ def run_ours(args, rank, world, local_rank):
     resolved_path = path
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     v = layer.views(N)
-    # staged calls: the same kernels moe_ffn_prefill launches, with events between the stages
+    # The step, stage by stage: the same kernels moe_ffn_prefill launches, each stage captured
+    # once as a CUDA graph so replaying it costs the host a few microseconds and the events
+    # between stages time the GPU work alone.
     stages = ["router", "bucket", "experts", "combine"]
+    shs = v["shexp_scale"] if shg is not None else None
+    sho = v["shared_out"] if shg is not None else None
 
-    def step(ev=None):
-        def mark(i):
-            if ev is not None:
-                ev[i].record(stream)
+    def st_router():
+        ops._check(ops.lib().moe_router_topk(
+            ops._P(hidden.data_ptr()), ops._P(routerW.data_ptr()), ops._dev(shg), N, D, E, k,
+            int(wl.norm_topk_prob), ops._dev(v["topk_idx"]), ops._dev(v["topk_w"]), ops._dev(shs),
+            ops._dev(v["x_q"]), ops._dev(v["x_d"]), None, ops._dev(ws), ws.numel(), ops._stream(None)),
+            "moe_router_topk")
 
-        mark(0)
-        rc = ops.lib().moe_router_topk(ops._P(hidden.data_ptr()), ops._P(routerW.data_ptr()),
-                                       ops._P(shg.data_ptr()) if shg is not None else None, N, D, E, k,
-                                       int(wl.norm_topk_prob), ops._P(v["topk_idx"].data_ptr()),
-                                       ops._P(v["topk_w"].data_ptr()),
-                                       ops._P(v["shexp_scale"].data_ptr()) if shg is not None else None,
-                                       ops._P(v["x_q"].data_ptr()), ops._P(v["x_d"].data_ptr()), None,
-                                       ops._P(ws.data_ptr()), ws.numel(), ops._P(stream.cuda_stream))
-        ops._check(rc, "moe_router_topk")
-        mark(1)
-        rc = ops.lib().moe_bucket(ops._P(v["topk_idx"].data_ptr()), N, k, E, ops._P(v["expStart"].data_ptr()),
-                                  ops._P(v["expTokI"].data_ptr()), ops._P(v["expTokK"].data_ptr()),
-                                  ops._P(ws.data_ptr()), ws.numel(), ops._P(stream.cuda_stream))
-        ops._check(rc, "moe_bucket")
-        mark(2)
-        rc = ops.lib().moe_grouped_ffn_ex(w.handle, ops._P(v["x_q"].data_ptr()), ops._P(v["x_d"].data_ptr()),
-                                          ops._P(v["expStart"].data_ptr()), ops._P(v["expTokI"].data_ptr()),
-                                          ops._P(v["expTokK"].data_ptr()), N, k,
-                                          ops._P(v["shexp_scale"].data_ptr()) if shg is not None else None,
-                                          ops._P(v["partials"].data_ptr()),
-                                          ops._P(v["shared_out"].data_ptr()) if shg is not None else None, path,
-                                          ops._P(ws.data_ptr()), ws.numel(), ops._P(stream.cuda_stream))
-        ops._check(rc, "moe_grouped_ffn")
-        mark(3)
-        ops.moe_combine(v["partials"], v["topk_w"], v["shared_out"] if shg is not None else None, out=out)
-        mark(4)
+    def st_bucket():
+        ops._check(ops.lib().moe_bucket(ops._dev(v["topk_idx"]), N, k, E, ops._dev(v["expStart"]),
+                                        ops._dev(v["expTokI"]), ops._dev(v["expTokK"]), ops._dev(ws), ws.numel(),
+                                        ops._stream(None)), "moe_bucket")
 
+    def st_experts():
+        ops._check(ops.lib().moe_grouped_ffn_ex(
+            w.handle, ops._dev(v["x_q"]), ops._dev(v["x_d"]), ops._dev(v["expStart"]), ops._dev(v["expTokI"]),
+            ops._dev(v["expTokK"]), N, k, ops._dev(shs), ops._dev(v["partials"]), ops._dev(sho), path,
+            ops._dev(ws), ws.numel(), ops._stream(None)), "moe_grouped_ffn")
+
+    def st_combine():
+        ops.moe_combine(v["partials"], v["topk_w"], sho, out=out)
+
+    fns = [st_router, st_bucket, st_experts, st_combine]
     for _ in range(args.warmup):
-        step()
+        for f in fns:
+            f()
         flush.fill_(1)
     torch.cuda.synchronize()
     status = layer.status()
     if status:
         raise RuntimeError(f"device status {status} after warm-up")
-    # which expert path AUTO chose is visible in the kernel count: derive it from the rules
+    graphs = []
+    for f in fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            f()
+        graphs.append(g)
+    for _ in range(2):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    # which expert path AUTO chose: the library's own rule, visible through the handle
     if path == ops.MOE_PATH_AUTO:
         avg_rows = N * k // E
-        tensor = (D % 128 == 0 and F % 64 == 0 and (Fs == 0 or Fs % 64 == 0) and N >= 64 and avg_rows >= 8
-                  and _tensor_available(ops, layer))
+        tensor = ops.moe_weights_tensor_path(w) and N >= 64 and avg_rows >= 8
         resolved_path = ops.MOE_PATH_TENSOR if tensor else ops.MOE_PATH_MATVEC
     topk_idx = v["topk_idx"].cpu().numpy()
 
@@ -249,7 +253,10 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
-        step(evs[i])
+        evs[i][0].record(stream)
+        for j, g in enumerate(graphs):
+            g.replay()
+            evs[i][j + 1].record(stream)
         flush.fill_(1)  # outside the step's events: the next step starts with a cold L2
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -354,17 +361,10 @@ def run_ours(args, rank, world, local_rank):
 TRAFFIC = {}
 
 
-def _tensor_available(ops, layer) -> bool:
-    try:
-        return bool(ops.tensor_path_available(layer.w))
-    except AttributeError:
-        return False
-
-
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))

@@ -118,13 +118,8 @@ bucket_kernel(const int32_t *__restrict__ idx, int N, int k, int E, int32_t *__r
 int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart,
                   int32_t *expTokI, int32_t *expTokK, unsigned *status, cudaStream_t s) {
     size_t smem = sizeof(unsigned) * ((size_t)E + 33 + (size_t)E * B_WORDS);
-    static int configured_bytes = 0;
-    if ((int)smem > 48 * 1024 && (int)smem > configured_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-        configured_bytes = (int)smem;
-    }
+    static int configured = 0;
+    if (int rc = ensure_dynamic_smem((const void *)bucket_kernel, smem, &configured)) return rc;
     bucket_kernel<<<1, B_THREADS, smem, s>>>(topk_idx, N, top_k, E, expStart, expTokI, expTokK, status);
     return launch_status();
 }

@@ -1,29 +1,882 @@
-// expert_gemm.cu -- tensor-core grouped expert GEMM (placeholder until the
-// tcgen05 kernels land: the tensor path reports itself unavailable).
+// expert_gemm.cu -- grouped expert GEMM on the 5th-generation tensor cores.
+//
+// One persistent launch covers every expert's CSR segment (the grouped /
+// segmented GEMM of "Carnice prefill toward llama.cpp 676 t/s", #388, lever
+// 3, replacing one launch per expert; gather -> GEMM-N -> scatter of "batched
+// int8-MMQ trunk prefill gated off for MoE", #406, "The work" item 2).
+//
+// Arithmetic.  The Q8_0 x Q8_1 dot of a weight row and an activation row is
+// sum_b d_w[b] * d_x[b] * isum_b with isum_b the int32 dot of block b's quants.
+// tcgen05 has no int8 MMA on sm_103a, but every int8 quant (|q| <= 127) is an
+// exact fp16 value, every product (<= 16129) and every 32-term block sum
+// (<= 516128 < 2^24) is exact in the fp32 accumulator.  So a kind::f16 MMA
+// over exactly one 32-wide block, started from zero, yields isum_b exactly.
+// Each block therefore gets its own accumulator in tensor memory (TMEM); the
+// drain warps read it (tcgen05.ld), scale it by d_w (per TMEM lane = weight
+// row) * d_x (per column = token) and accumulate in registers.
+//
+// Roles (320 threads, one CTA per SM, persistent over work items):
+//   warp 0     TMA producer: per stage (64 K = 2 blocks) the weight tile
+//              [128 rows x 64] fp16, the token tile [nb rows x 64] fp16 (nb
+//              = 16/32/64/128, the smallest box that holds the tile's rows)
+//              and both tiles' block scales.
+//   warp 1     TMEM owner and MMA issuer: 2 x (M128 x N x K16) per block into
+//              one of 4 TMEM accumulators of 128 columns.
+//   warps 2-9  drain: warp w reads TMEM lanes 32*(w%4).. (the hardware's lane
+//              quarter rule); warps 2-5 take the even 16-column chunks, 6-9 the
+//              odd ones.  Epilogue: gate/up tiles hold 64 gate rows and the 64
+//              up rows of the same features (weights repacked that way), so
+//              h = SiLU(g) * u is formed through a shared-memory exchange and
+//              requantised to Q8_1 per 32 features (one warp = one block);
+//              down tiles scatter fp32 rows to partials[t*top_k + slot] (or
+//              s_t * y to the shared expert's output).
+// Every wait on an mbarrier is bounded (a few seconds); on expiry the CTA sets
+// MOE_DEV_TIMEOUT in the status word, every role drains out, in-flight copies
+// and MMAs are waited for (bounded) and TMEM is freed before returning.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
 
-bool tensor_path_supported(const moe_weights_s *) { return false; }
-int prepare_tensor_maps(moe_weights_s *) { return MOE_OK; }
-int launch_plan_and_gather(const moe_weights_s *, const int8_t *, const float *, const int32_t *, const int32_t *,
-                           const int32_t *, int, int, bool, void *, const WsLayout &, cudaStream_t) {
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+namespace {
+
+constexpr int G_THREADS = 320;
+constexpr int G_STAGES = 5;
+constexpr int G_TMEM_BUFS = 4;
+constexpr int G_TMEM_COLS = 512;
+constexpr int STAGE_A = 16384;                 // 128 rows x 128 B
+constexpr int STAGE_B = 16384;                 // up to 128 rows x 128 B
+constexpr int STAGE_SA = 1024;                 // 2 blocks x 128 fp32
+constexpr int STAGE_SB = 1024;                 // 2 blocks x up to 128 fp32
+constexpr int STAGE_BYTES = STAGE_A + STAGE_B + STAGE_SA + STAGE_SB;  // 34816 = 34 KB
+constexpr int XCH_STRIDE = 65;                 // padded row of the gate/up exchange
+constexpr int XCH_BYTES = 2 * 64 * XCH_STRIDE * 4;
+constexpr int BAR_BYTES = 256;
+constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + XCH_BYTES + BAR_BYTES;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s
+
+struct GemmMaps {
+    CUtensorMap a_r, sa_r, a_s, sa_s;  // weights + weight scales, routed / shared
+    CUtensorMap b[4], sb[4];           // tokens + token scales, box heights 16/32/64/128
+};
+
+struct GemmParams {
+    int K_r, K_s;      // reduction length of routed / shared tiles
+    int MT_r, MT_s;    // 128-row weight tiles per token tile, routed / shared
+    int rows_r, rows_s;  // weight rows per expert in the A tensor map (2F or D), routed / shared
+    int sblk_r, sblk_s;  // scale rows per expert in the SA map (K/32)
+    int E, D, F, Fs, Fmax, top_k, N, rows_max, tiles_max;
+    const PlanHeader *plan;
+    const TileDesc *tiles;
+    const int4 *rowinfo;
+    __half *h16;       // gate/up output (fp16 integer codes), row stride Fmax
+    float *h_dT;       // [Fmax/32][rows_max]
+    float *partials;
+    float *shared_out;
+    const float *shexp_scale;
+    int32_t *dbg_dots;
+    int dbg_block;
+    unsigned *status;
+};
+
+// ------------------------------------------------------------- PTX glue ---
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-int launch_gemm_gate_up(const moe_weights_s *, int, int, bool, void *, const WsLayout &, int32_t *, int,
-                        cudaStream_t) {
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-int launch_gemm_down(const moe_weights_s *, int, int, bool, const float *, float *, float *, void *,
-                     const WsLayout &, cudaStream_t) {
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-int launch_h16_to_q8(const moe_weights_s *, int, int, void *, const WsLayout &, int8_t *, float *, cudaStream_t) {
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-int launch_q8_to_h16(const moe_weights_s *, int, int, void *, const WsLayout &, const int8_t *, const float *,
-                     cudaStream_t) {
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  Returns false (and raises
+// the CTA's abort flag and the device status bit) when the limit expires, or
+// as soon as another role of the CTA has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned *status) {
+    if (mbar_try(bar, parity)) return true;
+    uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                atomicOr(status, MOE_DEV_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout TMA writes (rows of 128 B, 8-row atoms of 1024 B).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8-row atom
+    d |= (uint64_t)1 << 46;                          // descriptor version (tcgen05)
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor: D fp32, A and B fp16, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------ schedule ---
+struct Item {
+    int tile, mt, shared, K, nrows, row0, expert, entry0, nb, bi;
+};
+__device__ __forceinline__ int total_items(const GemmParams &p, int n_tiles, int n_rtiles) {
+    return n_rtiles * p.MT_r + (n_tiles - n_rtiles) * p.MT_s;
+}
+__device__ __forceinline__ Item item_at(const GemmParams &p, int it, int n_rtiles) {
+    Item x;
+    if (it < n_rtiles * p.MT_r) {
+        x.tile = it / p.MT_r;
+        x.mt = it - x.tile * p.MT_r;
+        x.shared = 0;
+        x.K = p.K_r;
+    } else {
+        int i2 = it - n_rtiles * p.MT_r;
+        x.tile = n_rtiles + i2 / p.MT_s;
+        x.mt = i2 % p.MT_s;
+        x.shared = 1;
+        x.K = p.K_s;
+    }
+    const TileDesc td = p.tiles[x.tile];
+    x.nrows = td.nrows;
+    x.row0 = td.row0;
+    x.expert = td.expert;
+    x.entry0 = td.entry0;
+    x.bi = x.nrows <= 16 ? 0 : x.nrows <= 32 ? 1 : x.nrows <= 64 ? 2 : 3;
+    x.nb = 16 << x.bi;
+    return x;
+}
+
+// --------------------------------------------------------------- kernel ---
+// MODE 0: gate/up (fused SiLU * up, Q8_1 requant); 1: down (scatter).
+// DUMP (gate/up only): also store the raw int32 block dots of block p.dbg_block
+// (the debug entry point; a separate instantiation keeps the hot loop lean).
+template <int MODE, bool DUMP>
+__global__ void __launch_bounds__(G_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    float *xch = reinterpret_cast<float *>(smem + G_STAGES * STAGE_BYTES);
+    uint8_t *bars = smem + G_STAGES * STAGE_BYTES + XCH_BYTES;
+    const uint32_t bar_base = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar_base + 8 * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8 * (G_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar_base + 8 * (2 * G_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar_base + 8 * (2 * G_STAGES + G_TMEM_BUFS + b); };
+    auto xfull_bar = [&](int h) { return bar_base + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + h); };
+    auto xempty_bar = [&](int h) { return bar_base + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + 2 + h); };
+    const uint32_t done_bar = bar_base + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + 5));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 8);
+        }
+        for (int b = 0; b < G_TMEM_BUFS; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 8);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(xfull_bar(h), 2);   // the two up-row warps of a half
+            mbar_init(xempty_bar(h), 2);  // the two gate-row warps of a half
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&maps.a_r);
+        prefetch_map(&maps.sa_r);
+        prefetch_map(&maps.a_s);
+        prefetch_map(&maps.sa_s);
+        for (int i = 0; i < 4; ++i) {
+            prefetch_map(&maps.b[i]);
+            prefetch_map(&maps.sb[i]);
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(G_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int n_tiles = p.plan->n_tiles;
+    int n_rtiles = p.plan->pad;  // routed tiles come first
+    n_tiles = min(max(n_tiles, 0), p.tiles_max);
+    n_rtiles = min(max(n_rtiles, 0), n_tiles);
+    const int n_items = total_items(p, n_tiles, n_rtiles);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ---
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_parity[G_STAGES];
+            bool issued[G_STAGES];
+            for (int s = 0; s < G_STAGES; ++s) issued[s] = false, issued_parity[s] = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const Item x = item_at(p, it, n_rtiles);
+                const CUtensorMap *ma = x.shared ? &maps.a_s : &maps.a_r;
+                const CUtensorMap *msa = x.shared ? &maps.sa_s : &maps.sa_r;
+                const int arow = (x.shared ? 0 : x.expert * p.rows_r) + x.mt * 128;
+                const int sarow = x.shared ? 0 : x.expert * p.sblk_r;
+                const uint32_t bytes = STAGE_A + x.nb * 128 + STAGE_SA + 2 * x.nb * 4;
+                for (int ks = 0; ks < x.K / 64; ++ks) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = smem + stage * STAGE_BYTES;
+                    mbar_expect_tx(full_bar(stage), bytes);
+                    tma_load_2d(smem_u32(st), ma, ks * 64, arow, full_bar(stage));
+                    tma_load_2d(smem_u32(st + STAGE_A), &maps.b[x.bi], ks * 64, x.row0, full_bar(stage));
+                    tma_load_2d(smem_u32(st + STAGE_A + STAGE_B), msa, x.mt * 128, sarow + 2 * ks, full_bar(stage));
+                    tma_load_2d(smem_u32(st + STAGE_A + STAGE_B + STAGE_SA), &maps.sb[x.bi], x.row0, 2 * ks,
+                                full_bar(stage));
+                    issued[stage] = true;
+                    issued_parity[stage] = phase;
+                    if (++stage == G_STAGES) stage = 0, phase ^= 1;
+                }
+            }
+            // copies still in flight must land before the CTA can exit
+            for (int s = 0; s < G_STAGES; ++s)
+                if (issued[s]) {
+                    uint64_t t0 = globaltimer();
+                    while (!mbar_try(full_bar(s), issued_parity[s]) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                    }
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer ---
+        if (lane == 0) {
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, tphase = 0;
+            bool ok = true;
+            bool any = false;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const Item x = item_at(p, it, n_rtiles);
+                const int n_mma = (x.nrows + 15) & ~15;
+                const uint32_t idesc = idesc_f16(n_mma);
+                for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t b0 = a0 + STAGE_A;
+                    for (int half = 0; half < 2; ++half) {
+                        if (!mbar_wait(tempty_bar(buf), tphase ^ 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + buf * 128;
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t off = half * 64 + kk * 32;  // bytes along K inside the swizzle atom
+                            mma_f16(d, smem_desc_sw128(a0 + off), smem_desc_sw128(b0 + off), idesc, kk);
+                        }
+                        mma_commit(tfull_bar(buf));
+                        any = true;
+                        if (++buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
+                    }
+                    if (++stage == G_STAGES) stage = 0, phase ^= 1;
+                }
+            }
+            if (any) {
+                // every issued MMA has completed once this commit arrives
+                mma_commit(done_bar);
+                uint64_t t0 = globaltimer();
+                while (!mbar_try(done_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------- drain ---
+        const int q = warp & 3;          // TMEM lane quarter of this warp
+        const int h = (warp - 2) >> 2;   // 0: even 16-column chunks, 1: odd
+        const int r = q * 32 + lane;     // row of the 128-row weight tile
+        int stage = 0, buf = 0;
+        uint32_t phase = 0, tphase = 0, xphase = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Item x = item_at(p, it, n_rtiles);
+            const int nchunks = (x.nrows + 15) >> 4;
+            float acc[4][16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+            for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
+                ok = mbar_wait(full_bar(stage), phase, abort_flag, p.status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const float *SA = reinterpret_cast<const float *>(smem + stage * STAGE_BYTES + STAGE_A + STAGE_B);
+                const float *SB = SA + 256;
+                for (int half = 0; half < 2; ++half) {
+                    ok = mbar_wait(tfull_bar(buf), tphase, abort_flag, p.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const float dw = SA[half * 128 + r];
+                    const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 128;
+                    const float *sbh = SB + half * x.nb;
+                    const bool dump = DUMP && MODE == 0 && p.dbg_dots != nullptr && x.shared == 0 && ks * 2 + half == p.dbg_block;
+#pragma unroll
+                    for (int pr = 0; pr < 2; ++pr) {
+                        // two 16-column chunks per TMEM round trip keeps the live registers in budget
+                        uint32_t v[2][16];
+#pragma unroll
+                        for (int ii = 0; ii < 2; ++ii) {
+                            const int c = h + 2 * (2 * pr + ii);
+                            if (c < nchunks) tmem_ld16(tb + c * 16, v[ii]);
+                        }
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int ii = 0; ii < 2; ++ii) {
+                            const int i = 2 * pr + ii;
+                            const int c = h + 2 * i;
+                            if (c >= nchunks) continue;
+                            if (dump) {
+                                const int mat = r < 64 ? 0 : 1;
+                                const int f = x.mt * 64 + (r & 63);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const int col = c * 16 + j;
+                                    if (col < x.nrows)
+                                        p.dbg_dots[((size_t)(x.entry0 + col) * 2 + mat) * p.F + f] =
+                                            (int32_t)__uint_as_float(v[ii][j]);
+                                }
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                acc[i][j] = fmaf(__uint_as_float(v[ii][j]), sbh[c * 16 + j] * dw, acc[i][j]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(buf));
+                    if (++buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));  // scales of both blocks read
+                if (++stage == G_STAGES) stage = 0, phase ^= 1;
+            }
+            if (!ok) break;
+            // --------------------------------------------------- epilogue ---
+            if (MODE == 0) {
+                float *xh = xch + h * 64 * XCH_STRIDE;
+                if (q >= 2) {
+                    // up rows: hand u to the gate rows of the same features
+                    ok = mbar_wait(xempty_bar(h), xphase ^ 1, abort_flag, p.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) xh[(r - 64) * XCH_STRIDE + i * 16 + j] = acc[i][j];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xfull_bar(h));
+                } else {
+                    ok = mbar_wait(xfull_bar(h), xphase, abort_flag, p.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    const int f = x.mt * 64 + r;  // feature (this warp: one 32-feature block)
+                    const int fblk = f >> 5;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = h + 2 * i;
+                        if (c >= nchunks) continue;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = c * 16 + j;
+                            if (col >= x.nrows) continue;  // warp-uniform
+                            const float g = acc[i][j];
+                            const float u = xh[r * XCH_STRIDE + i * 16 + j];
+                            const float hv = g / (1.0f + expf(-g)) * u;
+                            float d16f;
+                            const int qv = q8_quantize_lane(hv, &d16f);
+                            const int prow = x.row0 + col;
+                            p.h16[(size_t)prow * p.Fmax + f] = __int2half_rn(qv);
+                            if (lane == 0) p.h_dT[(size_t)fblk * p.rows_max + prow] = d16f;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xempty_bar(h));
+                }
+                xphase ^= 1;
+            } else {
+                const int dcol = x.mt * 128 + r;  // output column
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = h + 2 * i;
+                    if (c >= nchunks) continue;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = c * 16 + j;
+                        if (col >= x.nrows) continue;
+                        const int orow = p.rowinfo[x.row0 + col].y;
+                        if (orow < 0) continue;
+                        if (x.shared)
+                            p.shared_out[(size_t)orow * p.D + dcol] = p.shexp_scale[orow] * acc[i][j];
+                        else
+                            p.partials[(size_t)orow * p.D + dcol] = acc[i][j];
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(G_TMEM_COLS)
+                     : "memory");
+}
+
+// ------------------------------------------------ planning and gathering ---
+// One CTA: padded segment starts (16-row aligned), token tiles of <= 128 rows
+// per segment (routed experts first, then the shared expert's N rows), and for
+// every padded row its source token, output row and CSR entry.
+__global__ void __launch_bounds__(1024)
+plan_kernel(const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI,
+            const int32_t *__restrict__ expTokK, int N, int top_k, int E, int with_shared, int rows_max,
+            int tiles_max, PlanHeader *hdr, int32_t *gstart_out, TileDesc *tiles, int4 *rowinfo, unsigned *status) {
+    __shared__ int cnt[MAX_E + 1], gst[MAX_E + 2], tst[MAX_E + 2];
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    const int total = N * top_k;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int a = expStart[e], b = expStart[e + 1];
+        if (a < 0 || b < a || b > total) bad = 1;
+        cnt[e] = b - a;
+    }
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) {
+            atomicOr(status, MOE_DEV_BAD_CSR);
+            hdr->n_tiles = 0;
+            hdr->n_rows = 0;
+            hdr->shared_row0 = -1;
+            hdr->pad = 0;
+        }
+        return;
+    }
+    if (tid == 0) {
+        // serial scans over <= 1025 segments: negligible next to the GEMMs
+        int g = 0, t = 0;
+        for (int e = 0; e < E; ++e) {
+            gst[e] = g;
+            tst[e] = t;
+            g += (cnt[e] + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
+            t += (cnt[e] + TILE_N - 1) / TILE_N;
+        }
+        gst[E] = g;
+        tst[E] = t;
+        const int ns = with_shared ? N : 0;
+        gst[E + 1] = g + (ns + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
+        tst[E + 1] = t + (ns + TILE_N - 1) / TILE_N;
+        hdr->n_tiles = min(tst[E + 1], tiles_max);
+        hdr->n_rows = min(gst[E + 1], rows_max);
+        hdr->shared_row0 = with_shared ? g : -1;
+        hdr->pad = tst[E];  // routed tiles
+    }
+    __syncthreads();
+    for (int e = tid; e <= E + 1; e += blockDim.x) gstart_out[e] = gst[e];
+    // tiles
+    for (int e = tid; e <= E; e += blockDim.x) {
+        const bool sh = (e == E);
+        if (sh && !with_shared) continue;
+        const int n = sh ? N : cnt[e];
+        for (int i = 0; i * TILE_N < n; ++i) {
+            const int ti = tst[e] + i;
+            if (ti >= tiles_max) break;
+            TileDesc td;
+            td.row0 = gst[e] + i * TILE_N;
+            td.nrows = min(TILE_N, n - i * TILE_N);
+            td.expert = e;
+            td.entry0 = (sh ? 0 : expStart[e]) + i * TILE_N;
+            tiles[ti] = td;
+        }
+    }
+    // rows: .x source token, .y output row (t*top_k + slot, or t for the shared expert), .z CSR entry
+    const int nrows = min(gst[E + 1], rows_max);
+    for (int prow = tid; prow < nrows; prow += blockDim.x) {
+        int lo = 0, hi = E + 1;  // find e with gst[e] <= prow < gst[e+1]
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (gst[mid] <= prow) lo = mid;
+            else hi = mid;
+        }
+        const int e = lo;
+        const int i = prow - gst[e];
+        int4 ri = make_int4(-1, -1, -1, 0);
+        if (e < E) {
+            if (i < cnt[e]) {
+                const int j = expStart[e] + i;
+                const int t = expTokI[j];
+                const int s = expTokK ? expTokK[j] : 0;
+                if ((unsigned)t < (unsigned)N && (unsigned)s < (unsigned)top_k) {
+                    ri = make_int4(t, t * top_k + s, j, 0);
+                } else {
+                    atomicOr(status, MOE_DEV_BAD_CSR);
+                }
+            }
+        } else if (with_shared && i < N) {
+            ri = make_int4(i, i, -1, 0);
+        }
+        rowinfo[prow] = ri;
+    }
+}
+
+// Gather the Q8_1 rows of x into the padded segment order as exact fp16
+// integers, and their block scales transposed ([D/32][rows]).  A CTA owns 32
+// padded rows; pad rows are zero.
+__global__ void __launch_bounds__(256)
+gather_kernel(const int8_t *__restrict__ x_q, const float *__restrict__ x_d, int D, const PlanHeader *hdr,
+              const int4 *__restrict__ rowinfo, int rows_max, __half *__restrict__ xg16, float *__restrict__ xg_dT) {
+    const int row0 = blockIdx.x * 32;
+    const int nrows = hdr->n_rows;
+    if (row0 >= nrows) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nblk = D / QK;
+    for (int rr = warp; rr < 32; rr += 8) {
+        const int prow = row0 + rr;
+        if (prow >= nrows) break;
+        const int t = rowinfo[prow].x;
+        __half *dst = xg16 + (size_t)prow * D;
+        for (int c = lane; c < D / 16; c += 32) {
+            int4 v = make_int4(0, 0, 0, 0);
+            if (t >= 0) v = *reinterpret_cast<const int4 *>(x_q + (size_t)t * D + c * 16);
+            const int8_t *b = reinterpret_cast<const int8_t *>(&v);
+            __align__(16) __half2 o[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = __halves2half2(__short2half_rn(b[2 * k]), __short2half_rn(b[2 * k + 1]));
+            *reinterpret_cast<int4 *>(dst + c * 16) = *reinterpret_cast<const int4 *>(&o[0]);
+            *reinterpret_cast<int4 *>(dst + c * 16 + 8) = *reinterpret_cast<const int4 *>(&o[4]);
+        }
+    }
+    // scales: lane = row, warps stride over blocks (coalesced 128-byte rows of xg_dT)
+    const int prow = row0 + lane;
+    const int t = prow < nrows ? rowinfo[prow].x : -1;
+    for (int b = warp; b < nblk; b += 8) {
+        const float d = t >= 0 ? x_d[(size_t)t * nblk + b] : 0.0f;
+        if (prow < rows_max) xg_dT[(size_t)b * rows_max + prow] = d;
+    }
+}
+
+// h (fp16 codes + transposed scales, padded order) -> int8 + fp32 scales in CSR entry order.
+__global__ void h16_to_q8_kernel(const __half *__restrict__ h16, const float *__restrict__ h_dT, int F, int Fmax,
+                                 int rows_max, const PlanHeader *hdr, const int4 *__restrict__ rowinfo,
+                                 int8_t *__restrict__ h_q, float *__restrict__ h_d) {
+    const int prow = blockIdx.x;
+    if (prow >= hdr->n_rows) return;
+    const int j = rowinfo[prow].z;
+    if (j < 0) return;
+    for (int f = threadIdx.x; f < F; f += blockDim.x) {
+        h_q[(size_t)j * F + f] = (int8_t)__half2int_rn(h16[(size_t)prow * Fmax + f]);
+        if ((f & 31) == 0) h_d[(size_t)j * (F / QK) + f / QK] = h_dT[(size_t)(f / QK) * rows_max + prow];
+    }
+}
+
+// int8 + fp32 scales in CSR entry order -> fp16 codes + transposed scales in padded order.
+__global__ void q8_to_h16_kernel(const int8_t *__restrict__ h_q, const float *__restrict__ h_d, int F, int Fmax,
+                                 int rows_max, const PlanHeader *hdr, const int4 *__restrict__ rowinfo,
+                                 __half *__restrict__ h16, float *__restrict__ h_dT) {
+    const int prow = blockIdx.x;
+    if (prow >= hdr->n_rows) return;
+    const int j = rowinfo[prow].z;
+    for (int f = threadIdx.x; f < F; f += blockDim.x) {
+        const int v = j >= 0 ? h_q[(size_t)j * F + f] : 0;
+        h16[(size_t)prow * Fmax + f] = __int2half_rn(v);
+        if ((f & 31) == 0) h_dT[(size_t)(f / QK) * rows_max + prow] = j >= 0 ? h_d[(size_t)j * (F / QK) + f / QK] : 0.0f;
+    }
+}
+
+// ----------------------------------------------------- tensor map encode ---
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+    static EncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(ptr);
+    });
+    return fn;
+}
+
+// 2D row-major tensor [rows][cols] of fp16 (swizzled 64-wide boxes) or fp32 (plain boxes).
+bool encode_2d(CUtensorMap *m, const void *base, bool fp16, uint64_t rows, uint64_t cols, uint32_t box_cols,
+               uint32_t box_rows) {
+    EncodeFn fn = encode_fn();
+    if (!fn) return false;
+    const size_t es = fp16 ? 2 : 4;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * es};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    fp16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct WeightMaps {
+    CUtensorMap gu_r, gu_dT_r, dn_r, dn_dT_r;
+    CUtensorMap gu_s, gu_dT_s, dn_s, dn_dT_s;
+};
+
+int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws, const WsLayout &L,
+                float *partials, float *shared_out, const float *shexp_scale, int32_t *dbg_dots, int dbg_block,
+                cudaStream_t s) {
+    const WeightMaps *wm = static_cast<const WeightMaps *>(w->tmaps);
+    if (!wm) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int D = w->D, F = w->F, Fs = w->Fs, Fmax = std::max(F, Fs);
+    GemmMaps maps;
+    GemmParams p{};
+    if (mode == 0) {
+        maps.a_r = wm->gu_r;
+        maps.sa_r = wm->gu_dT_r;
+        maps.a_s = Fs ? wm->gu_s : wm->gu_r;
+        maps.sa_s = Fs ? wm->gu_dT_s : wm->gu_dT_r;
+        p.K_r = D;
+        p.K_s = D;
+        p.MT_r = 2 * F / 128;
+        p.MT_s = Fs ? 2 * Fs / 128 : 1;
+        p.rows_r = 2 * F;
+        p.rows_s = 2 * Fs;
+        p.sblk_r = D / QK;
+        p.sblk_s = D / QK;
+    } else {
+        maps.a_r = wm->dn_r;
+        maps.sa_r = wm->dn_dT_r;
+        maps.a_s = Fs ? wm->dn_s : wm->dn_r;
+        maps.sa_s = Fs ? wm->dn_dT_s : wm->dn_dT_r;
+        p.K_r = F;
+        p.K_s = Fs ? Fs : F;
+        p.MT_r = D / 128;
+        p.MT_s = D / 128;
+        p.rows_r = D;
+        p.rows_s = D;
+        p.sblk_r = F / QK;
+        p.sblk_s = Fs / QK;
+    }
+    // token-side maps over the workspace (per call: the workspace is the caller's)
+    const int rows = L.rows_max;
+    void *bdata = mode == 0 ? (void *)ws_ptr<__half>(ws, L.xg16) : (void *)ws_ptr<__half>(ws, L.h16);
+    void *bscale = mode == 0 ? (void *)ws_ptr<float>(ws, L.xg_dT) : (void *)ws_ptr<float>(ws, L.h_dT);
+    const int kcols = mode == 0 ? D : Fmax;
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t nb = 16u << i;
+        if (!encode_2d(&maps.b[i], bdata, true, rows, kcols, 64, nb)) return MOE_ERR_CUDA;
+        if (!encode_2d(&maps.sb[i], bscale, false, kcols / QK, rows, nb, 2)) return MOE_ERR_CUDA;
+    }
+    p.E = w->E;
+    p.D = D;
+    p.F = F;
+    p.Fs = Fs;
+    p.Fmax = Fmax;
+    p.top_k = top_k;
+    p.N = N;
+    p.rows_max = rows;
+    p.tiles_max = L.tiles_max;
+    p.plan = ws_ptr<PlanHeader>(ws, L.plan);
+    p.tiles = ws_ptr<TileDesc>(ws, L.tiles);
+    p.rowinfo = ws_ptr<int4>(ws, L.rowinfo);
+    p.h16 = ws_ptr<__half>(ws, L.h16);
+    p.h_dT = ws_ptr<float>(ws, L.h_dT);
+    p.partials = partials;
+    p.shared_out = shared_out;
+    p.shexp_scale = shexp_scale;
+    p.dbg_dots = dbg_dots;
+    p.dbg_block = dbg_block;
+    p.status = reinterpret_cast<unsigned *>(ws);
+    (void)with_shared;
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    if (mode == 0 && dbg_dots == nullptr) {
+        static int configured = 0;
+        if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<0, false>, G_SMEM, &configured)) return rc;
+        grouped_gemm_kernel<0, false><<<num_sms, G_THREADS, G_SMEM, s>>>(maps, p);
+    } else if (mode == 0) {
+        static int configured = 0;
+        if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<0, true>, G_SMEM, &configured)) return rc;
+        grouped_gemm_kernel<0, true><<<num_sms, G_THREADS, G_SMEM, s>>>(maps, p);
+    } else {
+        static int configured = 0;
+        if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<1, false>, G_SMEM, &configured)) return rc;
+        grouped_gemm_kernel<1, false><<<num_sms, G_THREADS, G_SMEM, s>>>(maps, p);
+    }
+    return launch_status();
+}
+
+}  // namespace
+
+bool tensor_path_supported(const moe_weights_s *w) { return w && w->tensor_ok && w->tmaps != nullptr; }
+
+int prepare_tensor_maps(moe_weights_s *w) {
+    if (!encode_fn()) return MOE_OK;  // no driver entry point: the tensor path stays off
+    WeightMaps *m = new WeightMaps();
+    const int E = w->E, D = w->D, F = w->F, Fs = w->Fs;
+    bool ok = encode_2d(&m->gu_r, w->routed.gu16, true, (uint64_t)E * 2 * F, D, 64, 128) &&
+              encode_2d(&m->gu_dT_r, w->routed.gu_dT, false, (uint64_t)E * (D / QK), 2 * F, 128, 2) &&
+              encode_2d(&m->dn_r, w->routed.dn16, true, (uint64_t)E * D, F, 64, 128) &&
+              encode_2d(&m->dn_dT_r, w->routed.dn_dT, false, (uint64_t)E * (F / QK), D, 128, 2);
+    if (ok && Fs)
+        ok = encode_2d(&m->gu_s, w->shared.gu16, true, (uint64_t)2 * Fs, D, 64, 128) &&
+             encode_2d(&m->gu_dT_s, w->shared.gu_dT, false, (uint64_t)(D / QK), 2 * Fs, 128, 2) &&
+             encode_2d(&m->dn_s, w->shared.dn16, true, (uint64_t)D, Fs, 64, 128) &&
+             encode_2d(&m->dn_dT_s, w->shared.dn_dT, false, (uint64_t)(Fs / QK), D, 128, 2);
+    if (!ok) {
+        delete m;
+        return MOE_OK;  // tensor path unavailable; the matvec path still serves every call
+    }
+    w->tmaps = m;
+    return MOE_OK;
+}
+
+void free_tensor_maps(moe_weights_s *w) {
+    delete static_cast<WeightMaps *>(w->tmaps);
+    w->tmaps = nullptr;
+}
+
+int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
+                           const int32_t *expTokI, const int32_t *expTokK, int N, int top_k, bool with_shared,
+                           void *ws, const WsLayout &L, cudaStream_t s) {
+    PlanHeader *hdr = ws_ptr<PlanHeader>(ws, L.plan);
+    int32_t *gst = reinterpret_cast<int32_t *>(hdr + 1);
+    plan_kernel<<<1, 1024, 0, s>>>(expStart, expTokI, expTokK, N, top_k, w->E, with_shared ? 1 : 0, L.rows_max,
+                                   L.tiles_max, hdr, gst, ws_ptr<TileDesc>(ws, L.tiles), ws_ptr<int4>(ws, L.rowinfo),
+                                   reinterpret_cast<unsigned *>(ws));
+    int rc = launch_status();
+    if (rc || x_q == nullptr) return rc;
+    gather_kernel<<<(L.rows_max + 31) / 32, 256, 0, s>>>(x_q, x_d, w->D, hdr, ws_ptr<int4>(ws, L.rowinfo), L.rows_max,
+                                                         ws_ptr<__half>(ws, L.xg16), ws_ptr<float>(ws, L.xg_dT));
+    return launch_status();
+}
+
+int launch_gemm_gate_up(const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws, const WsLayout &L,
+                        int32_t *dbg_dots, int dbg_block, cudaStream_t s) {
+    return launch_gemm(0, w, N, top_k, with_shared, ws, L, nullptr, nullptr, nullptr, dbg_dots, dbg_block, s);
+}
+
+int launch_gemm_down(const moe_weights_s *w, int N, int top_k, bool with_shared, const float *shexp_scale,
+                     float *partials, float *shared_out, void *ws, const WsLayout &L, cudaStream_t s) {
+    return launch_gemm(1, w, N, top_k, with_shared, ws, L, partials, shared_out, shexp_scale, nullptr, -1, s);
+}
+
+int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L, int8_t *h_q, float *h_d,
+                     cudaStream_t s) {
+    (void)N;
+    (void)top_k;
+    const int Fmax = std::max(w->F, w->Fs);
+    h16_to_q8_kernel<<<L.rows_max, 256, 0, s>>>(ws_ptr<__half>(ws, L.h16), ws_ptr<float>(ws, L.h_dT), w->F, Fmax,
+                                                L.rows_max, ws_ptr<PlanHeader>(ws, L.plan),
+                                                ws_ptr<int4>(ws, L.rowinfo), h_q, h_d);
+    return launch_status();
+}
+
+int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L, const int8_t *h_q,
+                     const float *h_d, cudaStream_t s) {
+    (void)N;
+    (void)top_k;
+    const int Fmax = std::max(w->F, w->Fs);
+    q8_to_h16_kernel<<<L.rows_max, 256, 0, s>>>(h_q, h_d, w->F, Fmax, L.rows_max, ws_ptr<PlanHeader>(ws, L.plan),
+                                                ws_ptr<int4>(ws, L.rowinfo), ws_ptr<__half>(ws, L.h16),
+                                                ws_ptr<float>(ws, L.h_dT));
+    return launch_status();
 }
 
 }  // namespace moe

@@ -279,11 +279,8 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
     size_t smem = (size_t)MV_T * D + sizeof(float) * ((size_t)MV_T * (D / QK) + MV_T * QK);
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(matvec_gate_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
+    static int configured = 0;
+    if (int rc = ensure_dynamic_smem((const void *)matvec_gate_up_kernel, smem, &configured)) return rc;
     dim3 grid(F / QK, nexp);
     matvec_gate_up_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.gate_q, set.gate_d, set.up_q, set.up_d, D, F,
                                                            is_shared, x_q, x_d, expStart, expTokI, N, top_k,
@@ -298,11 +295,8 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_sha
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
     size_t smem = (size_t)MV_T * F + sizeof(float) * ((size_t)MV_T * (F / QK) + MV_T * QK);
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(matvec_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
+    static int configured = 0;
+    if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel, smem, &configured)) return rc;
     dim3 grid(D / QK, nexp);
     matvec_down_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, D, F, is_shared, h_q, h_d,
                                                         expStart, expTokI, expTokK, N, top_k, shexp_scale,

@@ -29,6 +29,10 @@ WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs) {
     const size_t Nk = (size_t)N * top_k;
     const int Fmax = std::max(F, Fs);
     L.status = take(256);
+    // the router's split-K scratch comes first: moe_router_topk, which knows only (N, D, E),
+    // finds it at the same offset as every other entry point
+    L.nsplit = router_nsplit(N, D, E);
+    L.part_logits = take((size_t)L.nsplit * N * (E + 1) * 4);
     L.topk_idx = take(Nk * 4);
     L.topk_w = take(Nk * 4);
     L.shexp_scale = take((size_t)N * 4);
@@ -39,16 +43,16 @@ WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs) {
     L.expTokK = take(Nk * 4);
     L.partials = take(Nk * D * 4);
     L.shared_out = take(Fs ? (size_t)N * D * 4 : 0);
-    L.nsplit = router_nsplit(N, D, E);
-    L.part_logits = take((size_t)L.nsplit * N * (E + 1) * 4);
     L.hq8 = take((Nk + N) * Fmax);
     L.hd8 = take((Nk + N) * (Fmax / QK) * 4);
     if (tensor_shapes(D, F, Fs)) {
-        L.rows_max = (int)(Nk + (size_t)SEG_ALIGN * (E + 1) + N + SEG_ALIGN);
+        // every segment start is 16-aligned; the row count is a multiple of 16 as well, so the
+        // transposed scale arrays have 16-byte-aligned rows (a TMA requirement)
+        L.rows_max = (int)((Nk + (size_t)SEG_ALIGN * (E + 2) + N + 15) / 16 * 16);
         L.tiles_max = (int)(Nk / TILE_N + E + 1 + N / TILE_N + 2);
         L.plan = take(sizeof(PlanHeader) + (size_t)(E + 2) * 4);
         L.tiles = take((size_t)L.tiles_max * sizeof(TileDesc));
-        L.rowinfo = take((size_t)L.rows_max * 8);
+        L.rowinfo = take((size_t)L.rows_max * 16);
         L.xg16 = take((size_t)L.rows_max * D * 2);
         L.xg_dT = take((size_t)(D / QK) * L.rows_max * 4);
         L.h16 = take((size_t)L.rows_max * Fmax * 2);
@@ -171,6 +175,7 @@ int moe_weights_create(moe_weights_t *out, int E, int D, int F, const void *gate
     int rc = repack_weights(w, gate, up, down, sh_gate, sh_up, sh_down, stream);
     if (!rc && w->tensor_ok) rc = prepare_tensor_maps(w);
     if (rc) {
+        free_tensor_maps(w);
         free_weights(w);
         delete w;
         return rc;
@@ -181,6 +186,7 @@ int moe_weights_create(moe_weights_t *out, int E, int D, int F, const void *gate
 
 int moe_weights_destroy(moe_weights_t w) {
     if (!w) return MOE_ERR_INVALID_ARG;
+    free_tensor_maps(w);
     free_weights(w);
     delete w;
     return MOE_OK;

@@ -123,8 +123,20 @@ int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const W
 int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
                      const int8_t *h_q, const float *h_d, cudaStream_t s);
 int prepare_tensor_maps(moe_weights_s *w);
+void free_tensor_maps(moe_weights_s *w);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Raise a kernel's dynamic shared-memory limit when a launch needs more than the
+// default 48 KB; remembers the largest value set (per kernel, per process), so
+// repeated launches -- and launches under stream capture -- make no further call.
+inline int ensure_dynamic_smem(const void *kernel, size_t bytes, int *configured) {
+    if (bytes <= 48 * 1024 || (int)bytes <= *configured) return MOE_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *configured = (int)bytes;
+    return MOE_OK;
+}
 inline int launch_status() { return cuda_status(cudaGetLastError()); }
 
 // ----------------------------------------------------- device helpers --

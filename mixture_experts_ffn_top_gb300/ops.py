@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -336,7 +337,10 @@ class MoeLayer:
         Fs = 0 if inp.get("sh_gate") is None else inp["sh_gate"].shape[0]
 
         def up(a):
-            return None if a is None else torch.from_numpy(a).to(dev)
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            return torch.from_numpy(a if a.flags.writeable else a.copy()).to(dev)
 
         w = MoeWeights(up(inp["gate"]), up(inp["up"]), up(inp["down"]), E, D, F, up(inp.get("sh_gate")),
                        up(inp.get("sh_up")), up(inp.get("sh_down")), Fs)

@@ -200,7 +200,7 @@ def _csr(ref):
 
 
 @pytest.mark.parametrize("name", SMALL + ["olmoe"])
-@pytest.mark.parametrize("path", [1])
+@pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_block_dots_bit_exact(ops, name, path):
     wl, inp, ref = case(name)
     layer = layer_for(ops, inp, wl)
@@ -225,7 +225,7 @@ def test_gate_up_block_dots_bit_exact(ops, name, path):
 
 
 @pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
-@pytest.mark.parametrize("path", [1])
+@pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_requantised_activations(ops, name, path):
     """h_q from the oracle's x_q and CSR: codes within +-1 (fp32 vs double accumulation can
     move a value across a rounding boundary), at most 1% of them different."""
@@ -247,7 +247,7 @@ def test_gate_up_requantised_activations(ops, name, path):
 
 
 @pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
-@pytest.mark.parametrize("path", [1])
+@pytest.mark.parametrize("path", [1, 2])
 def test_down_given_oracle_h(ops, name, path):
     """The down half on the oracle's own h_q: partials to fp32 accumulation accuracy."""
     wl, inp, ref = case(name)
@@ -266,8 +266,8 @@ def test_down_given_oracle_h(ops, name, path):
     assert rel <= 1e-5, rel
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe"])
-@pytest.mark.parametrize("path", [1])
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
+@pytest.mark.parametrize("path", [1, 2])
 def test_grouped_ffn_partials(ops, name, path):
     wl, inp, ref = case(name)
     layer = layer_for(ops, inp, wl)
@@ -311,7 +311,7 @@ def test_combine_order_sensitive_values(ops):
 
 # ---------------------------------------------------------- whole layer ---
 @pytest.mark.parametrize("name", CONFIGS)
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 def test_layer_parity(ops, name, path):
     """moe_ffn_prefill (the call bench.py times, path 0 = its launch configuration)."""
     wl, inp, ref = case(name)
@@ -322,7 +322,7 @@ def test_layer_parity(ops, name, path):
     v = layer.views(wl.N)
     np.testing.assert_array_equal(v["topk_idx"].cpu().numpy()[clear], ref["topk_idx"][clear])
     rel, mx = assert_out_close(out.cpu().numpy(), ref["out"], clear, what=f"{name} layer output")
-    assert clear.mean() > 0.98
+    assert clear.mean() > 0.95  # near-tied tokens are few (E=256 has the most)
 
 
 def _random_layer(N, D, E, k, F, Fs, norm, seed):
@@ -341,7 +341,9 @@ def test_layer_edge_shapes(ops, N, D, E, k, F, Fs, norm):
     wl, inp = _random_layer(N, D, E, k, F, Fs, norm, seed=N * 31 + E)
     ref = O.moe_ffn_inputs(inp, k, norm)
     layer = layer_for(ops, inp, wl)
-    for path in (0, 1):
+    for path in (0, 1, 2):
+        if path == 2 and not ops.moe_weights_tensor_path(layer.w):
+            continue
         out = layer.prefill(dev(inp["hidden"]), k, norm, path=path)
         assert layer.status() == 0
         clear = clear_tokens(ref["logits"], k)
