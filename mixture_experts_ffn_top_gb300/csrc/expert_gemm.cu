@@ -15,21 +15,26 @@
 // drain warps read it (tcgen05.ld), scale it by d_w (per TMEM lane = weight
 // row) * d_x (per column = token) and accumulate in registers.
 //
-// Roles (320 threads, one CTA per SM, persistent over work items):
-//   warp 0     TMA producer: per stage (64 K = 2 blocks) the weight tile
-//              [128 rows x 64] fp16, the token tile [nb rows x 64] fp16 (nb
-//              = 16/32/64/128, the smallest box that holds the tile's rows)
-//              and both tiles' block scales.
-//   warp 1     TMEM owner and MMA issuer: 2 x (M128 x N x K16) per block into
-//              one of 4 TMEM accumulators of 128 columns.
-//   warps 2-9  drain: warp w reads TMEM lanes 32*(w%4).. (the hardware's lane
-//              quarter rule); warps 2-5 take the even 16-column chunks, 6-9 the
-//              odd ones.  Epilogue: gate/up tiles hold 64 gate rows and the 64
-//              up rows of the same features (weights repacked that way), so
-//              h = SiLU(g) * u is formed through a shared-memory exchange and
-//              requantised to Q8_1 per 32 features (one warp = one block);
-//              down tiles scatter fp32 rows to partials[t*top_k + slot] (or
-//              s_t * y to the shared expert's output).
+// Roles (576 threads, one CTA per SM, persistent over work items):
+//   warp 0      TMA producer: per stage (64 K = 2 blocks) the weight tile
+//               [128 rows x 64] fp16 and the token tile [nb rows x 64] fp16
+//               (nb = 16/32/64/128, the smallest box that holds the tile's
+//               rows) into the tile ring, both tiles' block scales into the
+//               scale ring.
+//   warp 1      TMEM owner and MMA issuer: 2 x (M128 x N x K16) per block into
+//               one of 4 TMEM accumulators of 128 columns; a tile-ring slot is
+//               released by the commit of the MMAs that read it.
+//   warps 2-17  drain, 4 per SM sub-partition: warp w reads TMEM lanes
+//               32*(w%4).. (the hardware's lane-quarter rule); the four warps
+//               of column group g take columns 32i + 8g + [0, 8), so ragged
+//               tiles stay balanced.  The scaling runs on packed f32x2 math.
+//               Epilogue: gate/up tiles hold 64 gate rows and the 64 up rows of
+//               the same features (weights repacked that way); gate and up
+//               warps swap half of their columns through shared memory, each
+//               forms h = SiLU(g) * u for its half and requantises it to Q8_1
+//               per 32 features (one warp = one block); down tiles scatter fp32
+//               rows to partials[t*top_k + slot] (or s_t * y to the shared
+//               expert's output).
 // Every wait on an mbarrier is bounded (a few seconds); on expiry the CTA sets
 // MOE_DEV_TIMEOUT in the status word, every role drains out, in-flight copies
 // and MMAs are waited for (bounded) and TMEM is freed before returning.
@@ -44,19 +49,20 @@ namespace moe {
 
 namespace {
 
-constexpr int G_THREADS = 320;
-constexpr int G_STAGES = 5;
-constexpr int G_TMEM_BUFS = 4;
+constexpr int G_DRAIN_WARPS = 16;                 // 4 per SM sub-partition
+constexpr int G_THREADS = 64 + 32 * G_DRAIN_WARPS; // producer warp + MMA warp + drain warps
+constexpr int G_STAGES = 5;                        // weight + token tile ring (TMA -> MMA)
+constexpr int G_SSTAGES = 8;                       // block-scale ring (TMA -> drain)
+constexpr int G_TMEM_BUFS = 4;                     // per-block accumulators in TMEM
 constexpr int G_TMEM_COLS = 512;
-constexpr int STAGE_A = 16384;                 // 128 rows x 128 B
-constexpr int STAGE_B = 16384;                 // up to 128 rows x 128 B
-constexpr int STAGE_SA = 1024;                 // 2 blocks x 128 fp32
-constexpr int STAGE_SB = 1024;                 // 2 blocks x up to 128 fp32
-constexpr int STAGE_BYTES = STAGE_A + STAGE_B + STAGE_SA + STAGE_SB;  // 34816 = 34 KB
-constexpr int XCH_STRIDE = 65;                 // padded row of the gate/up exchange
-constexpr int XCH_BYTES = 2 * 64 * XCH_STRIDE * 4;
-constexpr int BAR_BYTES = 256;
-constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + XCH_BYTES + BAR_BYTES;
+constexpr int STAGE_A = 16384;                     // 128 weight rows x 128 B (64 fp16 = 2 blocks)
+constexpr int STAGE_B = 16384;                     // up to 128 token rows x 128 B
+constexpr int STAGE_BYTES = STAGE_A + STAGE_B;
+constexpr int SSTAGE_BYTES = 2048;                 // [2][128] weight scales + [2][nb] token scales
+constexpr int XCH_STRIDE = 33;                     // padded row of the gate/up exchange (32 columns)
+constexpr int XCH_BYTES = 4 * 64 * XCH_STRIDE * 4; // 4 column groups x 64 features
+constexpr int BAR_BYTES = 512;
+constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + XCH_BYTES + BAR_BYTES;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s
 
 struct GemmMaps {
@@ -213,6 +219,38 @@ __device__ __forceinline__ Item item_at(const GemmParams &p, int it, int n_rtile
 }
 
 // --------------------------------------------------------------- kernel ---
+// Ties the registers a tcgen05.ld wrote to the tcgen05.wait::ld before it, so no use of
+// them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_reg_fence(uint32_t (&v)[8]) {
+    asm volatile("" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]));
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_reg_fence32(uint32_t (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8)
+        asm volatile("" : "+r"(v[i]), "+r"(v[i + 1]), "+r"(v[i + 2]), "+r"(v[i + 3]), "+r"(v[i + 4]), "+r"(v[i + 5]),
+                     "+r"(v[i + 6]), "+r"(v[i + 7]));
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+// SiLU(g) * u with the fast exponential and division (the result is requantised to 8 bits)
+__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 // MODE 0: gate/up (fused SiLU * up, Q8_1 requant); 1: down (scatter).
 // DUMP (gate/up only): also store the raw int32 block dots of block p.dbg_block
 // (the debug entry point; a separate instantiation keeps the hot loop lean).
@@ -221,32 +259,41 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    float *xch = reinterpret_cast<float *>(smem + G_STAGES * STAGE_BYTES);
-    uint8_t *bars = smem + G_STAGES * STAGE_BYTES + XCH_BYTES;
+    uint8_t *sring = smem + G_STAGES * STAGE_BYTES;
+    float *xch = reinterpret_cast<float *>(sring + G_SSTAGES * SSTAGE_BYTES);
+    uint8_t *bars = reinterpret_cast<uint8_t *>(xch) + XCH_BYTES;
     const uint32_t bar_base = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar_base + 8 * s; };
-    auto empty_bar = [&](int s) { return bar_base + 8 * (G_STAGES + s); };
-    auto tfull_bar = [&](int b) { return bar_base + 8 * (2 * G_STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar_base + 8 * (2 * G_STAGES + G_TMEM_BUFS + b); };
-    auto xfull_bar = [&](int h) { return bar_base + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + h); };
-    auto xempty_bar = [&](int h) { return bar_base + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + 2 + h); };
-    const uint32_t done_bar = bar_base + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * (2 * G_STAGES + 2 * G_TMEM_BUFS + 5));
+    int nb_ = 0;
+    auto next_bar = [&](int n) {
+        const uint32_t b = bar_base + 8 * nb_;
+        nb_ += n;
+        return b;
+    };
+    const uint32_t full0 = next_bar(G_STAGES), empty0 = next_bar(G_STAGES);
+    const uint32_t sfull0 = next_bar(G_SSTAGES), sempty0 = next_bar(G_SSTAGES);
+    const uint32_t tfull0 = next_bar(G_TMEM_BUFS), tempty0 = next_bar(G_TMEM_BUFS);
+    const uint32_t xready0 = next_bar(4), xfree0 = next_bar(4);
+    const uint32_t done_bar = next_bar(1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * nb_);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 8);
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);  // released by the MMA commit
+        }
+        for (int s = 0; s < G_SSTAGES; ++s) {
+            mbar_init(sfull0 + 8 * s, 1);
+            mbar_init(sempty0 + 8 * s, G_DRAIN_WARPS);
         }
         for (int b = 0; b < G_TMEM_BUFS; ++b) {
-            mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 8);
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, G_DRAIN_WARPS);
         }
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(xfull_bar(h), 2);   // the two up-row warps of a half
-            mbar_init(xempty_bar(h), 2);  // the two gate-row warps of a half
+        for (int g = 0; g < 4; ++g) {
+            mbar_init(xready0 + 8 * g, 4);
+            mbar_init(xfree0 + 8 * g, 4);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -283,11 +330,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ---
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_parity[G_STAGES];
-            bool issued[G_STAGES];
-            for (int s = 0; s < G_STAGES; ++s) issued[s] = false, issued_parity[s] = 0;
+            int stage = 0, sstage = 0;
+            uint32_t phase = 0, sphase = 0;
+            // per slot: was it ever filled, and the parity of its last fill (bit masks)
+            uint32_t issued = 0, last_parity = 0, sissued = 0, last_sparity = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
                 const Item x = item_at(p, it, n_rtiles);
@@ -295,29 +341,41 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 const CUtensorMap *msa = x.shared ? &maps.sa_s : &maps.sa_r;
                 const int arow = (x.shared ? 0 : x.expert * p.rows_r) + x.mt * 128;
                 const int sarow = x.shared ? 0 : x.expert * p.sblk_r;
-                const uint32_t bytes = STAGE_A + x.nb * 128 + STAGE_SA + 2 * x.nb * 4;
                 for (int ks = 0; ks < x.K / 64; ++ks) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, p.status)) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status) ||
+                        !mbar_wait(sempty0 + 8 * sstage, sphase ^ 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + stage * STAGE_BYTES;
-                    mbar_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(smem_u32(st), ma, ks * 64, arow, full_bar(stage));
-                    tma_load_2d(smem_u32(st + STAGE_A), &maps.b[x.bi], ks * 64, x.row0, full_bar(stage));
-                    tma_load_2d(smem_u32(st + STAGE_A + STAGE_B), msa, x.mt * 128, sarow + 2 * ks, full_bar(stage));
-                    tma_load_2d(smem_u32(st + STAGE_A + STAGE_B + STAGE_SA), &maps.sb[x.bi], x.row0, 2 * ks,
-                                full_bar(stage));
-                    issued[stage] = true;
-                    issued_parity[stage] = phase;
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, STAGE_A + x.nb * 128);
+                    tma_load_2d(smem_u32(st), ma, ks * 64, arow, fb);
+                    tma_load_2d(smem_u32(st + STAGE_A), &maps.b[x.bi], ks * 64, x.row0, fb);
+                    uint8_t *ss = sring + sstage * SSTAGE_BYTES;
+                    const uint32_t sb = sfull0 + 8 * sstage;
+                    mbar_expect_tx(sb, 1024 + 2 * x.nb * 4);
+                    tma_load_2d(smem_u32(ss), msa, x.mt * 128, sarow + 2 * ks, sb);
+                    tma_load_2d(smem_u32(ss + 1024), &maps.sb[x.bi], x.row0, 2 * ks, sb);
+                    issued |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    sissued |= 1u << sstage;
+                    last_sparity = (last_sparity & ~(1u << sstage)) | (sphase << sstage);
                     if (++stage == G_STAGES) stage = 0, phase ^= 1;
+                    if (++sstage == G_SSTAGES) sstage = 0, sphase ^= 1;
                 }
             }
             // copies still in flight must land before the CTA can exit
             for (int s = 0; s < G_STAGES; ++s)
-                if (issued[s]) {
+                if (issued >> s & 1) {
                     uint64_t t0 = globaltimer();
-                    while (!mbar_try(full_bar(s), issued_parity[s]) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                    while (!mbar_try(full0 + 8 * s, last_parity >> s & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                    }
+                }
+            for (int s = 0; s < G_SSTAGES; ++s)
+                if (sissued >> s & 1) {
+                    uint64_t t0 = globaltimer();
+                    while (!mbar_try(sfull0 + 8 * s, last_sparity >> s & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
                     }
                 }
         }
@@ -330,10 +388,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             bool any = false;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
                 const Item x = item_at(p, it, n_rtiles);
-                const int n_mma = (x.nrows + 15) & ~15;
-                const uint32_t idesc = idesc_f16(n_mma);
+                const uint32_t idesc = idesc_f16((x.nrows + 15) & ~15);
                 for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -341,7 +398,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t b0 = a0 + STAGE_A;
                     for (int half = 0; half < 2; ++half) {
-                        if (!mbar_wait(tempty_bar(buf), tphase ^ 1, abort_flag, p.status)) {
+                        if (!mbar_wait(tempty0 + 8 * buf, tphase ^ 1, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
@@ -352,10 +409,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                             const uint32_t off = half * 64 + kk * 32;  // bytes along K inside the swizzle atom
                             mma_f16(d, smem_desc_sw128(a0 + off), smem_desc_sw128(b0 + off), idesc, kk);
                         }
-                        mma_commit(tfull_bar(buf));
+                        mma_commit(tfull0 + 8 * buf);
                         any = true;
                         if (++buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
                     }
+                    if (!ok) break;
+                    mma_commit(empty0 + 8 * stage);  // the tile slot is free once these MMAs are done
                     if (++stage == G_STAGES) stage = 0, phase ^= 1;
                 }
             }
@@ -369,135 +428,133 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
         }
     } else {
         // ------------------------------------------------------- drain ---
-        const int q = warp & 3;          // TMEM lane quarter of this warp
-        const int h = (warp - 2) >> 2;   // 0: even 16-column chunks, 1: odd
-        const int r = q * 32 + lane;     // row of the 128-row weight tile
-        int stage = 0, buf = 0;
-        uint32_t phase = 0, tphase = 0, xphase = 0;
+        const int q = warp & 3;              // TMEM lane quarter (= SM sub-partition) of this warp
+        const int grp = (warp - 2) >> 2;     // column group: columns 32i + 8*grp + [0, 8)
+        const int r = q * 32 + lane;         // row of the 128-row weight tile
+        int sstage = 0, buf = 0;
+        uint32_t sphase = 0, tphase = 0, xphase = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item x = item_at(p, it, n_rtiles);
-            const int nchunks = (x.nrows + 15) >> 4;
-            float acc[4][16];
+            // this warp's columns: 32*grp + [0, 32) of the token tile; acc[m] = columns 2m, 2m+1
+            const int c0 = 32 * grp;
+            const bool active = c0 < x.nrows;  // warp-uniform: whole groups beyond the tile idle
+            float2 acc[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+            for (int m = 0; m < 16; ++m) acc[m] = make_float2(0.0f, 0.0f);
             for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
-                ok = mbar_wait(full_bar(stage), phase, abort_flag, p.status);
+                ok = mbar_wait(sfull0 + 8 * sstage, sphase, abort_flag, p.status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const float *SA = reinterpret_cast<const float *>(smem + stage * STAGE_BYTES + STAGE_A + STAGE_B);
+                const float *SA = reinterpret_cast<const float *>(sring + sstage * SSTAGE_BYTES);
                 const float *SB = SA + 256;
                 for (int half = 0; half < 2; ++half) {
-                    ok = mbar_wait(tfull_bar(buf), tphase, abort_flag, p.status);
+                    ok = mbar_wait(tfull0 + 8 * buf, tphase, abort_flag, p.status);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
-                    const float dw = SA[half * 128 + r];
-                    const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 128;
-                    const float *sbh = SB + half * x.nb;
-                    const bool dump = DUMP && MODE == 0 && p.dbg_dots != nullptr && x.shared == 0 && ks * 2 + half == p.dbg_block;
-#pragma unroll
-                    for (int pr = 0; pr < 2; ++pr) {
-                        // two 16-column chunks per TMEM round trip keeps the live registers in budget
-                        uint32_t v[2][16];
-#pragma unroll
-                        for (int ii = 0; ii < 2; ++ii) {
-                            const int c = h + 2 * (2 * pr + ii);
-                            if (c < nchunks) tmem_ld16(tb + c * 16, v[ii]);
-                        }
+                    uint32_t v[32];
+                    if (active) {
+                        tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * 128 + c0, v);
                         tmem_wait_ld();
-#pragma unroll
-                        for (int ii = 0; ii < 2; ++ii) {
-                            const int i = 2 * pr + ii;
-                            const int c = h + 2 * i;
-                            if (c >= nchunks) continue;
-                            if (dump) {
-                                const int mat = r < 64 ? 0 : 1;
-                                const int f = x.mt * 64 + (r & 63);
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) {
-                                    const int col = c * 16 + j;
-                                    if (col < x.nrows)
-                                        p.dbg_dots[((size_t)(x.entry0 + col) * 2 + mat) * p.F + f] =
-                                            (int32_t)__uint_as_float(v[ii][j]);
-                                }
-                            }
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                acc[i][j] = fmaf(__uint_as_float(v[ii][j]), sbh[c * 16 + j] * dw, acc[i][j]);
-                        }
+                        tmem_reg_fence32(v);
                     }
+                    // the block is in registers: hand the TMEM buffer back before the math
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(buf));
+                    if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
                     if (++buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
+                    if (active) {
+                        if (DUMP && x.shared == 0 && ks * 2 + half == p.dbg_block) {
+                            const int mat = r < 64 ? 0 : 1;
+                            const int f = x.mt * 64 + (r & 63);
+                            for (int j = 0; j < 32 && c0 + j < x.nrows; ++j)
+                                p.dbg_dots[((size_t)(x.entry0 + c0 + j) * 2 + mat) * p.F + f] =
+                                    (int32_t)__uint_as_float(v[j]);
+                        }
+                        const float dw = SA[half * 128 + r];
+                        const float2 dw2 = make_float2(dw, dw);
+                        const float4 *sb4 = reinterpret_cast<const float4 *>(SB + half * x.nb + c0);
+#pragma unroll
+                        for (int g4 = 0; g4 < 8; ++g4) {
+                            const float4 s4 = sb4[g4];  // token scales of columns 4*g4 .. 4*g4+3 (broadcast)
+                            const float2 sa = __fmul2_rn(make_float2(s4.x, s4.y), dw2);
+                            const float2 sb = __fmul2_rn(make_float2(s4.z, s4.w), dw2);
+                            acc[2 * g4] = __ffma2_rn(
+                                make_float2(__uint_as_float(v[4 * g4]), __uint_as_float(v[4 * g4 + 1])), sa, acc[2 * g4]);
+                            acc[2 * g4 + 1] = __ffma2_rn(
+                                make_float2(__uint_as_float(v[4 * g4 + 2]), __uint_as_float(v[4 * g4 + 3])), sb,
+                                acc[2 * g4 + 1]);
+                        }
+                    }
                 }
                 if (!ok) break;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(stage));  // scales of both blocks read
-                if (++stage == G_STAGES) stage = 0, phase ^= 1;
+                if (lane == 0) mbar_arrive(sempty0 + 8 * sstage);  // scales of both blocks read
+                if (++sstage == G_SSTAGES) sstage = 0, sphase ^= 1;
             }
             if (!ok) break;
             // --------------------------------------------------- epilogue ---
             if (MODE == 0) {
-                float *xh = xch + h * 64 * XCH_STRIDE;
-                if (q >= 2) {
-                    // up rows: hand u to the gate rows of the same features
-                    ok = mbar_wait(xempty_bar(h), xphase ^ 1, abort_flag, p.status);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
+                // rows 0-63 hold gate, rows 64-127 up, of features mt*64 + (r & 63).  Gate warps
+                // finish the even columns of the group, up warps the odd ones: each side hands
+                // the other its accumulators for the other parity.
+                float *xg = xch + grp * 64 * XCH_STRIDE;
+                const int fr = r & 63;  // feature row within the tile
+                const bool is_gate = q < 2;
+                ok = mbar_wait(xfree0 + 8 * grp, xphase ^ 1, abort_flag, p.status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) xh[(r - 64) * XCH_STRIDE + i * 16 + j] = acc[i][j];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xfull_bar(h));
-                } else {
-                    ok = mbar_wait(xfull_bar(h), xphase, abort_flag, p.status);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    const int f = x.mt * 64 + r;  // feature (this warp: one 32-feature block)
+                for (int m = 0; m < 16; ++m) {
+                    if (is_gate) xg[fr * XCH_STRIDE + 2 * m + 1] = acc[m].y;  // gate of an odd column
+                    else xg[fr * XCH_STRIDE + 2 * m] = acc[m].x;              // up of an even column
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xready0 + 8 * grp);
+                ok = mbar_wait(xready0 + 8 * grp, xphase, abort_flag, p.status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (active) {
+                    const int f = x.mt * 64 + fr;  // this warp's 32 features form one Q8_1 block
                     const int fblk = f >> 5;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int c = h + 2 * i;
-                        if (c >= nchunks) continue;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int col = c * 16 + j;
-                            if (col >= x.nrows) continue;  // warp-uniform
-                            const float g = acc[i][j];
-                            const float u = xh[r * XCH_STRIDE + i * 16 + j];
-                            const float hv = g / (1.0f + expf(-g)) * u;
-                            float d16f;
-                            const int qv = q8_quantize_lane(hv, &d16f);
-                            const int prow = x.row0 + col;
-                            p.h16[(size_t)prow * p.Fmax + f] = __int2half_rn(qv);
-                            if (lane == 0) p.h_dT[(size_t)fblk * p.rows_max + prow] = d16f;
-                        }
+                    for (int m = 0; m < 16; ++m) {
+                        const int cl = 2 * m + (is_gate ? 0 : 1);
+                        const int col = c0 + cl;
+                        if (col >= x.nrows) break;  // warp-uniform
+                        const float other = xg[fr * XCH_STRIDE + cl];
+                        const float hv = is_gate ? swiglu(acc[m].x, other) : swiglu(other, acc[m].y);
+                        float d16f;
+                        const int qv = q8_quantize_lane(hv, &d16f);
+                        const int prow = x.row0 + col;
+                        p.h16[(size_t)prow * p.Fmax + f] = __int2half_rn(qv);
+                        if (lane == 0) p.h_dT[(size_t)fblk * p.rows_max + prow] = d16f;
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xempty_bar(h));
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfree0 + 8 * grp);
                 xphase ^= 1;
-            } else {
+            } else if (active) {
                 const int dcol = x.mt * 128 + r;  // output column
+                // lane L fetches the output row (and shared scale) of column c0 + L: one coalesced
+                // load instead of 32 dependent ones, then broadcast per column
+                const int my_col = c0 + lane;
+                int my_orow = -1;
+                float my_scale = 1.0f;
+                if (my_col < x.nrows) {
+                    my_orow = p.rowinfo[x.row0 + my_col].y;
+                    if (x.shared && my_orow >= 0) my_scale = p.shexp_scale[my_orow];
+                }
+                float *__restrict__ dst = x.shared ? p.shared_out : p.partials;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = h + 2 * i;
-                    if (c >= nchunks) continue;
+                for (int m = 0; m < 16; ++m) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = c * 16 + j;
-                        if (col >= x.nrows) continue;
-                        const int orow = p.rowinfo[x.row0 + col].y;
-                        if (orow < 0) continue;
-                        if (x.shared)
-                            p.shared_out[(size_t)orow * p.D + dcol] = p.shexp_scale[orow] * acc[i][j];
-                        else
-                            p.partials[(size_t)orow * p.D + dcol] = acc[i][j];
+                    for (int e2 = 0; e2 < 2; ++e2) {
+                        const float val = e2 ? acc[m].y : acc[m].x;
+                        const int orow = __shfl_sync(0xffffffffu, my_orow, 2 * m + e2);
+                        const float sc = __shfl_sync(0xffffffffu, my_scale, 2 * m + e2);
+                        if (orow >= 0) dst[(size_t)orow * p.D + dcol] = x.shared ? sc * val : val;
                     }
                 }
             }
