@@ -153,6 +153,24 @@ int moe_router_topk(const float *hidden, const float *routerW, const float *shex
                     int8_t *x_q, float *x_d, float *logits_out,
                     void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_router_topk for callers that cannot allocate device memory (no
+ * counterpart on the pages: it exists only for hosts whose device memory is
+ * owned by another allocator, or that forbid cudaMalloc after start-up).  Same
+ * arguments and results as moe_router_topk, without the workspace: the router's
+ * split-K partial logits go to an 8 MiB array inside the library (2^21 floats,
+ * held on every GPU that loads the library until exit).  The problem must fit:
+ * nsplit * N * (E + 1) <= 2^21 floats, nsplit being the router's split-K factor
+ * (at most max(1, D/256)); otherwise MOE_ERR_WORKSPACE_TOO_SMALL and nothing
+ * runs.  The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress, which may load the library's kernels onto that device)
+ * and should therefore come before any stream capture.  All calls on a device
+ * share the array, so calls that may overlap on the GPU race and must be
+ * ordered by the caller.  Allocates nothing. */
+int moe_router_topk_noalloc(const float *hidden, const float *routerW, const float *shexp_gate,
+                            int N, int D, int E, int top_k, int norm_topk_prob,
+                            int32_t *topk_idx, float *topk_w, float *shexp_scale,
+                            int8_t *x_q, float *x_d, float *logits_out, cudaStream_t stream);
+
 /* Softmax + top-k alone, from given logits [N][E] (same outputs as above).
  * Lets a caller check routing against logits computed elsewhere. */
 int moe_topk_from_logits(const float *logits, int N, int E, int top_k, int norm_topk_prob,

@@ -37,6 +37,7 @@ _SIGS = {
     "moe_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_workspace_status": (_I, [_P, _I, _P]),
     "moe_router_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_router_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_topk_from_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_quantize_q8_1": (_I, [_P, _I64, _P, _P, _P]),
     "moe_bucket": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -189,6 +190,26 @@ def moe_router_topk(hidden, routerW, shexp_gate, top_k, norm_topk_prob, ws, want
                                _dev(r["x_d"]), _dev(r["logits"]), _dev(ws, torch.uint8, "ws"), ws.numel(),
                                _stream(stream))
     _check(rc, "moe_router_topk")
+    return r
+
+
+def moe_router_topk_noalloc(hidden, routerW, shexp_gate, top_k, norm_topk_prob, want_logits=False, stream=None):
+    """moe_router_topk without a workspace (the library's fixed scratch); outputs as moe_router_topk."""
+    N, D = hidden.shape
+    E = routerW.shape[0]
+    dev = hidden.device
+    r = dict(topk_idx=torch.empty((N, top_k), dtype=torch.int32, device=dev),
+             topk_w=torch.empty((N, top_k), dtype=torch.float32, device=dev),
+             shexp_scale=torch.empty(N, dtype=torch.float32, device=dev) if shexp_gate is not None else None,
+             x_q=torch.empty((N, D), dtype=torch.int8, device=dev),
+             x_d=torch.empty((N, D // QK), dtype=torch.float32, device=dev),
+             logits=torch.empty((N, E), dtype=torch.float32, device=dev) if want_logits else None)
+    rc = lib().moe_router_topk_noalloc(_dev(hidden, torch.float32, "hidden"), _dev(routerW, torch.float32, "routerW"),
+                                       _dev(shexp_gate, torch.float32, "shexp_gate"), N, D, E, top_k,
+                                       int(norm_topk_prob), _dev(r["topk_idx"]), _dev(r["topk_w"]),
+                                       _dev(r["shexp_scale"]), _dev(r["x_q"]), _dev(r["x_d"]), _dev(r["logits"]),
+                                       _stream(stream))
+    _check(rc, "moe_router_topk_noalloc")
     return r
 
 

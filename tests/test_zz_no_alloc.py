@@ -1,0 +1,61 @@
+"""moe_router_topk_noalloc: the router for callers that cannot allocate device memory.
+
+Hosts whose device memory belongs to another allocator (or that forbid cudaMalloc
+after start-up) cannot hand the library a workspace; this entry point keeps the
+router's scratch in a fixed array inside the library instead.  Its results must
+equal those of moe_router_topk (same kernels, same split-K order) on two calls
+in a row, and a problem too large for the fixed array must be refused before
+anything runs.  This file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+
+from mixture_experts_ffn_top_gb300.workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_ffn_top_gb300 import build, ops as _ops
+
+    build.build()
+    torch.cuda.set_device(0)
+    return _ops
+
+
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared"])
+def test_noalloc_router_matches_workspace_router(ops, name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    hidden = torch.from_numpy(inp["hidden"]).cuda()
+    routerW = torch.from_numpy(inp["routerW"]).cuda()
+    shg = None if inp["shexp_gate"] is None else torch.from_numpy(inp["shexp_gate"]).cuda()
+    ws = ops.new_workspace(wl.N, wl.D, wl.E, wl.F, wl.top_k, wl.Fs)
+    ref = ops.moe_router_topk(hidden, routerW, shg, wl.top_k, wl.norm_topk_prob, ws, want_logits=True)
+    torch.cuda.synchronize()
+    for _ in range(2):  # the shared scratch keeps the previous call's contents
+        got = ops.moe_router_topk_noalloc(hidden, routerW, shg, wl.top_k, wl.norm_topk_prob, want_logits=True)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(got["logits"].cpu().numpy(), ref["logits"].cpu().numpy(), rtol=1e-6, atol=1e-6)
+        np.testing.assert_array_equal(got["topk_idx"].cpu().numpy(), ref["topk_idx"].cpu().numpy())
+        np.testing.assert_allclose(got["topk_w"].cpu().numpy(), ref["topk_w"].cpu().numpy(), rtol=1e-6, atol=1e-7)
+        np.testing.assert_array_equal(got["x_q"].cpu().numpy(), ref["x_q"].cpu().numpy())
+        np.testing.assert_array_equal(got["x_d"].cpu().numpy(), ref["x_d"].cpu().numpy())
+        if shg is not None:
+            np.testing.assert_allclose(got["shexp_scale"].cpu().numpy(), ref["shexp_scale"].cpu().numpy(),
+                                       rtol=1e-6, atol=1e-7)
+
+
+def test_noalloc_router_refuses_oversized_problem(ops):
+    # N * (E + 1) alone exceeds the 2^21-float scratch: refused on the host, nothing launched
+    N, D, E = 20000, 64, 128
+    hidden = torch.zeros((N, D), dtype=torch.float32, device="cuda")
+    routerW = torch.zeros((E, D), dtype=torch.float32, device="cuda")
+    with pytest.raises(ops.MoeError) as exc:
+        ops.moe_router_topk_noalloc(hidden, routerW, None, 8, False)
+    assert exc.value.code == -3
