@@ -40,6 +40,29 @@ L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def rank_hidden(wl, hidden0: np.ndarray, rank: int, world: int) -> np.ndarray:
+    """The token batch a rank processes: the workload's own batch on a single GPU, an
+    independent seeded batch of the same shape per rank when several replicas run."""
+    return hidden0 if world == 1 else make_hidden(wl, seed_offset=rank)
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Largest value over the ranks of the default process group (x itself when alone)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank's batch, over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -174,8 +197,7 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     wl = WORKLOADS[args.workload]
     inp = make_inputs(wl)
-    if rank != 0 or world > 1:
-        inp["hidden"] = make_hidden(wl, seed_offset=rank)  # each rank its own token batch
+    inp["hidden"] = rank_hidden(wl, inp["hidden"], rank, world)  # each rank its own token batch
     layer = ops.MoeLayer.from_numpy(inp, device=device, top_k=wl.top_k, max_tokens=wl.N)
     w = layer.w
     stream = torch.cuda.current_stream()
@@ -272,12 +294,8 @@ def run_ours(args, rank, world, local_rank):
         for j, s in enumerate(stages):
             stage_ms[s].append(e[j].elapsed_time(e[j + 1]))
         step_ms.append(e[0].elapsed_time(e[4]))
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * N / (ms / 1e3)
+    ms = max_over_ranks(statistics.mean(step_ms), device)
+    value = job_throughput(world, N, ms)
 
     # e2e: the public one-call API with pinned host buffers, H2D + D2H inside the timed region
     h_host = torch.from_numpy(inp["hidden"]).pin_memory()
@@ -302,11 +320,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_mean = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_mean], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_mean = float(t.item())
+    e2e_mean = max_over_ranks(statistics.mean(e2e_ms), device)
     if layer.status():
         raise RuntimeError("device status set during the e2e steps")
 
@@ -345,7 +359,7 @@ def run_ours(args, rank, world, local_rank):
         "layer_roofline_frac": layer_roof_s / (ms / 1e3),
         "algorithmic": work,
         "roofline": roofline,
-        "e2e": {"value": world * N / (e2e_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
+        "e2e": {"value": job_throughput(world, N, e2e_mean), "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
                 "d2h_bytes_per_step": N * D * 4, "ms_per_step": e2e_mean},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

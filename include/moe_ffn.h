@@ -244,6 +244,16 @@ int moe_debug_gate_up_block_dots(moe_weights_t w, const int8_t *x_q, const float
                                  int block, int32_t *dots, int path, void *ws, size_t ws_bytes,
                                  cudaStream_t stream);
 
+/* Failure-detection check of the tensor path: runs the gate/up grouped GEMM with
+ * its TMA producer told to issue nothing, so the MMA's first wait can never be
+ * satisfied.  Every device wait is bounded; after limit_ms (1..2000) the kernel
+ * gives up, sets MOE_DEV_TIMEOUT in the workspace status word, lets in-flight
+ * work drain, frees its tensor memory and returns, leaving the context usable.
+ * Returns the launch status; read the outcome with moe_workspace_status. */
+int moe_debug_expert_wait_timeout(moe_weights_t w, const int8_t *x_q, const float *x_d,
+                                  const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
+                                  int limit_ms, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * moe_combine -- batched weighted scatter-reduce (#129 "Scope"), one launch
  * over N x D: for every token t and column c

@@ -63,7 +63,7 @@ constexpr int XCH_STRIDE = 33;                     // padded row of the gate/up 
 constexpr int XCH_BYTES = 4 * 64 * XCH_STRIDE * 4; // 4 column groups x 64 features
 constexpr int BAR_BYTES = 512;
 constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + XCH_BYTES + BAR_BYTES;
-constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s: any healthy wait is microseconds
 
 struct GemmMaps {
     CUtensorMap a_r, sa_r, a_s, sa_s;  // weights + weight scales, routed / shared
@@ -87,6 +87,8 @@ struct GemmParams {
     int32_t *dbg_dots;
     int dbg_block;
     unsigned *status;
+    unsigned long long wait_ns;  // limit of every mbarrier wait
+    int starve;                  // failure-detection check: the producer issues no copy
 };
 
 // ------------------------------------------------------------- PTX glue ---
@@ -122,14 +124,14 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // the CTA's abort flag and the device status bit) when the limit expires, or
 // as soon as another role of the CTA has aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned *status) {
+                                          unsigned *status, unsigned long long limit_ns) {
     if (mbar_try(bar, parity)) return true;
     uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, MOE_DEV_TIMEOUT);
                 return false;
@@ -335,15 +337,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             // per slot: was it ever filled, and the parity of its last fill (bit masks)
             uint32_t issued = 0, last_parity = 0, sissued = 0, last_sparity = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            for (int it = blockIdx.x; it < n_items && ok && !p.starve; it += gridDim.x) {
                 const Item x = item_at(p, it, n_rtiles);
                 const CUtensorMap *ma = x.shared ? &maps.a_s : &maps.a_r;
                 const CUtensorMap *msa = x.shared ? &maps.sa_s : &maps.sa_r;
                 const int arow = (x.shared ? 0 : x.expert * p.rows_r) + x.mt * 128;
                 const int sarow = x.shared ? 0 : x.expert * p.sblk_r;
                 for (int ks = 0; ks < x.K / 64; ++ks) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status) ||
-                        !mbar_wait(sempty0 + 8 * sstage, sphase ^ 1, abort_flag, p.status)) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.wait_ns) ||
+                        !mbar_wait(sempty0 + 8 * sstage, sphase ^ 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -390,7 +392,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 const Item x = item_at(p, it, n_rtiles);
                 const uint32_t idesc = idesc_f16((x.nrows + 15) & ~15);
                 for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -398,7 +400,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t b0 = a0 + STAGE_A;
                     for (int half = 0; half < 2; ++half) {
-                        if (!mbar_wait(tempty0 + 8 * buf, tphase ^ 1, abort_flag, p.status)) {
+                        if (!mbar_wait(tempty0 + 8 * buf, tphase ^ 1, abort_flag, p.status, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -443,13 +445,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) acc[m] = make_float2(0.0f, 0.0f);
             for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
-                ok = mbar_wait(sfull0 + 8 * sstage, sphase, abort_flag, p.status);
+                ok = mbar_wait(sfull0 + 8 * sstage, sphase, abort_flag, p.status, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const float *SA = reinterpret_cast<const float *>(sring + sstage * SSTAGE_BYTES);
                 const float *SB = SA + 256;
                 for (int half = 0; half < 2; ++half) {
-                    ok = mbar_wait(tfull0 + 8 * buf, tphase, abort_flag, p.status);
+                    ok = mbar_wait(tfull0 + 8 * buf, tphase, abort_flag, p.status, p.wait_ns);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -502,7 +504,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 float *xg = xch + grp * 64 * XCH_STRIDE;
                 const int fr = r & 63;  // feature row within the tile
                 const bool is_gate = q < 2;
-                ok = mbar_wait(xfree0 + 8 * grp, xphase ^ 1, abort_flag, p.status);
+                ok = mbar_wait(xfree0 + 8 * grp, xphase ^ 1, abort_flag, p.status, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
 #pragma unroll
@@ -512,7 +514,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xready0 + 8 * grp);
-                ok = mbar_wait(xready0 + 8 * grp, xphase, abort_flag, p.status);
+                ok = mbar_wait(xready0 + 8 * grp, xphase, abort_flag, p.status, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if (active) {
@@ -772,7 +774,7 @@ struct WeightMaps {
 
 int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws, const WsLayout &L,
                 float *partials, float *shared_out, const float *shexp_scale, int32_t *dbg_dots, int dbg_block,
-                cudaStream_t s) {
+                cudaStream_t s, unsigned long long wait_ns = WAIT_LIMIT_NS, int starve = 0) {
     const WeightMaps *wm = static_cast<const WeightMaps *>(w->tmaps);
     if (!wm) return MOE_ERR_UNSUPPORTED_SHAPE;
     const int D = w->D, F = w->F, Fs = w->Fs, Fmax = std::max(F, Fs);
@@ -835,6 +837,8 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     p.dbg_dots = dbg_dots;
     p.dbg_block = dbg_block;
     p.status = reinterpret_cast<unsigned *>(ws);
+    p.wait_ns = wait_ns;
+    p.starve = starve;
     (void)with_shared;
     static int num_sms = 0;
     if (num_sms == 0) {
@@ -907,6 +911,11 @@ int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const floa
 int launch_gemm_gate_up(const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws, const WsLayout &L,
                         int32_t *dbg_dots, int dbg_block, cudaStream_t s) {
     return launch_gemm(0, w, N, top_k, with_shared, ws, L, nullptr, nullptr, nullptr, dbg_dots, dbg_block, s);
+}
+
+int launch_gemm_gate_up_starved(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
+                                unsigned long long wait_ns, cudaStream_t s) {
+    return launch_gemm(0, w, N, top_k, false, ws, L, nullptr, nullptr, nullptr, nullptr, -1, s, wait_ns, 1);
 }
 
 int launch_gemm_down(const moe_weights_s *w, int N, int top_k, bool with_shared, const float *shexp_scale,

@@ -347,6 +347,20 @@ int moe_debug_gate_up_block_dots(moe_weights_t w, const int8_t *x_q, const float
                                  stream);
 }
 
+int moe_debug_expert_wait_timeout(moe_weights_t w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
+                                  const int32_t *expTokI, int N, int top_k, int limit_ms, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+    if (!w || !x_q || !x_d || !expStart || !expTokI || limit_ms < 1 || limit_ms > 2000) return MOE_ERR_INVALID_ARG;
+    if (!tensor_path_supported(w)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!shape_ok(N, w->D, w->E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const WsLayout L = ws_layout(N, w->D, w->E, w->F, top_k, w->Fs);
+    int rc = check_ws(ws, ws_bytes, L);
+    if (rc) return rc;
+    rc = launch_plan_and_gather(w, x_q, x_d, expStart, expTokI, nullptr, N, top_k, false, ws, L, stream);
+    if (!rc) rc = launch_gemm_gate_up_starved(w, N, top_k, ws, L, (unsigned long long)limit_ms * 1000000ull, stream);
+    return rc;
+}
+
 int moe_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k, int D, float *out,
                 cudaStream_t stream) {
     if (!partials || !topk_w || !out) return MOE_ERR_INVALID_ARG;

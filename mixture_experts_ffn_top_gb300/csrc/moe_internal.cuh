@@ -115,6 +115,8 @@ int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const floa
                            void *ws, const WsLayout &L, cudaStream_t s);
 int launch_gemm_gate_up(const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws,
                         const WsLayout &L, int32_t *dbg_dots, int dbg_block, cudaStream_t s);
+int launch_gemm_gate_up_starved(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
+                                unsigned long long wait_ns, cudaStream_t s);
 int launch_gemm_down(const moe_weights_s *w, int N, int top_k, bool with_shared,
                      const float *shexp_scale, float *partials, float *shared_out, void *ws,
                      const WsLayout &L, cudaStream_t s);

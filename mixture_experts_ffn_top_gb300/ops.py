@@ -46,6 +46,7 @@ _SIGS = {
     "moe_expert_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_debug_gate_up_block_dots": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
+    "moe_debug_expert_wait_timeout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_ffn_prefill_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
@@ -287,6 +288,14 @@ def moe_debug_gate_up_block_dots(w: MoeWeights, x_q, x_d, expStart, expTokI, top
                                             _dev(dots), path, _dev(ws, torch.uint8), ws.numel(), _stream(stream))
     _check(rc, "moe_debug_gate_up_block_dots")
     return dots
+
+
+def moe_debug_expert_wait_timeout(w: MoeWeights, x_q, x_d, expStart, expTokI, top_k, limit_ms, ws, stream=None):
+    N = x_q.shape[0]
+    rc = lib().moe_debug_expert_wait_timeout(w.handle, _dev(x_q, torch.int8), _dev(x_d, torch.float32),
+                                             _dev(expStart, torch.int32), _dev(expTokI, torch.int32), N, top_k,
+                                             int(limit_ms), _dev(ws, torch.uint8), ws.numel(), _stream(stream))
+    _check(rc, "moe_debug_expert_wait_timeout")
 
 
 def moe_combine(partials, topk_w, shared=None, out=None, stream=None):

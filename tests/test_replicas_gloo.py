@@ -1,0 +1,65 @@
+"""bench.py's multi-rank logic on CPU ranks (gloo, world size 2): every rank gets its own
+seeded token batch of the workload's shape, the step time reported is the slowest rank's,
+and the whole-job throughput counts every rank's tokens.  No GPU is touched."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        from mixture_experts_ffn_top_gb300.workloads import WORKLOADS
+
+        wl = WORKLOADS["tiny"]
+        base = np.zeros((wl.N, wl.D), np.float32)
+        h = bench.rank_hidden(wl, base, rank, world)
+        ms = bench.max_over_ranks(1.0 + rank, "cpu")  # rank r took 1 + r ms
+        np.save(os.path.join(out_dir, f"h{rank}.npy"), h)
+        np.save(os.path.join(out_dir, f"ms{rank}.npy"), np.array([ms, bench.job_throughput(world, wl.N, ms)]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_cpu_ranks(tmp_path):
+    world, port = 2, _free_port()
+    mp.start_processes(_rank_main, args=(world, port, str(tmp_path)), nprocs=world, start_method="spawn", join=True)
+    h0, h1 = np.load(tmp_path / "h0.npy"), np.load(tmp_path / "h1.npy")
+    assert h0.shape == h1.shape == (64, 256)
+    assert not np.array_equal(h0, h1)          # independent batches per rank
+    assert abs(h0.std() - 1.0) < 0.05 and abs(h1.std() - 1.0) < 0.05
+    for r in range(world):
+        ms, tput = np.load(tmp_path / f"ms{r}.npy")
+        assert ms == 2.0                        # the slowest rank's time on every rank
+        assert tput == world * 64 / 2e-3        # all ranks' tokens over that time
+
+
+def test_single_rank_keeps_workload_batch():
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from mixture_experts_ffn_top_gb300.workloads import WORKLOADS
+
+    wl = WORKLOADS["tiny"]
+    base = np.ones((wl.N, wl.D), np.float32)
+    assert bench.rank_hidden(wl, base, 0, 1) is base
+    assert bench.max_over_ranks(3.5, "cpu") == 3.5
+    assert bench.job_throughput(1, 2048, 1.0) == 2048e3
