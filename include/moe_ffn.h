@@ -157,10 +157,10 @@ int moe_router_topk(const float *hidden, const float *routerW, const float *shex
  * counterpart on the pages: it exists only for hosts whose device memory is
  * owned by another allocator, or that forbid cudaMalloc after start-up).  Same
  * arguments and results as moe_router_topk, without the workspace: the router's
- * split-K partial logits go to an 8 MiB array inside the library (2^21 floats,
+ * split-K partial logits go to a 16 MiB array inside the library (2^22 floats,
  * held on every GPU that loads the library until exit).  The problem must fit:
- * nsplit * N * (E + 1) <= 2^21 floats, nsplit being the router's split-K factor
- * (at most max(1, D/256)); otherwise MOE_ERR_WORKSPACE_TOO_SMALL and nothing
+ * nsplit * N * (E + 1) <= 2^22 floats, nsplit being the router's split-K factor
+ * (at most max(1, D/128)); otherwise MOE_ERR_WORKSPACE_TOO_SMALL and nothing
  * runs.  The first call on a device looks the array's device address up
  * (cudaGetSymbolAddress, which may load the library's kernels onto that device)
  * and should therefore come before any stream capture.  All calls on a device
@@ -282,6 +282,18 @@ int moe_ffn_prefill(moe_weights_t w, const float *hidden, const float *routerW,
 int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *routerW,
                        const float *shexp_gate, int N, int top_k, int norm_topk_prob, float *out,
                        int path, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* moe_ffn_prefill_ex that also records seven caller-created CUDA events on
+ * `stream` around its stages, for measuring each kernel in place:
+ *   [0] start, [1] after the router (+softmax/top-k/Q8_1), [2] after bucketing
+ *   (which on the tensor path also writes the GEMM plan), [3] after the gather
+ *   (tensor path; nothing on the matvec path), [4] after gate/up, [5] after
+ *   down (both incl. the shared expert), [6] after the combine.
+ * stage_events: host array of 7 cudaEvent_t (created by the caller). */
+int moe_ffn_prefill_timed(moe_weights_t w, const float *hidden, const float *routerW,
+                          const float *shexp_gate, int N, int top_k, int norm_topk_prob, float *out,
+                          int path, void *ws, size_t ws_bytes, cudaStream_t stream,
+                          cudaEvent_t *stage_events);
 
 /* Device pointers to the intermediates moe_ffn_prefill leaves in `ws`
  * (valid after it ran on that workspace with the same shape); any output

@@ -4,14 +4,18 @@
 // launch over N x D.  The per-element order and rounding are fixed (one fused
 // multiply-add per slot, then one add), so the result is bit-reproducible:
 //   acc = +0; for s: acc = fma(w[t,s], partial[t*k+s], acc); acc += shared.
-// HBM-bound: each thread owns 4 consecutive columns (16-byte loads/stores);
-// partial rows are streamed once (evict-first loads), the output is written once.
+// HBM-bound: each thread owns 4 consecutive columns (16-byte loads/stores); for the
+// usual top_k the slot loads are all issued before the fma chain; partial rows are
+// streamed once (evict-first loads), the output is written once.
 #include "moe_internal.cuh"
 
 namespace moe {
 
 namespace {
 
+// KMAX > 0: top_k known at compile time (all slot loads issued before the fma chain);
+// KMAX == 0: any top_k.
+template <int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
                const float4 *__restrict__ shared, int N, int k, int D4, float4 *__restrict__ out) {
@@ -21,13 +25,30 @@ combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
         const int64_t t = i / D4;
         const int64_t c = i - t * D4;
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int s = 0; s < k; ++s) {
-            const float ws = w[t * k + s];
-            const float4 p = __ldcs(partials + (t * k + s) * D4 + c);
-            acc.x = __fmaf_rn(ws, p.x, acc.x);
-            acc.y = __fmaf_rn(ws, p.y, acc.y);
-            acc.z = __fmaf_rn(ws, p.z, acc.z);
-            acc.w = __fmaf_rn(ws, p.w, acc.w);
+        if (KMAX > 0) {
+            float4 p[KMAX > 0 ? KMAX : 1];
+            float ws[KMAX > 0 ? KMAX : 1];
+#pragma unroll
+            for (int s = 0; s < KMAX; ++s) {
+                p[s] = __ldcs(partials + (t * KMAX + s) * D4 + c);
+                ws[s] = w[t * KMAX + s];
+            }
+#pragma unroll
+            for (int s = 0; s < KMAX; ++s) {
+                acc.x = __fmaf_rn(ws[s], p[s].x, acc.x);
+                acc.y = __fmaf_rn(ws[s], p[s].y, acc.y);
+                acc.z = __fmaf_rn(ws[s], p[s].z, acc.z);
+                acc.w = __fmaf_rn(ws[s], p[s].w, acc.w);
+            }
+        } else {
+            for (int s = 0; s < k; ++s) {
+                const float ws = w[t * k + s];
+                const float4 p = __ldcs(partials + (t * k + s) * D4 + c);
+                acc.x = __fmaf_rn(ws, p.x, acc.x);
+                acc.y = __fmaf_rn(ws, p.y, acc.y);
+                acc.z = __fmaf_rn(ws, p.z, acc.z);
+                acc.w = __fmaf_rn(ws, p.w, acc.w);
+            }
         }
         if (shared != nullptr) {
             const float4 sv = __ldcs(shared + t * D4 + c);
@@ -50,9 +71,18 @@ int launch_combine(const float *partials, const float *topk_w, const float *shar
     const int64_t cap = 152 * 8;  // 8 resident CTAs of 256 threads per SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(partials), topk_w,
-                                                    reinterpret_cast<const float4 *>(shared), N, top_k, D4,
-                                                    reinterpret_cast<float4 *>(out));
+    const float4 *p4 = reinterpret_cast<const float4 *>(partials);
+    const float4 *s4 = reinterpret_cast<const float4 *>(shared);
+    float4 *o4 = reinterpret_cast<float4 *>(out);
+    const unsigned g = (unsigned)blocks;
+    switch (top_k) {
+        case 1: combine_kernel<1><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+        case 2: combine_kernel<2><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+        case 4: combine_kernel<4><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+        case 6: combine_kernel<6><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+        case 8: combine_kernel<8><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+        default: combine_kernel<0><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+    }
     return launch_status();
 }
 

@@ -669,36 +669,57 @@ plan_kernel(const int32_t *__restrict__ expStart, const int32_t *__restrict__ ex
 
 // Gather the Q8_1 rows of x into the padded segment order as exact fp16
 // integers, and their block scales transposed ([D/32][rows]).  A CTA owns 32
-// padded rows; pad rows are zero.
+// padded rows: their source tokens are read once, then every thread issues its
+// 16-byte row pieces back to back (many loads in flight); pad rows are zero.
 __global__ void __launch_bounds__(256)
 gather_kernel(const int8_t *__restrict__ x_q, const float *__restrict__ x_d, int D, const PlanHeader *hdr,
               const int4 *__restrict__ rowinfo, int rows_max, __half *__restrict__ xg16, float *__restrict__ xg_dT) {
+    __shared__ int src[32];
     const int row0 = blockIdx.x * 32;
     const int nrows = hdr->n_rows;
     if (row0 >= nrows) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nblk = D / QK;
-    for (int rr = warp; rr < 32; rr += 8) {
-        const int prow = row0 + rr;
-        if (prow >= nrows) break;
-        const int t = rowinfo[prow].x;
-        __half *dst = xg16 + (size_t)prow * D;
-        for (int c = lane; c < D / 16; c += 32) {
-            int4 v = make_int4(0, 0, 0, 0);
-            if (t >= 0) v = *reinterpret_cast<const int4 *>(x_q + (size_t)t * D + c * 16);
-            const int8_t *b = reinterpret_cast<const int8_t *>(&v);
+    if (threadIdx.x < 32) {
+        const int prow = row0 + threadIdx.x;
+        src[threadIdx.x] = prow < nrows ? rowinfo[prow].x : -1;
+    }
+    __syncthreads();
+    const int pieces = D / 16;  // 16 int8 -> 16 fp16 per piece
+    const int total = 32 * pieces;
+    constexpr int UNR = 4;
+    for (int base = threadIdx.x; base < total; base += 256 * UNR) {
+        int4 v[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int i = base + u * 256;
+            v[u] = make_int4(0, 0, 0, 0);
+            if (i < total) {
+                const int rr = i / pieces, c = i - rr * pieces;
+                const int t = src[rr];
+                if (t >= 0 && row0 + rr < nrows) v[u] = *reinterpret_cast<const int4 *>(x_q + (size_t)t * D + c * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int i = base + u * 256;
+            if (i >= total) continue;
+            const int rr = i / pieces, c = i - rr * pieces;
+            if (row0 + rr >= nrows) continue;
+            const int8_t *b = reinterpret_cast<const int8_t *>(&v[u]);
             __align__(16) __half2 o[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) o[k] = __halves2half2(__short2half_rn(b[2 * k]), __short2half_rn(b[2 * k + 1]));
-            *reinterpret_cast<int4 *>(dst + c * 16) = *reinterpret_cast<const int4 *>(&o[0]);
-            *reinterpret_cast<int4 *>(dst + c * 16 + 8) = *reinterpret_cast<const int4 *>(&o[4]);
+            __half *dst = xg16 + (size_t)(row0 + rr) * D + c * 16;
+            *reinterpret_cast<int4 *>(dst) = *reinterpret_cast<const int4 *>(&o[0]);
+            *reinterpret_cast<int4 *>(dst + 8) = *reinterpret_cast<const int4 *>(&o[4]);
         }
     }
     // scales: lane = row, warps stride over blocks (coalesced 128-byte rows of xg_dT)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nblk = D / QK;
     const int prow = row0 + lane;
-    const int t = prow < nrows ? rowinfo[prow].x : -1;
+    const int t = src[lane];
     for (int b = warp; b < nblk; b += 8) {
-        const float d = t >= 0 ? x_d[(size_t)t * nblk + b] : 0.0f;
+        const float d = (t >= 0 && prow < nrows) ? x_d[(size_t)t * nblk + b] : 0.0f;
         if (prow < rows_max) xg_dT[(size_t)b * rows_max + prow] = d;
     }
 }
@@ -895,13 +916,16 @@ void free_tensor_maps(moe_weights_s *w) {
 
 int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
                            const int32_t *expTokI, const int32_t *expTokK, int N, int top_k, bool with_shared,
-                           void *ws, const WsLayout &L, cudaStream_t s) {
+                           void *ws, const WsLayout &L, cudaStream_t s, bool plan_ready) {
     PlanHeader *hdr = ws_ptr<PlanHeader>(ws, L.plan);
     int32_t *gst = reinterpret_cast<int32_t *>(hdr + 1);
-    plan_kernel<<<1, 1024, 0, s>>>(expStart, expTokI, expTokK, N, top_k, w->E, with_shared ? 1 : 0, L.rows_max,
-                                   L.tiles_max, hdr, gst, ws_ptr<TileDesc>(ws, L.tiles), ws_ptr<int4>(ws, L.rowinfo),
-                                   reinterpret_cast<unsigned *>(ws));
-    int rc = launch_status();
+    int rc = MOE_OK;
+    if (!plan_ready) {
+        plan_kernel<<<1, 1024, 0, s>>>(expStart, expTokI, expTokK, N, top_k, w->E, with_shared ? 1 : 0, L.rows_max,
+                                       L.tiles_max, hdr, gst, ws_ptr<TileDesc>(ws, L.tiles),
+                                       ws_ptr<int4>(ws, L.rowinfo), reinterpret_cast<unsigned *>(ws));
+        rc = launch_status();
+    }
     if (rc || x_q == nullptr) return rc;
     gather_kernel<<<(L.rows_max + 31) / 32, 256, 0, s>>>(x_q, x_d, w->D, hdr, ws_ptr<int4>(ws, L.rowinfo), L.rows_max,
                                                          ws_ptr<__half>(ws, L.xg16), ws_ptr<float>(ws, L.xg_dT));

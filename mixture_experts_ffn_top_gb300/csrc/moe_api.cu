@@ -93,11 +93,12 @@ int pick_path(const moe_weights_s *w, int N, int top_k, int path) {
 int grouped_ffn_impl(moe_weights_s *w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
                      const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
                      const float *shexp_scale, float *partials, float *shared_out, int path, void *ws,
-                     const WsLayout &L, cudaStream_t s) {
+                     const WsLayout &L, cudaStream_t s, bool plan_ready = false) {
     unsigned *st = status_word(ws);
     const bool with_shared = shared_out != nullptr;
     if (path == MOE_PATH_TENSOR) {
-        int rc = launch_plan_and_gather(w, x_q, x_d, expStart, expTokI, expTokK, N, top_k, with_shared, ws, L, s);
+        int rc = launch_plan_and_gather(w, x_q, x_d, expStart, expTokI, expTokK, N, top_k, with_shared, ws, L, s,
+                                        plan_ready);
         if (!rc) rc = launch_gemm_gate_up(w, N, top_k, with_shared, ws, L, nullptr, -1, s);
         if (!rc) rc = launch_gemm_down(w, N, top_k, with_shared, shexp_scale, partials, shared_out, ws, L, s);
         return rc;
@@ -369,9 +370,9 @@ int moe_combine(const float *partials, const float *topk_w, const float *shared,
     return launch_combine(partials, topk_w, shared, N, top_k, D, out, stream);
 }
 
-int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
-                       int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
-                       cudaStream_t stream) {
+static int prefill_impl(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
+                        int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
+                        cudaStream_t stream, cudaEvent_t *ev) {
     if (!w || !hidden || !routerW || !out) return MOE_ERR_INVALID_ARG;
     if (shexp_gate && w->Fs == 0) return MOE_ERR_INVALID_ARG;
     const int D = w->D, E = w->E;
@@ -381,6 +382,9 @@ int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *router
     if (rc) return rc;
     int p = pick_path(w, N, top_k, path);
     if (p < 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    auto mark = [&](int i) {
+        if (ev != nullptr && rc == MOE_OK) rc = cuda_status(cudaEventRecord(ev[i], stream));
+    };
     int32_t *idx = ws_ptr<int32_t>(ws, L.topk_idx);
     float *tw = ws_ptr<float>(ws, L.topk_w);
     float *sh = shexp_gate ? ws_ptr<float>(ws, L.shexp_scale) : nullptr;
@@ -391,12 +395,62 @@ int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *router
     int32_t *tk = ws_ptr<int32_t>(ws, L.expTokK);
     float *part = ws_ptr<float>(ws, L.partials);
     float *shout = shexp_gate ? ws_ptr<float>(ws, L.shared_out) : nullptr;
+    mark(0);
     rc = launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh, xq, xd,
                        nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream);
-    if (!rc) rc = launch_bucket(idx, N, top_k, E, es, ti, tk, status_word(ws), stream);
-    if (!rc) rc = grouped_ffn_impl(w, xq, xd, es, ti, tk, N, top_k, sh, part, shout, p, ws, L, stream);
+    mark(1);
+    // on the tensor path the bucketing kernel also writes the GEMMs' plan
+    const bool tensor = (p == MOE_PATH_TENSOR);
+    if (!rc)
+        rc = launch_bucket(idx, N, top_k, E, es, ti, tk, status_word(ws), stream, tensor ? ws : nullptr,
+                           tensor ? &L : nullptr, shout != nullptr);
+    mark(2);
+    if (tensor) {
+        const bool with_shared = shout != nullptr;
+        if (!rc) rc = launch_plan_and_gather(w, xq, xd, es, ti, tk, N, top_k, with_shared, ws, L, stream, true);
+        mark(3);
+        if (!rc) rc = launch_gemm_gate_up(w, N, top_k, with_shared, ws, L, nullptr, -1, stream);
+        mark(4);
+        if (!rc) rc = launch_gemm_down(w, N, top_k, with_shared, sh, part, shout, ws, L, stream);
+        mark(5);
+    } else {
+        unsigned *st = status_word(ws);
+        int8_t *hq = ws_ptr<int8_t>(ws, L.hq8);
+        float *hd = ws_ptr<float>(ws, L.hd8);
+        const size_t Nk = (size_t)N * top_k;
+        const int Fmax = std::max(w->F, w->Fs);
+        mark(3);
+        if (!rc)
+            rc = launch_matvec_gate_up(w, w->routed, false, xq, xd, es, ti, N, top_k, hq, hd, nullptr, -1, st, stream);
+        if (!rc && shout)
+            rc = launch_matvec_gate_up(w, w->shared, true, xq, xd, nullptr, nullptr, N, top_k, hq + Nk * Fmax,
+                                       hd + Nk * (Fmax / QK), nullptr, -1, st, stream);
+        mark(4);
+        if (!rc)
+            rc = launch_matvec_down(w, w->routed, false, hq, hd, es, ti, tk, N, top_k, nullptr, part, st, stream);
+        if (!rc && shout)
+            rc = launch_matvec_down(w, w->shared, true, hq + Nk * Fmax, hd + Nk * (Fmax / QK), nullptr, nullptr,
+                                    nullptr, N, top_k, sh, shout, st, stream);
+        mark(5);
+    }
     if (!rc) rc = launch_combine(part, tw, shout, N, top_k, D, out, stream);
+    mark(6);
     return rc;
+}
+
+int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
+                       int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+    return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
+                        nullptr);
+}
+
+int moe_ffn_prefill_timed(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
+                          int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
+                          cudaStream_t stream, cudaEvent_t *stage_events) {
+    if (!stage_events) return MOE_ERR_INVALID_ARG;
+    return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
+                        stage_events);
 }
 
 int moe_ffn_prefill(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,

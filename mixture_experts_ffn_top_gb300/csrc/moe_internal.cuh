@@ -89,8 +89,10 @@ int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int no
                             float *w, cudaStream_t s);
 int launch_quantize_q8_1(const float *x, int64_t nblk, int8_t *q, float *d, cudaStream_t s);
 // bucket.cu
+// plan_ws/L non-null: also write the tensor path's plan into plan_ws (layout L)
 int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart,
-                  int32_t *expTokI, int32_t *expTokK, unsigned *status, cudaStream_t s);
+                  int32_t *expTokI, int32_t *expTokK, unsigned *status, cudaStream_t s,
+                  void *plan_ws = nullptr, const WsLayout *L = nullptr, bool with_shared = false);
 // expert_matvec.cu
 int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
                           const int8_t *x_q, const float *x_d, const int32_t *expStart,
@@ -109,10 +111,11 @@ int repack_weights(moe_weights_s *w, const void *gate, const void *up, const voi
 void free_weights(moe_weights_s *w);
 // expert_gemm.cu (tensor path)
 bool tensor_path_supported(const moe_weights_s *w);
+// plan_ready: the plan was already written (by the bucketing kernel); only gather
 int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const float *x_d,
                            const int32_t *expStart, const int32_t *expTokI,
                            const int32_t *expTokK, int N, int top_k, bool with_shared,
-                           void *ws, const WsLayout &L, cudaStream_t s);
+                           void *ws, const WsLayout &L, cudaStream_t s, bool plan_ready = false);
 int launch_gemm_gate_up(const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws,
                         const WsLayout &L, int32_t *dbg_dots, int dbg_block, cudaStream_t s);
 int launch_gemm_gate_up_starved(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,

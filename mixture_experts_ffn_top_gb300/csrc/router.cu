@@ -22,12 +22,15 @@ constexpr int RB_N = 64;   // experts per tile
 constexpr int RB_K = 32;   // K chunk = one Q8 block
 constexpr int R_THREADS = 256;
 
+// logits partials for one (token tile, expert tile, K split): 4x4 outputs per
+// thread from a double-buffered shared tile; the next K chunk is fetched into
+// registers while the current one is multiplied.
 __global__ void __launch_bounds__(R_THREADS)
 router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__ routerW,
                      const float *__restrict__ shexp_gate, int N, int D, int E, int Eext, int ksplit,
                      float *__restrict__ part, int8_t *__restrict__ x_q, float *__restrict__ x_d) {
-    __shared__ __align__(16) float Xs[RB_K][RB_M + 4];
-    __shared__ __align__(16) float Ws[RB_K][RB_N + 4];
+    __shared__ __align__(16) float Xs[2][RB_K][RB_M + 4];
+    __shared__ __align__(16) float Ws[2][RB_K][RB_N + 4];
     const int tid = threadIdx.x;
     const int t0 = blockIdx.x * RB_M;
     const int e0 = blockIdx.y * RB_N;
@@ -42,40 +45,62 @@ router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
 
-    for (int k0 = k_begin; k0 < k_end; k0 += RB_K) {
-        // stage hidden[t0..t0+64)[k0..k0+32) and W[e0..e0+64)[k0..k0+32), transposed (k-major)
+    // per chunk: 2 float4 of hidden (64 rows x 8 float4) and 2 float4 of W (64 rows x 8 float4)
+    float4 xr[2], wr[2];
+    auto fetch = [&](int k0) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            int i = tid + r * R_THREADS;  // 0..511 float4 slots
-            int row = i >> 3, c4 = (i & 7) * 4;
-            int t = t0 + row;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < N) v = *reinterpret_cast<const float4 *>(hidden + (size_t)t * D + k0 + c4);
-            Xs[c4 + 0][row] = v.x;
-            Xs[c4 + 1][row] = v.y;
-            Xs[c4 + 2][row] = v.z;
-            Xs[c4 + 3][row] = v.w;
-            int e = e0 + row;
-            float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < E)
-                wv = *reinterpret_cast<const float4 *>(routerW + (size_t)e * D + k0 + c4);
-            else if (e == E && shexp_gate != nullptr)
-                wv = *reinterpret_cast<const float4 *>(shexp_gate + k0 + c4);
-            Ws[c4 + 0][row] = wv.x;
-            Ws[c4 + 1][row] = wv.y;
-            Ws[c4 + 2][row] = wv.z;
-            Ws[c4 + 3][row] = wv.w;
+            const int i = tid + r * R_THREADS, row = i >> 3, c4 = (i & 7) * 4;
+            const int t = t0 + row;
+            xr[r] = t < N ? *reinterpret_cast<const float4 *>(hidden + (size_t)t * D + k0 + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = tid + r * R_THREADS, row = i >> 3, c4 = (i & 7) * 4;
+            const int e = e0 + row;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < E) v = *reinterpret_cast<const float4 *>(routerW + (size_t)e * D + k0 + c4);
+            else if (e == E && shexp_gate != nullptr) v = *reinterpret_cast<const float4 *>(shexp_gate + k0 + c4);
+            wr[r] = v;
+        }
+    };
+    auto stash = [&](int b) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = tid + r * R_THREADS, row = i >> 3, c4 = (i & 7) * 4;
+            Xs[b][c4 + 0][row] = xr[r].x;
+            Xs[b][c4 + 1][row] = xr[r].y;
+            Xs[b][c4 + 2][row] = xr[r].z;
+            Xs[b][c4 + 3][row] = xr[r].w;
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = tid + r * R_THREADS, row = i >> 3, c4 = (i & 7) * 4;
+            Ws[b][c4 + 0][row] = wr[r].x;
+            Ws[b][c4 + 1][row] = wr[r].y;
+            Ws[b][c4 + 2][row] = wr[r].z;
+            Ws[b][c4 + 3][row] = wr[r].w;
+        }
+    };
+    int b = 0;
+    if (k_begin < k_end) {
+        fetch(k_begin);
+        stash(0);
+    }
+    __syncthreads();
+    for (int k0 = k_begin; k0 < k_end; k0 += RB_K, b ^= 1) {
+        const bool more = k0 + RB_K < k_end;
+        if (more) fetch(k0 + RB_K);  // in flight during this chunk's math
         if (quantise) {
-            // Q8_1 of this K chunk for the tile's 64 tokens: warp w takes 8 tokens, lane = element
+            // Q8_1 of this K chunk (one block) for the tile's tokens: warp w takes 8 tokens
             const int warp = tid >> 5, lane = tid & 31;
 #pragma unroll
-            for (int r = 0; r < RB_M / 8; ++r) {
-                int row = warp * (RB_M / 8) + r;
-                int t = t0 + row;
+            for (int rr = 0; rr < RB_M / 8; ++rr) {
+                const int row = warp * (RB_M / 8) + rr;
+                const int t = t0 + row;
                 float d16f;
-                int q = q8_quantize_lane(Xs[lane][row], &d16f);
+                const int q = q8_quantize_lane(Xs[b][lane][row], &d16f);
                 if (t < N) {
                     x_q[(size_t)t * D + k0 + lane] = (int8_t)q;
                     if (lane == 0) x_d[(size_t)t * (D / QK) + k0 / QK] = d16f;
@@ -84,24 +109,25 @@ router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__
         }
 #pragma unroll 8
         for (int kk = 0; kk < RB_K; ++kk) {
-            float4 a = *reinterpret_cast<const float4 *>(&Xs[kk][ty * 4]);
-            float4 b = *reinterpret_cast<const float4 *>(&Ws[kk][tx * 4]);
-            float av[4] = {a.x, a.y, a.z, a.w};
-            float bv[4] = {b.x, b.y, b.z, b.w};
+            const float4 a = *reinterpret_cast<const float4 *>(&Xs[b][kk][ty * 4]);
+            const float4 w = *reinterpret_cast<const float4 *>(&Ws[b][kk][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
         }
+        if (more) stash(b ^ 1);  // the other buffer was last read two chunks ago
         __syncthreads();
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int t = t0 + ty * 4 + i;
+        const int t = t0 + ty * 4 + i;
         if (t >= N) continue;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            int e = e0 + tx * 4 + j;
+            const int e = e0 + tx * 4 + j;
             if (e < Eext) part[((size_t)split * N + t) * Eext + e] = acc[i][j];
         }
     }
@@ -220,10 +246,10 @@ int launch_softmax(const float *part, int nsplit, int N, int E, int Eext, int to
 }  // namespace
 
 int router_nsplit(int N, int D, int E) {
-    // enough CTAs to cover the SMs about twice, each split at least 256 deep
-    int tiles = ((N + RB_M - 1) / RB_M) * ((E + 1 + RB_N - 1) / RB_N);
-    int want = (2 * 152 + tiles - 1) / tiles;
-    int maxs = D / 256 > 0 ? D / 256 : 1;
+    // about four 8-warp CTAs per SM, each split at least 128 deep
+    int tiles = ((N + RB_M - 1) / RB_M) * ((E + RB_N - 1) / RB_N);
+    int want = (4 * 152 + tiles - 1) / tiles;
+    int maxs = D / 128 > 0 ? D / 128 : 1;
     int s = want < 1 ? 1 : (want > maxs ? maxs : want);
     while (s > 1 && (D / QK) % s != 0) --s;  // equal splits on block boundaries
     return s;

@@ -8,7 +8,7 @@
 // same router kernels with their split-K partial logits in a fixed array that
 // lives in the library's own device image instead.
 //
-// The array is g_router_noalloc_scratch below: 2^21 floats (8 MiB), present on
+// The array is g_router_noalloc_scratch below: 2^22 floats (16 MiB), present on
 // every GPU that loads the library until the process exits.  Every call on a
 // device shares it, so calls that overlap on the GPU (two streams, two host
 // threads) race on it: the caller must order them.  The kernels overwrite every
@@ -23,7 +23,7 @@ int router_nsplit(int N, int D, int E);
 
 namespace {
 
-constexpr size_t kNoAllocScratchFloats = size_t(1) << 21;  // 8 MiB
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 22;  // 16 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_router_noalloc_scratch[kNoAllocScratchFloats];

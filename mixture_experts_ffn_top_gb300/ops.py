@@ -50,6 +50,7 @@ _SIGS = {
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_ffn_prefill_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
+    "moe_ffn_prefill_timed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P, _P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
 }
 
@@ -319,6 +320,27 @@ def moe_ffn_prefill(w: MoeWeights, hidden, routerW, shexp_gate, top_k, norm_topk
                                   N, top_k, int(norm_topk_prob), _dev(out, torch.float32, "out"), path,
                                   _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     _check(rc, "moe_ffn_prefill")
+    return out
+
+
+PREFILL_STAGES = ["router", "bucket", "gather", "gate_up", "down", "combine"]
+
+
+def moe_ffn_prefill_timed(w: MoeWeights, hidden, routerW, shexp_gate, top_k, norm_topk_prob, ws, events, out=None,
+                          path=MOE_PATH_AUTO, stream=None):
+    """moe_ffn_prefill recording 7 torch.cuda.Event objects between its stages (see PREFILL_STAGES)."""
+    N = hidden.shape[0]
+    if out is None:
+        out = torch.empty((N, w.D), dtype=torch.float32, device=hidden.device)
+    for e in events:
+        if e.cuda_event == 0:
+            e.record()  # creates the underlying CUDA event
+    arr = (_P * 7)(*[_P(e.cuda_event) for e in events])
+    rc = lib().moe_ffn_prefill_timed(w.handle, _dev(hidden, torch.float32, "hidden"),
+                                     _dev(routerW, torch.float32, "routerW"), _dev(shexp_gate, torch.float32),
+                                     N, top_k, int(norm_topk_prob), _dev(out, torch.float32, "out"), path,
+                                     _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream), arr)
+    _check(rc, "moe_ffn_prefill_timed")
     return out
 
 

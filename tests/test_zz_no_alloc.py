@@ -52,8 +52,8 @@ def test_noalloc_router_matches_workspace_router(ops, name):
 
 
 def test_noalloc_router_refuses_oversized_problem(ops):
-    # N * (E + 1) alone exceeds the 2^21-float scratch: refused on the host, nothing launched
-    N, D, E = 20000, 64, 128
+    # N * (E + 1) alone exceeds the 2^22-float scratch: refused on the host, nothing launched
+    N, D, E = 40000, 64, 128
     hidden = torch.zeros((N, D), dtype=torch.float32, device="cuda")
     routerW = torch.zeros((E, D), dtype=torch.float32, device="cuda")
     with pytest.raises(ops.MoeError) as exc:
