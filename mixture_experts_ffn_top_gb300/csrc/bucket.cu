@@ -28,7 +28,7 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 }
 
 // Optional plan of the tensor path, derived from the finished CSR in the same CTA:
-// padded segment starts (16-row aligned), token tiles of <= 128 rows (routed
+// padded segment starts (16-row aligned), token tiles of <= TILE_N rows (routed
 // experts first, then the shared expert's N rows) and, for every padded row, its
 // source token, output row and CSR entry.
 struct PlanOut {
@@ -115,7 +115,7 @@ bucket_kernel(const int32_t *__restrict__ idx, int N, int k, int E, int32_t *__r
         return;
     }
     // exclusive scans (one expert per thread, E <= 1024): segment starts and, for the
-    // plan, 16-row padded starts and 128-row tile starts
+    // plan, 16-row padded starts and TILE_N-row tile starts
     {
         const int c = tid < E ? (int)cnt[tid] : 0;
         const int pc = (c + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;

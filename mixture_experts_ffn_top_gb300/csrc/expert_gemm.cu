@@ -49,25 +49,29 @@ namespace moe {
 
 namespace {
 
-constexpr int G_DRAIN_WARPS = 16;                 // 4 per SM sub-partition
+constexpr int G_DRAIN_WARPS = 12;                 // 3 per SM sub-partition (128 registers each)
+constexpr int G_GROUPS = G_DRAIN_WARPS / 4;        // column groups of 32 token columns
 constexpr int G_THREADS = 64 + 32 * G_DRAIN_WARPS; // producer warp + MMA warp + drain warps
-constexpr int G_STAGES = 5;                        // weight + token tile ring (TMA -> MMA)
+constexpr int G_STAGES = 6;                        // weight + token tile ring (TMA -> MMA)
 constexpr int G_SSTAGES = 8;                       // block-scale ring (TMA -> drain)
-constexpr int G_TMEM_BUFS = 4;                     // per-block accumulators in TMEM
+constexpr int G_TMEM_BUFS = 5;                     // per-block accumulators in TMEM
+constexpr int G_BUF_COLS = TILE_N;                 // 96 fp32 columns per accumulator
 constexpr int G_TMEM_COLS = 512;
 constexpr int STAGE_A = 16384;                     // 128 weight rows x 128 B (64 fp16 = 2 blocks)
-constexpr int STAGE_B = 16384;                     // up to 128 token rows x 128 B
+constexpr int STAGE_B = TILE_N * 128;              // up to 96 token rows x 128 B
 constexpr int STAGE_BYTES = STAGE_A + STAGE_B;
 constexpr int SSTAGE_BYTES = 2048;                 // [2][128] weight scales + [2][nb] token scales
 constexpr int XCH_STRIDE = 33;                     // padded row of the gate/up exchange (32 columns)
-constexpr int XCH_BYTES = 4 * 64 * XCH_STRIDE * 4; // 4 column groups x 64 features
+constexpr int XCH_BYTES = G_GROUPS * 64 * XCH_STRIDE * 4;
 constexpr int BAR_BYTES = 512;
 constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + XCH_BYTES + BAR_BYTES;
+static_assert(G_TMEM_BUFS * G_BUF_COLS <= G_TMEM_COLS, "TMEM ring exceeds the allocation");
+static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s: any healthy wait is microseconds
 
 struct GemmMaps {
     CUtensorMap a_r, sa_r, a_s, sa_s;  // weights + weight scales, routed / shared
-    CUtensorMap b[4], sb[4];           // tokens + token scales, box heights 16/32/64/128
+    CUtensorMap b[4], sb[4];           // tokens + token scales, box heights 16/32/64/96
 };
 
 struct GemmParams {
@@ -178,15 +182,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr)
-        : "memory");
-}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------ schedule ---
@@ -216,16 +211,12 @@ __device__ __forceinline__ Item item_at(const GemmParams &p, int it, int n_rtile
     x.expert = td.expert;
     x.entry0 = td.entry0;
     x.bi = x.nrows <= 16 ? 0 : x.nrows <= 32 ? 1 : x.nrows <= 64 ? 2 : 3;
-    x.nb = 16 << x.bi;
+    x.nb = x.bi < 3 ? (16 << x.bi) : TILE_N;
     return x;
 }
 
 // --------------------------------------------------------------- kernel ---
-// Ties the registers a tcgen05.ld wrote to the tcgen05.wait::ld before it, so no use of
-// them can be scheduled above the wait.
-__device__ __forceinline__ void tmem_reg_fence(uint32_t (&v)[8]) {
-    asm volatile("" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]));
-}
+// One warp reads 32 TMEM lanes x 32 consecutive fp32 columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -238,17 +229,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         : "r"(taddr)
         : "memory");
 }
+// Ties the registers a tcgen05.ld wrote to the tcgen05.wait::ld before it, so no use of
+// them can be scheduled above the wait.
 __device__ __forceinline__ void tmem_reg_fence32(uint32_t (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; i += 8)
         asm volatile("" : "+r"(v[i]), "+r"(v[i + 1]), "+r"(v[i + 2]), "+r"(v[i + 3]), "+r"(v[i + 4]), "+r"(v[i + 5]),
                      "+r"(v[i + 6]), "+r"(v[i + 7]));
-}
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-                 : "r"(taddr)
-                 : "memory");
 }
 // SiLU(g) * u with the fast exponential and division (the result is requantised to 8 bits)
 __device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
@@ -274,7 +261,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     const uint32_t full0 = next_bar(G_STAGES), empty0 = next_bar(G_STAGES);
     const uint32_t sfull0 = next_bar(G_SSTAGES), sempty0 = next_bar(G_SSTAGES);
     const uint32_t tfull0 = next_bar(G_TMEM_BUFS), tempty0 = next_bar(G_TMEM_BUFS);
-    const uint32_t xready0 = next_bar(4), xfree0 = next_bar(4);
+    const uint32_t xready0 = next_bar(G_GROUPS), xfree0 = next_bar(G_GROUPS);
     const uint32_t done_bar = next_bar(1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * nb_);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -293,7 +280,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             mbar_init(tfull0 + 8 * b, 1);
             mbar_init(tempty0 + 8 * b, G_DRAIN_WARPS);
         }
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < G_GROUPS; ++g) {
             mbar_init(xready0 + 8 * g, 4);
             mbar_init(xfree0 + 8 * g, 4);
         }
@@ -405,7 +392,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d = tmem_base + buf * 128;
+                        const uint32_t d = tmem_base + buf * G_BUF_COLS;
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint32_t off = half * 64 + kk * 32;  // bytes along K inside the swizzle atom
@@ -431,7 +418,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     } else {
         // ------------------------------------------------------- drain ---
         const int q = warp & 3;              // TMEM lane quarter (= SM sub-partition) of this warp
-        const int grp = (warp - 2) >> 2;     // column group: columns 32i + 8*grp + [0, 8)
+        const int grp = (warp - 2) >> 2;     // column group: token columns 32*grp + [0, 32)
         const int r = q * 32 + lane;         // row of the 128-row weight tile
         int sstage = 0, buf = 0;
         uint32_t sphase = 0, tphase = 0, xphase = 0;
@@ -444,57 +431,80 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             float2 acc[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m) acc[m] = make_float2(0.0f, 0.0f);
-            for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
+            const uint32_t tlane = tmem_base + ((uint32_t)(q * 32) << 16) + c0;
+            // Per stage (two K blocks in two TMEM slots): one wait for the second slot's commit
+            // (it covers both blocks), both TMEM loads, the scale wait overlapping them, then the
+            // slots go back to the MMA before the math, which interleaves the two blocks.
+            const int nst = x.K / 64;
+            uint32_t v0[32], v1[32];
+            for (int ks = 0; ks < nst && ok; ++ks) {
+                const int s0 = buf;
+                int s1 = buf + 1;
+                uint32_t ph1 = tphase;
+                if (s1 == G_TMEM_BUFS) s1 = 0, ph1 ^= 1;
+                ok = mbar_wait(tfull0 + 8 * s1, ph1, abort_flag, p.status, p.wait_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (active) {
+                    tmem_ld32(tlane + s0 * G_BUF_COLS, v0);
+                    tmem_ld32(tlane + s1 * G_BUF_COLS, v1);
+                }
                 ok = mbar_wait(sfull0 + 8 * sstage, sphase, abort_flag, p.status, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const float *SA = reinterpret_cast<const float *>(sring + sstage * SSTAGE_BYTES);
-                const float *SB = SA + 256;
-                for (int half = 0; half < 2; ++half) {
-                    ok = mbar_wait(tfull0 + 8 * buf, tphase, abort_flag, p.status, p.wait_ns);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-                    uint32_t v[32];
-                    if (active) {
-                        tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * 128 + c0, v);
-                        tmem_wait_ld();
-                        tmem_reg_fence32(v);
+                if (active) {
+                    tmem_wait_ld();
+                    tmem_reg_fence32(v0);
+                    tmem_reg_fence32(v1);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(tempty0 + 8 * s0);
+                    mbar_arrive(tempty0 + 8 * s1);
+                }
+                buf = s1 + 1;
+                tphase = ph1;
+                if (buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
+                if (active) {
+                    const float *SA = reinterpret_cast<const float *>(sring + sstage * SSTAGE_BYTES);
+                    const float *SB = SA + 256;
+                    if (DUMP && x.shared == 0 && (2 * ks == p.dbg_block || 2 * ks + 1 == p.dbg_block)) {
+                        const int mat = r < 64 ? 0 : 1;
+                        const int f = x.mt * 64 + (r & 63);
+                        const uint32_t *v = (2 * ks == p.dbg_block) ? v0 : v1;
+                        for (int j = 0; j < 32 && c0 + j < x.nrows; ++j)
+                            p.dbg_dots[((size_t)(x.entry0 + c0 + j) * 2 + mat) * p.F + f] = (int32_t)__uint_as_float(v[j]);
                     }
-                    // the block is in registers: hand the TMEM buffer back before the math
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-                    if (++buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
-                    if (active) {
-                        if (DUMP && x.shared == 0 && ks * 2 + half == p.dbg_block) {
-                            const int mat = r < 64 ? 0 : 1;
-                            const int f = x.mt * 64 + (r & 63);
-                            for (int j = 0; j < 32 && c0 + j < x.nrows; ++j)
-                                p.dbg_dots[((size_t)(x.entry0 + c0 + j) * 2 + mat) * p.F + f] =
-                                    (int32_t)__uint_as_float(v[j]);
-                        }
-                        const float dw = SA[half * 128 + r];
-                        const float2 dw2 = make_float2(dw, dw);
-                        const float4 *sb4 = reinterpret_cast<const float4 *>(SB + half * x.nb + c0);
+                    const float dwa = SA[r], dwb = SA[128 + r];
+                    const float2 dw2a = make_float2(dwa, dwa), dw2b = make_float2(dwb, dwb);
+                    const float4 *sa4 = reinterpret_cast<const float4 *>(SB + c0);
+                    const float4 *sb4 = reinterpret_cast<const float4 *>(SB + x.nb + c0);
 #pragma unroll
-                        for (int g4 = 0; g4 < 8; ++g4) {
-                            const float4 s4 = sb4[g4];  // token scales of columns 4*g4 .. 4*g4+3 (broadcast)
-                            const float2 sa = __fmul2_rn(make_float2(s4.x, s4.y), dw2);
-                            const float2 sb = __fmul2_rn(make_float2(s4.z, s4.w), dw2);
-                            acc[2 * g4] = __ffma2_rn(
-                                make_float2(__uint_as_float(v[4 * g4]), __uint_as_float(v[4 * g4 + 1])), sa, acc[2 * g4]);
-                            acc[2 * g4 + 1] = __ffma2_rn(
-                                make_float2(__uint_as_float(v[4 * g4 + 2]), __uint_as_float(v[4 * g4 + 3])), sb,
-                                acc[2 * g4 + 1]);
-                        }
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        // token scales of columns 4*g4 .. 4*g4+3 for the two blocks (broadcast loads)
+                        const float4 ta = sa4[g4], tb = sb4[g4];
+                        const float2 a01 = __fmul2_rn(make_float2(ta.x, ta.y), dw2a);
+                        const float2 a23 = __fmul2_rn(make_float2(ta.z, ta.w), dw2a);
+                        const float2 b01 = __fmul2_rn(make_float2(tb.x, tb.y), dw2b);
+                        const float2 b23 = __fmul2_rn(make_float2(tb.z, tb.w), dw2b);
+                        float2 u = __ffma2_rn(make_float2(__uint_as_float(v0[4 * g4]), __uint_as_float(v0[4 * g4 + 1])),
+                                              a01, acc[2 * g4]);
+                        float2 w = __ffma2_rn(
+                            make_float2(__uint_as_float(v0[4 * g4 + 2]), __uint_as_float(v0[4 * g4 + 3])), a23,
+                            acc[2 * g4 + 1]);
+                        acc[2 * g4] = __ffma2_rn(
+                            make_float2(__uint_as_float(v1[4 * g4]), __uint_as_float(v1[4 * g4 + 1])), b01, u);
+                        acc[2 * g4 + 1] = __ffma2_rn(
+                            make_float2(__uint_as_float(v1[4 * g4 + 2]), __uint_as_float(v1[4 * g4 + 3])), b23, w);
                     }
                 }
-                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sempty0 + 8 * sstage);  // scales of both blocks read
                 if (++sstage == G_SSTAGES) sstage = 0, sphase ^= 1;
             }
+            tmem_wait_ld();  // no TMEM load outlives the loop, even when it was cut short
             if (!ok) break;
             // --------------------------------------------------- epilogue ---
             if (MODE == 0) {
@@ -518,20 +528,35 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if (active) {
-                    const int f = x.mt * 64 + fr;  // this warp's 32 features form one Q8_1 block
+                    // The warp's 32 lanes hold the 32 features of one Q8_1 block for each of its
+                    // 16 columns.  Block maxima come from one warp reduction per column; the two
+                    // IEEE divisions per block (d = amax/127, 1/d) then run once, for all 16
+                    // columns side by side in lanes 0-15, and 1/d is broadcast back per column.
+                    const int f = x.mt * 64 + fr;
                     const int fblk = f >> 5;
+                    const int par = is_gate ? 0 : 1;  // this warp's column parity
+                    float hv[16];
+                    unsigned amax_mine = 0;
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
-                        const int cl = 2 * m + (is_gate ? 0 : 1);
-                        const int col = c0 + cl;
-                        if (col >= x.nrows) break;  // warp-uniform
+                        const int cl = 2 * m + par;
                         const float other = xg[fr * XCH_STRIDE + cl];
-                        const float hv = is_gate ? swiglu(acc[m].x, other) : swiglu(other, acc[m].y);
-                        float d16f;
-                        const int qv = q8_quantize_lane(hv, &d16f);
-                        const int prow = x.row0 + col;
-                        p.h16[(size_t)prow * p.Fmax + f] = __int2half_rn(qv);
-                        if (lane == 0) p.h_dT[(size_t)fblk * p.rows_max + prow] = d16f;
+                        hv[m] = is_gate ? swiglu(acc[m].x, other) : swiglu(other, acc[m].y);
+                        const unsigned am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[m])));
+                        if (lane == m) amax_mine = am;
+                    }
+                    const float d = __fdiv_rn(__uint_as_float(amax_mine), 127.0f);
+                    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+                    const int my_col = c0 + 2 * lane + par;  // column whose scale this lane holds
+                    if (lane < 16 && my_col < x.nrows)
+                        p.h_dT[(size_t)fblk * p.rows_max + x.row0 + my_col] = __half2float(__float2half_rn(d));
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const int col = c0 + 2 * m + par;
+                        const float idm = __shfl_sync(0xffffffffu, id, m);
+                        if (col >= x.nrows) break;  // warp-uniform
+                        const int qv = (int)roundf(__fmul_rn(hv[m], idm));
+                        p.h16[(size_t)(x.row0 + col) * p.Fmax + f] = __int2half_rn(qv);
                     }
                 }
                 __syncwarp();
@@ -571,7 +596,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
 }
 
 // ------------------------------------------------ planning and gathering ---
-// One CTA: padded segment starts (16-row aligned), token tiles of <= 128 rows
+// One CTA: padded segment starts (16-row aligned), token tiles of <= TILE_N rows
 // per segment (routed experts first, then the shared expert's N rows), and for
 // every padded row its source token, output row and CSR entry.
 __global__ void __launch_bounds__(1024)
@@ -834,7 +859,7 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     void *bscale = mode == 0 ? (void *)ws_ptr<float>(ws, L.xg_dT) : (void *)ws_ptr<float>(ws, L.h_dT);
     const int kcols = mode == 0 ? D : Fmax;
     for (int i = 0; i < 4; ++i) {
-        const uint32_t nb = 16u << i;
+        const uint32_t nb = i < 3 ? (16u << i) : (uint32_t)TILE_N;
         if (!encode_2d(&maps.b[i], bdata, true, rows, kcols, 64, nb)) return MOE_ERR_CUDA;
         if (!encode_2d(&maps.sb[i], bscale, false, kcols / QK, rows, nb, 2)) return MOE_ERR_CUDA;
     }

@@ -15,7 +15,7 @@ constexpr int Q8_0_BYTES = 34;  // fp16 scale + 32 int8
 constexpr int MAX_E = 1024;
 constexpr int SEG_ALIGN = 16;   // padded segment start (rows) in the tensor-core row space
 constexpr int TILE_M = 128;     // weight rows per tensor-core tile
-constexpr int TILE_N = 128;     // token rows per tensor-core tile (max)
+constexpr int TILE_N = 96;      // token rows per tensor-core tile (max)
 
 // ---------------------------------------------------------------- weights --
 // Library-owned device copy of the expert weights (see moe_weights_create).
