@@ -51,9 +51,10 @@ namespace {
 
 constexpr int G_DRAIN_WARPS = 12;                 // 3 per SM sub-partition (128 registers each)
 constexpr int G_GROUPS = G_DRAIN_WARPS / 4;        // column groups of 32 token columns
-constexpr int G_THREADS = 64 + 32 * G_DRAIN_WARPS; // producer warp + MMA warp + drain warps
+constexpr int G_ORCH_WARP = 2 + G_DRAIN_WARPS;    // warp that tells the MMA warp when a stage may go
+constexpr int G_THREADS = 96 + 32 * G_DRAIN_WARPS; // producer, MMA, drain warps, orchestrator
 constexpr int G_STAGES = 6;                        // weight + token tile ring (TMA -> MMA)
-constexpr int G_SSTAGES = 8;                       // block-scale ring (TMA -> drain)
+constexpr int G_SSTAGES = G_STAGES + 3;            // block-scale ring (TMA -> drain), one slot per stage
 constexpr int G_TMEM_BUFS = 5;                     // per-block accumulators in TMEM
 constexpr int G_BUF_COLS = TILE_N;                 // 96 fp32 columns per accumulator
 constexpr int G_TMEM_COLS = 512;
@@ -67,6 +68,13 @@ constexpr int BAR_BYTES = 512;
 constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + XCH_BYTES + BAR_BYTES;
 static_assert(G_TMEM_BUFS * G_BUF_COLS <= G_TMEM_COLS, "TMEM ring exceeds the allocation");
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+// Scale slot reuse needs no barrier of its own.  The producer loads stage L once the MMAs of stage
+// L - G_STAGES completed; those were issued only after the drain handed back the TMEM slots they
+// write, last used by the first block of stage L - G_STAGES - 2, and every drain warp hands those
+// back only after finishing the scale math of stage L - G_STAGES - 3.  Slot L % G_SSTAGES was last
+// used by stage L - G_SSTAGES, so G_SSTAGES >= G_STAGES + 3 keeps it unread by then.
+static_assert(G_SSTAGES >= G_STAGES + 3, "scale slots could be overwritten while still read");
+static_assert(G_TMEM_BUFS == 5, "the argument above assumes stage t's blocks reuse the slots of blocks 2t-5, 2t-4");
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s: any healthy wait is microseconds
 
 struct GemmMaps {
@@ -151,6 +159,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_shared(int *p, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -259,22 +275,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
         return b;
     };
     const uint32_t full0 = next_bar(G_STAGES), empty0 = next_bar(G_STAGES);
-    const uint32_t sfull0 = next_bar(G_SSTAGES), sempty0 = next_bar(G_SSTAGES);
     const uint32_t tfull0 = next_bar(G_TMEM_BUFS), tempty0 = next_bar(G_TMEM_BUFS);
     const uint32_t xready0 = next_bar(G_GROUPS), xfree0 = next_bar(G_GROUPS);
     const uint32_t done_bar = next_bar(1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * nb_);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *stages_ready = reinterpret_cast<int *>(tmem_slot + 2);  // orchestrator -> MMA warp
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, 1);   // the copies' arrival (tiles and scales)
             mbar_init(empty0 + 8 * s, 1);  // released by the MMA commit
-        }
-        for (int s = 0; s < G_SSTAGES; ++s) {
-            mbar_init(sfull0 + 8 * s, 1);
-            mbar_init(sempty0 + 8 * s, G_DRAIN_WARPS);
         }
         for (int b = 0; b < G_TMEM_BUFS; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
@@ -286,6 +298,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
+        *stages_ready = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -320,9 +333,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
         // ------------------------------------------------ TMA producer ---
         if (lane == 0) {
             int stage = 0, sstage = 0;
-            uint32_t phase = 0, sphase = 0;
+            uint32_t phase = 0;
             // per slot: was it ever filled, and the parity of its last fill (bit masks)
-            uint32_t issued = 0, last_parity = 0, sissued = 0, last_sparity = 0;
+            uint32_t issued = 0, last_parity = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok && !p.starve; it += gridDim.x) {
                 const Item x = item_at(p, it, n_rtiles);
@@ -331,27 +344,22 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 const int arow = (x.shared ? 0 : x.expert * p.rows_r) + x.mt * 128;
                 const int sarow = x.shared ? 0 : x.expert * p.sblk_r;
                 for (int ks = 0; ks < x.K / 64; ++ks) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.wait_ns) ||
-                        !mbar_wait(sempty0 + 8 * sstage, sphase ^ 1, abort_flag, p.status, p.wait_ns)) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + stage * STAGE_BYTES;
+                    uint8_t *ss = sring + sstage * SSTAGE_BYTES;
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_expect_tx(fb, STAGE_A + x.nb * 128);
+                    mbar_expect_tx(fb, STAGE_A + x.nb * 128 + 1024 + 2 * x.nb * 4);
                     tma_load_2d(smem_u32(st), ma, ks * 64, arow, fb);
                     tma_load_2d(smem_u32(st + STAGE_A), &maps.b[x.bi], ks * 64, x.row0, fb);
-                    uint8_t *ss = sring + sstage * SSTAGE_BYTES;
-                    const uint32_t sb = sfull0 + 8 * sstage;
-                    mbar_expect_tx(sb, 1024 + 2 * x.nb * 4);
-                    tma_load_2d(smem_u32(ss), msa, x.mt * 128, sarow + 2 * ks, sb);
-                    tma_load_2d(smem_u32(ss + 1024), &maps.sb[x.bi], x.row0, 2 * ks, sb);
+                    tma_load_2d(smem_u32(ss), msa, x.mt * 128, sarow + 2 * ks, fb);
+                    tma_load_2d(smem_u32(ss + 1024), &maps.sb[x.bi], x.row0, 2 * ks, fb);
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                    sissued |= 1u << sstage;
-                    last_sparity = (last_sparity & ~(1u << sstage)) | (sphase << sstage);
                     if (++stage == G_STAGES) stage = 0, phase ^= 1;
-                    if (++sstage == G_SSTAGES) sstage = 0, sphase ^= 1;
+                    if (++sstage == G_SSTAGES) sstage = 0;
                 }
             }
             // copies still in flight must land before the CTA can exit
@@ -361,37 +369,40 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     while (!mbar_try(full0 + 8 * s, last_parity >> s & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
                     }
                 }
-            for (int s = 0; s < G_SSTAGES; ++s)
-                if (sissued >> s & 1) {
-                    uint64_t t0 = globaltimer();
-                    while (!mbar_try(sfull0 + 8 * s, last_sparity >> s & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
-                    }
-                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ---
         if (lane == 0) {
-            int stage = 0, buf = 0;
-            uint32_t phase = 0, tphase = 0;
+            int stage = 0, buf = 0, mt = 0;  // mt: stages issued over the run
             bool ok = true;
             bool any = false;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
                 const Item x = item_at(p, it, n_rtiles);
                 const uint32_t idesc = idesc_f16((x.nrows + 15) & ~15);
                 for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) {
-                        ok = false;
-                        break;
+                    // A plain shared-memory poll: an mbarrier wait in the thread that issues the
+                    // MMAs stalls it for a few hundred cycles, a shared load for tens.
+                    if (ld_acquire_shared(stages_ready) <= mt) {
+                        uint64_t t0 = 0;
+                        for (uint32_t n = 1; ld_acquire_shared(stages_ready) <= mt; ++n) {
+                            if ((n & 255) == 0) {
+                                if (*abort_flag) { ok = false; break; }
+                                if (t0 == 0) t0 = globaltimer();
+                                else if (globaltimer() - t0 > p.wait_ns) {
+                                    *abort_flag = 1;
+                                    atomicOr(p.status, MOE_DEV_TIMEOUT);
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                        }
+                        if (!ok) break;
                     }
-                    tc_fence_after();
+                    ++mt;
+                    tc_fence_after();  // the stage's data has landed and its two TMEM slots are free
                     const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t b0 = a0 + STAGE_A;
                     for (int half = 0; half < 2; ++half) {
-                        if (!mbar_wait(tempty0 + 8 * buf, tphase ^ 1, abort_flag, p.status, p.wait_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
                         const uint32_t d = tmem_base + buf * G_BUF_COLS;
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
@@ -400,11 +411,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                         }
                         mma_commit(tfull0 + 8 * buf);
                         any = true;
-                        if (++buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
+                        if (++buf == G_TMEM_BUFS) buf = 0;
                     }
-                    if (!ok) break;
                     mma_commit(empty0 + 8 * stage);  // the tile slot is free once these MMAs are done
-                    if (++stage == G_STAGES) stage = 0, phase ^= 1;
+                    if (++stage == G_STAGES) stage = 0;
                 }
             }
             if (any) {
@@ -415,13 +425,37 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 }
             }
         }
+    } else if (warp == G_ORCH_WARP) {
+        // ---------------------------------------------------- orchestrator ---
+        // Per stage: wait until its tiles and scales have landed and the drain has handed back
+        // the TMEM slots of its two blocks, then publish the stage count to the MMA warp.
+        if (lane == 0) {
+            int stage = 0, t = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const Item x = item_at(p, it, n_rtiles);
+                for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
+                    ok = mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns);
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        const int j = 2 * t + h;  // block index over the run
+                        if (j >= G_TMEM_BUFS)
+                            ok = mbar_wait(tempty0 + 8 * (j % G_TMEM_BUFS), ((j / G_TMEM_BUFS) - 1) & 1, abort_flag,
+                                           p.status, p.wait_ns);
+                    }
+                    if (!ok) break;
+                    st_release_shared(stages_ready, ++t);
+                    if (++stage == G_STAGES) stage = 0, phase ^= 1;
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------- drain ---
         const int q = warp & 3;              // TMEM lane quarter (= SM sub-partition) of this warp
         const int grp = (warp - 2) >> 2;     // column group: token columns 32*grp + [0, 32)
         const int r = q * 32 + lane;         // row of the 128-row weight tile
         int sstage = 0, buf = 0;
-        uint32_t sphase = 0, tphase = 0, xphase = 0;
+        uint32_t tphase = 0, xphase = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item x = item_at(p, it, n_rtiles);
@@ -433,8 +467,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             for (int m = 0; m < 16; ++m) acc[m] = make_float2(0.0f, 0.0f);
             const uint32_t tlane = tmem_base + ((uint32_t)(q * 32) << 16) + c0;
             // Per stage (two K blocks in two TMEM slots): one wait for the second slot's commit
-            // (it covers both blocks), both TMEM loads, the scale wait overlapping them, then the
-            // slots go back to the MMA before the math, which interleaves the two blocks.
+            // (it covers both blocks, and the MMA warp only issued them once the stage's tiles and
+            // scales had landed), both TMEM loads, then the slots go back before the math, which
+            // interleaves the two blocks.
             const int nst = x.K / 64;
             uint32_t v0[32], v1[32];
             for (int ks = 0; ks < nst && ok; ++ks) {
@@ -450,9 +485,6 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     tmem_ld32(tlane + s0 * G_BUF_COLS, v0);
                     tmem_ld32(tlane + s1 * G_BUF_COLS, v1);
                 }
-                ok = mbar_wait(sfull0 + 8 * sstage, sphase, abort_flag, p.status, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
                 if (active) {
                     tmem_wait_ld();
                     tmem_reg_fence32(v0);
@@ -500,9 +532,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                             make_float2(__uint_as_float(v1[4 * g4 + 2]), __uint_as_float(v1[4 * g4 + 3])), b23, w);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sempty0 + 8 * sstage);  // scales of both blocks read
-                if (++sstage == G_SSTAGES) sstage = 0, sphase ^= 1;
+                if (++sstage == G_SSTAGES) sstage = 0;
             }
             tmem_wait_ld();  // no TMEM load outlives the loop, even when it was cut short
             if (!ok) break;
