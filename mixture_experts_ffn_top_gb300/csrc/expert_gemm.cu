@@ -428,7 +428,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     } else if (warp == G_ORCH_WARP) {
         // ---------------------------------------------------- orchestrator ---
         // Per stage: wait until its tiles and scales have landed and the drain has handed back
-        // the TMEM slots of its two blocks, then publish the stage count to the MMA warp.
+        // the TMEM slots of its two blocks, then publish the stage count to the MMA warp.  The
+        // slots of blocks 2t and 2t+1 were last used by blocks 2t-5 (stage t-3) and 2t-4 (stage
+        // t-2); every drain warp hands back stage t-3 before stage t-2, so the second slot's
+        // barrier alone tells that both are free.
         if (lane == 0) {
             int stage = 0, t = 0;
             uint32_t phase = 0;
@@ -437,12 +440,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 const Item x = item_at(p, it, n_rtiles);
                 for (int ks = 0; ks < x.K / 64 && ok; ++ks) {
                     ok = mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns);
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        const int j = 2 * t + h;  // block index over the run
-                        if (j >= G_TMEM_BUFS)
-                            ok = mbar_wait(tempty0 + 8 * (j % G_TMEM_BUFS), ((j / G_TMEM_BUFS) - 1) & 1, abort_flag,
-                                           p.status, p.wait_ns);
-                    }
+                    const int j = 2 * t + 1;  // second block of the stage, counted over the run
+                    if (ok && j >= G_TMEM_BUFS)
+                        ok = mbar_wait(tempty0 + 8 * (j % G_TMEM_BUFS), ((j / G_TMEM_BUFS) - 1) & 1, abort_flag,
+                                       p.status, p.wait_ns);
                     if (!ok) break;
                     st_release_shared(stages_ready, ++t);
                     if (++stage == G_STAGES) stage = 0, phase ^= 1;
