@@ -263,7 +263,9 @@ template <int MODE, bool DUMP>
 __global__ void __launch_bounds__(G_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned start for the swizzled tiles, kept as an offset from the shared array so
+    // the compiler still knows every derived pointer is shared memory (plain LDS/STS, not generic)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sring = smem + G_STAGES * STAGE_BYTES;
     float *xch = reinterpret_cast<float *>(sring + G_SSTAGES * SSTAGE_BYTES);
     uint8_t *bars = reinterpret_cast<uint8_t *>(xch) + XCH_BYTES;
