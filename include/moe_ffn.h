@@ -119,8 +119,9 @@ int moe_weights_tensor_path(moe_weights_t w);
 
 /* ---------------------------------------------------------------------------
  * Workspace: one caller-owned device buffer per concurrent call chain.  The
- * first 256 bytes hold the device status word.  moe_workspace_init zeroes
- * the status word (asynchronously); moe_workspace_status synchronises the
+ * first 256 bytes hold the device status word (and the bucketing kernel's
+ * grid-barrier words).  moe_workspace_init zeroes those 256 bytes
+ * (asynchronously); moe_workspace_status synchronises the
  * stream, returns the status word (host int, MOE_DEV_* bits) and, when
  * clear != 0, zeroes it.  Two call chains must not share a workspace.
  * moe_ffn_workspace_size covers every entry point below for that shape.
@@ -190,8 +191,16 @@ int moe_quantize_q8_1(const float *x, int64_t n_blocks, int8_t *q, float *d, cud
  *   expTokI  [N*top_k] int32 out: token of each entry (ascending per segment)
  *   expTokK  [N*top_k] int32 out: top-k slot of that token for this expert
  * A bad index or a repeated expert within a token sets MOE_DEV_BAD_ROUTING
- * and leaves every segment empty.  One kernel: histogram, scan and scatter.
+ * and leaves every segment empty.  One cooperative kernel: each CTA counts a
+ * token range, a grid barrier, then every CTA scans the count table and
+ * scatters its range (histogram, scan and scatter in one launch).
+ * ws: 256-byte aligned, at least moe_bucket_workspace_size(N, top_k, E)
+ * bytes (a moe_ffn_workspace_size workspace of the same N, E, top_k always
+ * is), initialised once by moe_workspace_init; the barrier keeps its words at
+ * zero between calls.  If the barrier times out (MOE_DEV_TIMEOUT) the outputs
+ * are undefined; run moe_workspace_init before the next call.
  * ------------------------------------------------------------------------- */
+size_t moe_bucket_workspace_size(int N, int top_k, int E);
 int moe_bucket(const int32_t *topk_idx, int N, int top_k, int E,
                int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
                void *ws, size_t ws_bytes, cudaStream_t stream);

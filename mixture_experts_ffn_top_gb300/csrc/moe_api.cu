@@ -32,7 +32,8 @@ WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs) {
     // the router's split-K scratch comes first: moe_router_topk, which knows only (N, D, E),
     // finds it at the same offset as every other entry point
     L.nsplit = router_nsplit(N, D, E);
-    L.part_logits = take((size_t)L.nsplit * N * (E + 1) * 4);
+    // ... and the bucketing's count table reuses it once the router is done with it
+    L.part_logits = take(std::max((size_t)L.nsplit * N * (E + 1) * 4, bucket_scratch_bytes(N, E)));
     L.topk_idx = take(Nk * 4);
     L.topk_w = take(Nk * 4);
     L.shexp_scale = take((size_t)N * 4);
@@ -257,12 +258,18 @@ int moe_quantize_q8_1(const float *x, int64_t n_blocks, int8_t *q, float *d, cud
     return launch_quantize_q8_1(x, n_blocks, q, d, stream);
 }
 
+size_t moe_bucket_workspace_size(int N, int top_k, int E) {
+    if (!shape_ok(N, QK, E, top_k)) return 0;
+    return moe::BUCKET_SCRATCH_OFFSET + moe::bucket_scratch_bytes(N, E);
+}
+
 int moe_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart, int32_t *expTokI,
                int32_t *expTokK, void *ws, size_t ws_bytes, cudaStream_t stream) {
     if (!topk_idx || !expStart || !expTokI || !expTokK || !ws) return MOE_ERR_INVALID_ARG;
     if (!shape_ok(N, QK, E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (ws_bytes < 256) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    return launch_bucket(topk_idx, N, top_k, E, expStart, expTokI, expTokK, status_word(ws), stream);
+    if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_bucket_workspace_size(N, top_k, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return launch_bucket(topk_idx, N, top_k, E, expStart, expTokI, expTokK, ws, stream);
 }
 
 int moe_grouped_ffn_ex(moe_weights_t w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
@@ -402,8 +409,7 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
     // on the tensor path the bucketing kernel also writes the GEMMs' plan
     const bool tensor = (p == MOE_PATH_TENSOR);
     if (!rc)
-        rc = launch_bucket(idx, N, top_k, E, es, ti, tk, status_word(ws), stream, tensor ? ws : nullptr,
-                           tensor ? &L : nullptr, shout != nullptr);
+        rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr);
     mark(2);
     if (tensor) {
         const bool with_shared = shout != nullptr;

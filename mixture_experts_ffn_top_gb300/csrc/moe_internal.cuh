@@ -89,10 +89,16 @@ int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int no
                             float *w, cudaStream_t s);
 int launch_quantize_q8_1(const float *x, int64_t nblk, int8_t *q, float *d, cudaStream_t s);
 // bucket.cu
-// plan_ws/L non-null: also write the tensor path's plan into plan_ws (layout L)
-int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart,
-                  int32_t *expTokI, int32_t *expTokK, unsigned *status, cudaStream_t s,
-                  void *plan_ws = nullptr, const WsLayout *L = nullptr, bool with_shared = false);
+// ws: the workspace (status word at 0, the grid barrier's two words at BUCKET_BARRIER_OFFSET
+// and +64, the per-range count table at BUCKET_SCRATCH_OFFSET, bucket_scratch_bytes long).
+// L non-null: also write the tensor path's plan into ws (layout L).
+constexpr size_t BUCKET_BARRIER_OFFSET = 64;
+constexpr size_t BUCKET_SCRATCH_OFFSET = 256;
+constexpr int BUCKET_TABLE_MAX = 65536;  // ints in the ranges x experts count table
+int bucket_grid(int N, int E, int *range_out);
+size_t bucket_scratch_bytes(int N, int E);
+int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart, int32_t *expTokI,
+                  int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L = nullptr, bool with_shared = false);
 // expert_matvec.cu
 int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
                           const int8_t *x_q, const float *x_d, const int32_t *expStart,

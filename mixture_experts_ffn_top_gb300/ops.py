@@ -40,6 +40,7 @@ _SIGS = {
     "moe_router_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_topk_from_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_quantize_q8_1": (_I, [_P, _I64, _P, _P, _P]),
+    "moe_bucket_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_bucket": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),

@@ -69,6 +69,19 @@ def test_workspace_size_rules(lib):
     assert f(16, 2048, 64, 1024, 33, 0) == 0        # top_k > 32
 
 
+def test_bucket_workspace_size(lib):
+    f = lib.moe_bucket_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    assert f(2048, 8, 64) > 256                     # status block + count table
+    assert f(2048, 8, 1024) >= f(2048, 8, 64)
+    assert f(0, 8, 64) == 0 and f(16, 33, 64) == 0 and f(16, 8, 4) == 0
+    full = lib.moe_ffn_workspace_size
+    full.restype = ctypes.c_size_t
+    for N, E, k in [(2048, 64, 8), (512, 256, 8), (40000, 64, 8), (20000, 1024, 2)]:
+        assert full(N, 2048, E, 1024, k, 0) >= f(N, k, E)
+
+
 def test_null_arguments_rejected_before_any_cuda_call(lib):
     V = ctypes.c_void_p
     lib.moe_combine.argtypes = [V, V, V, ctypes.c_int, ctypes.c_int, ctypes.c_int, V, V]

@@ -164,7 +164,7 @@ def test_bucket_bit_exact(ops, name):
 
 
 @pytest.mark.parametrize("N,E,k", [(1, 8, 2), (3, 8, 8), (1025, 64, 8), (4096, 128, 8), (2500, 1024, 32),
-                                   (7, 1, 1)])
+                                   (7, 1, 1), (40000, 64, 8), (20000, 1024, 2)])
 def test_bucket_random_shapes(ops, N, E, k):
     rng = np.random.default_rng(N + E + k)
     idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
@@ -192,6 +192,26 @@ def test_bucket_flags_bad_routing(ops, bad):
     assert word & 0x1
     assert np.all(es.cpu().numpy() == 0)  # every segment left empty
     assert ops.moe_workspace_status(ws) == 0  # cleared
+
+
+def test_bucket_flags_bad_routing_in_a_late_range(ops):
+    # many CTAs: the bad entry sits in the last token range, far from CTA 0
+    N, E, k = 5000, 64, 8
+    rng = np.random.default_rng(7)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    idx[N - 1, 3] = idx[N - 1, 0]
+    ws = ops.new_workspace(N, 64, E, 64, k)
+    es, ti, tk = ops.moe_bucket(dev(idx), E, ws)
+    assert ops.moe_workspace_status(ws) & 0x1
+    assert np.all(es.cpu().numpy() == 0)
+    # the barrier words are back at rest: a clean call on the same workspace works
+    idx[N - 1, 3] = (idx[N - 1, 0] + E // 2) % E if (idx[N - 1, 0] + E // 2) % E not in idx[N - 1] else \
+        next(e for e in range(E) if e not in idx[N - 1])
+    es, ti, tk = ops.moe_bucket(dev(idx), E, ws)
+    assert ops.moe_workspace_status(ws) == 0
+    res, rti, rtk = O.bucket(idx, E)
+    np.testing.assert_array_equal(es.cpu().numpy(), res)
+    np.testing.assert_array_equal(ti.cpu().numpy(), rti)
 
 
 # ------------------------------------------------------ grouped experts ---
