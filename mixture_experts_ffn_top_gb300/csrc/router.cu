@@ -93,18 +93,28 @@ router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__
         const bool more = k0 + RB_K < k_end;
         if (more) fetch(k0 + RB_K);  // in flight during this chunk's math
         if (quantise) {
-            // Q8_1 of this K chunk (one block) for the tile's tokens: warp w takes 8 tokens
+            // Q8_1 of this K chunk (one block) for the tile's tokens: warp w takes 8 tokens, one
+            // warp reduction per token for the block maximum; the two IEEE divisions of the rule
+            // (d = amax/127, then 1/d) run once for the 8 tokens side by side in lanes 0-7
             const int warp = tid >> 5, lane = tid & 31;
+            constexpr int RPW = RB_M / 8;  // rows per warp
+            float xv[RPW];
+            unsigned amax_mine = 0;
 #pragma unroll
-            for (int rr = 0; rr < RB_M / 8; ++rr) {
-                const int row = warp * (RB_M / 8) + rr;
-                const int t = t0 + row;
-                float d16f;
-                const int q = q8_quantize_lane(Xs[b][lane][row], &d16f);
-                if (t < N) {
-                    x_q[(size_t)t * D + k0 + lane] = (int8_t)q;
-                    if (lane == 0) x_d[(size_t)t * (D / QK) + k0 / QK] = d16f;
-                }
+            for (int rr = 0; rr < RPW; ++rr) {
+                xv[rr] = Xs[b][lane][warp * RPW + rr];
+                const unsigned am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(xv[rr])));
+                if (lane == rr) amax_mine = am;
+            }
+            const float d = __fdiv_rn(__uint_as_float(amax_mine), 127.0f);
+            const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+            if (lane < RPW && t0 + warp * RPW + lane < N)
+                x_d[(size_t)(t0 + warp * RPW + lane) * (D / QK) + k0 / QK] = __half2float(__float2half_rn(d));
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+                const int t = t0 + warp * RPW + rr;
+                const float idr = __shfl_sync(0xffffffffu, id, rr);
+                if (t < N) x_q[(size_t)t * D + k0 + lane] = (int8_t)(int)roundf(__fmul_rn(xv[rr], idr));
             }
         }
 #pragma unroll 8
@@ -148,8 +158,17 @@ softmax_topk_kernel(const float *__restrict__ part, int nsplit, int N, int E, in
         int e = lane + 32 * i;
         float v = -INFINITY;
         if (e < E) {
-            v = part[(size_t)t * Eext + e];
-            for (int s = 1; s < nsplit; ++s) v = __fadd_rn(v, part[((size_t)s * N + t) * Eext + e]);
+            // the split partials summed in split order; loads issued four at a time
+            const float *pp = part + (size_t)t * Eext + e;
+            const size_t stride = (size_t)N * Eext;
+            v = pp[0];
+            int s = 1;
+            for (; s + 4 <= nsplit; s += 4) {
+                const float a0 = pp[s * stride], a1 = pp[(s + 1) * stride], a2 = pp[(s + 2) * stride],
+                            a3 = pp[(s + 3) * stride];
+                v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a0), a1), a2), a3);
+            }
+            for (; s < nsplit; ++s) v = __fadd_rn(v, pp[s * stride]);
             if (logits_out) logits_out[(size_t)t * E + e] = v;
         }
         l[i] = v;
