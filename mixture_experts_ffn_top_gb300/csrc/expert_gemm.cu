@@ -50,10 +50,10 @@ namespace moe {
 namespace {
 
 constexpr int G_DRAIN_WARPS = 12;                 // 3 per SM sub-partition (128 registers each)
-constexpr int G_GROUPS = G_DRAIN_WARPS / 4;        // column groups of 32 token columns
 constexpr int G_ORCH_WARP = 2 + G_DRAIN_WARPS;    // warp that tells the MMA warp when a stage may go
-constexpr int G_THREADS = 96 + 32 * G_DRAIN_WARPS; // producer, MMA, drain warps, orchestrator
-constexpr int G_STAGES = 6;                        // weight + token tile ring (TMA -> MMA)
+constexpr int G_EPI_WARP = 3 + G_DRAIN_WARPS;     // warp that finishes each item from the hand-off buffer
+constexpr int G_THREADS = 128 + 32 * G_DRAIN_WARPS; // producer, MMA, drain warps, orchestrator, epilogue
+constexpr int G_STAGES = 5;                        // weight + token tile ring (TMA -> MMA)
 constexpr int G_SSTAGES = G_STAGES + 3;            // block-scale ring (TMA -> drain), one slot per stage
 constexpr int G_TMEM_BUFS = 5;                     // per-block accumulators in TMEM
 constexpr int G_BUF_COLS = TILE_N;                 // 96 fp32 columns per accumulator
@@ -62,10 +62,12 @@ constexpr int STAGE_A = 16384;                     // 128 weight rows x 128 B (6
 constexpr int STAGE_B = TILE_N * 128;              // up to 96 token rows x 128 B
 constexpr int STAGE_BYTES = STAGE_A + STAGE_B;
 constexpr int SSTAGE_BYTES = 2048;                 // [2][128] weight scales + [2][nb] token scales
-constexpr int XCH_STRIDE = 33;                     // padded row of the gate/up exchange (32 columns)
-constexpr int XCH_BYTES = G_GROUPS * 64 * XCH_STRIDE * 4;
+constexpr int HAND_STRIDE = 132;                   // floats per token column of the hand-off buffer (128 rows + pad)
+constexpr int HAND_BYTES = TILE_N * HAND_STRIDE * 4;
 constexpr int BAR_BYTES = 512;
-constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + XCH_BYTES + BAR_BYTES;
+constexpr int EPI_BYTES = TILE_N * 8;                // the epilogue warp's output rows and scales
+constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + HAND_BYTES + BAR_BYTES + EPI_BYTES;
+static_assert(G_SMEM <= 227 * 1024, "shared memory budget");
 static_assert(G_TMEM_BUFS * G_BUF_COLS <= G_TMEM_COLS, "TMEM ring exceeds the allocation");
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 // Scale slot reuse needs no barrier of its own.  The producer loads stage L once the MMAs of stage
@@ -267,8 +269,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     // the compiler still knows every derived pointer is shared memory (plain LDS/STS, not generic)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sring = smem + G_STAGES * STAGE_BYTES;
-    float *xch = reinterpret_cast<float *>(sring + G_SSTAGES * SSTAGE_BYTES);
-    uint8_t *bars = reinterpret_cast<uint8_t *>(xch) + XCH_BYTES;
+    // hand-off buffer: an item's accumulators, token column c at hand[c * HAND_STRIDE + row]
+    float *hand = reinterpret_cast<float *>(sring + G_SSTAGES * SSTAGE_BYTES);
+    uint8_t *bars = reinterpret_cast<uint8_t *>(hand) + HAND_BYTES;
+    int *epi_row = reinterpret_cast<int *>(bars + BAR_BYTES);  // [TILE_N] output row per column
+    float *epi_scale = reinterpret_cast<float *>(epi_row + TILE_N);  // [TILE_N] shared-expert scale
     const uint32_t bar_base = smem_u32(bars);
     int nb_ = 0;
     auto next_bar = [&](int n) {
@@ -278,7 +283,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     };
     const uint32_t full0 = next_bar(G_STAGES), empty0 = next_bar(G_STAGES);
     const uint32_t tfull0 = next_bar(G_TMEM_BUFS), tempty0 = next_bar(G_TMEM_BUFS);
-    const uint32_t xready0 = next_bar(G_GROUPS), xfree0 = next_bar(G_GROUPS);
+    const uint32_t hfull = next_bar(1), hempty = next_bar(1);
     const uint32_t done_bar = next_bar(1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * nb_);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -294,10 +299,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             mbar_init(tfull0 + 8 * b, 1);
             mbar_init(tempty0 + 8 * b, G_DRAIN_WARPS);
         }
-        for (int g = 0; g < G_GROUPS; ++g) {
-            mbar_init(xready0 + 8 * g, 4);
-            mbar_init(xfree0 + 8 * g, 4);
-        }
+        mbar_init(hfull, G_DRAIN_WARPS);  // every drain warp has stored its columns
+        mbar_init(hempty, 1);             // the epilogue warp is done with the buffer
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         *stages_ready = 0;
@@ -452,13 +455,111 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 }
             }
         }
+    } else if (warp == G_EPI_WARP) {
+        // -------------------------------------------------------- epilogue ---
+        uint32_t hphase = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Item x = item_at(p, it, n_rtiles);
+            // down: output row (and shared-expert scale) of columns lane, lane + 32, lane + 64,
+            // loaded before the wait so they land while the drain works on the item
+            int orow[3] = {-1, -1, -1};
+            float oscale[3] = {1.0f, 1.0f, 1.0f};
+            if (MODE == 1) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int col = lane + 32 * j;
+                    if (col < x.nrows) {
+                        if (x.shared) {
+                            orow[j] = x.entry0 + col;  // shared-expert rows map row i to token i
+                            oscale[j] = p.shexp_scale[orow[j]];
+                        } else {
+                            orow[j] = p.rowinfo[x.row0 + col].y;
+                        }
+                    }
+                }
+            }
+            ok = mbar_wait(hfull, hphase, abort_flag, p.status, p.wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (MODE == 0) {
+                // rows 0-63 hold gate, rows 64-127 up, of features mt*64 + (row & 63).  One lane
+                // per (token column, 32-feature block): SiLU(gate) * up of the block's 32 features,
+                // then the Q8_1 rule on them, 32 fp16 codes stored as one 64-byte run.
+                for (int fb = 0; fb < 2; ++fb) {
+                    for (int col = lane; col < x.nrows; col += 32) {
+                        const float *gcol = hand + col * HAND_STRIDE + 32 * fb;
+                        const float *ucol = gcol + 64;
+                        float hv[32];
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 g = *reinterpret_cast<const float4 *>(gcol + 4 * i4);
+                            const float4 u = *reinterpret_cast<const float4 *>(ucol + 4 * i4);
+                            hv[4 * i4 + 0] = swiglu(g.x, u.x);
+                            hv[4 * i4 + 1] = swiglu(g.y, u.y);
+                            hv[4 * i4 + 2] = swiglu(g.z, u.z);
+                            hv[4 * i4 + 3] = swiglu(g.w, u.w);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(hv[4 * i4 + k]));
+                        }
+                        const float d = __fdiv_rn(amax, 127.0f);
+                        const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+                        const int prow = x.row0 + col;
+                        const int f0 = x.mt * 64 + 32 * fb;
+                        p.h_dT[(size_t)(f0 >> 5) * p.rows_max + prow] = __half2float(__float2half_rn(d));
+                        __align__(16) __half2 hq[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            hq[i] = __halves2half2(__int2half_rn((int)roundf(__fmul_rn(hv[2 * i], id))),
+                                                   __int2half_rn((int)roundf(__fmul_rn(hv[2 * i + 1], id))));
+                        int4 *dst = reinterpret_cast<int4 *>(p.h16 + (size_t)prow * p.Fmax + f0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = reinterpret_cast<const int4 *>(hq)[i];
+                    }
+                }
+            } else {
+                // one token column at a time: its 128 output features, 4 per lane, one 512-byte row;
+                // four columns in flight per step
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int col = lane + 32 * j;
+                    if (col < TILE_N) {
+                        epi_row[col] = orow[j];
+                        epi_scale[col] = oscale[j];
+                    }
+                }
+                __syncwarp();
+                float *__restrict__ dstb = x.shared ? p.shared_out : p.partials;
+                for (int col = 0; col < x.nrows; col += 4) {
+                    float4 v[4];
+                    int o[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = min(col + u, TILE_N - 1);
+                        o[u] = col + u < x.nrows ? epi_row[c] : -1;
+                        v[u] = *reinterpret_cast<const float4 *>(hand + c * HAND_STRIDE + 4 * lane);
+                        if (x.shared) {
+                            const float sc = epi_scale[c];
+                            v[u] = make_float4(sc * v[u].x, sc * v[u].y, sc * v[u].z, sc * v[u].w);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (o[u] >= 0) *reinterpret_cast<float4 *>(dstb + (size_t)o[u] * p.D + x.mt * 128 + 4 * lane) = v[u];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(hempty);
+            hphase ^= 1;
+        }
     } else {
         // ------------------------------------------------------- drain ---
         const int q = warp & 3;              // TMEM lane quarter (= SM sub-partition) of this warp
         const int grp = (warp - 2) >> 2;     // column group: token columns 32*grp + [0, 32)
         const int r = q * 32 + lane;         // row of the 128-row weight tile
         int sstage = 0, buf = 0;
-        uint32_t tphase = 0, xphase = 0;
+        uint32_t tphase = 0, hphase = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item x = item_at(p, it, n_rtiles);
@@ -539,85 +640,21 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
             }
             tmem_wait_ld();  // no TMEM load outlives the loop, even when it was cut short
             if (!ok) break;
-            // --------------------------------------------------- epilogue ---
-            if (MODE == 0) {
-                // rows 0-63 hold gate, rows 64-127 up, of features mt*64 + (r & 63).  Gate warps
-                // finish the even columns of the group, up warps the odd ones: each side hands
-                // the other its accumulators for the other parity.
-                float *xg = xch + grp * 64 * XCH_STRIDE;
-                const int fr = r & 63;  // feature row within the tile
-                const bool is_gate = q < 2;
-                ok = mbar_wait(xfree0 + 8 * grp, xphase ^ 1, abort_flag, p.status, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
+            // ------------------------------------------------------ hand-off ---
+            // the epilogue warp finishes the item from shared memory while this warp moves on
+            ok = mbar_wait(hempty, hphase ^ 1, abort_flag, p.status, p.wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (active) {
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
-                    if (is_gate) xg[fr * XCH_STRIDE + 2 * m + 1] = acc[m].y;  // gate of an odd column
-                    else xg[fr * XCH_STRIDE + 2 * m] = acc[m].x;              // up of an even column
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xready0 + 8 * grp);
-                ok = mbar_wait(xready0 + 8 * grp, xphase, abort_flag, p.status, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                if (active) {
-                    // The warp's 32 lanes hold the 32 features of one Q8_1 block for each of its
-                    // 16 columns.  Block maxima come from one warp reduction per column; the two
-                    // IEEE divisions per block (d = amax/127, 1/d) then run once, for all 16
-                    // columns side by side in lanes 0-15, and 1/d is broadcast back per column.
-                    const int f = x.mt * 64 + fr;
-                    const int fblk = f >> 5;
-                    const int par = is_gate ? 0 : 1;  // this warp's column parity
-                    float hv[16];
-                    unsigned amax_mine = 0;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        const int cl = 2 * m + par;
-                        const float other = xg[fr * XCH_STRIDE + cl];
-                        hv[m] = is_gate ? swiglu(acc[m].x, other) : swiglu(other, acc[m].y);
-                        const unsigned am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[m])));
-                        if (lane == m) amax_mine = am;
-                    }
-                    const float d = __fdiv_rn(__uint_as_float(amax_mine), 127.0f);
-                    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-                    const int my_col = c0 + 2 * lane + par;  // column whose scale this lane holds
-                    if (lane < 16 && my_col < x.nrows)
-                        p.h_dT[(size_t)fblk * p.rows_max + x.row0 + my_col] = __half2float(__float2half_rn(d));
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        const int col = c0 + 2 * m + par;
-                        const float idm = __shfl_sync(0xffffffffu, id, m);
-                        if (col >= x.nrows) break;  // warp-uniform
-                        const int qv = (int)roundf(__fmul_rn(hv[m], idm));
-                        p.h16[(size_t)(x.row0 + col) * p.Fmax + f] = __int2half_rn(qv);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xfree0 + 8 * grp);
-                xphase ^= 1;
-            } else if (active) {
-                const int dcol = x.mt * 128 + r;  // output column
-                // lane L fetches the output row (and shared scale) of column c0 + L: one coalesced
-                // load instead of 32 dependent ones, then broadcast per column
-                const int my_col = c0 + lane;
-                int my_orow = -1;
-                float my_scale = 1.0f;
-                if (my_col < x.nrows) {
-                    my_orow = p.rowinfo[x.row0 + my_col].y;
-                    if (x.shared && my_orow >= 0) my_scale = p.shexp_scale[my_orow];
-                }
-                float *__restrict__ dst = x.shared ? p.shared_out : p.partials;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const float val = e2 ? acc[m].y : acc[m].x;
-                        const int orow = __shfl_sync(0xffffffffu, my_orow, 2 * m + e2);
-                        const float sc = __shfl_sync(0xffffffffu, my_scale, 2 * m + e2);
-                        if (orow >= 0) dst[(size_t)orow * p.D + dcol] = x.shared ? sc * val : val;
-                    }
+                    hand[(c0 + 2 * m) * HAND_STRIDE + r] = acc[m].x;
+                    hand[(c0 + 2 * m + 1) * HAND_STRIDE + r] = acc[m].y;
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(hfull);
+            hphase ^= 1;
         }
     }
     tc_fence_before();
