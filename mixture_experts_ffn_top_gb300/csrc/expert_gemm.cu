@@ -763,61 +763,75 @@ plan_kernel(const int32_t *__restrict__ expStart, const int32_t *__restrict__ ex
 }
 
 // Gather the Q8_1 rows of x into the padded segment order as exact fp16
-// integers, and their block scales transposed ([D/32][rows]).  A CTA owns 32
-// padded rows: their source tokens are read once, then every thread issues its
-// 16-byte row pieces back to back (many loads in flight); pad rows are zero.
+// integers, and their block scales transposed ([D/32][rows]).  A CTA owns
+// GATHER_ROWS padded rows (one wave of CTAs for the OLMoE shape); a warp takes
+// two of them.  Each lane turns 8 int8 codes into 8 fp16 values per step, so a
+// warp reads 256 contiguous bytes and writes 512; all of a row pair's loads are
+// issued before the first store.  Pad rows are zero.
+constexpr int GATHER_ROWS = 16;
+constexpr int GATHER_UNR = 8;
+// 4 signed bytes -> 4 fp16 integers: the byte b + 128 goes into the mantissa of 1024
+// (0x6400 | (b ^ 0x80) is the fp16 value 1152 + b), then 1152 is subtracted; exact for
+// every int8, since fp16 spaces the integers of [1024, 2048) one apart.
+__device__ __forceinline__ uint2 i8x4_to_h16x4(uint32_t v) {
+    const uint32_t u = v ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(u, 0x64646464u, 0x5140);  // bytes 0, 1 over 0x64 high halves
+    const uint32_t hi = __byte_perm(u, 0x64646464u, 0x7362);  // bytes 2, 3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    const __half2 a = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
+    const __half2 b = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+}
+
 __global__ void __launch_bounds__(256)
 gather_kernel(const int8_t *__restrict__ x_q, const float *__restrict__ x_d, int D, const PlanHeader *hdr,
               const int4 *__restrict__ rowinfo, int rows_max, __half *__restrict__ xg16, float *__restrict__ xg_dT) {
-    __shared__ int src[32];
-    const int row0 = blockIdx.x * 32;
+    __shared__ int src[GATHER_ROWS];
+    const int row0 = blockIdx.x * GATHER_ROWS;
     const int nrows = hdr->n_rows;
     if (row0 >= nrows) return;
-    if (threadIdx.x < 32) {
+    if (threadIdx.x < GATHER_ROWS) {
         const int prow = row0 + threadIdx.x;
         src[threadIdx.x] = prow < nrows ? rowinfo[prow].x : -1;
     }
     __syncthreads();
-    const int pieces = D / 16;  // 16 int8 -> 16 fp16 per piece
-    const int total = 32 * pieces;
-    constexpr int UNR = 4;
-    for (int base = threadIdx.x; base < total; base += 256 * UNR) {
-        int4 v[UNR];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n8 = D / 8;  // 8-code pieces per row
+    const int ra = 2 * warp, rb = 2 * warp + 1;
+    const int ta = row0 + ra < nrows ? src[ra] : -2, tb = row0 + rb < nrows ? src[rb] : -2;  // -2: past the rows
+    for (int c0 = lane; c0 < n8; c0 += 32 * GATHER_UNR) {
+        uint2 va[GATHER_UNR], vb[GATHER_UNR];
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int i = base + u * 256;
-            v[u] = make_int4(0, 0, 0, 0);
-            if (i < total) {
-                const int rr = i / pieces, c = i - rr * pieces;
-                const int t = src[rr];
-                if (t >= 0 && row0 + rr < nrows) v[u] = *reinterpret_cast<const int4 *>(x_q + (size_t)t * D + c * 16);
+        for (int u = 0; u < GATHER_UNR; ++u) {
+            const int c = c0 + 32 * u;
+            va[u] = (ta >= 0 && c < n8) ? reinterpret_cast<const uint2 *>(x_q + (size_t)ta * D)[c] : make_uint2(0, 0);
+            vb[u] = (tb >= 0 && c < n8) ? reinterpret_cast<const uint2 *>(x_q + (size_t)tb * D)[c] : make_uint2(0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < GATHER_UNR; ++u) {
+            const int c = c0 + 32 * u;
+            if (c >= n8) break;
+            if (ta != -2) {
+                const uint2 a = i8x4_to_h16x4(va[u].x), b = i8x4_to_h16x4(va[u].y);
+                reinterpret_cast<uint4 *>(xg16 + (size_t)(row0 + ra) * D)[c] = make_uint4(a.x, a.y, b.x, b.y);
+            }
+            if (tb != -2) {
+                const uint2 a = i8x4_to_h16x4(vb[u].x), b = i8x4_to_h16x4(vb[u].y);
+                reinterpret_cast<uint4 *>(xg16 + (size_t)(row0 + rb) * D)[c] = make_uint4(a.x, a.y, b.x, b.y);
             }
         }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int i = base + u * 256;
-            if (i >= total) continue;
-            const int rr = i / pieces, c = i - rr * pieces;
-            if (row0 + rr >= nrows) continue;
-            const int8_t *b = reinterpret_cast<const int8_t *>(&v[u]);
-            __align__(16) __half2 o[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] = __halves2half2(__short2half_rn(b[2 * k]), __short2half_rn(b[2 * k + 1]));
-            __half *dst = xg16 + (size_t)(row0 + rr) * D + c * 16;
-            *reinterpret_cast<int4 *>(dst) = *reinterpret_cast<const int4 *>(&o[0]);
-            *reinterpret_cast<int4 *>(dst + 8) = *reinterpret_cast<const int4 *>(&o[4]);
-        }
     }
-    // scales: lane = row, warps stride over blocks (coalesced 128-byte rows of xg_dT)
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // scales: 16 consecutive rows of one block per half warp (64-byte runs of xg_dT)
     const int nblk = D / QK;
-    const int prow = row0 + lane;
-    const int t = src[lane];
-    for (int b = warp; b < nblk; b += 8) {
+    const int rr = threadIdx.x & (GATHER_ROWS - 1);
+    const int prow = row0 + rr;
+    const int t = src[rr];
+    for (int b = threadIdx.x / GATHER_ROWS; b < nblk; b += 256 / GATHER_ROWS) {
         const float d = (t >= 0 && prow < nrows) ? x_d[(size_t)t * nblk + b] : 0.0f;
         if (prow < rows_max) xg_dT[(size_t)b * rows_max + prow] = d;
     }
 }
+static_assert(2 * (256 / 32) == GATHER_ROWS, "two rows per warp");
 
 // h (fp16 codes + transposed scales, padded order) -> int8 + fp32 scales in CSR entry order.
 __global__ void h16_to_q8_kernel(const __half *__restrict__ h16, const float *__restrict__ h_dT, int F, int Fmax,
@@ -1022,7 +1036,7 @@ int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const floa
         rc = launch_status();
     }
     if (rc || x_q == nullptr) return rc;
-    gather_kernel<<<(L.rows_max + 31) / 32, 256, 0, s>>>(x_q, x_d, w->D, hdr, ws_ptr<int4>(ws, L.rowinfo), L.rows_max,
+    gather_kernel<<<(L.rows_max + GATHER_ROWS - 1) / GATHER_ROWS, 256, 0, s>>>(x_q, x_d, w->D, hdr, ws_ptr<int4>(ws, L.rowinfo), L.rows_max,
                                                          ws_ptr<__half>(ws, L.xg16), ws_ptr<float>(ws, L.xg_dT));
     return launch_status();
 }

@@ -116,6 +116,34 @@ def test_router_parity(ops, name):
         np.testing.assert_allclose(r["shexp_scale"].cpu().numpy(), ref["shexp_scale"], rtol=1e-5, atol=1e-7)
 
 
+@pytest.mark.parametrize("N,D,E,k,Fs,norm", [
+    (1100, 512, 48, 6, 32, True),    # ragged last token tile, shared gate row
+    (1024, 2048, 64, 8, 0, False),   # one full expert tile
+    (1040, 256, 33, 3, 0, True),     # one expert past a 32-wide lane group
+])
+def test_router_ragged_shapes(ops, N, D, E, k, Fs, norm):
+    """Router, routing and Q8_1 of x on shapes with ragged token and expert tiles."""
+    wl, inp = _random_layer(N, D, E, k, 32, Fs, norm, seed=N + E)
+    ws = new_ws(ops, wl)
+    gate = None if inp["shexp_gate"] is None else dev(inp["shexp_gate"])
+    r = ops.moe_router_topk(dev(inp["hidden"]), dev(inp["routerW"]), gate, k, norm, ws, want_logits=True)
+    assert ops.moe_workspace_status(ws) == 0
+    ref_logits = O.router_logits(inp["hidden"], inp["routerW"])
+    tol = logit_tol(ref_logits)
+    assert np.all(np.abs(r["logits"].cpu().numpy() - ref_logits) <= tol[:, None])
+    ridx, rw, _ = O.softmax_topk(ref_logits, k, norm)
+    clear = clear_tokens(ref_logits, k)
+    assert clear.mean() > 0.9
+    np.testing.assert_array_equal(r["topk_idx"].cpu().numpy()[clear], ridx[clear])
+    np.testing.assert_allclose(r["topk_w"].cpu().numpy()[clear], rw[clear], rtol=W_RTOL, atol=1e-7)
+    xq, xd16, _ = O.quantize_q8_1(inp["hidden"])
+    np.testing.assert_array_equal(r["x_q"].cpu().numpy(), xq)
+    np.testing.assert_array_equal(r["x_d"].cpu().numpy(), O.halves(xd16))
+    if Fs:
+        g = O.router_logits(inp["hidden"], inp["shexp_gate"].reshape(1, D))[:, 0]
+        np.testing.assert_allclose(r["shexp_scale"].cpu().numpy(), O.sigmoid(g), rtol=1e-5, atol=1e-7)
+
+
 @pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared", "skewed"])
 def test_topk_from_oracle_logits_bit_exact(ops, name):
     """Given the oracle's logits, every token's routing is identical (ties to the lower index)."""
