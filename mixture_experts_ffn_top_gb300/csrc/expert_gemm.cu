@@ -15,26 +15,34 @@
 // drain warps read it (tcgen05.ld), scale it by d_w (per TMEM lane = weight
 // row) * d_x (per column = token) and accumulate in registers.
 //
-// Roles (576 threads, one CTA per SM, persistent over work items):
+// Roles (512 threads, one CTA per SM, persistent over work items):
 //   warp 0      TMA producer: per stage (64 K = 2 blocks) the weight tile
 //               [128 rows x 64] fp16 and the token tile [nb rows x 64] fp16
-//               (nb = 16/32/64/128, the smallest box that holds the tile's
-//               rows) into the tile ring, both tiles' block scales into the
-//               scale ring.
+//               (nb = 16/32/64/96, the smallest box that holds the tile's
+//               rows) into the 5-slot tile ring, both tiles' block scales into
+//               the 8-slot scale ring, one mbarrier per stage.
 //   warp 1      TMEM owner and MMA issuer: 2 x (M128 x N x K16) per block into
-//               one of 4 TMEM accumulators of 128 columns; a tile-ring slot is
-//               released by the commit of the MMAs that read it.
-//   warps 2-17  drain, 4 per SM sub-partition: warp w reads TMEM lanes
-//               32*(w%4).. (the hardware's lane-quarter rule); the four warps
-//               of column group g take columns 32i + 8g + [0, 8), so ragged
-//               tiles stay balanced.  The scaling runs on packed f32x2 math.
-//               Epilogue: gate/up tiles hold 64 gate rows and the 64 up rows of
-//               the same features (weights repacked that way); gate and up
-//               warps swap half of their columns through shared memory, each
-//               forms h = SiLU(g) * u for its half and requantises it to Q8_1
-//               per 32 features (one warp = one block); down tiles scatter fp32
-//               rows to partials[t*top_k + slot] (or s_t * y to the shared
-//               expert's output).
+//               one of 5 TMEM accumulators of 96 columns; a tile-ring slot is
+//               released by the commit of the MMAs that read it.  It starts a
+//               stage when the orchestrator's stage count (a shared word it
+//               polls) says so.
+//   warps 2-13  drain, 3 per SM sub-partition: warp w reads TMEM lanes
+//               32*(w%4).. (the hardware's lane-quarter rule) and token
+//               columns 32*((w-2)/4) + [0, 32).  Per stage one wait for the
+//               second block's commit, both TMEM loads, the two slots handed
+//               back, then the scale math of both blocks on packed f32x2 math.
+//               At the end of an item the fp32 accumulators go to a shared
+//               hand-off buffer.
+//   warp 14     orchestrator: waits for a stage's copies and for the drain to
+//               hand back the TMEM slots the stage will write, then publishes
+//               the stage count to the MMA warp.
+//   warp 15     epilogue: finishes each item from the hand-off buffer while the
+//               drain moves on.  Gate/up tiles hold 64 gate rows and the 64 up
+//               rows of the same features (weights repacked that way): one lane
+//               per (token column, 32-feature block) forms h = SiLU(g) * u,
+//               requantises it to Q8_1 and stores 32 fp16 codes; down tiles
+//               store fp32 rows to partials[t*top_k + slot] (or s_t * y to the
+//               shared expert's output).
 // Every wait on an mbarrier is bounded (a few seconds); on expiry the CTA sets
 // MOE_DEV_TIMEOUT in the status word, every role drains out, in-flight copies
 // and MMAs are waited for (bounded) and TMEM is freed before returning.
@@ -169,6 +177,16 @@ __device__ __forceinline__ int ld_acquire_shared(const int *p) {
 }
 __device__ __forceinline__ void st_release_shared(int *p, int v) {
     asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_evict_last(float *dst, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -531,6 +549,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 }
                 __syncwarp();
                 float *__restrict__ dstb = x.shared ? p.shared_out : p.partials;
+                // the combine reads these rows next: ask L2 to keep them over the streamed weights
+                const uint64_t keep = l2_evict_last_policy();
                 for (int col = 0; col < x.nrows; col += 4) {
                     float4 v[4];
                     int o[4];
@@ -546,7 +566,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     }
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        if (o[u] >= 0) *reinterpret_cast<float4 *>(dstb + (size_t)o[u] * p.D + x.mt * 128 + 4 * lane) = v[u];
+                        if (o[u] >= 0) st_evict_last(dstb + (size_t)o[u] * p.D + x.mt * 128 + 4 * lane, v[u], keep);
                 }
             }
             __syncwarp();
