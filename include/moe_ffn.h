@@ -292,6 +292,25 @@ int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *router
                        const float *shexp_gate, int N, int top_k, int norm_topk_prob, float *out,
                        int path, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_ffn_prefill_ex with hidden and out in HOST memory (the layer as a host
+ * program calls it).  No staging copies: the router reads the hidden rows and
+ * the combine writes the output rows in place over the host link (NVLink-C2C
+ * on Grace-Blackwell), so that traffic overlaps the two kernels' own work.
+ *   hidden_host [N][D] fp32, out_host [N][D] fp32: host memory the device can
+ *   address -- pinned (cudaHostAlloc, cudaHostRegister) on any system, or any
+ *   host allocation where the device reports pageable access through the host
+ *   page tables.  Device (or managed) memory, or unreachable host memory:
+ *   MOE_ERR_INVALID_ARG and nothing is launched.  routerW, shexp_gate, ws as
+ *   for moe_ffn_prefill (device memory).  The call is asynchronous like the
+ *   others: out_host holds the result once `stream` has reached the end of it. */
+int moe_ffn_prefill_host(moe_weights_t w, const float *hidden_host, const float *routerW,
+                         const float *shexp_gate, int N, int top_k, int norm_topk_prob,
+                         float *out_host, int path, void *ws, size_t ws_bytes, cudaStream_t stream);
+/* 1 when `p` is host memory the current device can address (what
+ * moe_ffn_prefill_host accepts), 0 otherwise (device or managed memory,
+ * NULL, or pageable memory on a system without host page-table access). */
+int moe_host_memory_addressable(const void *p);
+
 /* moe_ffn_prefill_ex that also records seven caller-created CUDA events on
  * `stream` around its stages, for measuring each kernel in place:
  *   [0] start, [1] after the router (+softmax/top-k/Q8_1), [2] after bucketing

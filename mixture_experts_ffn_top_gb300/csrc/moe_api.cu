@@ -1,6 +1,7 @@
 // moe_api.cu -- the C ABI (include/moe_ffn.h): argument checks, workspace
 // layout and the launch sequence of each entry point.  No entry point on the
-// hot path allocates, synchronises or touches host memory.
+// hot path allocates or synchronises; only moe_ffn_prefill_host's kernels touch
+// host memory (the caller's hidden and output rows, in place).
 #include <algorithm>
 #include <new>
 
@@ -447,6 +448,36 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
 int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
                        int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
                        cudaStream_t stream) {
+    return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
+                        nullptr);
+}
+
+// The device address of host memory the GPU can reach (pinned: its mapped address; unregistered:
+// itself, where the device walks the host page tables), or nullptr.
+static const void *host_view(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    if (a.type != cudaMemoryTypeUnregistered) return nullptr;
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev) != cudaSuccess)
+        return nullptr;
+    return pageable ? p : nullptr;
+}
+
+int moe_host_memory_addressable(const void *p) { return p != nullptr && host_view(p) != nullptr ? 1 : 0; }
+
+int moe_ffn_prefill_host(moe_weights_t w, const float *hidden_host, const float *routerW, const float *shexp_gate,
+                         int N, int top_k, int norm_topk_prob, float *out_host, int path, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (!hidden_host || !out_host) return MOE_ERR_INVALID_ARG;
+    const float *hidden = static_cast<const float *>(host_view(hidden_host));
+    float *out = static_cast<float *>(const_cast<void *>(host_view(out_host)));
+    if (!hidden || !out) return MOE_ERR_INVALID_ARG;
     return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
                         nullptr);
 }

@@ -52,6 +52,8 @@ _SIGS = {
     "moe_ffn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_ffn_prefill_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_ffn_prefill_timed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P, _P]),
+    "moe_ffn_prefill_host": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
+    "moe_host_memory_addressable": (_I, [_P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
 }
 
@@ -322,6 +324,35 @@ def moe_ffn_prefill(w: MoeWeights, hidden, routerW, shexp_gate, top_k, norm_topk
                                   _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     _check(rc, "moe_ffn_prefill")
     return out
+
+
+def _host(t: torch.Tensor, name: str):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous() or t.dtype != torch.float32:
+        raise ValueError(f"{name} must be a contiguous float32 tensor")
+    return _P(t.data_ptr())
+
+
+def moe_host_memory_addressable(t: torch.Tensor) -> bool:
+    """Whether the tensor's memory can be passed to moe_ffn_prefill_host (host memory the device reaches)."""
+    return bool(lib().moe_host_memory_addressable(_P(t.data_ptr())))
+
+
+def moe_ffn_prefill_host(w: MoeWeights, hidden_host, routerW, shexp_gate, top_k, norm_topk_prob, ws, out_host,
+                         path=MOE_PATH_AUTO, stream=None):
+    """moe_ffn_prefill with hidden and the output in host memory (pinned, or pageable where the device
+    walks the host page tables): the kernels read and write them in place.  Asynchronous: out_host is
+    complete once `stream` is."""
+    N = hidden_host.shape[0]
+    if tuple(out_host.shape) != (N, w.D):
+        raise ValueError("out_host must be [N, D]")
+    rc = lib().moe_ffn_prefill_host(w.handle, _host(hidden_host, "hidden_host"),
+                                    _dev(routerW, torch.float32, "routerW"), _dev(shexp_gate, torch.float32),
+                                    N, top_k, int(norm_topk_prob), _host(out_host, "out_host"), path,
+                                    _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check(rc, "moe_ffn_prefill_host")
+    return out_host
 
 
 PREFILL_STAGES = ["router", "bucket", "gather", "gate_up", "down", "combine"]

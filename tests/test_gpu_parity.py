@@ -398,6 +398,51 @@ def test_layer_edge_shapes(ops, N, D, E, k, F, Fs, norm):
         assert_out_close(out.cpu().numpy(), ref["out"], clear, what=f"edge N={N} E={E} k={k}")
 
 
+@pytest.mark.parametrize("name", ["tiny", "qwen3moe_shared"])
+def test_prefill_host_buffers_match_device_buffers(ops, name):
+    """The host-buffer entry point reads hidden and writes out in place: same kernels, same bits."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    want = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob).cpu().numpy()
+    h_host = torch.from_numpy(inp["hidden"]).pin_memory()
+    o_host = torch.full((wl.N, wl.D), float("nan"), dtype=torch.float32).pin_memory()
+    ops.moe_ffn_prefill_host(layer.w, h_host, layer.routerW, layer.shexp_gate, wl.top_k, wl.norm_topk_prob,
+                             layer.ws, o_host)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    np.testing.assert_array_equal(o_host.numpy(), want)
+    assert_out_close(o_host.numpy(), ref["out"], clear_tokens(ref["logits"], wl.top_k), what=f"{name} host buffers")
+
+
+def test_prefill_host_rejects_device_memory(ops):
+    wl, inp, _ = case("tiny")
+    layer = layer_for(ops, inp, wl)
+    h_dev = dev(inp["hidden"])
+    o_host = torch.empty((wl.N, wl.D), dtype=torch.float32).pin_memory()
+    assert not ops.moe_host_memory_addressable(h_dev)
+    rc = ops.lib().moe_ffn_prefill_host(layer.w.handle, ops._P(h_dev.data_ptr()), ops._P(layer.routerW.data_ptr()),
+                                        None, wl.N, wl.top_k, int(wl.norm_topk_prob), ops._P(o_host.data_ptr()), 0,
+                                        ops._P(layer.ws.data_ptr()), layer.ws.numel(),
+                                        ops._P(torch.cuda.current_stream().cuda_stream))
+    assert rc == -1
+
+
+def test_prefill_host_pageable_memory_where_addressable(ops):
+    """Pageable host memory works exactly where the device walks the host page tables."""
+    wl, inp, _ = case("tiny")
+    layer = layer_for(ops, inp, wl)
+    h_pg = torch.from_numpy(inp["hidden"].copy())
+    o_pg = torch.full((wl.N, wl.D), float("nan"), dtype=torch.float32)
+    if ops.moe_host_memory_addressable(h_pg) and ops.moe_host_memory_addressable(o_pg):
+        ops.moe_ffn_prefill_host(layer.w, h_pg, layer.routerW, None, wl.top_k, wl.norm_topk_prob, layer.ws, o_pg)
+        torch.cuda.synchronize()
+        want = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob).cpu().numpy()
+        np.testing.assert_array_equal(o_pg.numpy(), want)
+    else:
+        with pytest.raises(ops.MoeError):
+            ops.moe_ffn_prefill_host(layer.w, h_pg, layer.routerW, None, wl.top_k, wl.norm_topk_prob, layer.ws, o_pg)
+
+
 def test_zero_hidden_gives_zero(ops):
     wl, inp = _random_layer(16, 256, 8, 2, 128, 64, False, seed=5)
     inp["hidden"][:] = 0.0
