@@ -300,9 +300,10 @@ int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *router
  *   address -- pinned (cudaHostAlloc, cudaHostRegister) on any system, or any
  *   host allocation where the device reports pageable access through the host
  *   page tables.  Device (or managed) memory, or unreachable host memory:
- *   MOE_ERR_INVALID_ARG and nothing is launched.  routerW, shexp_gate, ws as
- *   for moe_ffn_prefill (device memory).  The call is asynchronous like the
- *   others: out_host holds the result once `stream` has reached the end of it. */
+ *   MOE_ERR_INVALID_ARG and nothing is launched.  out_host may not alias
+ *   hidden_host.  routerW, shexp_gate, ws as for moe_ffn_prefill (device
+ *   memory).  The call is asynchronous like the others: out_host holds the
+ *   result once `stream` has reached the end of it. */
 int moe_ffn_prefill_host(moe_weights_t w, const float *hidden_host, const float *routerW,
                          const float *shexp_gate, int N, int top_k, int norm_topk_prob,
                          float *out_host, int path, void *ws, size_t ws_bytes, cudaStream_t stream);
