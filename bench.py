@@ -134,30 +134,35 @@ class ClockSampler:
             self.proc.kill()
         if self._t:
             self._t.join(timeout=2)
-        inside = [ln for t, ln in self.lines if t_begin <= t <= t_end]
-        n_inside = len(inside)
-        if not inside:
-            before = [ln for t, ln in self.lines if t < t_begin][-1:]
-            after = [ln for t, ln in self.lines if t > t_end][:1]
-            inside = before + after
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in inside:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = max(mx, float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
-                "samples_in_window": n_inside}
+        return clock_summary(self.lines, t_begin, t_end)
+
+
+def clock_summary(lines, t_begin: float, t_end: float):
+    """Median SM clock, max clock and throttle reasons of the (time, csv line) samples taken inside
+    [t_begin, t_end]; when none fell inside (a window shorter than the sampling period), the last
+    sample before it and the first after it."""
+    inside = [ln for t, ln in lines if t_begin <= t <= t_end]
+    n_inside = len(inside)
+    if not inside:
+        inside = [ln for t, ln in lines if t < t_begin][-1:] + [ln for t, ln in lines if t > t_end][:1]
+    sm, mx, reasons = [], 0.0, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in inside:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx = max(mx, float(parts[1]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[4:8]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+            "samples_in_window": n_inside}
 
 
 def cpu_baseline(wl, inp, sample_tokens: int, min_seconds: float = 10.0, max_passes: int = 20):

@@ -63,3 +63,22 @@ def test_single_rank_keeps_workload_batch():
     assert bench.rank_hidden(wl, base, 0, 1) is base
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.job_throughput(1, 2048, 1.0) == 2048e3
+
+
+def test_clock_summary_window_and_reasons():
+    """bench.py's clock record: samples inside the timed window, or its two neighbours when the
+    window is shorter than the sampling period; throttle reasons read from the 'Active' columns."""
+    import bench
+    row = "{sm}, 2070, 900.0, 0x0, {hw}, Not Active, Not Active, {cap}"
+    lines = [(0.0, row.format(sm=1900, hw="Not Active", cap="Not Active")),
+             (1.0, row.format(sm=2070, hw="Not Active", cap="Active")),
+             (2.0, row.format(sm=2040, hw="Not Active", cap="Not Active")),
+             (3.0, row.format(sm=1500, hw="Active", cap="Not Active")),
+             (4.0, "garbage")]
+    c = bench.clock_summary(lines, 0.5, 2.5)
+    assert c == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2,
+                 "samples_in_window": 2}
+    c = bench.clock_summary(lines, 2.2, 2.4)  # no sample inside: the ones at 2.0 and 3.0
+    assert c["samples_in_window"] == 0 and c["samples"] == 2
+    assert c["sm_mhz"] == 1770.0 and c["reasons"] == ["hw_slowdown"]
+    assert bench.clock_summary([], 0.0, 1.0) is None
