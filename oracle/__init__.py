@@ -212,15 +212,22 @@ def shared_expert(sh_gate, sh_up, sh_down, xq, xd16, s):
     return S, hq, hd16
 
 
-def combine(partials, w, S=None):
+def combine(partials, w, S=None, R=None):
+    """Slot-order combine, then the shared row S; with a residual R also + R (the host combine's
+    (routed + shared) + resid)."""
     partials = _f32(partials)
     w = _f32(w)
     N, k = w.shape
     D = partials.shape[1]
     assert partials.shape[0] == N * k
     out = np.empty((N, D), np.float32)
-    _L().oracle_combine(_p(partials), _p(w), _p(None if S is None else _f32(S)), _I64(N), _I(k), _I(D),
-                        _p(out))
+    Sp = _p(None if S is None else _f32(S))
+    if R is None:
+        _L().oracle_combine(_p(partials), _p(w), Sp, _I64(N), _I(k), _I(D), _p(out))
+    else:
+        R = _f32(R)
+        assert R.shape == (N, D)
+        _L().oracle_combine_residual(_p(partials), _p(w), Sp, _p(R), _I64(N), _I(k), _I(D), _p(out))
     return out
 
 

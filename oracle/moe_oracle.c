@@ -443,6 +443,29 @@ void oracle_combine(const float *partials, const float *w, const float *S, int64
         }
 }
 
+/* ------------------------------------------------------------------------
+ * Combine with the residual add of the pages' host combine ("Carnice prefill
+ * toward llama.cpp 676 t/s", #388, "Dead ends": the per-layer combine is
+ * (routed + shared*scale) + resid): the combine above, then one more fp32 add
+ * of the residual row R[t]:
+ *   out[t,c] = (acc + S[t,c]) + R[t,c].
+ * ---------------------------------------------------------------------- */
+void oracle_combine_residual(const float *partials, const float *w, const float *S, const float *R, int64_t N,
+                             int k, int D, float *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < N; ++t)
+        for (int c = 0; c < D; ++c) {
+            float acc = 0.0f;
+            for (int s = 0; s < k; ++s)
+                acc = fmaf(w[t * k + s], partials[(t * k + s) * (int64_t)D + c], acc);
+            if (S)
+                acc = acc + S[t * D + c];
+            acc = acc + R[t * D + c];
+            out[t * D + c] = acc;
+        }
+}
+
 /* Threads the OpenMP runtime will use (reported beside oracle timings). */
 int oracle_num_threads(void)
 {

@@ -46,6 +46,10 @@ MUTATIONS = [
      "acc = acc + w[t * k + s] * partials[(t * k + s) * (int64_t)D + c];"),
     ("combine_reverse_order", "for (int s = 0; s < k; ++s)\n                acc = fmaf(w[t * k + s], partials[(t * k + s) * (int64_t)D + c], acc);",
      "for (int s = k - 1; s >= 0; --s)\n                acc = fmaf(w[t * k + s], partials[(t * k + s) * (int64_t)D + c], acc);"),
+    ("combine_residual_first",
+     "            if (S)\n                acc = acc + S[t * D + c];\n            acc = acc + R[t * D + c];",
+     "            acc = acc + R[t * D + c];\n            if (S)\n                acc = acc + S[t * D + c];"),
+    ("combine_residual_dropped", "            acc = acc + R[t * D + c];\n", ""),
     ("combine_shared_first", "            float acc = 0.0f;\n            for (int s = 0; s < k; ++s)",
      "            float acc = S ? S[t * D + c] : 0.0f;\n            if (S) S = S + 0 * c;\n            for (int s = 0; s < k; ++s)"),
 ]

@@ -438,6 +438,32 @@ def test_combine_adds_shared_after_slots():
     assert float(O.combine(p, w, S)[0, 0]) == 2.0 ** 24
 
 
+def test_combine_residual_zero_is_the_plain_combine():
+    rng = np.random.default_rng(15)
+    p = rng.standard_normal((3 * 4, 24)).astype(np.float32)
+    w = rng.random((3, 4)).astype(np.float32)
+    S = rng.standard_normal((3, 24)).astype(np.float32)
+    np.testing.assert_array_equal(O.combine(p, w, S, R=np.zeros((3, 24), np.float32)), O.combine(p, w, S))
+
+
+def test_combine_residual_single_slot_is_one_fp32_add():
+    """k = 1, w = 1, no shared row: out = partial + residual, one IEEE fp32 addition."""
+    rng = np.random.default_rng(16)
+    p = (rng.standard_normal((6, 32)) * 10.0 ** rng.integers(-6, 6, (6, 1))).astype(np.float32)
+    R = (rng.standard_normal((6, 32)) * 10.0 ** rng.integers(-6, 6, (6, 1))).astype(np.float32)
+    np.testing.assert_array_equal(O.combine(p, np.ones((6, 1), np.float32), R=R), p + R)
+
+
+def test_combine_residual_added_after_the_shared_row():
+    """(routed + shared) + resid: 1 + 2^-24 ties to even (1), then + 2^-23 is exact; adding the
+    residual first, or the two rows together first, ties the other way and gives 1 + 2^-22."""
+    p = np.array([[1.0]], np.float32)
+    w = np.ones((1, 1), np.float32)
+    S = np.array([[2.0 ** -24]], np.float32)
+    R = np.array([[2.0 ** -23]], np.float32)
+    assert float(O.combine(p, w, S, R)[0, 0]) == 1.0 + 2.0 ** -23
+
+
 # ---------------------------------------------------- regression fixture ---
 def test_tiny_layer_matches_recorded_fixture():
     """tests/golden/tiny_layer.json (written by tests/golden/make_golden.py from this oracle):
