@@ -321,6 +321,31 @@ def run_ours(args, rank, world, local_rank):
     if layer.status():
         raise RuntimeError("device status set during the e2e steps")
 
+    # the same layer with the residual add fused into its combine (out = residual + FFN(hidden)),
+    # device buffers, timed like the main steps
+    residual = torch.randn((N, D), dtype=torch.float32, device=device, generator=None)
+    res_out = torch.empty_like(residual)
+
+    def res_step():
+        ops.moe_ffn_prefill_residual(w, hidden, routerW, shg, residual, k, wl.norm_topk_prob, ws, out=res_out,
+                                     path=path)
+
+    for _ in range(max(1, args.warmup)):
+        res_step()
+    res_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        res_step()
+        e1.record(stream)
+        e1.synchronize()
+        res_ms.append(e0.elapsed_time(e1))
+    res_mean = max_over_ranks(statistics.mean(res_ms), device)
+    if layer.status():
+        raise RuntimeError("device status set during the residual steps")
+
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -366,6 +391,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": job_throughput(world, N, e2e_mean), "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
                 "d2h_bytes_per_step": N * D * 4, "ms_per_step": e2e_mean,
                 "api": "moe_ffn_prefill_host on pinned host buffers (read and written in place over the host link)"},
+        "with_residual": {"value": job_throughput(world, N, res_mean), "unit": UNIT, "ms_per_step": res_mean,
+                          "api": "moe_ffn_prefill_residual (residual add fused into the combine)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "wall_s_timed_region": t_wall,

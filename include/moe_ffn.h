@@ -276,6 +276,15 @@ int moe_debug_expert_wait_timeout(moe_weights_t w, const int8_t *x_q, const floa
  * ------------------------------------------------------------------------- */
 int moe_combine(const float *partials, const float *topk_w, const float *shared,
                 int N, int top_k, int D, float *out, cudaStream_t stream);
+/* moe_combine followed by the residual add of the pages' per-layer combine,
+ * (routed + shared) + resid ("Carnice prefill toward llama.cpp 676 t/s", #388,
+ * "Dead ends"): after the shared row, acc = acc + residual[t][c] (one fp32
+ * add), out[t][c] = acc.  residual [N][D] fp32, 16-byte aligned; it may be
+ * `out` itself (an in-place residual update), otherwise it may not overlap
+ * out.  residual == NULL is moe_combine. */
+int moe_combine_residual(const float *partials, const float *topk_w, const float *shared,
+                         const float *residual, int N, int top_k, int D, float *out,
+                         cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_ffn_prefill -- the whole layer in one call (all of the above, on one
@@ -291,6 +300,13 @@ int moe_ffn_prefill(moe_weights_t w, const float *hidden, const float *routerW,
 int moe_ffn_prefill_ex(moe_weights_t w, const float *hidden, const float *routerW,
                        const float *shexp_gate, int N, int top_k, int norm_topk_prob, float *out,
                        int path, void *ws, size_t ws_bytes, cudaStream_t stream);
+/* moe_ffn_prefill_ex whose combine also adds the residual row (moe_combine_residual):
+ * out = residual + FFN(hidden).  residual [N][D] fp32, non-NULL, 16-byte aligned;
+ * it may be `out` itself (the residual stream updated in place). */
+int moe_ffn_prefill_residual(moe_weights_t w, const float *hidden, const float *routerW,
+                             const float *shexp_gate, const float *residual, int N, int top_k,
+                             int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
 
 /* moe_ffn_prefill_ex with hidden and out in HOST memory (the layer as a host
  * program calls it).  No staging copies: the router reads the hidden rows and

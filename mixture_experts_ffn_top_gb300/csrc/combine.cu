@@ -4,6 +4,8 @@
 // launch over N x D.  The per-element order and rounding are fixed (one fused
 // multiply-add per slot, then one add), so the result is bit-reproducible:
 //   acc = +0; for s: acc = fma(w[t,s], partial[t*k+s], acc); acc += shared.
+// With a residual row (the pages' per-layer combine is (routed + shared) + resid,
+// "Carnice prefill toward llama.cpp 676 t/s", #388, "Dead ends") one more add: acc += resid.
 // HBM-bound: each thread owns 4 consecutive columns (16-byte loads/stores); for the
 // usual top_k the slot loads are all issued before the fma chain; partial rows are
 // streamed once (evict-first loads), the output is written once.
@@ -18,7 +20,7 @@ namespace {
 template <int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
-               const float4 *__restrict__ shared, int N, int k, int D4, float4 *__restrict__ out) {
+               const float4 *__restrict__ shared, const float4 *residual, int N, int k, int D4, float4 *out) {
     const int64_t total = (int64_t)N * D4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -57,14 +59,21 @@ combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
             acc.z = __fadd_rn(acc.z, sv.z);
             acc.w = __fadd_rn(acc.w, sv.w);
         }
+        if (residual != nullptr) {  // may be `out` itself: read before the write of the same element
+            const float4 rv = residual[i];
+            acc.x = __fadd_rn(acc.x, rv.x);
+            acc.y = __fadd_rn(acc.y, rv.y);
+            acc.z = __fadd_rn(acc.z, rv.z);
+            acc.w = __fadd_rn(acc.w, rv.w);
+        }
         out[i] = acc;
     }
 }
 
 }  // namespace
 
-int launch_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k,
-                   int D, float *out, cudaStream_t s) {
+int launch_combine(const float *partials, const float *topk_w, const float *shared, const float *residual, int N,
+                   int top_k, int D, float *out, cudaStream_t s) {
     const int D4 = D / 4;
     const int64_t total = (int64_t)N * D4;
     int64_t blocks = (total + 255) / 256;
@@ -73,15 +82,16 @@ int launch_combine(const float *partials, const float *topk_w, const float *shar
     if (blocks < 1) blocks = 1;
     const float4 *p4 = reinterpret_cast<const float4 *>(partials);
     const float4 *s4 = reinterpret_cast<const float4 *>(shared);
+    const float4 *r4 = reinterpret_cast<const float4 *>(residual);
     float4 *o4 = reinterpret_cast<float4 *>(out);
     const unsigned g = (unsigned)blocks;
     switch (top_k) {
-        case 1: combine_kernel<1><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
-        case 2: combine_kernel<2><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
-        case 4: combine_kernel<4><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
-        case 6: combine_kernel<6><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
-        case 8: combine_kernel<8><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
-        default: combine_kernel<0><<<g, 256, 0, s>>>(p4, topk_w, s4, N, top_k, D4, o4); break;
+        case 1: combine_kernel<1><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
+        case 2: combine_kernel<2><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
+        case 4: combine_kernel<4><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
+        case 6: combine_kernel<6><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
+        case 8: combine_kernel<8><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
+        default: combine_kernel<0><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
     }
     return launch_status();
 }

@@ -370,18 +370,25 @@ int moe_debug_expert_wait_timeout(moe_weights_t w, const int8_t *x_q, const floa
     return rc;
 }
 
-int moe_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k, int D, float *out,
-                cudaStream_t stream) {
+int moe_combine_residual(const float *partials, const float *topk_w, const float *shared, const float *residual,
+                         int N, int top_k, int D, float *out, cudaStream_t stream) {
     if (!partials || !topk_w || !out) return MOE_ERR_INVALID_ARG;
     if (N < 1 || top_k < 1 || D < 4 || D % 4) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (((uintptr_t)partials | (uintptr_t)out | (uintptr_t)shared) % 16) return MOE_ERR_INVALID_ARG;
-    return launch_combine(partials, topk_w, shared, N, top_k, D, out, stream);
+    if (((uintptr_t)partials | (uintptr_t)out | (uintptr_t)shared | (uintptr_t)residual) % 16)
+        return MOE_ERR_INVALID_ARG;
+    return launch_combine(partials, topk_w, shared, residual, N, top_k, D, out, stream);
+}
+
+int moe_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k, int D, float *out,
+                cudaStream_t stream) {
+    return moe_combine_residual(partials, topk_w, shared, nullptr, N, top_k, D, out, stream);
 }
 
 static int prefill_impl(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
                         int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
-                        cudaStream_t stream, cudaEvent_t *ev) {
+                        cudaStream_t stream, cudaEvent_t *ev, const float *residual = nullptr) {
     if (!w || !hidden || !routerW || !out) return MOE_ERR_INVALID_ARG;
+    if (residual && ((uintptr_t)residual % 16 || w->D % 4)) return MOE_ERR_INVALID_ARG;
     if (shexp_gate && w->Fs == 0) return MOE_ERR_INVALID_ARG;
     const int D = w->D, E = w->E;
     if (!shape_ok(N, D, E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -440,7 +447,7 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
                                     nullptr, N, top_k, sh, shout, st, stream);
         mark(5);
     }
-    if (!rc) rc = launch_combine(part, tw, shout, N, top_k, D, out, stream);
+    if (!rc) rc = launch_combine(part, tw, shout, residual, N, top_k, D, out, stream);
     mark(6);
     return rc;
 }
@@ -480,6 +487,14 @@ int moe_ffn_prefill_host(moe_weights_t w, const float *hidden_host, const float 
     if (!hidden || !out) return MOE_ERR_INVALID_ARG;
     return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
                         nullptr);
+}
+
+int moe_ffn_prefill_residual(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate,
+                             const float *residual, int N, int top_k, int norm_topk_prob, float *out, int path,
+                             void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!residual) return MOE_ERR_INVALID_ARG;
+    return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
+                        nullptr, residual);
 }
 
 int moe_ffn_prefill_timed(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,

@@ -109,7 +109,7 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &ws, bool is_shar
                        const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
                        const float *shexp_scale, float *out, unsigned *status, cudaStream_t s);
 // combine.cu
-int launch_combine(const float *partials, const float *topk_w, const float *shared, int N,
+int launch_combine(const float *partials, const float *topk_w, const float *shared, const float *residual, int N,
                    int top_k, int D, float *out, cudaStream_t s);
 // weights.cu
 int repack_weights(moe_weights_s *w, const void *gate, const void *up, const void *down,

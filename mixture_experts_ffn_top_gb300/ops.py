@@ -54,6 +54,8 @@ _SIGS = {
     "moe_ffn_prefill_timed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P, _P]),
     "moe_ffn_prefill_host": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_host_memory_addressable": (_I, [_P]),
+    "moe_combine_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_ffn_prefill_residual": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
 }
 
@@ -310,6 +312,33 @@ def moe_combine(partials, topk_w, shared=None, out=None, stream=None):
     _check(lib().moe_combine(_dev(partials, torch.float32, "partials"), _dev(topk_w, torch.float32, "topk_w"),
                              _dev(shared, torch.float32, "shared"), N, k, D, _dev(out, torch.float32, "out"),
                              _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_combine_residual(partials, topk_w, shared, residual, out=None, stream=None):
+    """moe_combine, then + residual (the per-layer combine's residual add).  out may be residual."""
+    N, k = topk_w.shape
+    D = partials.shape[1]
+    if out is None:
+        out = torch.empty((N, D), dtype=torch.float32, device=partials.device)
+    _check(lib().moe_combine_residual(_dev(partials, torch.float32, "partials"), _dev(topk_w, torch.float32, "topk_w"),
+                                      _dev(shared, torch.float32, "shared"), _dev(residual, torch.float32, "residual"),
+                                      N, k, D, _dev(out, torch.float32, "out"), _stream(stream)), "moe_combine_residual")
+    return out
+
+
+def moe_ffn_prefill_residual(w: MoeWeights, hidden, routerW, shexp_gate, residual, top_k, norm_topk_prob, ws,
+                             out=None, path=MOE_PATH_AUTO, stream=None):
+    """The layer with the residual add fused into its combine: out = residual + FFN(hidden)."""
+    N = hidden.shape[0]
+    if out is None:
+        out = torch.empty((N, w.D), dtype=torch.float32, device=hidden.device)
+    rc = lib().moe_ffn_prefill_residual(w.handle, _dev(hidden, torch.float32, "hidden"),
+                                        _dev(routerW, torch.float32, "routerW"), _dev(shexp_gate, torch.float32),
+                                        _dev(residual, torch.float32, "residual"), N, top_k, int(norm_topk_prob),
+                                        _dev(out, torch.float32, "out"), path, _dev(ws, torch.uint8, "ws"), ws.numel(),
+                                        _stream(stream))
+    _check(rc, "moe_ffn_prefill_residual")
     return out
 
 

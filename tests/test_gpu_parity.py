@@ -357,6 +357,52 @@ def test_combine_order_sensitive_values(ops):
     assert out[0, 0] == 2.0 ** 24 and out[1, 0] == 2.0 ** -11 + 2.0 ** -24 and out[2, 0] == 2.0 ** 24
 
 
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared"])
+def test_combine_residual_bit_exact(ops, name):
+    """(routed + shared) + resid against the oracle, out of place and in place (out = residual)."""
+    wl, inp, ref = case(name)
+    R = np.random.default_rng(31).standard_normal((wl.N, wl.D)).astype(np.float32)
+    S = dev(ref["shared_out"]) if wl.has_shared else None
+    want = O.combine(ref["partials"], ref["topk_w"], ref["shared_out"] if wl.has_shared else None, R)
+    out = ops.moe_combine_residual(dev(ref["partials"]), dev(ref["topk_w"]), S, dev(R))
+    np.testing.assert_array_equal(out.cpu().numpy(), want)
+    r_dev = dev(R)
+    ops.moe_combine_residual(dev(ref["partials"]), dev(ref["topk_w"]), S, r_dev, out=r_dev)
+    np.testing.assert_array_equal(r_dev.cpu().numpy(), want)
+
+
+def test_combine_residual_order_sensitive_values(ops):
+    """1 + 2^-24 ties to even before the residual 2^-23 is added: 1 + 2^-23, not 1 + 2^-22."""
+    p = np.zeros((2, 4), np.float32)
+    p[0, 0] = 1.0
+    w = np.ones((2, 1), np.float32)
+    S = np.zeros((2, 4), np.float32)
+    S[0, 0] = 2.0 ** -24
+    R = np.zeros((2, 4), np.float32)
+    R[0, 0] = 2.0 ** -23
+    R[1] = [1.0, -2.0, 3.5, -0.0]
+    out = ops.moe_combine_residual(dev(p), dev(w), dev(S), dev(R)).cpu().numpy()
+    np.testing.assert_array_equal(out, O.combine(p, w, S, R))
+    assert out[0, 0] == 1.0 + 2.0 ** -23
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3moe_shared", "olmoe"])
+def test_layer_with_residual(ops, name):
+    """moe_ffn_prefill_residual = the layer output plus the residual row, bit for bit, also in place."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    R = torch.from_numpy(np.random.default_rng(32).standard_normal((wl.N, wl.D)).astype(np.float32)).cuda()
+    plain = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob)
+    want = (plain + R).cpu().numpy()
+    got = ops.moe_ffn_prefill_residual(layer.w, dev(inp["hidden"]), layer.routerW, layer.shexp_gate, R, wl.top_k,
+                                       wl.norm_topk_prob, layer.ws)
+    assert layer.status() == 0
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+    ops.moe_ffn_prefill_residual(layer.w, dev(inp["hidden"]), layer.routerW, layer.shexp_gate, R, wl.top_k,
+                                 wl.norm_topk_prob, layer.ws, out=R)
+    np.testing.assert_array_equal(R.cpu().numpy(), want)
+
+
 # ---------------------------------------------------------- whole layer ---
 @pytest.mark.parametrize("name", CONFIGS)
 @pytest.mark.parametrize("path", [0, 1, 2])
