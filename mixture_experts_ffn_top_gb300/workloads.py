@@ -31,6 +31,16 @@ row-major along the reduction dimension.  Packing the weights is how the
 synthetic *inputs* are manufactured; both the oracle and the CUDA path take
 the resulting bytes as given.
 
+Workloads with ``wfmt="q4_k"`` deliver the same draws as GGUF Q4_K
+super-blocks instead (256 values in 144 bytes: fp16 d and dmin, twelve bytes
+of packed 6-bit sub-block scales and mins, 4-bit quants; value
+d*sc_j*q - dmin*m_j), the K-quant the pages name next to Q8_0 (#406
+references: "Q8_0/Q4_K MMQ").  The packer below picks, per 32-wide sub-block,
+the step (max - min)/15 and the offset -min (min clipped at 0), codes them
+against the super-block's fp16 d = max step/63 and dmin = max offset/63, then
+rounds every value to its 4-bit code; any valid encoding would do, since both
+sides decode the bytes.
+
 The pages ("batched int8-MMQ trunk prefill gated off for MoE", #406; "Carnice
 prefill toward llama.cpp 676 t/s", #388) benchmark whole models (OLMoE-1B-7B,
 a 35B-A3B hybrid) whose trained weights are not used here: these synthetic
@@ -47,6 +57,8 @@ import numpy as np
 
 QK = 32
 Q8_0_BYTES = 34
+QK_K = 256
+Q4_K_BYTES = 144
 
 
 @dataclass(frozen=True)
@@ -61,6 +73,7 @@ class Workload:
     norm_topk_prob: bool
     seed: int
     skew: bool = False
+    wfmt: str = "q8_0"  # expert weight format: "q8_0" or "q4_k"
 
     @property
     def has_shared(self) -> bool:
@@ -76,6 +89,8 @@ class Workload:
             s += f" shared_Fs={self.Fs}"
         if self.skew:
             s += " zipf_skew=1.2"
+        if self.wfmt != "q8_0":
+            s += f" weights={self.wfmt}"
         return s + f" seed={self.seed}"
 
 
@@ -89,7 +104,23 @@ WORKLOADS = {
                                 norm_topk_prob=True, seed=3),
     "skewed": Workload("skewed", N=4096, D=2048, E=128, top_k=8, F=768, Fs=0, norm_topk_prob=True,
                        seed=4, skew=True),
+    # the same layer family with Q4_K expert weights (D, F, Fs multiples of 256)
+    "tiny_q4k": Workload("tiny_q4k", N=64, D=256, E=8, top_k=2, F=256, Fs=0, norm_topk_prob=False, seed=0,
+                         wfmt="q4_k"),
+    "q4k_shared": Workload("q4k_shared", N=256, D=512, E=16, top_k=4, F=256, Fs=256, norm_topk_prob=True,
+                           seed=5, wfmt="q4_k"),
+    "olmoe_q4k": Workload("olmoe_q4k", N=2048, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False,
+                          seed=1, wfmt="q4_k"),
 }
+
+
+def row_bytes(wfmt: str, K: int) -> int:
+    """Bytes of one weight row of K values in the given block format."""
+    if wfmt == "q4_k":
+        assert K % QK_K == 0
+        return K // QK_K * Q4_K_BYTES
+    assert wfmt == "q8_0" and K % QK == 0
+    return K // QK * Q8_0_BYTES
 
 
 def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
@@ -115,22 +146,57 @@ def pack_q8_0(w: np.ndarray) -> np.ndarray:
     return out.reshape(rows, (K // QK) * Q8_0_BYTES)
 
 
-def _expert(seed: int, e: int, D: int, F: int):
+def pack_q4_k(w: np.ndarray) -> np.ndarray:
+    """Pack fp32 weights ``[rows, K]`` into GGUF Q4_K super-blocks ``uint8[rows, K/256*144]``."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, K = w.shape
+    assert K % QK_K == 0
+    nsb = K // QK_K
+    x = w.reshape(rows, nsb, 8, QK).astype(np.float64)
+    lo = np.minimum(x.min(axis=3), 0.0)
+    step = (x.max(axis=3) - lo) / 15.0
+    off = -lo
+    d16 = (step.max(axis=2) / 63.0).astype(np.float16)
+    dmin16 = (off.max(axis=2) / 63.0).astype(np.float16)
+    d = d16.astype(np.float64)[..., None]
+    dmin = dmin16.astype(np.float64)[..., None]
+    sc = np.where(d > 0, np.clip(np.rint(step / np.where(d > 0, d, 1.0)), 0, 63), 0).astype(np.uint8)
+    m = np.where(dmin > 0, np.clip(np.rint(off / np.where(dmin > 0, dmin, 1.0)), 0, 63), 0).astype(np.uint8)
+    qstep = (d * sc)[..., None]
+    qoff = (dmin * m)[..., None]
+    q = np.where(qstep > 0, np.clip(np.rint((x + qoff) / np.where(qstep > 0, qstep, 1.0)), 0, 15), 0)
+    q = q.astype(np.uint8)  # [rows, nsb, 8, 32]
+    out = np.zeros((rows, nsb, Q4_K_BYTES), np.uint8)
+    out[..., 0:2] = d16.view(np.uint8).reshape(rows, nsb, 2)
+    out[..., 2:4] = dmin16.view(np.uint8).reshape(rows, nsb, 2)
+    out[..., 4:8] = sc[..., 0:4] | ((sc[..., 4:8] >> 4) << 6)
+    out[..., 8:12] = m[..., 0:4] | ((m[..., 4:8] >> 4) << 6)
+    out[..., 12:16] = (sc[..., 4:8] & 15) | ((m[..., 4:8] & 15) << 4)
+    for g in range(4):
+        out[..., 16 + 32 * g:48 + 32 * g] = q[..., 2 * g, :] | (q[..., 2 * g + 1, :] << 4)
+    return out.reshape(rows, nsb * Q4_K_BYTES)
+
+
+def pack_weights(w: np.ndarray, wfmt: str) -> np.ndarray:
+    return pack_q4_k(w) if wfmt == "q4_k" else pack_q8_0(w)
+
+
+def _expert(seed: int, e: int, D: int, F: int, wfmt: str = "q8_0"):
     rng = np.random.default_rng([seed, 2, e])
-    g = pack_q8_0(_normal(rng, (F, D), 0.02))
-    u = pack_q8_0(_normal(rng, (F, D), 0.02))
-    d = pack_q8_0(_normal(rng, (D, F), 0.02))
+    g = pack_weights(_normal(rng, (F, D), 0.02), wfmt)
+    u = pack_weights(_normal(rng, (F, D), 0.02), wfmt)
+    d = pack_weights(_normal(rng, (D, F), 0.02), wfmt)
     return g, u, d
 
 
 @lru_cache(maxsize=8)
-def _experts(seed: int, E: int, D: int, F: int):
-    gate = np.empty((E, F, (D // QK) * Q8_0_BYTES), np.uint8)
+def _experts(seed: int, E: int, D: int, F: int, wfmt: str = "q8_0"):
+    gate = np.empty((E, F, row_bytes(wfmt, D)), np.uint8)
     up = np.empty_like(gate)
-    down = np.empty((E, D, (F // QK) * Q8_0_BYTES), np.uint8)
+    down = np.empty((E, D, row_bytes(wfmt, F)), np.uint8)
 
     def one(e):
-        gate[e], up[e], down[e] = _expert(seed, e, D, F)
+        gate[e], up[e], down[e] = _expert(seed, e, D, F, wfmt)
 
     with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
         list(ex.map(one, range(E)))
@@ -143,8 +209,9 @@ def make_inputs(wl: Workload) -> dict:
     """Draw one workload's inputs.  Returns numpy arrays:
 
     hidden f32[N,D], routerW f32[E,D], shexp_gate f32[D] or None,
-    gate/up u8[E,F,D/32*34], down u8[E,D,F/32*34],
-    sh_gate/sh_up u8[Fs,D/32*34], sh_down u8[D,Fs/32*34] (or None).
+    gate/up u8[E,F,row_bytes(D)], down u8[E,D,row_bytes(F)],
+    sh_gate/sh_up u8[Fs,row_bytes(D)], sh_down u8[D,row_bytes(Fs)] (or None),
+    wfmt: the block format of those byte rows ("q8_0": D/32*34 bytes, "q4_k": D/256*144).
     The expert arrays are shared read-only between calls with equal shapes.
     """
     N, D, E, F, Fs = wl.N, wl.D, wl.E, wl.F, wl.Fs
@@ -153,20 +220,20 @@ def make_inputs(wl: Workload) -> dict:
     rng = np.random.default_rng([wl.seed, 1])
     routerW = _normal(rng, (E, D), 1.0 / np.sqrt(D))
     shexp_gate = _normal(rng, (D,), 1.0 / np.sqrt(D)) if Fs else None
-    gate, up, down = _experts(wl.seed, E, D, F)
+    gate, up, down = _experts(wl.seed, E, D, F, wl.wfmt)
     sh_gate = sh_up = sh_down = None
     if Fs:
         srng = np.random.default_rng([wl.seed, 3])
-        sh_gate = pack_q8_0(_normal(srng, (Fs, D), 0.02))
-        sh_up = pack_q8_0(_normal(srng, (Fs, D), 0.02))
-        sh_down = pack_q8_0(_normal(srng, (D, Fs), 0.02))
+        sh_gate = pack_weights(_normal(srng, (Fs, D), 0.02), wl.wfmt)
+        sh_up = pack_weights(_normal(srng, (Fs, D), 0.02), wl.wfmt)
+        sh_down = pack_weights(_normal(srng, (D, Fs), 0.02), wl.wfmt)
     if wl.skew:
         perm = rng.permutation(E)
         bias = (1.5 * -1.2 * np.log(perm + 1.0)).astype(np.float32)
         hidden[:, D - 1] = 1.0
         routerW[:, D - 1] = bias
     return dict(hidden=hidden, routerW=routerW, shexp_gate=shexp_gate,
-                gate=gate, up=up, down=down, sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down)
+                gate=gate, up=up, down=down, sh_gate=sh_gate, sh_up=sh_up, sh_down=sh_down, wfmt=wl.wfmt)
 
 
 def make_hidden(wl: Workload, seed_offset: int = 0) -> np.ndarray:

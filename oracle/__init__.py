@@ -153,7 +153,33 @@ def block_dots(w_row: np.ndarray, aq: np.ndarray) -> np.ndarray:
     return out
 
 
-def expert_gate_up(Wg, Wu, D: int, F: int, xq, xd16):
+FORMATS = {"q8_0": 0, "q4_k": 1}  # weight formats the oracle reads (GGUF block layouts)
+
+
+def _fmt(fmt: str) -> int:
+    if fmt not in FORMATS:
+        raise ValueError(f"unknown weight format {fmt!r}")
+    return FORMATS[fmt]
+
+
+def block_dots_q4_k(w_row: np.ndarray, aq: np.ndarray) -> np.ndarray:
+    """int32 dots of a Q4_K row's 32-wide sub-blocks (quants 0..15) with an activation row."""
+    w_row = np.ascontiguousarray(w_row, dtype=np.uint8)
+    aq = np.ascontiguousarray(aq, dtype=np.int8)
+    out = np.empty(aq.size // QK, np.int32)
+    _L().oracle_block_dots_q4_k(_p(w_row), _p(aq), _I(aq.size), _p(out))
+    return out
+
+
+def q4_k_dequant(w_row: np.ndarray, K: int) -> np.ndarray:
+    """A Q4_K row decoded to K fp32 values (d*sc*q - dmin*m, rounded once)."""
+    w_row = np.ascontiguousarray(w_row, dtype=np.uint8)
+    out = np.empty(K, np.float32)
+    _L().oracle_q4_k_dequant(_p(w_row), _I(K), _p(out))
+    return out
+
+
+def expert_gate_up(Wg, Wu, D: int, F: int, xq, xd16, fmt: str = "q8_0"):
     """One activation row through one expert's gate/up half -> (h, hq, hd16, g, u)."""
     Wg = np.ascontiguousarray(Wg, np.uint8)
     Wu = np.ascontiguousarray(Wu, np.uint8)
@@ -164,21 +190,21 @@ def expert_gate_up(Wg, Wu, D: int, F: int, xq, xd16):
     hd16 = np.empty(F // QK, np.uint16)
     g = np.empty(F, np.float64)
     u = np.empty(F, np.float64)
-    _L().oracle_expert_gate_up(_p(Wg), _p(Wu), _I(D), _I(F), _p(xq), _p(xd16),
-                               _p(h), _p(hq), _p(hd16), _p(g), _p(u))
+    _L().oracle_expert_gate_up_fmt(_I(_fmt(fmt)), _p(Wg), _p(Wu), _I(D), _I(F), _p(xq), _p(xd16),
+                                   _p(h), _p(hq), _p(hd16), _p(g), _p(u))
     return h, hq, hd16, g, u
 
 
-def expert_down(Wd, D: int, F: int, hq, hd16) -> np.ndarray:
+def expert_down(Wd, D: int, F: int, hq, hd16, fmt: str = "q8_0") -> np.ndarray:
     Wd = np.ascontiguousarray(Wd, np.uint8)
     hq = np.ascontiguousarray(hq, np.int8)
     hd16 = np.ascontiguousarray(hd16, np.uint16)
     y = np.empty(D, np.float64)
-    _L().oracle_expert_down(_p(Wd), _I(D), _I(F), _p(hq), _p(hd16), _p(y))
+    _L().oracle_expert_down_fmt(_I(_fmt(fmt)), _p(Wd), _I(D), _I(F), _p(hq), _p(hd16), _p(y))
     return y
 
 
-def grouped_ffn(gate, up, down, xq, xd16, expStart, expTokI, expTokK, k: int):
+def grouped_ffn(gate, up, down, xq, xd16, expStart, expTokI, expTokK, k: int, fmt: str = "q8_0"):
     """Routed experts over the CSR -> (partials f32[N*k, D], hq int8[N*k, F], hd16 u16[N*k, F/32])."""
     E, F, _ = gate.shape
     D = down.shape[1]
@@ -187,7 +213,7 @@ def grouped_ffn(gate, up, down, xq, xd16, expStart, expTokI, expTokK, k: int):
     total = int(expStart[E])
     hq = np.zeros((max(total, 1), F), np.int8)
     hd16 = np.zeros((max(total, 1), F // QK), np.uint16)
-    _L().oracle_grouped_ffn(_p(np.ascontiguousarray(gate)), _p(np.ascontiguousarray(up)),
+    _L().oracle_grouped_ffn_fmt(_I(_fmt(fmt)), _p(np.ascontiguousarray(gate)), _p(np.ascontiguousarray(up)),
                             _p(np.ascontiguousarray(down)), _I(E), _I(D), _I(F),
                             _p(np.ascontiguousarray(xq)), _p(np.ascontiguousarray(xd16)),
                             _p(np.ascontiguousarray(expStart, np.int32)),
@@ -197,7 +223,7 @@ def grouped_ffn(gate, up, down, xq, xd16, expStart, expTokI, expTokK, k: int):
     return partials, hq[:total], hd16[:total]
 
 
-def shared_expert(sh_gate, sh_up, sh_down, xq, xd16, s):
+def shared_expert(sh_gate, sh_up, sh_down, xq, xd16, s, fmt: str = "q8_0"):
     """Sigmoid-gated shared expert -> (S f32[N, D], hq int8[N, Fs], hd16)."""
     Fs = sh_gate.shape[0]
     D = sh_down.shape[0]
@@ -205,7 +231,7 @@ def shared_expert(sh_gate, sh_up, sh_down, xq, xd16, s):
     S = np.empty((N, D), np.float32)
     hq = np.empty((N, Fs), np.int8)
     hd16 = np.empty((N, Fs // QK), np.uint16)
-    _L().oracle_shared_expert(_p(np.ascontiguousarray(sh_gate)), _p(np.ascontiguousarray(sh_up)),
+    _L().oracle_shared_expert_fmt(_I(_fmt(fmt)), _p(np.ascontiguousarray(sh_gate)), _p(np.ascontiguousarray(sh_up)),
                               _p(np.ascontiguousarray(sh_down)), _I(D), _I(Fs),
                               _p(np.ascontiguousarray(xq)), _p(np.ascontiguousarray(xd16)),
                               _p(_f32(s)), _I64(N), _p(S), _p(hq), _p(hd16))
@@ -233,7 +259,7 @@ def combine(partials, w, S=None, R=None):
 
 # ---------------------------------------------------------- whole layer ---
 def moe_ffn(hidden, routerW, gate, up, down, top_k: int, norm_topk_prob: bool,
-            shexp_gate=None, sh_gate=None, sh_up=None, sh_down=None, keep: bool = True) -> dict:
+            shexp_gate=None, sh_gate=None, sh_up=None, sh_down=None, keep: bool = True, fmt: str = "q8_0") -> dict:
     """The whole layer, step by step.  Returns every intermediate (keep=True) and ``out``."""
     hidden = _f32(hidden)
     N, D = hidden.shape
@@ -248,11 +274,11 @@ def moe_ffn(hidden, routerW, gate, up, down, top_k: int, norm_topk_prob: bool,
     r["x_q"], r["x_d16"], r["x_s16"] = quantize_q8_1(hidden)
     r["expStart"], r["expTokI"], r["expTokK"] = bucket(r["topk_idx"], E)
     r["partials"], r["h_q"], r["h_d16"] = grouped_ffn(gate, up, down, r["x_q"], r["x_d16"], r["expStart"],
-                                                      r["expTokI"], r["expTokK"], top_k)
+                                                      r["expTokI"], r["expTokK"], top_k, fmt)
     S = None
     if shared:
         S, r["sh_h_q"], r["sh_h_d16"] = shared_expert(sh_gate, sh_up, sh_down, r["x_q"], r["x_d16"],
-                                                      r["shexp_scale"])
+                                                      r["shexp_scale"], fmt)
         r["shared_out"] = S
     r["out"] = combine(r["partials"], r["topk_w"], S)
     if not keep:
@@ -264,4 +290,4 @@ def moe_ffn_inputs(inp: dict, top_k: int, norm_topk_prob: bool, keep: bool = Tru
     """``moe_ffn`` over a dict made by ``mixture_experts_ffn_top_gb300.workloads.make_inputs``."""
     return moe_ffn(inp["hidden"], inp["routerW"], inp["gate"], inp["up"], inp["down"], top_k,
                    norm_topk_prob, inp.get("shexp_gate"), inp.get("sh_gate"), inp.get("sh_up"),
-                   inp.get("sh_down"), keep=keep)
+                   inp.get("sh_down"), keep=keep, fmt=inp.get("wfmt", "q8_0"))

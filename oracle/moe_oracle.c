@@ -290,6 +290,107 @@ void oracle_block_dots(const uint8_t *w_row, const int8_t *aq, int nblk, int32_t
 }
 
 /* ------------------------------------------------------------------------
+ * Q4_K weights (the K-quant the pages' MMQ work names next to Q8_0: #406
+ * references "Q8_0/Q4_K MMQ"; its layout is the GGUF one, which the pages do
+ * not spell out).  A super-block of QK_K = 256 values is 144 bytes: fp16 d,
+ * fp16 dmin, 12 bytes holding eight 6-bit sub-block scales sc_j and mins m_j,
+ * 128 bytes of 4-bit quants q in [0, 15].  Value i of sub-block j:
+ *   w = d * sc_j * q_i - dmin * m_j.
+ * Packing of the 12 bytes: for j < 4, sc_j and m_j are the low 6 bits of
+ * bytes j and j + 4; for j >= 4, the low (high) nibble of byte j + 4 gives
+ * the low 4 bits of sc_j (m_j) and the top 2 bits of byte j - 4 (byte j) its
+ * high 2 bits.  Quants: the 64 values of sub-blocks 2g and 2g + 1 share 32
+ * bytes, sub-block 2g in the low nibbles, 2g + 1 in the high ones.
+ * Dot with a Q8_1 row, per 32-wide sub-block b (exact int32 isum_b as for
+ * Q8_0, plus the activation's code sum xsum_b for the min term):
+ *   result = sum_b fp16(da_b) * (d * sc_b * isum_b - dmin * m_b * xsum_b)
+ * accumulated in double (each term is exact in double).
+ * ---------------------------------------------------------------------- */
+#define QK_K 256
+#define Q4_K_BYTES 144
+enum { FMT_Q8_0 = 0, FMT_Q4_K = 1 };
+
+static void q4_k_scale_min(const uint8_t *s12, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = s12[j] & 63;
+        *m = s12[j + 4] & 63;
+    } else {
+        *sc = (s12[j + 4] & 15) | ((s12[j - 4] >> 6) << 4);
+        *m = (s12[j + 4] >> 4) | ((s12[j] >> 6) << 4);
+    }
+}
+
+static void q4_k_quants(const uint8_t *qs, int j, int8_t *q)
+{
+    const uint8_t *p = qs + 32 * (j / 2);
+    for (int l = 0; l < QK; ++l)
+        q[l] = (int8_t)((j & 1) ? (p[l] >> 4) : (p[l] & 15));
+}
+
+static double q4_k_row_dot(const uint8_t *w_row, const int8_t *aq, const uint16_t *ad16, int K)
+{
+    double acc = 0.0;
+    for (int sb = 0; sb < K / QK_K; ++sb) {
+        const uint8_t *blk = w_row + (size_t)sb * Q4_K_BYTES;
+        double d = oracle_half_to_float(load_u16(blk));
+        double dmin = oracle_half_to_float(load_u16(blk + 2));
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            int8_t q[QK];
+            q4_k_scale_min(blk + 4, j, &sc, &m);
+            q4_k_quants(blk + 16, j, q);
+            int b = sb * 8 + j;
+            int32_t isum = block_isum(q, aq + b * QK);
+            int32_t xsum = 0;
+            for (int l = 0; l < QK; ++l)
+                xsum += aq[b * QK + l];
+            acc += (double)oracle_half_to_float(ad16[b]) * (d * sc * (double)isum - dmin * m * (double)xsum);
+        }
+    }
+    return acc;
+}
+
+/* Dequantised Q4_K row (K values, each rounded once to fp32), for the pins. */
+void oracle_q4_k_dequant(const uint8_t *w_row, int K, float *out)
+{
+    for (int sb = 0; sb < K / QK_K; ++sb) {
+        const uint8_t *blk = w_row + (size_t)sb * Q4_K_BYTES;
+        double d = oracle_half_to_float(load_u16(blk));
+        double dmin = oracle_half_to_float(load_u16(blk + 2));
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            int8_t q[QK];
+            q4_k_scale_min(blk + 4, j, &sc, &m);
+            q4_k_quants(blk + 16, j, q);
+            for (int l = 0; l < QK; ++l)
+                out[sb * QK_K + j * QK + l] = (float)(d * sc * q[l] - dmin * m);
+        }
+    }
+}
+
+/* int32 block dots of a Q4_K row (quants 0..15) against an activation row. */
+void oracle_block_dots_q4_k(const uint8_t *w_row, const int8_t *aq, int K, int32_t *out)
+{
+    for (int sb = 0; sb < K / QK_K; ++sb)
+        for (int j = 0; j < 8; ++j) {
+            int8_t q[QK];
+            q4_k_quants(w_row + (size_t)sb * Q4_K_BYTES + 16, j, q);
+            out[sb * 8 + j] = block_isum(q, aq + (sb * 8 + j) * QK);
+        }
+}
+
+static size_t row_bytes(int fmt, int K)
+{
+    return fmt == FMT_Q4_K ? (size_t)(K / QK_K) * Q4_K_BYTES : (size_t)(K / QK) * Q8_0_BYTES;
+}
+
+static double row_dot(int fmt, const uint8_t *w_row, const int8_t *aq, const uint16_t *ad16, int K)
+{
+    return fmt == FMT_Q4_K ? q4_k_row_dot(w_row, aq, ad16, K) : q8_row_dot(w_row, aq, ad16, K / QK);
+}
+
+/* ------------------------------------------------------------------------
  * SwiGLU expert, gate/up half, for one activation row (#129 intro: the
  * routed-expert gate/up/down GEMMs; #406 "The work" item 2):
  *   g_r = <W_g[r], x_q>,  u_r = <W_u[r], x_q>   (q8_row_dot, double)
@@ -297,15 +398,14 @@ void oracle_block_dots(const uint8_t *w_row, const int8_t *aq, int nblk, int32_t
  * then h -> Q8_1 (oracle_quantize_q8_1).  Optional g/u outputs (double).
  * Wg, Wu: [F rows][D/32 blocks] Q8_0.
  * ---------------------------------------------------------------------- */
-static void expert_gate_up_row(const uint8_t *Wg, const uint8_t *Wu, int D, int F,
+static void expert_gate_up_row(int fmt, const uint8_t *Wg, const uint8_t *Wu, int D, int F,
                                const int8_t *xq, const uint16_t *xd16,
                                float *h, int8_t *hq, uint16_t *hd16, double *g_out, double *u_out)
 {
-    int nblk = D / QK;
-    size_t row_bytes = (size_t)nblk * Q8_0_BYTES;
+    size_t rb = row_bytes(fmt, D);
     for (int r = 0; r < F; ++r) {
-        double g = q8_row_dot(Wg + r * row_bytes, xq, xd16, nblk);
-        double u = q8_row_dot(Wu + r * row_bytes, xq, xd16, nblk);
+        double g = row_dot(fmt, Wg + r * rb, xq, xd16, D);
+        double u = row_dot(fmt, Wu + r * rb, xq, xd16, D);
         if (g_out)
             g_out[r] = g;
         if (u_out)
@@ -315,28 +415,27 @@ static void expert_gate_up_row(const uint8_t *Wg, const uint8_t *Wu, int D, int 
     oracle_quantize_q8_1(h, F / QK, hq, hd16, NULL);
 }
 
-/* Down half: y_c = <W_d[c], h_q> in double, c = 0..D-1.  Wd: [D][F/32]. */
-static void expert_down_row(const uint8_t *Wd, int D, int F, const int8_t *hq, const uint16_t *hd16,
+/* Down half: y_c = <W_d[c], h_q> in double, c = 0..D-1.  Wd: [D] rows of K = F. */
+static void expert_down_row(int fmt, const uint8_t *Wd, int D, int F, const int8_t *hq, const uint16_t *hd16,
                             double *y)
 {
-    int nblk = F / QK;
-    size_t row_bytes = (size_t)nblk * Q8_0_BYTES;
+    size_t rb = row_bytes(fmt, F);
     for (int c = 0; c < D; ++c)
-        y[c] = q8_row_dot(Wd + c * row_bytes, hq, hd16, nblk);
+        y[c] = row_dot(fmt, Wd + c * rb, hq, hd16, F);
 }
 
-/* Exported single-row pieces, for the pins. */
-void oracle_expert_gate_up(const uint8_t *Wg, const uint8_t *Wu, int D, int F,
-                           const int8_t *xq, const uint16_t *xd16,
-                           float *h, int8_t *hq, uint16_t *hd16, double *g, double *u)
+/* Exported single-row pieces, for the pins (fmt: 0 Q8_0, 1 Q4_K). */
+void oracle_expert_gate_up_fmt(int fmt, const uint8_t *Wg, const uint8_t *Wu, int D, int F,
+                               const int8_t *xq, const uint16_t *xd16,
+                               float *h, int8_t *hq, uint16_t *hd16, double *g, double *u)
 {
-    expert_gate_up_row(Wg, Wu, D, F, xq, xd16, h, hq, hd16, g, u);
+    expert_gate_up_row(fmt, Wg, Wu, D, F, xq, xd16, h, hq, hd16, g, u);
 }
 
-void oracle_expert_down(const uint8_t *Wd, int D, int F, const int8_t *hq, const uint16_t *hd16,
-                        double *y)
+void oracle_expert_down_fmt(int fmt, const uint8_t *Wd, int D, int F, const int8_t *hq, const uint16_t *hd16,
+                            double *y)
 {
-    expert_down_row(Wd, D, F, hq, hd16, y);
+    expert_down_row(fmt, Wd, D, F, hq, hd16, y);
 }
 
 /* ------------------------------------------------------------------------
@@ -348,13 +447,13 @@ void oracle_expert_down(const uint8_t *Wd, int D, int F, const int8_t *hq, const
  * gate/up: [E][F][D/32] Q8_0; down: [E][D][F/32] Q8_0.
  * hq/hd16 (nullable) receive the segment-ordered requantised activations.
  * ---------------------------------------------------------------------- */
-void oracle_grouped_ffn(const uint8_t *gate, const uint8_t *up, const uint8_t *down,
-                        int E, int D, int F, const int8_t *xq, const uint16_t *xd16,
-                        const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
-                        int k, float *partials, int8_t *hq_out, uint16_t *hd16_out)
+void oracle_grouped_ffn_fmt(int fmt, const uint8_t *gate, const uint8_t *up, const uint8_t *down,
+                            int E, int D, int F, const int8_t *xq, const uint16_t *xd16,
+                            const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
+                            int k, float *partials, int8_t *hq_out, uint16_t *hd16_out)
 {
-    size_t gu_bytes = (size_t)F * (D / QK) * Q8_0_BYTES; /* one expert's gate (or up) */
-    size_t dn_bytes = (size_t)D * (F / QK) * Q8_0_BYTES;
+    size_t gu_bytes = (size_t)F * row_bytes(fmt, D); /* one expert's gate (or up) */
+    size_t dn_bytes = (size_t)D * row_bytes(fmt, F);
     int64_t total = expStart[E];
 #pragma omp parallel
     {
@@ -369,13 +468,13 @@ void oracle_grouped_ffn(const uint8_t *gate, const uint8_t *up, const uint8_t *d
                 ++e;
             int64_t t = expTokI[j];
             int s = expTokK[j];
-            expert_gate_up_row(gate + e * gu_bytes, up + e * gu_bytes, D, F,
+            expert_gate_up_row(fmt, gate + e * gu_bytes, up + e * gu_bytes, D, F,
                                xq + t * D, xd16 + t * (D / QK), h, hq, hd, NULL, NULL);
             if (hq_out) {
                 memcpy(hq_out + j * F, hq, (size_t)F);
                 memcpy(hd16_out + j * (F / QK), hd, sizeof(uint16_t) * (size_t)(F / QK));
             }
-            expert_down_row(down + e * dn_bytes, D, F, hq, hd, y);
+            expert_down_row(fmt, down + e * dn_bytes, D, F, hq, hd, y);
             float *dst = partials + (t * k + s) * (int64_t)D;
             for (int c = 0; c < D; ++c)
                 dst[c] = (float)y[c];
@@ -393,9 +492,9 @@ void oracle_grouped_ffn(const uint8_t *gate, const uint8_t *up, const uint8_t *d
  *   S[t,c] = fp32( s_t * y_c ),  y = W_sd Q8_1(SiLU(W_sg x_q[t]) * (W_su x_q[t]))
  * sg/su: [Fs][D/32]; sd: [D][Fs/32].
  * ---------------------------------------------------------------------- */
-void oracle_shared_expert(const uint8_t *sg, const uint8_t *su, const uint8_t *sd, int D, int Fs,
-                          const int8_t *xq, const uint16_t *xd16, const float *s, int64_t N,
-                          float *S, int8_t *hq_out, uint16_t *hd16_out)
+void oracle_shared_expert_fmt(int fmt, const uint8_t *sg, const uint8_t *su, const uint8_t *sd, int D, int Fs,
+                              const int8_t *xq, const uint16_t *xd16, const float *s, int64_t N,
+                              float *S, int8_t *hq_out, uint16_t *hd16_out)
 {
 #pragma omp parallel
     {
@@ -405,12 +504,12 @@ void oracle_shared_expert(const uint8_t *sg, const uint8_t *su, const uint8_t *s
         double *y = (double *)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic, 4)
         for (int64_t t = 0; t < N; ++t) {
-            expert_gate_up_row(sg, su, D, Fs, xq + t * D, xd16 + t * (D / QK), h, hq, hd, NULL, NULL);
+            expert_gate_up_row(fmt, sg, su, D, Fs, xq + t * D, xd16 + t * (D / QK), h, hq, hd, NULL, NULL);
             if (hq_out) {
                 memcpy(hq_out + t * Fs, hq, (size_t)Fs);
                 memcpy(hd16_out + t * (Fs / QK), hd, sizeof(uint16_t) * (size_t)(Fs / QK));
             }
-            expert_down_row(sd, D, Fs, hq, hd, y);
+            expert_down_row(fmt, sd, D, Fs, hq, hd, y);
             for (int c = 0; c < D; ++c)
                 S[t * D + c] = (float)((double)s[t] * y[c]);
         }

@@ -46,6 +46,11 @@ MUTATIONS = [
      "acc = acc + w[t * k + s] * partials[(t * k + s) * (int64_t)D + c];"),
     ("combine_reverse_order", "for (int s = 0; s < k; ++s)\n                acc = fmaf(w[t * k + s], partials[(t * k + s) * (int64_t)D + c], acc);",
      "for (int s = k - 1; s >= 0; --s)\n                acc = fmaf(w[t * k + s], partials[(t * k + s) * (int64_t)D + c], acc);"),
+    ("q4k_min_sign", "(d * sc * (double)isum - dmin * m * (double)xsum)", "(d * sc * (double)isum + dmin * m * (double)xsum)"),
+    ("q4k_min_uses_isum", "(d * sc * (double)isum - dmin * m * (double)xsum)", "(d * sc * (double)isum - dmin * m * (double)isum)"),
+    ("q4k_nibble_order", "q[l] = (int8_t)((j & 1) ? (p[l] >> 4) : (p[l] & 15));",
+     "q[l] = (int8_t)((j & 1) ? (p[l] & 15) : (p[l] >> 4));"),
+    ("q4k_scale_high_bits", "*sc = (s12[j + 4] & 15) | ((s12[j - 4] >> 6) << 4);", "*sc = (s12[j + 4] & 15);"),
     ("combine_residual_first",
      "            if (S)\n                acc = acc + S[t * D + c];\n            acc = acc + R[t * D + c];",
      "            acc = acc + R[t * D + c];\n            if (S)\n                acc = acc + S[t * D + c];"),

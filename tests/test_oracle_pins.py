@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from mixture_experts_ffn_top_gb300.workloads import QK, Q8_0_BYTES, pack_q8_0
+from mixture_experts_ffn_top_gb300.workloads import QK, Q4_K_BYTES, Q8_0_BYTES, QK_K, pack_q4_k, pack_q8_0
 
 F32_EPS = np.finfo(np.float32).eps
 
@@ -26,6 +26,22 @@ def dequant_q8_0(rows_bytes: np.ndarray) -> np.ndarray:
     d = b[..., :2].copy().view(np.float16)[..., 0].astype(np.float64)
     q = b[..., 2:].view(np.int8).astype(np.float64)
     return (q * d[..., None]).reshape(rows, -1)
+
+
+def dequant_q4_k(rows_bytes: np.ndarray) -> np.ndarray:
+    """Q4_K bytes [rows, nsb*144] -> float64 [rows, nsb*256] (the GGUF super-block definition:
+    fp16 d, fp16 dmin, 12 bytes of 6-bit scales/mins, 4-bit quants; d*sc_j*q - dmin*m_j)."""
+    rows = rows_bytes.shape[0]
+    b = rows_bytes.reshape(rows, -1, Q4_K_BYTES).astype(np.int64)
+    d = rows_bytes.reshape(rows, -1, Q4_K_BYTES)[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = rows_bytes.reshape(rows, -1, Q4_K_BYTES)[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    s12 = b[..., 4:16]
+    sc = np.concatenate([s12[..., 0:4] & 63, (s12[..., 8:12] & 15) | ((s12[..., 0:4] >> 6) << 4)], axis=-1)
+    mn = np.concatenate([s12[..., 4:8] & 63, (s12[..., 8:12] >> 4) | ((s12[..., 4:8] >> 6) << 4)], axis=-1)
+    qs = b[..., 16:].reshape(rows, -1, 4, 32)
+    q = np.stack([qs & 15, qs >> 4], axis=3).reshape(rows, -1, 8, 32)  # sub-block 2g low, 2g+1 high
+    v = d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None]
+    return v.reshape(rows, -1)
 
 
 def dequant_q8(q: np.ndarray, d16: np.ndarray) -> np.ndarray:
@@ -266,6 +282,99 @@ def test_block_dots_integer_brute_force():
     wmax[0, 32:] = -1.0
     got = O.block_dots(pack_q8_0(wmax)[0], np.full(64, 127, np.int8))
     assert got.tolist() == [32 * 127 * 127, -32 * 127 * 127]
+
+
+def _hand_q4_k_block() -> np.ndarray:
+    """One Q4_K super-block written byte by byte: d = 1, dmin = 0.5, sc = 1..7, 63 and
+    m = 0..6, 40 (bytes below), every quant byte 0x2F (even sub-blocks q = 15, odd q = 2)."""
+    blk = np.zeros(Q4_K_BYTES, np.uint8)
+    blk[0:2] = [0x00, 0x3C]                 # fp16 1.0
+    blk[2:4] = [0x00, 0x38]                 # fp16 0.5
+    blk[4:8] = [1, 2, 3, 4 | (3 << 6)]      # sc_0..3, top bits of sc_7 = 63 >> 4 = 3
+    blk[8:12] = [0, 1, 2, 3 | (2 << 6)]     # m_0..3, top bits of m_7 = 40 >> 4 = 2
+    blk[12:16] = [5 | (4 << 4), 6 | (5 << 4), 7 | (6 << 4), 15 | (8 << 4)]  # low bits of sc_4..7 / m_4..7
+    blk[16:] = 0x2F
+    return blk
+
+
+def test_q4_k_hand_block_decodes_to_the_format_values():
+    """d*sc_j*q - dmin*m_j on the hand-written block, worked out by hand: sub-block 0: 1*1*15 - 0 = 15;
+    1: 2*2 - 0.5 = 3.5; 2: 3*15 - 1 = 44; 3: 4*2 - 1.5 = 6.5; 4: 5*15 - 2 = 73; 5: 6*2 - 2.5 = 9.5;
+    6: 7*15 - 3 = 102; 7: 63*2 - 20 = 106."""
+    want = [15.0, 3.5, 44.0, 6.5, 73.0, 9.5, 102.0, 106.0]
+    got = O.q4_k_dequant(_hand_q4_k_block(), QK_K).reshape(8, 32)
+    for j in range(8):
+        assert np.all(got[j] == want[j]), (j, got[j][:4])
+    assert np.all(dequant_q4_k(_hand_q4_k_block()[None])[0].reshape(8, 32) == np.array(want)[:, None])
+
+
+def test_q4_k_dequant_matches_format_definition():
+    rng = np.random.default_rng(40)
+    rows = pack_q4_k((rng.standard_normal((6, 512)) * 0.02).astype(np.float32))
+    ref = dequant_q4_k(rows).astype(np.float32)
+    got = np.stack([O.q4_k_dequant(r, 512) for r in rows])
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_q4_k_block_dots_integer_brute_force():
+    rng = np.random.default_rng(41)
+    rows = pack_q4_k((rng.standard_normal((1, 512)) * 0.02).astype(np.float32))
+    aq = rng.integers(-127, 128, 512).astype(np.int8)
+    qs = rows[0].reshape(-1, Q4_K_BYTES)[:, 16:].astype(np.int64).reshape(-1, 4, 32)
+    q = np.stack([qs & 15, qs >> 4], axis=2).reshape(-1, 32)  # sub-blocks in order
+    ref = (q * aq.reshape(-1, 32).astype(np.int64)).sum(axis=1)
+    np.testing.assert_array_equal(O.block_dots_q4_k(rows[0], aq), ref)
+    # extreme block: 32 * 15 * 127 is exact
+    hand = _hand_q4_k_block()
+    assert O.block_dots_q4_k(hand, np.full(256, 127, np.int8))[0] == 32 * 15 * 127
+
+
+@pytest.fixture(scope="module")
+def small_expert_q4_k():
+    rng = np.random.default_rng(42)
+    D, F = 256, 256
+    Wg = pack_q4_k((rng.standard_normal((F, D)) * 0.02).astype(np.float32))
+    Wu = pack_q4_k((rng.standard_normal((F, D)) * 0.02).astype(np.float32))
+    Wd = pack_q4_k((rng.standard_normal((D, F)) * 0.02).astype(np.float32))
+    x = rng.standard_normal(D).astype(np.float32)
+    xq, xd16, _ = O.quantize_q8_1(x)
+    return D, F, Wg, Wu, Wd, xq, xd16
+
+
+def test_q4_k_expert_matches_dequantised_matmul(small_expert_q4_k):
+    """Q4_K gate/up and down against numpy float64 matmuls of the dequantised operands: the min
+    term (dmin*m_j times the activation block's code sum) is part of the same number."""
+    D, F, Wg, Wu, Wd, xq, xd16 = small_expert_q4_k
+    h, hq, hd16, g, u = O.expert_gate_up(Wg, Wu, D, F, xq, xd16, fmt="q4_k")
+    xdq = dequant_q8(xq, xd16)
+    for got, W in ((g, Wg), (u, Wu)):
+        Wdq = dequant_q4_k(W)
+        assert np.all(np.abs(got - Wdq @ xdq) <= 1e-12 * (np.abs(Wdq) @ np.abs(xdq)))
+    y = O.expert_down(Wd, D, F, hq, hd16, fmt="q4_k")
+    Wdd = dequant_q4_k(Wd)
+    hdq = dequant_q8(hq, hd16)
+    assert np.all(np.abs(y - Wdd @ hdq) <= 1e-12 * (np.abs(Wdd) @ np.abs(hdq)))
+    # the same bytes read as the wrong format do not give the same numbers
+    assert not np.allclose(g, dequant_q4_k(Wg)[:, ::-1] @ xdq, rtol=1e-3)
+
+
+def test_q4_k_single_expert_layer_is_dense_swiglu():
+    rng = np.random.default_rng(43)
+    N, D, F = 8, 256, 256
+    hidden = rng.standard_normal((N, D)).astype(np.float32)
+    routerW = (rng.standard_normal((1, D)) / np.sqrt(D)).astype(np.float32)
+    pk = lambda r, c: pack_q4_k((rng.standard_normal((r, c)) * 0.02).astype(np.float32))  # noqa: E731
+    inp = dict(hidden=hidden, routerW=routerW, gate=pk(F, D)[None], up=pk(F, D)[None], down=pk(D, F)[None],
+               wfmt="q4_k")
+    r = O.moe_ffn_inputs(inp, 1, True)
+    assert np.all(r["topk_w"] == 1.0)
+    xdq = dequant_q8(r["x_q"], r["x_d16"])
+    g = xdq @ dequant_q4_k(inp["gate"][0]).T
+    u = xdq @ dequant_q4_k(inp["up"][0]).T
+    ref = (g / (1 + np.exp(-g)) * u) @ dequant_q4_k(inp["down"][0]).T
+    assert np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref) < 1e-2
+    ref_exact = dequant_q8(r["h_q"], r["h_d16"]) @ dequant_q4_k(inp["down"][0]).T
+    np.testing.assert_allclose(r["out"][r["expTokI"]], ref_exact.astype(np.float32), rtol=1e-6, atol=1e-9)
 
 
 # ---------------------------------------------------------- expert FFN -----
