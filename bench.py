@@ -32,7 +32,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mixture_experts_ffn_top_gb300.workloads import QK, Q8_0_BYTES, WORKLOADS, make_hidden, make_inputs  # noqa: E402
+from mixture_experts_ffn_top_gb300.workloads import QK, Q8_0_BYTES, WORKLOADS, make_hidden, make_inputs, row_bytes  # noqa: E402,F401
 
 METRIC = "MoE-FFN prefill tokens/s/layer, OLMoE shape N=2048; % of int8 tensor peak"
 UNIT = "tokens/s"
@@ -74,12 +74,13 @@ def load_peaks():
 
 
 def algorithmic_work(wl, topk_idx: np.ndarray | None):
-    """Algorithmic bytes and int8 ops of one layer pass: touched experts' Q8_0 weights, hidden read
-    once, routerW, (shared expert weights and gate), output written once; ops = 2 * MACs."""
+    """Algorithmic bytes and int8 ops of one layer pass: touched experts' weights (in their block
+    format, Q8_0 or Q4_K), hidden read once, routerW, (shared expert weights and gate), output written
+    once; ops = 2 * MACs."""
     N, D, E, F, Fs, k = wl.N, wl.D, wl.E, wl.F, wl.Fs, wl.top_k
-    per_expert = 3 * F * D // QK * Q8_0_BYTES
+    per_expert = 3 * F * row_bytes(wl.wfmt, D)
     touched = E if topk_idx is None else int(np.unique(topk_idx).size)
-    wbytes = touched * per_expert + (3 * Fs * D // QK * Q8_0_BYTES if Fs else 0)
+    wbytes = touched * per_expert + (3 * Fs * row_bytes(wl.wfmt, D) if Fs else 0)
     bytes_ = wbytes + N * D * 4 + E * D * 4 + (D * 4 if Fs else 0) + N * D * 4
     ops = 2 * N * k * 3 * F * D + (2 * N * 3 * Fs * D if Fs else 0)
     ops_gate_up = 2 * N * k * 2 * F * D + (2 * N * 2 * Fs * D if Fs else 0)  # the gate/up launch alone

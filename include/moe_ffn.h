@@ -109,6 +109,28 @@ int moe_weights_create(moe_weights_t *out, int E, int D, int F,
                        const void *gate_q8_0, const void *up_q8_0, const void *down_q8_0,
                        int Fs, const void *sh_gate_q8_0, const void *sh_up_q8_0,
                        const void *sh_down_q8_0, cudaStream_t stream);
+
+/* Block format of the caller's expert weights. */
+enum moe_weight_format {
+    MOE_WFMT_Q8_0 = 0, /* GGUF Q8_0: 34-byte blocks of 32 (fp16 d, 32 int8) */
+    MOE_WFMT_Q4_K = 1  /* GGUF Q4_K: 144-byte super-blocks of 256 (fp16 d, fp16 dmin, 12 bytes
+                          of 6-bit sub-block scales sc_j and mins m_j, 128 bytes of 4-bit
+                          quants q): value = d*sc_j*q - dmin*m_j ("Q8_0/Q4_K MMQ", #406
+                          references).  Needs D, F, Fs multiples of 256. */
+};
+/* moe_weights_create for either format: the same arrays, rows in `format`'s
+ * blocks ([E][F][D/256] super-blocks for Q4_K gate/up, [E][D][F/256] down,
+ * and likewise for the shared expert).  A Q4_K layer computes, per 32-wide
+ * sub-block b, the exact int32 dot of the quants (0..15) with the Q8_1
+ * activation codes and the code sum of the activation block:
+ *   sum_b d_x[b] * (d*sc_b * isum_b - dmin*m_b * xsum_b).
+ * MOE_ERR_UNSUPPORTED_SHAPE for shapes the format cannot hold. */
+int moe_weights_create_ex(moe_weights_t *out, int format, int E, int D, int F,
+                          const void *gate, const void *up, const void *down, int Fs,
+                          const void *sh_gate, const void *sh_up, const void *sh_down,
+                          cudaStream_t stream);
+/* MOE_WFMT_* of a weights handle, or MOE_ERR_INVALID_ARG for NULL. */
+int moe_weights_format(moe_weights_t w);
 int moe_weights_destroy(moe_weights_t w);
 /* Shape of a weights handle (any output pointer may be NULL; host pointers). */
 int moe_weights_shape(moe_weights_t w, int *E, int *D, int *F, int *Fs);

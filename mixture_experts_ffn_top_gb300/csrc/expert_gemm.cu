@@ -70,12 +70,16 @@ constexpr int STAGE_A = 16384;                     // 128 weight rows x 128 B (6
 constexpr int STAGE_B = TILE_N * 128;              // up to 96 token rows x 128 B
 constexpr int STAGE_BYTES = STAGE_A + STAGE_B;
 constexpr int SSTAGE_BYTES = 2048;                 // [2][128] weight scales + [2][nb] token scales
+// Q4_K: + [2][128] weight mins (at 2048) + [2][nb] token code sums times scale (at 3072)
+__host__ __device__ constexpr int sstage_bytes(int wf) { return wf ? 4096 : SSTAGE_BYTES; }
 constexpr int HAND_STRIDE = 132;                   // floats per token column of the hand-off buffer (128 rows + pad)
 constexpr int HAND_BYTES = TILE_N * HAND_STRIDE * 4;
 constexpr int BAR_BYTES = 512;
 constexpr int EPI_BYTES = TILE_N * 8;                // the epilogue warp's output rows and scales
-constexpr int G_SMEM = 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * SSTAGE_BYTES + HAND_BYTES + BAR_BYTES + EPI_BYTES;
-static_assert(G_SMEM <= 227 * 1024, "shared memory budget");
+__host__ __device__ constexpr int g_smem(int wf) {
+    return 1024 + G_STAGES * STAGE_BYTES + G_SSTAGES * sstage_bytes(wf) + HAND_BYTES + BAR_BYTES + EPI_BYTES;
+}
+static_assert(g_smem(1) <= 227 * 1024, "shared memory budget");
 static_assert(G_TMEM_BUFS * G_BUF_COLS <= G_TMEM_COLS, "TMEM ring exceeds the allocation");
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 // Scale slot reuse needs no barrier of its own.  The producer loads stage L once the MMAs of stage
@@ -90,6 +94,8 @@ constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s: any healthy
 struct GemmMaps {
     CUtensorMap a_r, sa_r, a_s, sa_s;  // weights + weight scales, routed / shared
     CUtensorMap b[4], sb[4];           // tokens + token scales, box heights 16/32/64/96
+    CUtensorMap sm_r, sm_s;            // Q4_K: weight mins, routed / shared
+    CUtensorMap sx[4];                 // Q4_K: token code sums times scale, box heights as sb
 };
 
 struct GemmParams {
@@ -103,6 +109,7 @@ struct GemmParams {
     const int4 *rowinfo;
     __half *h16;       // gate/up output (fp16 integer codes), row stride Fmax
     float *h_dT;       // [Fmax/32][rows_max]
+    float *h_sT;       // Q4_K: [Fmax/32][rows_max] code sum of each h block times its scale
     float *partials;
     float *shared_out;
     const float *shexp_scale;
@@ -279,7 +286,9 @@ __device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g,
 // MODE 0: gate/up (fused SiLU * up, Q8_1 requant); 1: down (scatter).
 // DUMP (gate/up only): also store the raw int32 block dots of block p.dbg_block
 // (the debug entry point; a separate instantiation keeps the hot loop lean).
-template <int MODE, bool DUMP>
+// WF: weight format (0 Q8_0, 1 Q4_K: the weight is d*sc*q - dmin*m per 32-block, so each block
+// also subtracts (dmin*m) * (d_x * sum of the block's activation codes)).
+template <int MODE, bool DUMP, int WF>
 __global__ void __launch_bounds__(G_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -288,7 +297,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sring = smem + G_STAGES * STAGE_BYTES;
     // hand-off buffer: an item's accumulators, token column c at hand[c * HAND_STRIDE + row]
-    float *hand = reinterpret_cast<float *>(sring + G_SSTAGES * SSTAGE_BYTES);
+    constexpr int SSB = sstage_bytes(WF);
+    float *hand = reinterpret_cast<float *>(sring + G_SSTAGES * SSB);
     uint8_t *bars = reinterpret_cast<uint8_t *>(hand) + HAND_BYTES;
     int *epi_row = reinterpret_cast<int *>(bars + BAR_BYTES);  // [TILE_N] output row per column
     float *epi_scale = reinterpret_cast<float *>(epi_row + TILE_N);  // [TILE_N] shared-expert scale
@@ -372,13 +382,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                         break;
                     }
                     uint8_t *st = smem + stage * STAGE_BYTES;
-                    uint8_t *ss = sring + sstage * SSTAGE_BYTES;
+                    uint8_t *ss = sring + sstage * SSB;
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_expect_tx(fb, STAGE_A + x.nb * 128 + 1024 + 2 * x.nb * 4);
+                    mbar_expect_tx(fb, STAGE_A + x.nb * 128 + (WF ? 2 : 1) * (1024 + 2 * x.nb * 4));
                     tma_load_2d(smem_u32(st), ma, ks * 64, arow, fb);
                     tma_load_2d(smem_u32(st + STAGE_A), &maps.b[x.bi], ks * 64, x.row0, fb);
                     tma_load_2d(smem_u32(ss), msa, x.mt * 128, sarow + 2 * ks, fb);
                     tma_load_2d(smem_u32(ss + 1024), &maps.sb[x.bi], x.row0, 2 * ks, fb);
+                    if (WF) {
+                        tma_load_2d(smem_u32(ss + 2048), x.shared ? &maps.sm_s : &maps.sm_r, x.mt * 128,
+                                    sarow + 2 * ks, fb);
+                        tma_load_2d(smem_u32(ss + 3072), &maps.sx[x.bi], x.row0, 2 * ks, fb);
+                    }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == G_STAGES) stage = 0, phase ^= 1;
@@ -525,12 +540,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                         const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
                         const int prow = x.row0 + col;
                         const int f0 = x.mt * 64 + 32 * fb;
-                        p.h_dT[(size_t)(f0 >> 5) * p.rows_max + prow] = __half2float(__float2half_rn(d));
+                        const float d16 = __half2float(__float2half_rn(d));
+                        p.h_dT[(size_t)(f0 >> 5) * p.rows_max + prow] = d16;
                         __align__(16) __half2 hq[16];
+                        int qsum = 0;  // the block's code sum (the down GEMM's Q4_K min term)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            hq[i] = __halves2half2(__int2half_rn((int)roundf(__fmul_rn(hv[2 * i], id))),
-                                                   __int2half_rn((int)roundf(__fmul_rn(hv[2 * i + 1], id))));
+                        for (int i = 0; i < 16; ++i) {
+                            const int q0 = (int)roundf(__fmul_rn(hv[2 * i], id));
+                            const int q1 = (int)roundf(__fmul_rn(hv[2 * i + 1], id));
+                            qsum += q0 + q1;
+                            hq[i] = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+                        }
+                        if (WF) p.h_sT[(size_t)(f0 >> 5) * p.rows_max + prow] = d16 * (float)qsum;
                         int4 *dst = reinterpret_cast<int4 *>(p.h16 + (size_t)prow * p.Fmax + f0);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) dst[i] = reinterpret_cast<const int4 *>(hq)[i];
@@ -624,7 +645,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 tphase = ph1;
                 if (buf == G_TMEM_BUFS) buf = 0, tphase ^= 1;
                 if (active) {
-                    const float *SA = reinterpret_cast<const float *>(sring + sstage * SSTAGE_BYTES);
+                    const float *SA = reinterpret_cast<const float *>(sring + sstage * SSB);
                     const float *SB = SA + 256;
                     if (DUMP && x.shared == 0 && (2 * ks == p.dbg_block || 2 * ks + 1 == p.dbg_block)) {
                         const int mat = r < 64 ? 0 : 1;
@@ -637,6 +658,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     const float2 dw2a = make_float2(dwa, dwa), dw2b = make_float2(dwb, dwb);
                     const float4 *sa4 = reinterpret_cast<const float4 *>(SB + c0);
                     const float4 *sb4 = reinterpret_cast<const float4 *>(SB + x.nb + c0);
+                    // Q4_K: minus the mins of the two blocks (weight rows) and the code sums times scale
+                    // (token columns), both staged behind the scales
+                    const float *SMn = SA + 512, *SX = SA + 768;
+                    const float2 nma = WF ? make_float2(-SMn[r], -SMn[r]) : make_float2(0.f, 0.f);
+                    const float2 nmb = WF ? make_float2(-SMn[128 + r], -SMn[128 + r]) : make_float2(0.f, 0.f);
+                    const float4 *xa4 = reinterpret_cast<const float4 *>(SX + c0);
+                    const float4 *xb4 = reinterpret_cast<const float4 *>(SX + x.nb + c0);
 #pragma unroll
                     for (int g4 = 0; g4 < 8; ++g4) {
                         // token scales of columns 4*g4 .. 4*g4+3 for the two blocks (broadcast loads)
@@ -650,10 +678,21 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                         float2 w = __ffma2_rn(
                             make_float2(__uint_as_float(v0[4 * g4 + 2]), __uint_as_float(v0[4 * g4 + 3])), a23,
                             acc[2 * g4 + 1]);
-                        acc[2 * g4] = __ffma2_rn(
-                            make_float2(__uint_as_float(v1[4 * g4]), __uint_as_float(v1[4 * g4 + 1])), b01, u);
-                        acc[2 * g4 + 1] = __ffma2_rn(
-                            make_float2(__uint_as_float(v1[4 * g4 + 2]), __uint_as_float(v1[4 * g4 + 3])), b23, w);
+                        if (WF) {
+                            const float4 xa = xa4[g4];
+                            u = __ffma2_rn(make_float2(xa.x, xa.y), nma, u);
+                            w = __ffma2_rn(make_float2(xa.z, xa.w), nma, w);
+                        }
+                        u = __ffma2_rn(make_float2(__uint_as_float(v1[4 * g4]), __uint_as_float(v1[4 * g4 + 1])), b01, u);
+                        w = __ffma2_rn(make_float2(__uint_as_float(v1[4 * g4 + 2]), __uint_as_float(v1[4 * g4 + 3])), b23,
+                                       w);
+                        if (WF) {
+                            const float4 xb = xb4[g4];
+                            u = __ffma2_rn(make_float2(xb.x, xb.y), nmb, u);
+                            w = __ffma2_rn(make_float2(xb.z, xb.w), nmb, w);
+                        }
+                        acc[2 * g4] = u;
+                        acc[2 * g4 + 1] = w;
                     }
                 }
                 if (++sstage == G_SSTAGES) sstage = 0;
@@ -805,7 +844,8 @@ __device__ __forceinline__ uint2 i8x4_to_h16x4(uint32_t v) {
 
 __global__ void __launch_bounds__(256)
 gather_kernel(const int8_t *__restrict__ x_q, const float *__restrict__ x_d, int D, const PlanHeader *hdr,
-              const int4 *__restrict__ rowinfo, int rows_max, __half *__restrict__ xg16, float *__restrict__ xg_dT) {
+              const int4 *__restrict__ rowinfo, int rows_max, __half *__restrict__ xg16, float *__restrict__ xg_dT,
+              float *__restrict__ xg_sT) {
     __shared__ int src[GATHER_ROWS];
     const int row0 = blockIdx.x * GATHER_ROWS;
     const int nrows = hdr->n_rows;
@@ -847,8 +887,19 @@ gather_kernel(const int8_t *__restrict__ x_q, const float *__restrict__ x_d, int
     const int prow = row0 + rr;
     const int t = src[rr];
     for (int b = threadIdx.x / GATHER_ROWS; b < nblk; b += 256 / GATHER_ROWS) {
-        const float d = (t >= 0 && prow < nrows) ? x_d[(size_t)t * nblk + b] : 0.0f;
+        const bool live = t >= 0 && prow < nrows;
+        const float d = live ? x_d[(size_t)t * nblk + b] : 0.0f;
         if (prow < rows_max) xg_dT[(size_t)b * rows_max + prow] = d;
+        if (xg_sT != nullptr && prow < rows_max) {  // Q4_K weights: the block's code sum times its scale
+            int sum = 0;
+            if (live) {
+                const int4 *src = reinterpret_cast<const int4 *>(x_q + (size_t)t * D + (size_t)b * QK);
+                const int4 a = src[0], c = src[1];
+                sum = __dp4a(a.x, 0x01010101, __dp4a(a.y, 0x01010101, __dp4a(a.z, 0x01010101, __dp4a(a.w, 0x01010101, 0))));
+                sum = __dp4a(c.x, 0x01010101, __dp4a(c.y, 0x01010101, __dp4a(c.z, 0x01010101, __dp4a(c.w, 0x01010101, sum))));
+            }
+            xg_sT[(size_t)b * rows_max + prow] = d * (float)sum;
+        }
     }
 }
 static_assert(2 * (256 / 32) == GATHER_ROWS, "two rows per warp");
@@ -870,14 +921,22 @@ __global__ void h16_to_q8_kernel(const __half *__restrict__ h16, const float *__
 // int8 + fp32 scales in CSR entry order -> fp16 codes + transposed scales in padded order.
 __global__ void q8_to_h16_kernel(const int8_t *__restrict__ h_q, const float *__restrict__ h_d, int F, int Fmax,
                                  int rows_max, const PlanHeader *hdr, const int4 *__restrict__ rowinfo,
-                                 __half *__restrict__ h16, float *__restrict__ h_dT) {
+                                 __half *__restrict__ h16, float *__restrict__ h_dT, float *__restrict__ h_sT) {
     const int prow = blockIdx.x;
     if (prow >= hdr->n_rows) return;
     const int j = rowinfo[prow].z;
     for (int f = threadIdx.x; f < F; f += blockDim.x) {
         const int v = j >= 0 ? h_q[(size_t)j * F + f] : 0;
         h16[(size_t)prow * Fmax + f] = __int2half_rn(v);
-        if ((f & 31) == 0) h_dT[(size_t)(f / QK) * rows_max + prow] = j >= 0 ? h_d[(size_t)j * (F / QK) + f / QK] : 0.0f;
+        if ((f & 31) == 0) {
+            const float d = j >= 0 ? h_d[(size_t)j * (F / QK) + f / QK] : 0.0f;
+            h_dT[(size_t)(f / QK) * rows_max + prow] = d;
+            if (h_sT != nullptr) {  // Q4_K weights: the block's code sum times its scale
+                int sum = 0;
+                for (int i = 0; i < QK && j >= 0; ++i) sum += h_q[(size_t)j * F + f + i];
+                h_sT[(size_t)(f / QK) * rows_max + prow] = d * (float)sum;
+            }
+        }
     }
 }
 
@@ -920,7 +979,18 @@ bool encode_2d(CUtensorMap *m, const void *base, bool fp16, uint64_t rows, uint6
 struct WeightMaps {
     CUtensorMap gu_r, gu_dT_r, dn_r, dn_dT_r;
     CUtensorMap gu_s, gu_dT_s, dn_s, dn_dT_s;
+    CUtensorMap gu_mT_r, dn_mT_r, gu_mT_s, dn_mT_s;  // Q4_K mins, as the scales
 };
+
+// One instantiation per (mode, dump, weight format), each with its own dynamic shared memory size.
+template <int MODE, bool DUMP, int WF>
+int run_gemm(const GemmMaps &maps, const GemmParams &p, int num_sms, cudaStream_t s) {
+    static int configured = 0;
+    if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<MODE, DUMP, WF>, g_smem(WF), &configured))
+        return rc;
+    grouped_gemm_kernel<MODE, DUMP, WF><<<num_sms, G_THREADS, g_smem(WF), s>>>(maps, p);
+    return launch_status();
+}
 
 int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_shared, void *ws, const WsLayout &L,
                 float *partials, float *shared_out, const float *shexp_scale, int32_t *dbg_dots, int dbg_block,
@@ -930,11 +1000,16 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     const int D = w->D, F = w->F, Fs = w->Fs, Fmax = std::max(F, Fs);
     GemmMaps maps;
     GemmParams p{};
+    const int wf = w->wfmt == MOE_WFMT_Q4_K ? 1 : 0;
     if (mode == 0) {
         maps.a_r = wm->gu_r;
         maps.sa_r = wm->gu_dT_r;
         maps.a_s = Fs ? wm->gu_s : wm->gu_r;
         maps.sa_s = Fs ? wm->gu_dT_s : wm->gu_dT_r;
+        if (wf) {
+            maps.sm_r = wm->gu_mT_r;
+            maps.sm_s = Fs ? wm->gu_mT_s : wm->gu_mT_r;
+        }
         p.K_r = D;
         p.K_s = D;
         p.MT_r = 2 * F / 128;
@@ -948,6 +1023,10 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
         maps.sa_r = wm->dn_dT_r;
         maps.a_s = Fs ? wm->dn_s : wm->dn_r;
         maps.sa_s = Fs ? wm->dn_dT_s : wm->dn_dT_r;
+        if (wf) {
+            maps.sm_r = wm->dn_mT_r;
+            maps.sm_s = Fs ? wm->dn_mT_s : wm->dn_mT_r;
+        }
         p.K_r = F;
         p.K_s = Fs ? Fs : F;
         p.MT_r = D / 128;
@@ -961,11 +1040,13 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     const int rows = L.rows_max;
     void *bdata = mode == 0 ? (void *)ws_ptr<__half>(ws, L.xg16) : (void *)ws_ptr<__half>(ws, L.h16);
     void *bscale = mode == 0 ? (void *)ws_ptr<float>(ws, L.xg_dT) : (void *)ws_ptr<float>(ws, L.h_dT);
+    void *bsum = mode == 0 ? (void *)ws_ptr<float>(ws, L.xg_sT) : (void *)ws_ptr<float>(ws, L.h_sT);
     const int kcols = mode == 0 ? D : Fmax;
     for (int i = 0; i < 4; ++i) {
         const uint32_t nb = i < 3 ? (16u << i) : (uint32_t)TILE_N;
         if (!encode_2d(&maps.b[i], bdata, true, rows, kcols, 64, nb)) return MOE_ERR_CUDA;
         if (!encode_2d(&maps.sb[i], bscale, false, kcols / QK, rows, nb, 2)) return MOE_ERR_CUDA;
+        if (wf && !encode_2d(&maps.sx[i], bsum, false, kcols / QK, rows, nb, 2)) return MOE_ERR_CUDA;
     }
     p.E = w->E;
     p.D = D;
@@ -981,6 +1062,7 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     p.rowinfo = ws_ptr<int4>(ws, L.rowinfo);
     p.h16 = ws_ptr<__half>(ws, L.h16);
     p.h_dT = ws_ptr<float>(ws, L.h_dT);
+    p.h_sT = ws_ptr<float>(ws, L.h_sT);
     p.partials = partials;
     p.shared_out = shared_out;
     p.shexp_scale = shexp_scale;
@@ -997,20 +1079,11 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
             cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    if (mode == 0 && dbg_dots == nullptr) {
-        static int configured = 0;
-        if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<0, false>, G_SMEM, &configured)) return rc;
-        grouped_gemm_kernel<0, false><<<num_sms, G_THREADS, G_SMEM, s>>>(maps, p);
-    } else if (mode == 0) {
-        static int configured = 0;
-        if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<0, true>, G_SMEM, &configured)) return rc;
-        grouped_gemm_kernel<0, true><<<num_sms, G_THREADS, G_SMEM, s>>>(maps, p);
-    } else {
-        static int configured = 0;
-        if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<1, false>, G_SMEM, &configured)) return rc;
-        grouped_gemm_kernel<1, false><<<num_sms, G_THREADS, G_SMEM, s>>>(maps, p);
-    }
-    return launch_status();
+    const bool dump = mode == 0 && dbg_dots != nullptr;
+    if (mode == 0)
+        return dump ? (wf ? run_gemm<0, true, 1>(maps, p, num_sms, s) : run_gemm<0, true, 0>(maps, p, num_sms, s))
+                    : (wf ? run_gemm<0, false, 1>(maps, p, num_sms, s) : run_gemm<0, false, 0>(maps, p, num_sms, s));
+    return wf ? run_gemm<1, false, 1>(maps, p, num_sms, s) : run_gemm<1, false, 0>(maps, p, num_sms, s);
 }
 
 }  // namespace
@@ -1030,6 +1103,13 @@ int prepare_tensor_maps(moe_weights_s *w) {
              encode_2d(&m->gu_dT_s, w->shared.gu_dT, false, (uint64_t)(D / QK), 2 * Fs, 128, 2) &&
              encode_2d(&m->dn_s, w->shared.dn16, true, (uint64_t)D, Fs, 64, 128) &&
              encode_2d(&m->dn_dT_s, w->shared.dn_dT, false, (uint64_t)(Fs / QK), D, 128, 2);
+    if (ok && w->wfmt == MOE_WFMT_Q4_K) {
+        ok = encode_2d(&m->gu_mT_r, w->routed.gu_mT, false, (uint64_t)E * (D / QK), 2 * F, 128, 2) &&
+             encode_2d(&m->dn_mT_r, w->routed.dn_mT, false, (uint64_t)E * (F / QK), D, 128, 2);
+        if (ok && Fs)
+            ok = encode_2d(&m->gu_mT_s, w->shared.gu_mT, false, (uint64_t)(D / QK), 2 * Fs, 128, 2) &&
+                 encode_2d(&m->dn_mT_s, w->shared.dn_mT, false, (uint64_t)(Fs / QK), D, 128, 2);
+    }
     if (!ok) {
         delete m;
         return MOE_OK;  // tensor path unavailable; the matvec path still serves every call
@@ -1056,8 +1136,9 @@ int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const floa
         rc = launch_status();
     }
     if (rc || x_q == nullptr) return rc;
-    gather_kernel<<<(L.rows_max + GATHER_ROWS - 1) / GATHER_ROWS, 256, 0, s>>>(x_q, x_d, w->D, hdr, ws_ptr<int4>(ws, L.rowinfo), L.rows_max,
-                                                         ws_ptr<__half>(ws, L.xg16), ws_ptr<float>(ws, L.xg_dT));
+    gather_kernel<<<(L.rows_max + GATHER_ROWS - 1) / GATHER_ROWS, 256, 0, s>>>(
+        x_q, x_d, w->D, hdr, ws_ptr<int4>(ws, L.rowinfo), L.rows_max, ws_ptr<__half>(ws, L.xg16),
+        ws_ptr<float>(ws, L.xg_dT), w->wfmt == MOE_WFMT_Q4_K ? ws_ptr<float>(ws, L.xg_sT) : nullptr);
     return launch_status();
 }
 
@@ -1094,7 +1175,8 @@ int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const W
     const int Fmax = std::max(w->F, w->Fs);
     q8_to_h16_kernel<<<L.rows_max, 256, 0, s>>>(h_q, h_d, w->F, Fmax, L.rows_max, ws_ptr<PlanHeader>(ws, L.plan),
                                                 ws_ptr<int4>(ws, L.rowinfo), ws_ptr<__half>(ws, L.h16),
-                                                ws_ptr<float>(ws, L.h_dT));
+                                                ws_ptr<float>(ws, L.h_dT),
+                                                w->wfmt == MOE_WFMT_Q4_K ? ws_ptr<float>(ws, L.h_sT) : nullptr);
     return launch_status();
 }
 

@@ -9,7 +9,10 @@
 // once.  Each warp owns 4 rows; lane l reads 16-byte pieces l, l+32, ... of a
 // row (coalesced 512 B per warp step).  Two neighbouring lanes hold the two
 // halves of a 32-block; their dp4a sums are exchanged with one shuffle, which
-// gives the exact int32 block dot isum_b, then acc += (d_w * d_x) * isum_b.
+// gives the exact int32 block dot isum_b, then acc += (d_w * d_x) * isum_b.  Q4_K
+// weights (repacked to quants 0..15 with per-block scale d*sc and min dmin*m)
+// add the min term: the same lanes also sum the activation codes (dp4a with
+// ones), and acc -= (m_w * d_x) * xsum_b.
 //
 // gate/up kernel: rows = features f (gate and up), output h = SiLU(g) * u,
 //   requantised to Q8_1 per 32 features inside the CTA (the CTA owns exactly
@@ -57,9 +60,9 @@ __device__ __forceinline__ Seg segment_of(bool is_shared, int e, const int32_t *
 // Dot of one weight row (int8 [K], scales [K/32]) against MV_T staged activation rows.
 // Returns per-token fp32 sums, reduced across the warp (valid in every lane).
 // If dbg != nullptr, the even lane owning block dbg_block stores its isum per token.
-__device__ __forceinline__ void row_dot(const int8_t *__restrict__ wq, const float *__restrict__ wd, int K,
-                                        const int8_t *xs, const float *xds, int lane, float acc[MV_T],
-                                        int dbg_block, int dbg_isum[MV_T]) {
+__device__ __forceinline__ void row_dot(const int8_t *__restrict__ wq, const float *__restrict__ wd,
+                                        const float *__restrict__ wm, int K, const int8_t *xs, const float *xds,
+                                        int lane, float acc[MV_T], int dbg_block, int dbg_isum[MV_T]) {
 #pragma unroll
     for (int tt = 0; tt < MV_T; ++tt) acc[tt] = 0.0f;
     const int nchunks = K / 16;  // even: K is a multiple of 32
@@ -69,25 +72,33 @@ __device__ __forceinline__ void row_dot(const int8_t *__restrict__ wq, const flo
         const bool active = c < nchunks;  // lanes l and l^1 are active together
         const int b = c >> 1;
         int4 w = make_int4(0, 0, 0, 0);
-        float dw = 0.0f;
+        float dw = 0.0f, mw = 0.0f;
         if (active) {
             w = *reinterpret_cast<const int4 *>(wq + (size_t)c * 16);
             dw = wd[b];
+            if (wm != nullptr) mw = wm[b];
         }
-        int part[MV_T];
+        const int4 ones = make_int4(0x01010101, 0x01010101, 0x01010101, 0x01010101);
+        int part[MV_T], xpart[MV_T];
 #pragma unroll
         for (int tt = 0; tt < MV_T; ++tt) {
             part[tt] = 0;
+            xpart[tt] = 0;
             if (active) {
                 int4 x = *reinterpret_cast<const int4 *>(xs + (size_t)tt * K + c * 16);
                 part[tt] = dp4a16(w, x);
+                if (wm != nullptr) xpart[tt] = dp4a16(ones, x);
             }
         }
 #pragma unroll
         for (int tt = 0; tt < MV_T; ++tt) {
             int isum = part[tt] + __shfl_xor_sync(0xffffffffu, part[tt], 1);
+            int xsum = 0;
+            if (wm != nullptr) xsum = xpart[tt] + __shfl_xor_sync(0xffffffffu, xpart[tt], 1);
             if (active && (c & 1) == 0) {
-                acc[tt] = fmaf(dw * xds[tt * (K / QK) + b], (float)isum, acc[tt]);
+                const float dx = xds[tt * (K / QK) + b];
+                acc[tt] = fmaf(dw * dx, (float)isum, acc[tt]);
+                if (wm != nullptr) acc[tt] = fmaf(-(mw * dx), (float)xsum, acc[tt]);
                 if (b == dbg_block) dbg_isum[tt] = isum;
             }
         }
@@ -116,8 +127,9 @@ __device__ __forceinline__ void stage_rows(const int8_t *__restrict__ q, const f
 
 // grid (F/32, nexp); h_q/h_d rows: routed -> CSR entry j, shared -> token t.
 __global__ void __launch_bounds__(MV_WARPS * 32)
-matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ gd,
-                      const int8_t *__restrict__ uq, const float *__restrict__ ud, int D, int F,
+matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ gd, const float *__restrict__ gm,
+                      const int8_t *__restrict__ uq, const float *__restrict__ ud, const float *__restrict__ um,
+                      int D, int F,
                       bool is_shared, const int8_t *__restrict__ x_q, const float *__restrict__ x_d,
                       const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI, int N,
                       int top_k, int8_t *__restrict__ h_q, float *__restrict__ h_d,
@@ -159,8 +171,9 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
             const int f = fb * QK + fl;
             float g[MV_T], u[MV_T];
             int dg[MV_T], du[MV_T];
-            row_dot(gq + (mat_off + f) * D, gd + (mat_off + f) * (D / QK), D, xs, xds, lane, g, dbg_block, dg);
-            row_dot(uq + (mat_off + f) * D, ud + (mat_off + f) * (D / QK), D, xs, xds, lane, u, dbg_block, du);
+            const size_t so = (mat_off + f) * (D / QK);
+            row_dot(gq + (mat_off + f) * D, gd + so, gm ? gm + so : nullptr, D, xs, xds, lane, g, dbg_block, dg);
+            row_dot(uq + (mat_off + f) * D, ud + so, um ? um + so : nullptr, D, xs, xds, lane, u, dbg_block, du);
             if (dbg_dots != nullptr && dbg_block >= 0) {
                 // the even lane that owns block dbg_block (16-byte piece 2*dbg_block) holds the isums
                 if (lane == ((2 * dbg_block) & 31)) {
@@ -199,7 +212,8 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
 
 // grid (D/32, nexp)
 __global__ void __launch_bounds__(MV_WARPS * 32)
-matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, int D, int F,
+matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, const float *__restrict__ dm,
+                   int D, int F,
                    bool is_shared, const int8_t *__restrict__ h_q, const float *__restrict__ h_d,
                    const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI,
                    const int32_t *__restrict__ expTokK, int N, int top_k,
@@ -252,7 +266,8 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
             const int c = cb * QK + cl;
             float y[MV_T];
             int unused[MV_T];
-            row_dot(dq + (mat_off + c) * F, dd + (mat_off + c) * (F / QK), F, hs, hds, lane, y, -1, unused);
+            const size_t so = (mat_off + c) * (F / QK);
+            row_dot(dq + (mat_off + c) * F, dd + so, dm ? dm + so : nullptr, F, hs, hds, lane, y, -1, unused);
             if (lane == 0) {
 #pragma unroll
                 for (int tt = 0; tt < MV_T; ++tt) ys[tt * QK + cl] = y[tt];
@@ -282,7 +297,8 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_
     static int configured = 0;
     if (int rc = ensure_dynamic_smem((const void *)matvec_gate_up_kernel, smem, &configured)) return rc;
     dim3 grid(F / QK, nexp);
-    matvec_gate_up_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.gate_q, set.gate_d, set.up_q, set.up_d, D, F,
+    matvec_gate_up_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.gate_q, set.gate_d, set.gate_m, set.up_q, set.up_d,
+                                                           set.up_m, D, F,
                                                            is_shared, x_q, x_d, expStart, expTokI, N, top_k,
                                                            h_q, h_d, dbg_dots, dbg_block, status);
     return launch_status();
@@ -298,7 +314,7 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_sha
     static int configured = 0;
     if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel, smem, &configured)) return rc;
     dim3 grid(D / QK, nexp);
-    matvec_down_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, D, F, is_shared, h_q, h_d,
+    matvec_down_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, is_shared, h_q, h_d,
                                                         expStart, expTokI, expTokK, N, top_k, shexp_scale,
                                                         out, status);
     return launch_status();

@@ -59,6 +59,8 @@ WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs) {
         L.xg_dT = take((size_t)(D / QK) * L.rows_max * 4);
         L.h16 = take((size_t)L.rows_max * Fmax * 2);
         L.h_dT = take((size_t)(Fmax / QK) * L.rows_max * 4);
+        L.xg_sT = take((size_t)(D / QK) * L.rows_max * 4);
+        L.h_sT = take((size_t)(Fmax / QK) * L.rows_max * 4);
     }
     L.total = off;
     return L;
@@ -156,11 +158,21 @@ int moe_status_from_word(int word) {
 
 int moe_weights_create(moe_weights_t *out, int E, int D, int F, const void *gate, const void *up, const void *down,
                        int Fs, const void *sh_gate, const void *sh_up, const void *sh_down, cudaStream_t stream) {
+    return moe_weights_create_ex(out, MOE_WFMT_Q8_0, E, D, F, gate, up, down, Fs, sh_gate, sh_up, sh_down, stream);
+}
+
+int moe_weights_format(moe_weights_t w) { return w ? w->wfmt : MOE_ERR_INVALID_ARG; }
+
+int moe_weights_create_ex(moe_weights_t *out, int format, int E, int D, int F, const void *gate, const void *up,
+                          const void *down, int Fs, const void *sh_gate, const void *sh_up, const void *sh_down,
+                          cudaStream_t stream) {
     if (out == nullptr) return MOE_ERR_INVALID_ARG;
     *out = nullptr;
     if (!gate || !up || !down) return MOE_ERR_INVALID_ARG;
+    if (format != MOE_WFMT_Q8_0 && format != MOE_WFMT_Q4_K) return MOE_ERR_INVALID_ARG;
     if (Fs < 0 || (Fs > 0 && (!sh_gate || !sh_up || !sh_down))) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > MAX_E || D < QK || D % QK || F < QK || F % QK || Fs % QK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (format == MOE_WFMT_Q4_K && (D % QK_K || F % QK_K || Fs % QK_K)) return MOE_ERR_UNSUPPORTED_SHAPE;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -174,6 +186,7 @@ int moe_weights_create(moe_weights_t *out, int E, int D, int F, const void *gate
     w->F = F;
     w->Fs = Fs;
     w->device = dev;
+    w->wfmt = format;
     w->tensor_ok = tensor_shapes(D, F, Fs);
     int rc = repack_weights(w, gate, up, down, sh_gate, sh_up, sh_down, stream);
     if (!rc && w->tensor_ok) rc = prepare_tensor_maps(w);

@@ -10,7 +10,9 @@
 
 namespace moe {
 
-constexpr int QK = 32;          // values per Q8 block
+constexpr int QK = 32;          // values per Q8 block (and per Q4_K sub-block)
+constexpr int QK_K = 256;       // values per Q4_K super-block
+constexpr int Q4_K_BYTES = 144; // fp16 d, fp16 dmin, 12 bytes of 6-bit scales/mins, 128 bytes of nibbles
 constexpr int Q8_0_BYTES = 34;  // fp16 scale + 32 int8
 constexpr int MAX_E = 1024;
 constexpr int SEG_ALIGN = 16;   // padded segment start (rows) in the tensor-core row space
@@ -27,11 +29,15 @@ struct WeightSet {
     float *gate_d = nullptr, *up_d = nullptr;   // [nexp][F][D/32]
     int8_t *down_q = nullptr;                   // [nexp][D][F]
     float *down_d = nullptr;                    // [nexp][D][F/32]
+    // Q4_K only: per-32-block mins dmin*m (the weight is d*sc*q - dmin*m, quants 0..15 above)
+    float *gate_m = nullptr, *up_m = nullptr, *down_m = nullptr;  // same shapes as the scales
     // tensor path: exact fp16 integers in tile-interleaved order + transposed scales
     __half *gu16 = nullptr;   // [nexp][2F][D]: 128-row tile mt = 64 gate rows then 64 up rows
     float *gu_dT = nullptr;   // [nexp][D/32][2F] (same row order)
     __half *dn16 = nullptr;   // [nexp][D][F]
     float *dn_dT = nullptr;   // [nexp][F/32][D]
+    float *gu_mT = nullptr;   // Q4_K: mins, as gu_dT
+    float *dn_mT = nullptr;   // Q4_K: mins, as dn_dT
 };
 
 }  // namespace moe
@@ -39,6 +45,7 @@ struct WeightSet {
 struct moe_weights_s {
     int E = 0, D = 0, F = 0, Fs = 0;
     int device = -1;
+    int wfmt = MOE_WFMT_Q8_0;  // block format of the caller's expert weights
     bool tensor_ok = false;  // shapes fit the tensor-core path
     moe::WeightSet routed;   // E experts
     moe::WeightSet shared;   // 1 expert (Fs > 0)
@@ -55,6 +62,7 @@ struct WsLayout {
     size_t partials, shared_out, part_logits, total;
     // tensor path
     size_t plan, tiles, rowinfo, xg16, xg_dT, h16, h_dT;
+    size_t xg_sT, h_sT;  // Q4_K: per-block code sums times scale ([K/32][rows], as the scales)
     // matvec path
     size_t hq8, hd8;
     int nsplit;      // router split-K factor

@@ -1,4 +1,4 @@
-// weights.cu -- one-time repack of the caller's Q8_0 expert tensors into the
+// weights.cu -- one-time repack of the caller's Q8_0 (or Q4_K) expert tensors into the
 // library-owned layouts the kernels read (load time, not on the hot path).
 //
 // GGUF Q8_0 stores each 32-block as 34 bytes (fp16 scale + 32 int8), which
@@ -62,14 +62,76 @@ __global__ void repack_kernel(const uint8_t *__restrict__ src, int nmat, int row
     }
 }
 
-int repack(const void *src, int nmat, int rows, int K, int8_t *q, float *d, __half *h16, float *dT,
-           int interleave, int up_half, cudaStream_t s) {
+// Q4_K rows (K/256 super-blocks of 144 bytes each) into the same layouts: quants 0..15 as int8
+// (and exact fp16), per-32-block scale d*sc_j and min dmin*m_j as fp32 (both exact: 11-bit
+// fp16 times a 6-bit integer).  One thread per 32-wide sub-block.
+__global__ void repack_q4k_kernel(const uint8_t *__restrict__ src, int nmat, int rows, int nblk,
+                                  int8_t *__restrict__ q, float *__restrict__ d, float *__restrict__ mn,
+                                  __half *__restrict__ h16, float *__restrict__ dT, float *__restrict__ mT,
+                                  int interleave_gu, int up_half) {
+    const int64_t total = (int64_t)nmat * rows * nblk;
+    const int64_t row_bytes = (int64_t)(nblk / 8) * Q4_K_BYTES;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t mr = i / nblk;  // matrix * rows + row
+        const int b = (int)(i - mr * nblk);
+        const int m = (int)(mr / rows);
+        const int r = (int)(mr - (int64_t)m * rows);
+        const int j = b & 7;  // sub-block inside its super-block
+        const uint8_t *blk = src + mr * row_bytes + (int64_t)(b >> 3) * Q4_K_BYTES;
+        const float dd = __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(blk[2] | (blk[3] << 8))));
+        const uint8_t *s12 = blk + 4;
+        int sc, mm;
+        if (j < 4) {
+            sc = s12[j] & 63;
+            mm = s12[j + 4] & 63;
+        } else {
+            sc = (s12[j + 4] & 15) | ((s12[j - 4] >> 6) << 4);
+            mm = (s12[j + 4] >> 4) | ((s12[j] >> 6) << 4);
+        }
+        const float scale = dd * (float)sc, minv = dmin * (float)mm;
+        const uint8_t *qs = blk + 16 + 32 * (j >> 1);
+        alignas(16) int8_t vals[QK];
+#pragma unroll
+        for (int l = 0; l < QK; ++l) vals[l] = (int8_t)((j & 1) ? (qs[l] >> 4) : (qs[l] & 15));
+        const int K = nblk * QK;
+        if (q != nullptr) {
+            int4 *dst = reinterpret_cast<int4 *>(q + mr * K + (int64_t)b * QK);
+            dst[0] = *reinterpret_cast<const int4 *>(vals);
+            dst[1] = *reinterpret_cast<const int4 *>(vals + 16);
+            d[mr * nblk + b] = scale;
+            mn[mr * nblk + b] = minv;
+        }
+        if (h16 != nullptr) {
+            int64_t rr = r;
+            int64_t rows_out = rows;
+            if (interleave_gu) {
+                rows_out = 2 * (int64_t)rows;
+                rr = (int64_t)(r / 64) * 128 + (up_half ? 64 : 0) + (r % 64);
+            }
+            __half *dst = h16 + ((int64_t)m * rows_out + rr) * K + (int64_t)b * QK;
+#pragma unroll
+            for (int l = 0; l < QK; l += 2)
+                *reinterpret_cast<__half2 *>(dst + l) = __halves2half2(__int2half_rn(vals[l]), __int2half_rn(vals[l + 1]));
+            dT[((int64_t)m * nblk + b) * rows_out + rr] = scale;
+            mT[((int64_t)m * nblk + b) * rows_out + rr] = minv;
+        }
+    }
+}
+
+int repack(int wfmt, const void *src, int nmat, int rows, int K, int8_t *q, float *d, float *mn, __half *h16,
+           float *dT, float *mT, int interleave, int up_half, cudaStream_t s) {
     int64_t total = (int64_t)nmat * rows * (K / QK);
     if (total == 0) return MOE_OK;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    repack_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
-                                                   h16, dT, interleave, up_half);
+    if (wfmt == MOE_WFMT_Q4_K)
+        repack_q4k_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
+                                                           mn, h16, dT, mT, interleave, up_half);
+    else
+        repack_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
+                                                       h16, dT, interleave, up_half);
     return launch_status();
 }
 
@@ -78,7 +140,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
 // Sizes of one weight set's arrays; carve == true assigns pointers from base.
-static size_t layout_set(WeightSet &ws, int nexp, int D, int F, bool tensor, char *base) {
+static size_t layout_set(WeightSet &ws, int nexp, int D, int F, bool tensor, int wfmt, char *base) {
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -94,11 +156,21 @@ static size_t layout_set(WeightSet &ws, int nexp, int D, int F, bool tensor, cha
     ws.up_d = (float *)take(gu / QK * sizeof(float));
     ws.down_q = (int8_t *)take(dn);
     ws.down_d = (float *)take(dn / QK * sizeof(float));
+    const bool mins = wfmt == MOE_WFMT_Q4_K;
+    if (mins) {
+        ws.gate_m = (float *)take(gu / QK * sizeof(float));
+        ws.up_m = (float *)take(gu / QK * sizeof(float));
+        ws.down_m = (float *)take(dn / QK * sizeof(float));
+    }
     if (tensor) {
         ws.gu16 = (__half *)take(2 * gu * sizeof(__half));
         ws.gu_dT = (float *)take(2 * gu / QK * sizeof(float));
         ws.dn16 = (__half *)take(dn * sizeof(__half));
         ws.dn_dT = (float *)take(dn / QK * sizeof(float));
+        if (mins) {
+            ws.gu_mT = (float *)take(2 * gu / QK * sizeof(float));
+            ws.dn_mT = (float *)take(dn / QK * sizeof(float));
+        }
     }
     return off;
 }
@@ -107,19 +179,21 @@ int repack_weights(moe_weights_s *w, const void *gate, const void *up, const voi
                    const void *sh_up, const void *sh_down, cudaStream_t s) {
     const int E = w->E, D = w->D, F = w->F, Fs = w->Fs;
     const bool tensor = w->tensor_ok;
-    size_t r_bytes = layout_set(w->routed, E, D, F, tensor, nullptr);
-    size_t s_bytes = Fs ? layout_set(w->shared, 1, D, Fs, tensor, nullptr) : 0;
+    const int wf = w->wfmt;
+    size_t r_bytes = layout_set(w->routed, E, D, F, tensor, wf, nullptr);
+    size_t s_bytes = Fs ? layout_set(w->shared, 1, D, Fs, tensor, wf, nullptr) : 0;
     char *arena = nullptr;
     if (cudaMalloc(&arena, r_bytes + s_bytes) != cudaSuccess) return MOE_ERR_CUDA;
     w->bytes = r_bytes + s_bytes;
-    layout_set(w->routed, E, D, F, tensor, arena);
-    if (Fs) layout_set(w->shared, 1, D, Fs, tensor, arena + r_bytes);
+    layout_set(w->routed, E, D, F, tensor, wf, arena);
+    if (Fs) layout_set(w->shared, 1, D, Fs, tensor, wf, arena + r_bytes);
     // the arena start doubles as the handle's allocation
     w->routed_arena_ = arena;
     auto sets = [&](WeightSet &ws, int nexp, int Fx, const void *g, const void *u, const void *dn) {
-        int rc = repack(g, nexp, Fx, D, ws.gate_q, ws.gate_d, ws.gu16, ws.gu_dT, 1, 0, s);
-        if (!rc) rc = repack(u, nexp, Fx, D, ws.up_q, ws.up_d, ws.gu16, ws.gu_dT, 1, 1, s);
-        if (!rc) rc = repack(dn, nexp, D, Fx, ws.down_q, ws.down_d, ws.dn16, ws.dn_dT, 0, 0, s);
+        int rc = repack(wf, g, nexp, Fx, D, ws.gate_q, ws.gate_d, ws.gate_m, ws.gu16, ws.gu_dT, ws.gu_mT, 1, 0, s);
+        if (!rc) rc = repack(wf, u, nexp, Fx, D, ws.up_q, ws.up_d, ws.up_m, ws.gu16, ws.gu_dT, ws.gu_mT, 1, 1, s);
+        if (!rc)
+            rc = repack(wf, dn, nexp, D, Fx, ws.down_q, ws.down_d, ws.down_m, ws.dn16, ws.dn_dT, ws.dn_mT, 0, 0, s);
         return rc;
     };
     int rc = sets(w->routed, E, F, gate, up, down);

@@ -29,6 +29,8 @@ _SIGS = {
     "moe_abi_version": (_I, []),
     "moe_status_from_word": (_I, [_I]),
     "moe_weights_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "moe_weights_create_ex": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "moe_weights_format": (_I, [_P]),
     "moe_weights_destroy": (_I, [_P]),
     "moe_weights_shape": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "moe_weights_device_bytes": (_SZ, [_P]),
@@ -108,19 +110,26 @@ def _stream(stream) -> _P:
 
 
 # --------------------------------------------------------------- weights ---
+WEIGHT_FORMATS = {"q8_0": 0, "q4_k": 1}  # MOE_WFMT_*
+
+
 class MoeWeights:
     """Library-owned expert weights (moe_weights_create / moe_weights_destroy)."""
 
     def __init__(self, gate: torch.Tensor, up: torch.Tensor, down: torch.Tensor, E: int, D: int, F: int,
                  sh_gate: torch.Tensor | None = None, sh_up: torch.Tensor | None = None,
-                 sh_down: torch.Tensor | None = None, Fs: int = 0, stream=None):
+                 sh_down: torch.Tensor | None = None, Fs: int = 0, stream=None, wfmt: str = "q8_0"):
         self.handle = _P()
         self.E, self.D, self.F, self.Fs = E, D, F, Fs
-        rc = lib().moe_weights_create(ctypes.byref(self.handle), E, D, F, _dev(gate, torch.uint8, "gate"),
-                                      _dev(up, torch.uint8, "up"), _dev(down, torch.uint8, "down"), Fs,
-                                      _dev(sh_gate, torch.uint8, "sh_gate"), _dev(sh_up, torch.uint8, "sh_up"),
-                                      _dev(sh_down, torch.uint8, "sh_down"), _stream(stream))
-        _check(rc, "moe_weights_create")
+        self.wfmt = wfmt
+        if wfmt not in WEIGHT_FORMATS:
+            raise ValueError(f"unknown weight format {wfmt!r}")
+        rc = lib().moe_weights_create_ex(ctypes.byref(self.handle), WEIGHT_FORMATS[wfmt], E, D, F,
+                                         _dev(gate, torch.uint8, "gate"), _dev(up, torch.uint8, "up"),
+                                         _dev(down, torch.uint8, "down"), Fs, _dev(sh_gate, torch.uint8, "sh_gate"),
+                                         _dev(sh_up, torch.uint8, "sh_up"), _dev(sh_down, torch.uint8, "sh_down"),
+                                         _stream(stream))
+        _check(rc, "moe_weights_create_ex")
 
     @property
     def device_bytes(self) -> int:
@@ -145,8 +154,14 @@ def moe_weights_tensor_path(w: MoeWeights) -> bool:
 tensor_path_available = moe_weights_tensor_path
 
 
-def moe_weights_create(E, D, F, gate, up, down, Fs=0, sh_gate=None, sh_up=None, sh_down=None, stream=None):
-    return MoeWeights(gate, up, down, E, D, F, sh_gate, sh_up, sh_down, Fs, stream)
+def moe_weights_create(E, D, F, gate, up, down, Fs=0, sh_gate=None, sh_up=None, sh_down=None, stream=None,
+                       wfmt="q8_0"):
+    return MoeWeights(gate, up, down, E, D, F, sh_gate, sh_up, sh_down, Fs, stream, wfmt)
+
+
+def moe_weights_format(w: MoeWeights) -> str:
+    code = int(lib().moe_weights_format(w.handle))
+    return {v: k for k, v in WEIGHT_FORMATS.items()}[code]
 
 
 def moe_weights_destroy(w: MoeWeights) -> None:
@@ -456,7 +471,7 @@ class MoeLayer:
             return torch.from_numpy(a if a.flags.writeable else a.copy()).to(dev)
 
         w = MoeWeights(up(inp["gate"]), up(inp["up"]), up(inp["down"]), E, D, F, up(inp.get("sh_gate")),
-                       up(inp.get("sh_up")), up(inp.get("sh_down")), Fs)
+                       up(inp.get("sh_up")), up(inp.get("sh_down")), Fs, wfmt=inp.get("wfmt", "q8_0"))
         k = top_k if top_k is not None else min(8, E)
         N = max_tokens if max_tokens is not None else inp["hidden"].shape[0]
         return cls(w, up(inp["routerW"]), up(inp.get("shexp_gate")), N, k)

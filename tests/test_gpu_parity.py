@@ -26,6 +26,7 @@ W_RTOL = 2e-5
 
 CONFIGS = ["tiny", "olmoe", "decode_n1", "decode_n4", "decode_n8", "qwen3moe_shared", "skewed"]
 SMALL = ["tiny", "decode_n4", "qwen3moe_shared"]
+Q4K = ["tiny_q4k", "q4k_shared", "olmoe_q4k"]  # the same layer with Q4_K expert weights
 
 
 @pytest.fixture(scope="module")
@@ -247,7 +248,7 @@ def _csr(ref):
     return dev(ref["expStart"]), dev(ref["expTokI"]), dev(ref["expTokK"])
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe"])
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "tiny_q4k", "olmoe_q4k"])
 @pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_block_dots_bit_exact(ops, name, path):
     wl, inp, ref = case(name)
@@ -268,11 +269,14 @@ def test_gate_up_block_dots_bit_exact(ops, name, path):
             t = int(ref["expTokI"][j])
             for mat, W in ((0, inp["gate"]), (1, inp["up"])):
                 for f in (0, wl.F // 2 + 3, wl.F - 1):
-                    ref_dot = O.block_dots(W[e, f], ref["x_q"][t])[block]
+                    if wl.wfmt == "q4_k":
+                        ref_dot = O.block_dots_q4_k(W[e, f], ref["x_q"][t])[block]
+                    else:
+                        ref_dot = O.block_dots(W[e, f], ref["x_q"][t])[block]
                     assert dots[j, mat, f] == ref_dot, (j, mat, f, block)
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_requantised_activations(ops, name, path):
     """h_q from the oracle's x_q and CSR: codes within +-1 (fp32 vs double accumulation can
@@ -294,7 +298,7 @@ def test_gate_up_requantised_activations(ops, name, path):
     np.testing.assert_allclose(hd, rd, rtol=1e-3, atol=1e-30)
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_down_given_oracle_h(ops, name, path):
     """The down half on the oracle's own h_q: partials to fp32 accumulation accuracy."""
@@ -314,7 +318,7 @@ def test_down_given_oracle_h(ops, name, path):
     assert rel <= 1e-5, rel
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"])
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_grouped_ffn_partials(ops, name, path):
     wl, inp, ref = case(name)
@@ -404,7 +408,7 @@ def test_layer_with_residual(ops, name):
 
 
 # ---------------------------------------------------------- whole layer ---
-@pytest.mark.parametrize("name", CONFIGS)
+@pytest.mark.parametrize("name", CONFIGS + Q4K)
 @pytest.mark.parametrize("path", [0, 1, 2])
 def test_layer_parity(ops, name, path):
     """moe_ffn_prefill (the call bench.py times, path 0 = its launch configuration)."""
@@ -487,6 +491,20 @@ def test_prefill_host_pageable_memory_where_addressable(ops):
     else:
         with pytest.raises(ops.MoeError):
             ops.moe_ffn_prefill_host(layer.w, h_pg, layer.routerW, None, wl.top_k, wl.norm_topk_prob, layer.ws, o_pg)
+
+
+def test_q4_k_weights_handle_and_shapes(ops):
+    """The handle reports its format; Q4_K needs D, F, Fs multiples of 256 (UNSUPPORTED_SHAPE otherwise)."""
+    wl, inp, _ = case("tiny_q4k")
+    layer = layer_for(ops, inp, wl)
+    assert ops.moe_weights_format(layer.w) == "q4_k"
+    wl8, inp8, _ = case("tiny")
+    assert ops.moe_weights_format(layer_for(ops, inp8, wl8).w) == "q8_0"
+    g = torch.zeros((2, 128, 144), dtype=torch.uint8, device="cuda")  # D = 256 but F = 128
+    d = torch.zeros((2, 256, 72), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ops.MoeError) as e:
+        ops.MoeWeights(g, g, d, 2, 256, 128, wfmt="q4_k")
+    assert e.value.code == -2
 
 
 def test_zero_hidden_gives_zero(ops):
