@@ -406,8 +406,8 @@ def run_ours(args, rank, world, local_rank):
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, keyed by
 # (stage, workload), with the sha256 prefix of the kernel source the counters were taken on
 # (profiles/grouped_gemm_olmoe.md); reported only while the source is unchanged.
-TRAFFIC = {("gate_up", "olmoe"): (678.344192e6, "mixture_experts_ffn_top_gb300/csrc/expert_gemm.cu",
-                                  "f991bb656e664d44")}
+TRAFFIC = {("gate_up", "olmoe"): (679.342080e6, "mixture_experts_ffn_top_gb300/csrc/expert_gemm.cu",
+                                  "3eab63c9dc15455b")}
 
 
 def measured_traffic(stage, workload):
