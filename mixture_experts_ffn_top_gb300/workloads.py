@@ -41,6 +41,16 @@ against the super-block's fp16 d = max step/63 and dmin = max offset/63, then
 rounds every value to its 4-bit code; any valid encoding would do, since both
 sides decode the bytes.
 
+Workloads with ``wfmt="q3_k"`` deliver GGUF Q3_K super-blocks (256 values in
+110 bytes: a 32-byte high-bit mask, 64 bytes of 2-bit low parts, twelve bytes
+of sixteen packed 6-bit signed sub-block scales s_j, fp16 d; value d*s_j*q with
+q in [-4, 3]), the format of the routed experts on the Carnice prefill page
+(#388 "Key references": the Q3_K GPU kernel).  The packer takes, per 16-wide
+sub-block, the value of largest magnitude v and the step -v/4 (so v codes to
+-4, the longer side of the range), codes the steps against the super-block's
+fp16 d = max |step|/32, clips s_j to [-32, 31], then rounds every value to its
+3-bit code.  Steps of either sign occur, and so do s_j = -32 with q = -4.
+
 The pages ("batched int8-MMQ trunk prefill gated off for MoE", #406; "Carnice
 prefill toward llama.cpp 676 t/s", #388) benchmark whole models (OLMoE-1B-7B,
 a 35B-A3B hybrid) whose trained weights are not used here: these synthetic
@@ -59,6 +69,7 @@ QK = 32
 Q8_0_BYTES = 34
 QK_K = 256
 Q4_K_BYTES = 144
+Q3_K_BYTES = 110
 
 
 @dataclass(frozen=True)
@@ -73,7 +84,7 @@ class Workload:
     norm_topk_prob: bool
     seed: int
     skew: bool = False
-    wfmt: str = "q8_0"  # expert weight format: "q8_0" or "q4_k"
+    wfmt: str = "q8_0"  # expert weight format: "q8_0", "q4_k" or "q3_k"
 
     @property
     def has_shared(self) -> bool:
@@ -111,14 +122,21 @@ WORKLOADS = {
                            seed=5, wfmt="q4_k"),
     "olmoe_q4k": Workload("olmoe_q4k", N=2048, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False,
                           seed=1, wfmt="q4_k"),
+    # and with Q3_K expert weights
+    "tiny_q3k": Workload("tiny_q3k", N=64, D=256, E=8, top_k=2, F=256, Fs=0, norm_topk_prob=False, seed=0,
+                         wfmt="q3_k"),
+    "q3k_shared": Workload("q3k_shared", N=256, D=512, E=16, top_k=4, F=256, Fs=256, norm_topk_prob=True,
+                           seed=6, wfmt="q3_k"),
+    "olmoe_q3k": Workload("olmoe_q3k", N=2048, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False,
+                          seed=1, wfmt="q3_k"),
 }
 
 
 def row_bytes(wfmt: str, K: int) -> int:
     """Bytes of one weight row of K values in the given block format."""
-    if wfmt == "q4_k":
+    if wfmt in ("q4_k", "q3_k"):
         assert K % QK_K == 0
-        return K // QK_K * Q4_K_BYTES
+        return K // QK_K * (Q4_K_BYTES if wfmt == "q4_k" else Q3_K_BYTES)
     assert wfmt == "q8_0" and K % QK == 0
     return K // QK * Q8_0_BYTES
 
@@ -177,8 +195,44 @@ def pack_q4_k(w: np.ndarray) -> np.ndarray:
     return out.reshape(rows, nsb * Q4_K_BYTES)
 
 
+def pack_q3_k(w: np.ndarray) -> np.ndarray:
+    """Pack fp32 weights ``[rows, K]`` into GGUF Q3_K super-blocks ``uint8[rows, K/256*110]``."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, K = w.shape
+    assert K % QK_K == 0
+    nsb = K // QK_K
+    x = w.reshape(rows, nsb, 16, 16).astype(np.float64)
+    big = np.take_along_axis(x, np.abs(x).argmax(axis=3)[..., None], axis=3)[..., 0]
+    step = -big / 4.0  # [rows, nsb, 16]
+    d16 = (np.abs(step).max(axis=2) / 32.0).astype(np.float16)
+    d = d16.astype(np.float64)[..., None]
+    s = np.where(d > 0, np.clip(np.rint(step / np.where(d > 0, d, 1.0)), -32, 31), 0)
+    qstep = (d * s)[..., None]
+    q = np.where(qstep != 0, np.clip(np.rint(x / np.where(qstep != 0, qstep, 1.0)), -4, 3), 0)
+    q = (q.astype(np.int64) + 4).reshape(rows, nsb, QK_K)  # 0..7: low two bits + high bit
+    raw = (s.astype(np.int64) + 32).astype(np.uint8)  # [rows, nsb, 16], 0..63
+    out = np.zeros((rows, nsb, Q3_K_BYTES), np.uint8)
+    hbit = (q >> 2) & 1
+    low = q & 3
+    for b in range(8):  # hmask: bit b of byte l holds value 32*b + l
+        out[..., 0:32] |= (hbit[..., 32 * b:32 * b + 32] << b).astype(np.uint8)
+    for i0 in range(0, QK_K, 32):  # qs: value i in byte 32 + 32*(i/128) + i%32 at bits 2*((i%128)/32)
+        byte0 = 32 + 32 * (i0 // 128)
+        shift = 2 * ((i0 % 128) // 32)
+        out[..., byte0:byte0 + 32] |= (low[..., i0:i0 + 32] << shift).astype(np.uint8)
+    out[..., 96:104] = (raw[..., 0:8] & 15) | ((raw[..., 8:16] & 15) << 4)
+    for g in range(4):  # byte 100 + 8 + m: high bits of scales m, m+4, m+8, m+12
+        out[..., 104:108] |= ((raw[..., 4 * g:4 * g + 4] >> 4) << (2 * g)).astype(np.uint8)
+    out[..., 108:110] = d16.view(np.uint8).reshape(rows, nsb, 2)
+    return out.reshape(rows, nsb * Q3_K_BYTES)
+
+
 def pack_weights(w: np.ndarray, wfmt: str) -> np.ndarray:
-    return pack_q4_k(w) if wfmt == "q4_k" else pack_q8_0(w)
+    if wfmt == "q4_k":
+        return pack_q4_k(w)
+    if wfmt == "q3_k":
+        return pack_q3_k(w)
+    return pack_q8_0(w)
 
 
 def _expert(seed: int, e: int, D: int, F: int, wfmt: str = "q8_0"):
@@ -211,7 +265,8 @@ def make_inputs(wl: Workload) -> dict:
     hidden f32[N,D], routerW f32[E,D], shexp_gate f32[D] or None,
     gate/up u8[E,F,row_bytes(D)], down u8[E,D,row_bytes(F)],
     sh_gate/sh_up u8[Fs,row_bytes(D)], sh_down u8[D,row_bytes(Fs)] (or None),
-    wfmt: the block format of those byte rows ("q8_0": D/32*34 bytes, "q4_k": D/256*144).
+    wfmt: the block format of those byte rows ("q8_0": D/32*34 bytes, "q4_k": D/256*144,
+    "q3_k": D/256*110).
     The expert arrays are shared read-only between calls with equal shapes.
     """
     N, D, E, F, Fs = wl.N, wl.D, wl.E, wl.F, wl.Fs

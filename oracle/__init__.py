@@ -153,7 +153,7 @@ def block_dots(w_row: np.ndarray, aq: np.ndarray) -> np.ndarray:
     return out
 
 
-FORMATS = {"q8_0": 0, "q4_k": 1}  # weight formats the oracle reads (GGUF block layouts)
+FORMATS = {"q8_0": 0, "q4_k": 1, "q3_k": 2}  # weight formats the oracle reads (GGUF block layouts)
 
 
 def _fmt(fmt: str) -> int:
@@ -176,6 +176,23 @@ def q4_k_dequant(w_row: np.ndarray, K: int) -> np.ndarray:
     w_row = np.ascontiguousarray(w_row, dtype=np.uint8)
     out = np.empty(K, np.float32)
     _L().oracle_q4_k_dequant(_p(w_row), _I(K), _p(out))
+    return out
+
+
+def block_dots_q3_k(w_row: np.ndarray, aq: np.ndarray) -> np.ndarray:
+    """Per 32-wide block of a Q3_K row: s_2b*isum_2b + s_2b+1*isum_2b+1 (int32)."""
+    w_row = np.ascontiguousarray(w_row, dtype=np.uint8)
+    aq = np.ascontiguousarray(aq, dtype=np.int8)
+    out = np.empty(aq.size // QK, np.int32)
+    _L().oracle_block_dots_q3_k(_p(w_row), _p(aq), _I(aq.size), _p(out))
+    return out
+
+
+def q3_k_dequant(w_row: np.ndarray, K: int) -> np.ndarray:
+    """A Q3_K row decoded to K fp32 values (d*s_j*q, rounded once)."""
+    w_row = np.ascontiguousarray(w_row, dtype=np.uint8)
+    out = np.empty(K, np.float32)
+    _L().oracle_q3_k_dequant(_p(w_row), _I(K), _p(out))
     return out
 
 

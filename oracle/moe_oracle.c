@@ -380,14 +380,106 @@ void oracle_block_dots_q4_k(const uint8_t *w_row, const int8_t *aq, int K, int32
         }
 }
 
+/* ------------------------------------------------------------------------
+ * Q3_K weights (the Carnice prefill page, #388 "Key references", names a
+ * Q3_K GPU expert kernel and Q3_K x Q8 CPU dots: the routed experts of that
+ * model are Q3_K; the layout is the GGUF one, which the pages do not spell
+ * out).  A super-block of QK_K = 256 values is 110 bytes:
+ *   bytes   0..31  hmask: bit (i / 32) of byte (i % 32) is value i's high bit h_i;
+ *   bytes  32..95  qs: bits 2*((i % 128) / 32) .. +1 of byte 32*(i / 128) + i % 32
+ *                  are value i's low two bits l_i;
+ *   bytes  96..107 sixteen 6-bit scales, one per 16-wide sub-block j = i / 16:
+ *                  low 4 bits = nibble (j / 8) of byte j % 8, high 2 bits =
+ *                  bits 2*(j / 4) .. +1 of byte 8 + j % 4; s_j = that - 32;
+ *   bytes 108..109 fp16 d.
+ * q_i = l_i - 4 when h_i is clear, l_i when it is set (q in [-4, 3]), and
+ *   w_i = d * s_j * q_i.
+ * Dot with a Q8_1 row, per 32-wide activation block b (sub-blocks 2b, 2b+1):
+ *   result = sum_b fp16(da_b) * d * (s_2b * isum_2b + s_2b+1 * isum_2b+1)
+ * with isum_j the exact int32 dot of sub-block j's q with the activation
+ * codes; accumulated in double (each term is exact in double).
+ * ---------------------------------------------------------------------- */
+#define Q3_K_BYTES 110
+enum { FMT_Q3_K = 2 };
+
+static int q3_k_scale(const uint8_t *blk, int j)
+{
+    const uint8_t *s12 = blk + 96;
+    int lo = (s12[j % 8] >> (4 * (j / 8))) & 15;
+    int hi = (s12[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return (lo | (hi << 4)) - 32;
+}
+
+static int q3_k_quant(const uint8_t *blk, int i)
+{
+    int l = (blk[32 + 32 * (i / 128) + i % 32] >> (2 * ((i % 128) / 32))) & 3;
+    int h = (blk[i % 32] >> (i / 32)) & 1;
+    return h ? l : l - 4;
+}
+
+/* sum over 32-wide block b of one super-block: s_j-weighted int dots (exact). */
+static int64_t q3_k_block_sisum(const uint8_t *blk, int b, const int8_t *aq_sb)
+{
+    int64_t sisum = 0;
+    for (int half = 0; half < 2; ++half) {
+        int j = 2 * b + half;
+        int32_t isum = 0;
+        for (int l = 0; l < 16; ++l)
+            isum += q3_k_quant(blk, 16 * j + l) * (int32_t)aq_sb[16 * j + l];
+        sisum += (int64_t)q3_k_scale(blk, j) * isum;
+    }
+    return sisum;
+}
+
+static double q3_k_row_dot(const uint8_t *w_row, const int8_t *aq, const uint16_t *ad16, int K)
+{
+    double acc = 0.0;
+    for (int sb = 0; sb < K / QK_K; ++sb) {
+        const uint8_t *blk = w_row + (size_t)sb * Q3_K_BYTES;
+        double d = oracle_half_to_float(load_u16(blk + 108));
+        for (int b = 0; b < 8; ++b) {
+            int64_t sisum = q3_k_block_sisum(blk, b, aq + sb * QK_K);
+            acc += (double)oracle_half_to_float(ad16[sb * 8 + b]) * d * (double)sisum;
+        }
+    }
+    return acc;
+}
+
+/* Dequantised Q3_K row (K values, each rounded once to fp32), for the pins. */
+void oracle_q3_k_dequant(const uint8_t *w_row, int K, float *out)
+{
+    for (int sb = 0; sb < K / QK_K; ++sb) {
+        const uint8_t *blk = w_row + (size_t)sb * Q3_K_BYTES;
+        double d = oracle_half_to_float(load_u16(blk + 108));
+        for (int i = 0; i < QK_K; ++i)
+            out[sb * QK_K + i] = (float)(d * q3_k_scale(blk, i / 16) * q3_k_quant(blk, i));
+    }
+}
+
+/* Per 32-wide block of a Q3_K row: s_2b * isum_2b + s_2b+1 * isum_2b+1 (int32). */
+void oracle_block_dots_q3_k(const uint8_t *w_row, const int8_t *aq, int K, int32_t *out)
+{
+    for (int sb = 0; sb < K / QK_K; ++sb)
+        for (int b = 0; b < 8; ++b)
+            out[sb * 8 + b] = (int32_t)q3_k_block_sisum(w_row + (size_t)sb * Q3_K_BYTES, b, aq + sb * QK_K);
+}
+
 static size_t row_bytes(int fmt, int K)
 {
-    return fmt == FMT_Q4_K ? (size_t)(K / QK_K) * Q4_K_BYTES : (size_t)(K / QK) * Q8_0_BYTES;
+    if (fmt == FMT_Q4_K)
+        return (size_t)(K / QK_K) * Q4_K_BYTES;
+    if (fmt == FMT_Q3_K)
+        return (size_t)(K / QK_K) * Q3_K_BYTES;
+    return (size_t)(K / QK) * Q8_0_BYTES;
 }
 
 static double row_dot(int fmt, const uint8_t *w_row, const int8_t *aq, const uint16_t *ad16, int K)
 {
-    return fmt == FMT_Q4_K ? q4_k_row_dot(w_row, aq, ad16, K) : q8_row_dot(w_row, aq, ad16, K / QK);
+    if (fmt == FMT_Q4_K)
+        return q4_k_row_dot(w_row, aq, ad16, K);
+    if (fmt == FMT_Q3_K)
+        return q3_k_row_dot(w_row, aq, ad16, K);
+    return q8_row_dot(w_row, aq, ad16, K / QK);
 }
 
 /* ------------------------------------------------------------------------
@@ -424,7 +516,7 @@ static void expert_down_row(int fmt, const uint8_t *Wd, int D, int F, const int8
         y[c] = row_dot(fmt, Wd + c * rb, hq, hd16, F);
 }
 
-/* Exported single-row pieces, for the pins (fmt: 0 Q8_0, 1 Q4_K). */
+/* Exported single-row pieces, for the pins (fmt: 0 Q8_0, 1 Q4_K, 2 Q3_K). */
 void oracle_expert_gate_up_fmt(int fmt, const uint8_t *Wg, const uint8_t *Wu, int D, int F,
                                const int8_t *xq, const uint16_t *xd16,
                                float *h, int8_t *hq, uint16_t *hd16, double *g, double *u)

@@ -51,6 +51,13 @@ MUTATIONS = [
     ("q4k_nibble_order", "q[l] = (int8_t)((j & 1) ? (p[l] >> 4) : (p[l] & 15));",
      "q[l] = (int8_t)((j & 1) ? (p[l] & 15) : (p[l] >> 4));"),
     ("q4k_scale_high_bits", "*sc = (s12[j + 4] & 15) | ((s12[j - 4] >> 6) << 4);", "*sc = (s12[j + 4] & 15);"),
+    ("q3k_high_bit_sense", "return h ? l : l - 4;", "return h ? l - 4 : l;"),
+    ("q3k_scale_offset", "return (lo | (hi << 4)) - 32;", "return (lo | (hi << 4)) - 31;"),
+    ("q3k_low_bits_shift", "(2 * ((i % 128) / 32))) & 3;", "(2 * ((i % 64) / 16))) & 3;"),
+    ("q3k_scale_high_bits_byte", "int hi = (s12[8 + j % 4] >> (2 * (j / 4))) & 3;",
+     "int hi = (s12[8 + j / 4] >> (2 * (j % 4))) & 3;"),
+    ("q3k_one_scale_per_block", "sisum += (int64_t)q3_k_scale(blk, j) * isum;",
+     "sisum += (int64_t)q3_k_scale(blk, 2 * b) * isum;"),
     ("combine_residual_first",
      "            if (S)\n                acc = acc + S[t * D + c];\n            acc = acc + R[t * D + c];",
      "            acc = acc + R[t * D + c];\n            if (S)\n                acc = acc + S[t * D + c];"),

@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 
 import oracle as O
-from mixture_experts_ffn_top_gb300.workloads import QK, Q4_K_BYTES, Q8_0_BYTES, QK_K, pack_q4_k, pack_q8_0
+from mixture_experts_ffn_top_gb300.workloads import (QK, Q3_K_BYTES, Q4_K_BYTES, Q8_0_BYTES, QK_K, pack_q3_k,
+                                                     pack_q4_k, pack_q8_0)
 
 F32_EPS = np.finfo(np.float32).eps
 
@@ -42,6 +43,30 @@ def dequant_q4_k(rows_bytes: np.ndarray) -> np.ndarray:
     q = np.stack([qs & 15, qs >> 4], axis=3).reshape(rows, -1, 8, 32)  # sub-block 2g low, 2g+1 high
     v = d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None]
     return v.reshape(rows, -1)
+
+
+def q3_k_fields(rows_bytes: np.ndarray):
+    """Q3_K bytes [rows, nsb*110] -> (d [rows, nsb], s [rows, nsb, 16], q [rows, nsb, 256]) decoded field by
+    field from the GGUF super-block definition: 32-byte high-bit mask, 64 bytes of 2-bit low parts,
+    12 bytes of sixteen 6-bit scales (offset 32), fp16 d; q = low - 4*(1 - high)."""
+    rows = rows_bytes.shape[0]
+    b = rows_bytes.reshape(rows, -1, Q3_K_BYTES).astype(np.int64)
+    d = rows_bytes.reshape(rows, -1, Q3_K_BYTES)[..., 108:110].copy().view(np.float16)[..., 0].astype(np.float64)
+    high = (b[..., None, 0:32] >> np.arange(8)[:, None]) & 1  # [.., 8, 32]: bit k of byte l = value 32k + l
+    qs = b[..., 32:96].reshape(rows, -1, 2, 1, 32)  # two 128-value halves
+    low = ((qs >> (2 * np.arange(4))[:, None]) & 3).reshape(rows, -1, 8, 32)  # value 128h + 32g + l
+    q = (low - 4 * (1 - high)).reshape(rows, -1, QK_K)
+    s12 = b[..., 96:108]
+    lo = np.concatenate([s12[..., 0:8] & 15, s12[..., 0:8] >> 4], axis=-1)  # scales 0..7, 8..15
+    hi = np.concatenate([(s12[..., 8:12] >> (2 * g)) & 3 for g in range(4)], axis=-1)  # scale 4g + m
+    return d, (lo | (hi << 4)) - 32, q
+
+
+def dequant_q3_k(rows_bytes: np.ndarray) -> np.ndarray:
+    """Q3_K bytes -> float64 [rows, nsb*256]: d*s_j*q_i, j = i/16."""
+    d, sc, q = q3_k_fields(rows_bytes)
+    v = d[..., None, None] * sc[..., None] * q.reshape(*q.shape[:-1], 16, 16)
+    return v.reshape(rows_bytes.shape[0], -1)
 
 
 def dequant_q8(q: np.ndarray, d16: np.ndarray) -> np.ndarray:
@@ -374,6 +399,113 @@ def test_q4_k_single_expert_layer_is_dense_swiglu():
     ref = (g / (1 + np.exp(-g)) * u) @ dequant_q4_k(inp["down"][0]).T
     assert np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref) < 1e-2
     ref_exact = dequant_q8(r["h_q"], r["h_d16"]) @ dequant_q4_k(inp["down"][0]).T
+    np.testing.assert_allclose(r["out"][r["expTokI"]], ref_exact.astype(np.float32), rtol=1e-6, atol=1e-9)
+
+
+_Q3_RAW = [0, 5, 9, 13, 17, 21, 25, 29, 34, 38, 42, 46, 50, 54, 58, 63]  # 6-bit scale fields; s_j = raw - 32
+
+
+def _hand_q3_k_block() -> np.ndarray:
+    """One Q3_K super-block written byte by byte: d = 0.5, scale fields _Q3_RAW (s_0 = -32, s_15 = 31),
+    value i coded as q_i = (i % 8) - 4, so every quant byte repeats one 2-bit field and every
+    hmask byte is all ones (l % 8 >= 4) or all zeros."""
+    blk = np.zeros(Q3_K_BYTES, np.uint8)
+    for l in range(32):
+        blk[l] = 0xFF if l % 8 >= 4 else 0x00
+        blk[32 + l] = blk[64 + l] = ((l % 8) & 3) * 0x55
+    for j in range(8):
+        blk[96 + j] = (_Q3_RAW[j] & 15) | ((_Q3_RAW[j + 8] & 15) << 4)
+    for m in range(4):
+        blk[104 + m] = sum((_Q3_RAW[4 * g + m] >> 4) << (2 * g) for g in range(4))
+    blk[108:110] = [0x00, 0x38]  # fp16 0.5
+    return blk
+
+
+def test_q3_k_hand_block_decodes_to_the_format_values():
+    """d*s_j*q on the hand-written block, by hand: value 0 = 0.5*(-32)*(-4) = 64; value 7 = 0.5*(-32)*3 = -48;
+    value 16 = 0.5*(-27)*(-4) = 54; value 255 = 0.5*31*3 = 46.5; in general 0.5*(raw_(i/16) - 32)*((i % 8) - 4)."""
+    got = O.q3_k_dequant(_hand_q3_k_block(), QK_K)
+    assert (got[0], got[7], got[16], got[255]) == (64.0, -48.0, 54.0, 46.5)
+    want = np.array([0.5 * (_Q3_RAW[i // 16] - 32) * ((i % 8) - 4) for i in range(QK_K)])
+    assert np.all(got == want)
+    assert np.all(dequant_q3_k(_hand_q3_k_block()[None])[0] == want)
+
+
+def test_q3_k_dequant_matches_format_definition():
+    rng = np.random.default_rng(50)
+    rows = pack_q3_k((rng.standard_normal((6, 512)) * 0.02).astype(np.float32))
+    ref = dequant_q3_k(rows).astype(np.float32)
+    got = np.stack([O.q3_k_dequant(r, 512) for r in rows])
+    np.testing.assert_array_equal(got, ref)
+    # the generator reaches both ends of the code range, both signs of scale and s = -32 with q = -4
+    _, sc, q = q3_k_fields(rows)
+    assert q.min() == -4 and q.max() == 3 and (sc < 0).any() and (sc > 0).any()
+    assert ((np.repeat(sc, 16, axis=-1) == -32) & (q == -4)).any()
+
+
+def test_q3_k_block_dots_integer_brute_force():
+    rng = np.random.default_rng(51)
+    rows = pack_q3_k((rng.standard_normal((1, 512)) * 0.02).astype(np.float32))
+    aq = rng.integers(-127, 128, 512).astype(np.int8)
+    # integer codes s_j * q_i from the field-by-field decoder
+    _, sc, q = q3_k_fields(rows)
+    codes = (np.repeat(sc, 16, axis=-1) * q).reshape(-1, 32)
+    ref = (codes * aq.reshape(-1, 32).astype(np.int64)).sum(axis=1)
+    np.testing.assert_array_equal(O.block_dots_q3_k(rows[0], aq), ref)
+    # hand block against all-127 codes: block 0 = 127 * (-32 * -8 + -27 * -8) = 59944
+    assert O.block_dots_q3_k(_hand_q3_k_block(), np.full(256, 127, np.int8))[0] == 127 * 8 * (32 + 27)
+    # extreme block: every q = -4 with s = -32 gives 2 * 16 * 128 * 127 per 32-wide block, exact
+    ext = np.zeros(Q3_K_BYTES, np.uint8)
+    ext[108:110] = [0x00, 0x3C]
+    got = O.block_dots_q3_k(ext, np.full(256, 127, np.int8))
+    assert got.tolist() == [32 * 128 * 127] * 8
+
+
+@pytest.fixture(scope="module")
+def small_expert_q3_k():
+    rng = np.random.default_rng(52)
+    D, F = 256, 512
+    Wg = pack_q3_k((rng.standard_normal((F, D)) * 0.02).astype(np.float32))
+    Wu = pack_q3_k((rng.standard_normal((F, D)) * 0.02).astype(np.float32))
+    Wd = pack_q3_k((rng.standard_normal((D, F)) * 0.02).astype(np.float32))
+    x = rng.standard_normal(D).astype(np.float32)
+    xq, xd16, _ = O.quantize_q8_1(x)
+    return D, F, Wg, Wu, Wd, xq, xd16
+
+
+def test_q3_k_expert_matches_dequantised_matmul(small_expert_q3_k):
+    """Q3_K gate/up and down against numpy float64 matmuls of the dequantised operands."""
+    D, F, Wg, Wu, Wd, xq, xd16 = small_expert_q3_k
+    h, hq, hd16, g, u = O.expert_gate_up(Wg, Wu, D, F, xq, xd16, fmt="q3_k")
+    xdq = dequant_q8(xq, xd16)
+    for got, W in ((g, Wg), (u, Wu)):
+        Wdq = dequant_q3_k(W)
+        assert np.all(np.abs(got - Wdq @ xdq) <= 1e-12 * (np.abs(Wdq) @ np.abs(xdq)))
+    y = O.expert_down(Wd, D, F, hq, hd16, fmt="q3_k")
+    Wdd = dequant_q3_k(Wd)
+    hdq = dequant_q8(hq, hd16)
+    assert np.all(np.abs(y - Wdd @ hdq) <= 1e-12 * (np.abs(Wdd) @ np.abs(hdq)))
+    # an unknown format is refused, not guessed
+    with pytest.raises(ValueError):
+        O.expert_gate_up(Wg, Wu, D, F, xq, xd16, fmt="q5_k")
+
+
+def test_q3_k_single_expert_layer_is_dense_swiglu():
+    rng = np.random.default_rng(53)
+    N, D, F = 8, 256, 256
+    hidden = rng.standard_normal((N, D)).astype(np.float32)
+    routerW = (rng.standard_normal((1, D)) / np.sqrt(D)).astype(np.float32)
+    pk = lambda r, c: pack_q3_k((rng.standard_normal((r, c)) * 0.02).astype(np.float32))  # noqa: E731
+    inp = dict(hidden=hidden, routerW=routerW, gate=pk(F, D)[None], up=pk(F, D)[None], down=pk(D, F)[None],
+               wfmt="q3_k")
+    r = O.moe_ffn_inputs(inp, 1, True)
+    assert np.all(r["topk_w"] == 1.0)
+    xdq = dequant_q8(r["x_q"], r["x_d16"])
+    g = xdq @ dequant_q3_k(inp["gate"][0]).T
+    u = xdq @ dequant_q3_k(inp["up"][0]).T
+    ref = (g / (1 + np.exp(-g)) * u) @ dequant_q3_k(inp["down"][0]).T
+    assert np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref) < 1e-2
+    ref_exact = dequant_q8(r["h_q"], r["h_d16"]) @ dequant_q3_k(inp["down"][0]).T
     np.testing.assert_allclose(r["out"][r["expTokI"]], ref_exact.astype(np.float32), rtol=1e-6, atol=1e-9)
 
 
