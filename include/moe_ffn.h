@@ -113,10 +113,15 @@ int moe_weights_create(moe_weights_t *out, int E, int D, int F,
 /* Block format of the caller's expert weights. */
 enum moe_weight_format {
     MOE_WFMT_Q8_0 = 0, /* GGUF Q8_0: 34-byte blocks of 32 (fp16 d, 32 int8) */
-    MOE_WFMT_Q4_K = 1  /* GGUF Q4_K: 144-byte super-blocks of 256 (fp16 d, fp16 dmin, 12 bytes
+    MOE_WFMT_Q4_K = 1, /* GGUF Q4_K: 144-byte super-blocks of 256 (fp16 d, fp16 dmin, 12 bytes
                           of 6-bit sub-block scales sc_j and mins m_j, 128 bytes of 4-bit
                           quants q): value = d*sc_j*q - dmin*m_j ("Q8_0/Q4_K MMQ", #406
                           references).  Needs D, F, Fs multiples of 256. */
+    MOE_WFMT_Q3_K = 2  /* GGUF Q3_K: 110-byte super-blocks of 256 (32 bytes of high bits, 64
+                          bytes of 2-bit low parts, 12 bytes of sixteen 6-bit scales s_j + 32,
+                          fp16 d): value = d*s_j*q, q in [-4, 3], one s_j per 16 values (the
+                          routed experts' format on the Carnice prefill page, #388 "Key
+                          references").  Needs D, F, Fs multiples of 256. */
 };
 /* moe_weights_create for either format: the same arrays, rows in `format`'s
  * blocks ([E][F][D/256] super-blocks for Q4_K gate/up, [E][D][F/256] down,
@@ -124,7 +129,14 @@ enum moe_weight_format {
  * sub-block b, the exact int32 dot of the quants (0..15) with the Q8_1
  * activation codes and the code sum of the activation block:
  *   sum_b d_x[b] * (d*sc_b * isum_b - dmin*m_b * xsum_b).
- * MOE_ERR_UNSUPPORTED_SHAPE for shapes the format cannot hold. */
+ * A Q3_K layer folds the 16-wide sub-block scales into the integer codes at
+ * load time: per 32-wide block b it stores c_i = -s_j*q_i (always in
+ * [-128, 124], one int8) with the block scale -d, and computes
+ *   sum_b d_x[b] * (-d) * (sum_i c_i * x_i) = sum_b d_x[b] * d * (s_2b*isum_2b + s_2b+1*isum_2b+1),
+ * the same exact block integer as the format's own definition (the signs
+ * cancel in every product).
+ * MOE_ERR_UNSUPPORTED_SHAPE for shapes the format cannot hold; an unknown
+ * format is MOE_ERR_INVALID_ARG. */
 int moe_weights_create_ex(moe_weights_t *out, int format, int E, int D, int F,
                           const void *gate, const void *up, const void *down, int Fs,
                           const void *sh_gate, const void *sh_up, const void *sh_down,
@@ -269,7 +281,9 @@ int moe_expert_down(moe_weights_t w, const int8_t *h_q, const float *h_d,
 /* Raw int32 block dot products of the gate/up GEMM for one 32-block `block`
  * of the reduction dimension: dots [N*top_k][2][F] int32, entry j in segment
  * order, [.][0][f] = isum(W_g[e][f], x_t), [.][1][f] = isum(W_u[e][f], x_t),
- * as computed inside the selected path's kernel. */
+ * as computed inside the selected path's kernel.  The weight codes are the
+ * stored ones: Q8_0 quants, Q4_K quants 0..15, and for Q3_K c_i = -s_j*q_i,
+ * so a Q3_K dot is -(s_2b*isum_2b + s_2b+1*isum_2b+1). */
 int moe_debug_gate_up_block_dots(moe_weights_t w, const int8_t *x_q, const float *x_d,
                                  const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
                                  int block, int32_t *dots, int path, void *ws, size_t ws_bytes,

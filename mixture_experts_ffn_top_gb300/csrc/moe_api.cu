@@ -169,10 +169,10 @@ int moe_weights_create_ex(moe_weights_t *out, int format, int E, int D, int F, c
     if (out == nullptr) return MOE_ERR_INVALID_ARG;
     *out = nullptr;
     if (!gate || !up || !down) return MOE_ERR_INVALID_ARG;
-    if (format != MOE_WFMT_Q8_0 && format != MOE_WFMT_Q4_K) return MOE_ERR_INVALID_ARG;
+    if (format != MOE_WFMT_Q8_0 && format != MOE_WFMT_Q4_K && format != MOE_WFMT_Q3_K) return MOE_ERR_INVALID_ARG;
     if (Fs < 0 || (Fs > 0 && (!sh_gate || !sh_up || !sh_down))) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > MAX_E || D < QK || D % QK || F < QK || F % QK || Fs % QK) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (format == MOE_WFMT_Q4_K && (D % QK_K || F % QK_K || Fs % QK_K)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (format != MOE_WFMT_Q8_0 && (D % QK_K || F % QK_K || Fs % QK_K)) return MOE_ERR_UNSUPPORTED_SHAPE;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

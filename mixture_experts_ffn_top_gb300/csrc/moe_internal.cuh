@@ -11,8 +11,9 @@
 namespace moe {
 
 constexpr int QK = 32;          // values per Q8 block (and per Q4_K sub-block)
-constexpr int QK_K = 256;       // values per Q4_K super-block
+constexpr int QK_K = 256;       // values per K-quant super-block
 constexpr int Q4_K_BYTES = 144; // fp16 d, fp16 dmin, 12 bytes of 6-bit scales/mins, 128 bytes of nibbles
+constexpr int Q3_K_BYTES = 110; // 32 bytes high bits, 64 bytes 2-bit low parts, 12 bytes 6-bit scales, fp16 d
 constexpr int Q8_0_BYTES = 34;  // fp16 scale + 32 int8
 constexpr int MAX_E = 1024;
 constexpr int SEG_ALIGN = 16;   // padded segment start (rows) in the tensor-core row space

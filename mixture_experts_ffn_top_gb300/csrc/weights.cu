@@ -1,4 +1,4 @@
-// weights.cu -- one-time repack of the caller's Q8_0 (or Q4_K) expert tensors into the
+// weights.cu -- one-time repack of the caller's Q8_0 (or Q4_K, Q3_K) expert tensors into the
 // library-owned layouts the kernels read (load time, not on the hot path).
 //
 // GGUF Q8_0 stores each 32-block as 34 bytes (fp16 scale + 32 int8), which
@@ -9,7 +9,7 @@
 //   - int8 quants [rows][K] (16-byte aligned rows) and fp32 scales [rows][K/32]
 //     (the fp16 scale widened exactly), read by the matvec path;
 //   - for the tensor-core path: the quants again as exact fp16 integers
-//     (|q| <= 127 is exact in fp16), gate and up interleaved per 128-row tile
+//     (integers up to 2048 are exact in fp16), gate and up interleaved per 128-row tile
 //     (rows 0-63 gate f0..f0+63, rows 64-127 up f0..f0+63) so one MMA tile
 //     yields gate and up of the same 64 features; scales transposed to
 //     [K/32][rows] so a TMA box of 128 rows x 2 blocks is one copy.
@@ -20,6 +20,48 @@
 namespace moe {
 
 namespace {
+
+// Stores one decoded 32-block (codes vals, scale) of row r of matrix m (mr = m * rows + r) into
+// the matvec layout (q, d: int8 row-major, fp32 [rows][nblk]) and the tensor-core layout (h16
+// exact fp16 codes, gate/up interleaved per 128-row tile; dT scales [nblk][rows_out]).
+__device__ __forceinline__ void store_block(const int8_t *vals, float scale, int64_t mr, int b, int m, int r,
+                                            int rows, int nblk, int8_t *__restrict__ q, float *__restrict__ d,
+                                            __half *__restrict__ h16, float *__restrict__ dT, int interleave_gu,
+                                            int up_half) {
+    const int K = nblk * QK;
+    if (q != nullptr) {
+        int4 *dst = reinterpret_cast<int4 *>(q + mr * K + (int64_t)b * QK);
+        dst[0] = *reinterpret_cast<const int4 *>(vals);
+        dst[1] = *reinterpret_cast<const int4 *>(vals + 16);
+        d[mr * nblk + b] = scale;
+    }
+    if (h16 != nullptr) {
+        // row inside the tensor-core operand of this matrix
+        int64_t rr = r;
+        int64_t rows_out = rows;
+        if (interleave_gu) {  // gate/up pair: [2*rows] rows, 64-row halves per 128-row tile
+            rows_out = 2 * (int64_t)rows;
+            rr = (int64_t)(r / 64) * 128 + (up_half ? 64 : 0) + (r % 64);
+        }
+        __half *dst = h16 + ((int64_t)m * rows_out + rr) * K + (int64_t)b * QK;
+#pragma unroll
+        for (int j = 0; j < QK; j += 2)
+            *reinterpret_cast<__half2 *>(dst + j) = __halves2half2(__int2half_rn(vals[j]), __int2half_rn(vals[j + 1]));
+        dT[((int64_t)m * nblk + b) * rows_out + rr] = scale;
+    }
+}
+
+// Position of the block in the tensor-core operand's transposed scale array, for extra
+// per-block arrays laid out like dT (the Q4_K mins).
+__device__ __forceinline__ int64_t dT_index(int64_t m, int b, int r, int rows, int nblk, int interleave_gu,
+                                            int up_half) {
+    int64_t rr = r, rows_out = rows;
+    if (interleave_gu) {
+        rows_out = 2 * (int64_t)rows;
+        rr = (int64_t)(r / 64) * 128 + (up_half ? 64 : 0) + (r % 64);
+    }
+    return (m * nblk + b) * rows_out + rr;
+}
 
 // One thread per 32-block.  src: [nmat][rows][nblk] AoS blocks.
 __global__ void repack_kernel(const uint8_t *__restrict__ src, int nmat, int rows, int nblk,
@@ -33,32 +75,11 @@ __global__ void repack_kernel(const uint8_t *__restrict__ src, int nmat, int row
         const int m = (int)(mr / rows);
         const int r = (int)(mr - (int64_t)m * rows);
         const uint8_t *blk = src + i * Q8_0_BYTES;
-        const __half dh = __ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8)));
-        const float df = __half2float(dh);
+        const float df = __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
         alignas(16) int8_t vals[QK];
 #pragma unroll
         for (int j = 0; j < QK; ++j) vals[j] = (int8_t)blk[2 + j];
-        const int K = nblk * QK;
-        if (q != nullptr) {
-            int4 *dst = reinterpret_cast<int4 *>(q + mr * K + (int64_t)b * QK);
-            dst[0] = *reinterpret_cast<const int4 *>(vals);
-            dst[1] = *reinterpret_cast<const int4 *>(vals + 16);
-            d[mr * nblk + b] = df;
-        }
-        if (h16 != nullptr) {
-            // row inside the tensor-core operand of this matrix
-            int64_t rr = r;
-            int64_t rows_out = rows;
-            if (interleave_gu) {  // gate/up pair: [2*rows] rows, 64-row halves per 128-row tile
-                rows_out = 2 * (int64_t)rows;
-                rr = (int64_t)(r / 64) * 128 + (up_half ? 64 : 0) + (r % 64);
-            }
-            __half *dst = h16 + ((int64_t)m * rows_out + rr) * K + (int64_t)b * QK;
-#pragma unroll
-            for (int j = 0; j < QK; j += 2)
-                *reinterpret_cast<__half2 *>(dst + j) = __halves2half2(__int2half_rn(vals[j]), __int2half_rn(vals[j + 1]));
-            dT[((int64_t)m * nblk + b) * rows_out + rr] = df;
-        }
+        store_block(vals, df, mr, b, m, r, rows, nblk, q, d, h16, dT, interleave_gu, up_half);
     }
 }
 
@@ -95,28 +116,55 @@ __global__ void repack_q4k_kernel(const uint8_t *__restrict__ src, int nmat, int
         alignas(16) int8_t vals[QK];
 #pragma unroll
         for (int l = 0; l < QK; ++l) vals[l] = (int8_t)((j & 1) ? (qs[l] >> 4) : (qs[l] & 15));
-        const int K = nblk * QK;
-        if (q != nullptr) {
-            int4 *dst = reinterpret_cast<int4 *>(q + mr * K + (int64_t)b * QK);
-            dst[0] = *reinterpret_cast<const int4 *>(vals);
-            dst[1] = *reinterpret_cast<const int4 *>(vals + 16);
-            d[mr * nblk + b] = scale;
-            mn[mr * nblk + b] = minv;
-        }
-        if (h16 != nullptr) {
-            int64_t rr = r;
-            int64_t rows_out = rows;
-            if (interleave_gu) {
-                rows_out = 2 * (int64_t)rows;
-                rr = (int64_t)(r / 64) * 128 + (up_half ? 64 : 0) + (r % 64);
-            }
-            __half *dst = h16 + ((int64_t)m * rows_out + rr) * K + (int64_t)b * QK;
+        store_block(vals, scale, mr, b, m, r, rows, nblk, q, d, h16, dT, interleave_gu, up_half);
+        if (q != nullptr) mn[mr * nblk + b] = minv;
+        if (h16 != nullptr) mT[dT_index(m, b, r, rows, nblk, interleave_gu, up_half)] = minv;
+    }
+}
+
+// Q3_K rows (K/256 super-blocks of 110 bytes each) into the Q8_0 layouts.  Value i of a
+// super-block is d * s_j * q_i with q_i in [-4, 3] and one signed 6-bit scale s_j per 16 values;
+// the kernels work per 32-wide block with one scale, so the repack folds s_j into the codes.
+// s_j * q_i spans [-124, 128], one past int8; its negation c_i = -s_j * q_i spans [-128, 124],
+// so the codes are stored negated with the block scale -d (exact: the signs cancel in every
+// product the kernels form).  One thread per 32-wide block b (sub-blocks 2b', 2b'+1 of its
+// super-block, b' = b mod 8):
+//   high bit of value 32b' + l: bit b' of byte l;
+//   low two bits: bits 2*(b' mod 4) of byte 32 + 32*(b' / 4) + l;
+//   6-bit scale field of sub-block j: low 4 bits from nibble j / 8 of byte 96 + j mod 8, high
+//   2 bits from bits 2*(j / 4) of byte 104 + j mod 4; s_j = field - 32; fp16 d at byte 108.
+__global__ void repack_q3k_kernel(const uint8_t *__restrict__ src, int nmat, int rows, int nblk,
+                                  int8_t *__restrict__ q, float *__restrict__ d, __half *__restrict__ h16,
+                                  float *__restrict__ dT, int interleave_gu, int up_half) {
+    const int64_t total = (int64_t)nmat * rows * nblk;
+    const int64_t row_bytes = (int64_t)(nblk / 8) * Q3_K_BYTES;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t mr = i / nblk;  // matrix * rows + row
+        const int b = (int)(i - mr * nblk);
+        const int m = (int)(mr / rows);
+        const int r = (int)(mr - (int64_t)m * rows);
+        const int bb = b & 7;  // 32-wide block inside its super-block
+        const uint8_t *blk = src + mr * row_bytes + (int64_t)(b >> 3) * Q3_K_BYTES;
+        const float dd = __half2float(__ushort_as_half((unsigned short)(blk[108] | (blk[109] << 8))));
+        int s[2];
 #pragma unroll
-            for (int l = 0; l < QK; l += 2)
-                *reinterpret_cast<__half2 *>(dst + l) = __halves2half2(__int2half_rn(vals[l]), __int2half_rn(vals[l + 1]));
-            dT[((int64_t)m * nblk + b) * rows_out + rr] = scale;
-            mT[((int64_t)m * nblk + b) * rows_out + rr] = minv;
+        for (int h = 0; h < 2; ++h) {
+            const int j = 2 * bb + h;
+            const int lo = (blk[96 + (j & 7)] >> (4 * (j >> 3))) & 15;
+            const int hi = (blk[104 + (j & 3)] >> (2 * (j >> 2))) & 3;
+            s[h] = (lo | (hi << 4)) - 32;
         }
+        const uint8_t *qs = blk + 32 + 32 * (bb >> 2);
+        const int shift = 2 * (bb & 3);
+        alignas(16) int8_t vals[QK];
+#pragma unroll
+        for (int l = 0; l < QK; ++l) {
+            const int low = (qs[l] >> shift) & 3;
+            const int qv = ((blk[l] >> bb) & 1) ? low : low - 4;
+            vals[l] = (int8_t)(-s[l >> 4] * qv);
+        }
+        store_block(vals, -dd, mr, b, m, r, rows, nblk, q, d, h16, dT, interleave_gu, up_half);
     }
 }
 
@@ -129,6 +177,9 @@ int repack(int wfmt, const void *src, int nmat, int rows, int K, int8_t *q, floa
     if (wfmt == MOE_WFMT_Q4_K)
         repack_q4k_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
                                                            mn, h16, dT, mT, interleave, up_half);
+    else if (wfmt == MOE_WFMT_Q3_K)
+        repack_q3k_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
+                                                           h16, dT, interleave, up_half);
     else
         repack_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
                                                        h16, dT, interleave, up_half);

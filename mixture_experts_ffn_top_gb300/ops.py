@@ -110,7 +110,7 @@ def _stream(stream) -> _P:
 
 
 # --------------------------------------------------------------- weights ---
-WEIGHT_FORMATS = {"q8_0": 0, "q4_k": 1}  # MOE_WFMT_*
+WEIGHT_FORMATS = {"q8_0": 0, "q4_k": 1, "q3_k": 2}  # MOE_WFMT_*
 
 
 class MoeWeights:

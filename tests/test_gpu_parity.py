@@ -27,6 +27,7 @@ W_RTOL = 2e-5
 CONFIGS = ["tiny", "olmoe", "decode_n1", "decode_n4", "decode_n8", "qwen3moe_shared", "skewed"]
 SMALL = ["tiny", "decode_n4", "qwen3moe_shared"]
 Q4K = ["tiny_q4k", "q4k_shared", "olmoe_q4k"]  # the same layer with Q4_K expert weights
+Q3K = ["tiny_q3k", "q3k_shared", "olmoe_q3k"]  # and with Q3_K expert weights
 
 
 @pytest.fixture(scope="module")
@@ -248,7 +249,7 @@ def _csr(ref):
     return dev(ref["expStart"]), dev(ref["expTokI"]), dev(ref["expTokK"])
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "tiny_q4k", "olmoe_q4k"])
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "tiny_q4k", "olmoe_q4k", "tiny_q3k", "olmoe_q3k"])
 @pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_block_dots_bit_exact(ops, name, path):
     wl, inp, ref = case(name)
@@ -271,12 +272,14 @@ def test_gate_up_block_dots_bit_exact(ops, name, path):
                 for f in (0, wl.F // 2 + 3, wl.F - 1):
                     if wl.wfmt == "q4_k":
                         ref_dot = O.block_dots_q4_k(W[e, f], ref["x_q"][t])[block]
+                    elif wl.wfmt == "q3_k":  # the library stores the codes -s_j*q_i
+                        ref_dot = -O.block_dots_q3_k(W[e, f], ref["x_q"][t])[block]
                     else:
                         ref_dot = O.block_dots(W[e, f], ref["x_q"][t])[block]
                     assert dots[j, mat, f] == ref_dot, (j, mat, f, block)
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K)
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K + Q3K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_requantised_activations(ops, name, path):
     """h_q from the oracle's x_q and CSR: codes within +-1 (fp32 vs double accumulation can
@@ -298,7 +301,7 @@ def test_gate_up_requantised_activations(ops, name, path):
     np.testing.assert_allclose(hd, rd, rtol=1e-3, atol=1e-30)
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K)
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K + Q3K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_down_given_oracle_h(ops, name, path):
     """The down half on the oracle's own h_q: partials to fp32 accumulation accuracy."""
@@ -318,7 +321,7 @@ def test_down_given_oracle_h(ops, name, path):
     assert rel <= 1e-5, rel
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K)
+@pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K + Q3K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_grouped_ffn_partials(ops, name, path):
     wl, inp, ref = case(name)
@@ -408,7 +411,7 @@ def test_layer_with_residual(ops, name):
 
 
 # ---------------------------------------------------------- whole layer ---
-@pytest.mark.parametrize("name", CONFIGS + Q4K)
+@pytest.mark.parametrize("name", CONFIGS + Q4K + Q3K)
 @pytest.mark.parametrize("path", [0, 1, 2])
 def test_layer_parity(ops, name, path):
     """moe_ffn_prefill (the call bench.py times, path 0 = its launch configuration)."""
@@ -505,6 +508,43 @@ def test_q4_k_weights_handle_and_shapes(ops):
     with pytest.raises(ops.MoeError) as e:
         ops.MoeWeights(g, g, d, 2, 256, 128, wfmt="q4_k")
     assert e.value.code == -2
+
+
+def test_q3_k_weights_handle_and_shapes(ops):
+    wl, inp, _ = case("tiny_q3k")
+    assert ops.moe_weights_format(layer_for(ops, inp, wl).w) == "q3_k"
+    g = torch.zeros((2, 128, 110), dtype=torch.uint8, device="cuda")  # D = 256 but F = 128
+    d = torch.zeros((2, 256, 55), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ops.MoeError) as e:
+        ops.MoeWeights(g, g, d, 2, 256, 128, wfmt="q3_k")
+    assert e.value.code == -2
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_q3_k_extreme_codes(ops, path):
+    """Rows whose every value is q = -4 with s = -32 (s*q = 128, one past int8: the library
+    stores the negated codes): block dots exact and the layer within tolerance."""
+    wl = WORKLOADS["tiny_q3k"]
+    inp = dict(make_inputs(wl))
+    ext = np.zeros(110, np.uint8)
+    ext[108:110] = np.array([np.float16(2.0 ** -12)]).view(np.uint8)
+    for key in ("gate", "up", "down"):
+        inp[key] = inp[key].copy()
+        v = inp[key].reshape(inp[key].shape[0], inp[key].shape[1], -1, 110)
+        v[:, ::5] = ext  # every fifth row of every expert
+    ref = O.moe_ffn_inputs(inp, wl.top_k, wl.norm_topk_prob)
+    layer = layer_for(ops, inp, wl)
+    es, ti, _ = _csr(ref)
+    dots = ops.moe_debug_gate_up_block_dots(layer.w, dev(ref["x_q"]), dev(O.halves(ref["x_d16"])), es, ti,
+                                            wl.top_k, 1, layer.ws, path=path).cpu().numpy()
+    for j in range(0, int(ref["expStart"][-1]), 7):
+        e = int(np.searchsorted(ref["expStart"], j, side="right") - 1)
+        t = int(ref["expTokI"][j])
+        for f in (0, 5, 1, wl.F - 1):
+            assert dots[j, 0, f] == -O.block_dots_q3_k(inp["gate"][e, f], ref["x_q"][t])[1]
+    out = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=path)
+    assert layer.status() == 0
+    assert_out_close(out.cpu().numpy(), ref["out"], clear_tokens(ref["logits"], wl.top_k), what="q3_k extreme")
 
 
 def test_zero_hidden_gives_zero(ops):
