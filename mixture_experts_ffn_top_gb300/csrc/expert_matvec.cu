@@ -4,15 +4,19 @@
 // per-expert launches; lever 2: Q8_1 activations with int8 dp4a dots).
 //
 // Weight-stationary: a CTA owns 32 rows of one expert's matrix and streams
-// each row once per chunk of 8 tokens of the expert's CSR segment, so for
-// decode batches (a few tokens per expert) every touched weight byte is read
-// once.  Each warp owns 4 rows; lane l reads 16-byte pieces l, l+32, ... of a
-// row (coalesced 512 B per warp step).  Two neighbouring lanes hold the two
-// halves of a 32-block; their dp4a sums are exchanged with one shuffle, which
-// gives the exact int32 block dot isum_b, then acc += (d_w * d_x) * isum_b.  Q4_K
-// weights (repacked to quants 0..15 with per-block scale d*sc and min dmin*m)
-// add the min term: the same lanes also sum the activation codes (dp4a with
-// ones), and acc -= (m_w * d_x) * xsum_b.
+// each row once per chunk of up to 8 tokens of the expert's CSR segment, so
+// for decode batches (a few tokens per expert) every touched weight byte is
+// read once.  The chunk's arithmetic is specialised on its token count
+// (1, 2, 4 or 8 slots), so a one-token segment costs one token's work.
+// Each warp takes its rows two at a time (gate and up of one feature, or two
+// output columns); lane l owns the 32-wide blocks l, l + 32, ... of both rows
+// and loads all of them (2 x 16 contiguous bytes per block and row) before
+// any arithmetic, so the row pair's bytes are in flight together.  Per block
+// the lane forms the exact int32 dot isum_b (8 dp4a) with each staged token
+// and accumulates (d_w * d_x) * isum_b; the lanes' sums are reduced at the
+// end.  Q4_K weights (repacked to quants 0..15 with per-block scale d*sc and
+// min dmin*m) add the min term: the lane also sums the activation codes
+// (dp4a with ones) and accumulates -(m_w * d_x) * xsum_b.
 //
 // gate/up kernel: rows = features f (gate and up), output h = SiLU(g) * u,
 //   requantised to Q8_1 per 32 features inside the CTA (the CTA owns exactly
@@ -25,17 +29,27 @@ namespace moe {
 
 namespace {
 
-constexpr int MV_T = 8;         // tokens per chunk
+constexpr int MV_T = 8;         // tokens per chunk at most
 constexpr int MV_WARPS = 8;     // 256 threads
 constexpr int MV_ROWS_PER_WARP = 4;
 
-__device__ __forceinline__ int dp4a16(int4 w, int4 x) {
+__device__ __forceinline__ int dp4a32(const int4 (&w)[2], int4 x0, int4 x1) {
     int s = 0;
-    s = __dp4a(w.x, x.x, s);
-    s = __dp4a(w.y, x.y, s);
-    s = __dp4a(w.z, x.z, s);
-    s = __dp4a(w.w, x.w, s);
+    s = __dp4a(w[0].x, x0.x, s);
+    s = __dp4a(w[0].y, x0.y, s);
+    s = __dp4a(w[0].z, x0.z, s);
+    s = __dp4a(w[0].w, x0.w, s);
+    s = __dp4a(w[1].x, x1.x, s);
+    s = __dp4a(w[1].y, x1.y, s);
+    s = __dp4a(w[1].z, x1.z, s);
+    s = __dp4a(w[1].w, x1.w, s);
     return s;
+}
+// sum of the 32 int8 codes of an activation block
+__device__ __forceinline__ int codesum32(int4 x0, int4 x1) {
+    const int4 ones[2] = {make_int4(0x01010101, 0x01010101, 0x01010101, 0x01010101),
+                          make_int4(0x01010101, 0x01010101, 0x01010101, 0x01010101)};
+    return dp4a32(ones, x0, x1);
 }
 
 // Segment of expert e: [s0, s1) in CSR entries; shared expert: all N tokens.
@@ -57,71 +71,150 @@ __device__ __forceinline__ Seg segment_of(bool is_shared, int e, const int32_t *
     return g;
 }
 
-// Dot of one weight row (int8 [K], scales [K/32]) against MV_T staged activation rows.
-// Returns per-token fp32 sums, reduced across the warp (valid in every lane).
-// If dbg != nullptr, the even lane owning block dbg_block stores its isum per token.
-__device__ __forceinline__ void row_dot(const int8_t *__restrict__ wq, const float *__restrict__ wd,
-                                        const float *__restrict__ wm, int K, const int8_t *xs, const float *xds,
-                                        int lane, float acc[MV_T], int dbg_block, int dbg_isum[MV_T]) {
+// Dots of two weight rows a, b (int8 [K], fp32 scales [K/32], fp32 mins or NULL) with T staged
+// activation rows (xs [T][K] int8, xds [T][K/32] fp32).  Returns per-token fp32 sums, reduced
+// across the warp (valid in every lane).  The lane owning block dbg_block stores its isums.
+template <int T>
+__device__ __forceinline__ void two_rows_dot(const int8_t *__restrict__ wa, const float *__restrict__ da,
+                                             const float *__restrict__ ma, const int8_t *__restrict__ wb,
+                                             const float *__restrict__ db, const float *__restrict__ mb, int K,
+                                             const int8_t *xs, const float *xds, int lane, float (&acc_a)[T],
+                                             float (&acc_b)[T], int dbg_block, int (&dbg_a)[T], int (&dbg_b)[T]) {
+    const int nblk = K / QK;
 #pragma unroll
-    for (int tt = 0; tt < MV_T; ++tt) acc[tt] = 0.0f;
-    const int nchunks = K / 16;  // even: K is a multiple of 32
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-        // every lane runs every step (the shuffle below needs the whole warp)
-        const int c = c0 + lane;
-        const bool active = c < nchunks;  // lanes l and l^1 are active together
-        const int b = c >> 1;
-        int4 w = make_int4(0, 0, 0, 0);
-        float dw = 0.0f, mw = 0.0f;
-        if (active) {
-            w = *reinterpret_cast<const int4 *>(wq + (size_t)c * 16);
-            dw = wd[b];
-            if (wm != nullptr) mw = wm[b];
-        }
-        const int4 ones = make_int4(0x01010101, 0x01010101, 0x01010101, 0x01010101);
-        int part[MV_T], xpart[MV_T];
+    for (int tt = 0; tt < T; ++tt) acc_a[tt] = acc_b[tt] = 0.0f;
+    for (int b0 = 0; b0 < nblk; b0 += 64) {
+        int4 qa[2][2], qb[2][2];
+        float sa[2], sb[2], na[2], nb[2];
 #pragma unroll
-        for (int tt = 0; tt < MV_T; ++tt) {
-            part[tt] = 0;
-            xpart[tt] = 0;
-            if (active) {
-                int4 x = *reinterpret_cast<const int4 *>(xs + (size_t)tt * K + c * 16);
-                part[tt] = dp4a16(w, x);
-                if (wm != nullptr) xpart[tt] = dp4a16(ones, x);
+        for (int u = 0; u < 2; ++u) {
+            const int b = b0 + 32 * u + lane;
+            qa[u][0] = qa[u][1] = qb[u][0] = qb[u][1] = make_int4(0, 0, 0, 0);
+            sa[u] = sb[u] = na[u] = nb[u] = 0.0f;
+            if (b < nblk) {
+                const int4 *pa = reinterpret_cast<const int4 *>(wa + (size_t)b * QK);
+                const int4 *pb = reinterpret_cast<const int4 *>(wb + (size_t)b * QK);
+                qa[u][0] = __ldcs(pa);
+                qa[u][1] = __ldcs(pa + 1);
+                qb[u][0] = __ldcs(pb);
+                qb[u][1] = __ldcs(pb + 1);
+                sa[u] = __ldcs(da + b);
+                sb[u] = __ldcs(db + b);
+                if (ma != nullptr) {
+                    na[u] = __ldcs(ma + b);
+                    nb[u] = __ldcs(mb + b);
+                }
             }
         }
 #pragma unroll
-        for (int tt = 0; tt < MV_T; ++tt) {
-            int isum = part[tt] + __shfl_xor_sync(0xffffffffu, part[tt], 1);
-            int xsum = 0;
-            if (wm != nullptr) xsum = xpart[tt] + __shfl_xor_sync(0xffffffffu, xpart[tt], 1);
-            if (active && (c & 1) == 0) {
-                const float dx = xds[tt * (K / QK) + b];
-                acc[tt] = fmaf(dw * dx, (float)isum, acc[tt]);
-                if (wm != nullptr) acc[tt] = fmaf(-(mw * dx), (float)xsum, acc[tt]);
-                if (b == dbg_block) dbg_isum[tt] = isum;
+        for (int u = 0; u < 2; ++u) {
+            const int b = b0 + 32 * u + lane;
+            if (b >= nblk) continue;
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) {
+                const int4 *px = reinterpret_cast<const int4 *>(xs + (size_t)tt * K + (size_t)b * QK);
+                const int4 x0 = px[0], x1 = px[1];
+                const float dx = xds[tt * nblk + b];
+                const int ia = dp4a32(qa[u], x0, x1), ib = dp4a32(qb[u], x0, x1);
+                acc_a[tt] = fmaf(sa[u] * dx, (float)ia, acc_a[tt]);
+                acc_b[tt] = fmaf(sb[u] * dx, (float)ib, acc_b[tt]);
+                if (ma != nullptr) {
+                    const float xsum = (float)codesum32(x0, x1);
+                    acc_a[tt] = fmaf(-(na[u] * dx), xsum, acc_a[tt]);
+                    acc_b[tt] = fmaf(-(nb[u] * dx), xsum, acc_b[tt]);
+                }
+                if (b == dbg_block) {
+                    dbg_a[tt] = ia;
+                    dbg_b[tt] = ib;
+                }
             }
         }
     }
 #pragma unroll
-    for (int tt = 0; tt < MV_T; ++tt) acc[tt] = warp_sum(acc[tt]);
+    for (int tt = 0; tt < T; ++tt) {
+        acc_a[tt] = warp_sum(acc_a[tt]);
+        acc_b[tt] = warp_sum(acc_b[tt]);
+    }
 }
 
-// Stage up to MV_T activation rows (int8 [K] + fp32 scales [K/32]) into shared memory;
-// missing rows are zero.  rows[tt] < 0 means "no row".
+// Stage T activation rows (int8 [K] + fp32 scales [K/32]) into shared memory; rows[tt] < 0
+// (no row) stages zeros.
 __device__ __forceinline__ void stage_rows(const int8_t *__restrict__ q, const float *__restrict__ d, int K,
-                                           const int *rows, int8_t *xs, float *xds) {
+                                           const int *rows, int T, int8_t *xs, float *xds) {
     const int per_row16 = K / 16;
-    for (int i = threadIdx.x; i < MV_T * per_row16; i += blockDim.x) {
+    for (int i = threadIdx.x; i < T * per_row16; i += blockDim.x) {
         int tt = i / per_row16, c = i - tt * per_row16;
         int4 v = make_int4(0, 0, 0, 0);
         if (rows[tt] >= 0) v = *reinterpret_cast<const int4 *>(q + (size_t)rows[tt] * K + c * 16);
         *reinterpret_cast<int4 *>(xs + (size_t)tt * K + c * 16) = v;
     }
     const int nb = K / QK;
-    for (int i = threadIdx.x; i < MV_T * nb; i += blockDim.x) {
+    for (int i = threadIdx.x; i < T * nb; i += blockDim.x) {
         int tt = i / nb, b = i - tt * nb;
         xds[i] = rows[tt] >= 0 ? d[(size_t)rows[tt] * nb + b] : 0.0f;
+    }
+}
+
+// Slots of a chunk of cnt tokens, rounded up to the specialisations 1, 2, 4, 8.
+__device__ __forceinline__ int chunk_slots(int cnt) { return cnt <= 1 ? 1 : cnt <= 2 ? 2 : cnt <= 4 ? 4 : 8; }
+
+struct GateUpArgs {
+    const int8_t *gq, *uq;
+    const float *gd, *gm, *ud, *um;
+    int D, F;
+    size_t mat_off;
+    int8_t *h_q;
+    float *h_d;
+    int32_t *dbg_dots;
+    int dbg_block;
+};
+
+// One chunk of T token slots of the gate/up kernel: every warp's 4 features, then the Q8_1
+// requantisation of the 32-feature block per token.
+template <int T>
+__device__ __forceinline__ void gate_up_chunk(const GateUpArgs &a, int fb, const int *rows, const int *entries,
+                                              const int8_t *xs, const float *xds, float *hs) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = a.D;
+    for (int r = 0; r < MV_ROWS_PER_WARP; ++r) {
+        const int fl = warp * MV_ROWS_PER_WARP + r;  // feature within the 32-block
+        const int f = fb * QK + fl;
+        float g[T], u[T];
+        int dg[T], du[T];
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) dg[tt] = du[tt] = 0;
+        const size_t so = (a.mat_off + f) * (D / QK);
+        two_rows_dot<T>(a.gq + (a.mat_off + f) * D, a.gd + so, a.gm ? a.gm + so : nullptr, a.uq + (a.mat_off + f) * D,
+                        a.ud + so, a.um ? a.um + so : nullptr, D, xs, xds, lane, g, u, a.dbg_block, dg, du);
+        if (a.dbg_dots != nullptr && a.dbg_block >= 0 && lane == (a.dbg_block & 31)) {
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) {
+                const int j = entries[tt];
+                if (j < 0 || rows[tt] < 0) continue;
+                a.dbg_dots[((size_t)j * 2 + 0) * a.F + f] = dg[tt];
+                a.dbg_dots[((size_t)j * 2 + 1) * a.F + f] = du[tt];
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) {
+                const float gv = g[tt];
+                const float silu = gv / (1.0f + expf(-gv));
+                hs[tt * QK + fl] = silu * u[tt];
+            }
+        }
+    }
+    __syncthreads();
+    // requantise: warp tt takes token tt, lane = feature of the 32-block
+    if (warp < T) {
+        const int tt = warp;
+        float d16f;
+        const int q = q8_quantize_lane(hs[tt * QK + lane], &d16f);
+        const int j = entries[tt];
+        if (j >= 0 && rows[tt] >= 0) {
+            a.h_q[(size_t)j * a.F + fb * QK + lane] = (int8_t)q;
+            if (lane == 0) a.h_d[(size_t)j * (a.F / QK) + fb] = d16f;
+        }
     }
 }
 
@@ -141,15 +234,15 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
     __shared__ int rows[MV_T];
     __shared__ int entries[MV_T];
     const int fb = blockIdx.x, e = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Seg sg = segment_of(is_shared, e, expStart, N, top_k);
     if (!sg.ok) {
         if (threadIdx.x == 0) atomicOr(status, MOE_DEV_BAD_CSR);
         return;
     }
-    const size_t mat_off = (size_t)(is_shared ? 0 : e) * F;
+    GateUpArgs a{gq, uq, gd, gm, ud, um, D, F, (size_t)(is_shared ? 0 : e) * F, h_q, h_d, dbg_dots, dbg_block};
     for (int j0 = sg.s0; j0 < sg.s1; j0 += MV_T) {
         __syncthreads();  // previous chunk fully consumed
+        const int T = chunk_slots(min(MV_T, sg.s1 - j0));
         if (threadIdx.x < MV_T) {
             int j = j0 + threadIdx.x;
             int t = -1;
@@ -164,48 +257,57 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
             entries[threadIdx.x] = (j < sg.s1) ? j : -1;
         }
         __syncthreads();
-        stage_rows(x_q, x_d, D, rows, xs, xds);
+        stage_rows(x_q, x_d, D, rows, T, xs, xds);
         __syncthreads();
-        for (int r = 0; r < MV_ROWS_PER_WARP; ++r) {
-            const int fl = warp * MV_ROWS_PER_WARP + r;  // feature within the 32-block
-            const int f = fb * QK + fl;
-            float g[MV_T], u[MV_T];
-            int dg[MV_T], du[MV_T];
-            const size_t so = (mat_off + f) * (D / QK);
-            row_dot(gq + (mat_off + f) * D, gd + so, gm ? gm + so : nullptr, D, xs, xds, lane, g, dbg_block, dg);
-            row_dot(uq + (mat_off + f) * D, ud + so, um ? um + so : nullptr, D, xs, xds, lane, u, dbg_block, du);
-            if (dbg_dots != nullptr && dbg_block >= 0) {
-                // the even lane that owns block dbg_block (16-byte piece 2*dbg_block) holds the isums
-                if (lane == ((2 * dbg_block) & 31)) {
+        switch (T) {
+        case 1: gate_up_chunk<1>(a, fb, rows, entries, xs, xds, hs); break;
+        case 2: gate_up_chunk<2>(a, fb, rows, entries, xs, xds, hs); break;
+        case 4: gate_up_chunk<4>(a, fb, rows, entries, xs, xds, hs); break;
+        default: gate_up_chunk<8>(a, fb, rows, entries, xs, xds, hs); break;
+        }
+    }
+}
+
+struct DownArgs {
+    const int8_t *dq;
+    const float *dd, *dm;
+    int D, F;
+    size_t mat_off;
+    bool is_shared;
+    float *out;
+};
+
+// One chunk of T token slots of the down kernel: every warp's 4 output columns (two pairs),
+// then the stores of the 32-column block per token.
+template <int T>
+__device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int *orows, const float *oscale,
+                                           const int8_t *hs, const float *hds, float *ys) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int F = a.F;
+    for (int r = 0; r < MV_ROWS_PER_WARP; r += 2) {
+        const int cl = warp * MV_ROWS_PER_WARP + r;
+        const int c = cb * QK + cl;
+        float ya[T], yb[T];
+        int unused_a[T], unused_b[T];
+        const size_t so = (a.mat_off + c) * (F / QK), so1 = so + F / QK;
+        two_rows_dot<T>(a.dq + (a.mat_off + c) * F, a.dd + so, a.dm ? a.dm + so : nullptr,
+                        a.dq + (a.mat_off + c + 1) * F, a.dd + so1, a.dm ? a.dm + so1 : nullptr, F, hs, hds, lane,
+                        ya, yb, -1, unused_a, unused_b);
+        if (lane == 0) {
 #pragma unroll
-                    for (int tt = 0; tt < MV_T; ++tt) {
-                        int j = entries[tt];
-                        if (j < 0 || rows[tt] < 0) continue;
-                        dbg_dots[((size_t)j * 2 + 0) * F + f] = dg[tt];
-                        dbg_dots[((size_t)j * 2 + 1) * F + f] = du[tt];
-                    }
-                }
-            }
-            if (lane == 0) {
-#pragma unroll
-                for (int tt = 0; tt < MV_T; ++tt) {
-                    float gv = g[tt];
-                    float silu = gv / (1.0f + expf(-gv));
-                    hs[tt * QK + fl] = silu * u[tt];
-                }
+            for (int tt = 0; tt < T; ++tt) {
+                ys[tt * QK + cl] = ya[tt];
+                ys[tt * QK + cl + 1] = yb[tt];
             }
         }
-        __syncthreads();
-        // requantise: warp tt takes token tt, lane = feature of the 32-block
-        if (warp < MV_T) {
-            const int tt = warp;
-            float d16f;
-            int q = q8_quantize_lane(hs[tt * QK + lane], &d16f);
-            int j = entries[tt];
-            if (j >= 0 && rows[tt] >= 0) {
-                h_q[(size_t)j * F + fb * QK + lane] = (int8_t)q;
-                if (lane == 0) h_d[(size_t)j * (F / QK) + fb] = d16f;
-            }
+    }
+    __syncthreads();
+    if (warp < T) {
+        const int tt = warp;
+        if (orows[tt] >= 0) {
+            float v = ys[tt * QK + lane];
+            if (a.is_shared) v = oscale[tt] * v;
+            a.out[(size_t)orows[tt] * a.D + cb * QK + lane] = v;
         }
     }
 }
@@ -226,15 +328,15 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
     __shared__ int orows[MV_T];
     __shared__ float oscale[MV_T];
     const int cb = blockIdx.x, e = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Seg sg = segment_of(is_shared, e, expStart, N, top_k);
     if (!sg.ok) {
         if (threadIdx.x == 0) atomicOr(status, MOE_DEV_BAD_CSR);
         return;
     }
-    const size_t mat_off = (size_t)(is_shared ? 0 : e) * D;
+    DownArgs a{dq, dd, dm, D, F, (size_t)(is_shared ? 0 : e) * D, is_shared, out};
     for (int j0 = sg.s0; j0 < sg.s1; j0 += MV_T) {
         __syncthreads();
+        const int T = chunk_slots(min(MV_T, sg.s1 - j0));
         if (threadIdx.x < MV_T) {
             int j = j0 + threadIdx.x;
             int hr = -1, orow = -1;
@@ -259,28 +361,13 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
             oscale[threadIdx.x] = sc;
         }
         __syncthreads();
-        stage_rows(h_q, h_d, F, hrows, hs, hds);
+        stage_rows(h_q, h_d, F, hrows, T, hs, hds);
         __syncthreads();
-        for (int r = 0; r < MV_ROWS_PER_WARP; ++r) {
-            const int cl = warp * MV_ROWS_PER_WARP + r;
-            const int c = cb * QK + cl;
-            float y[MV_T];
-            int unused[MV_T];
-            const size_t so = (mat_off + c) * (F / QK);
-            row_dot(dq + (mat_off + c) * F, dd + so, dm ? dm + so : nullptr, F, hs, hds, lane, y, -1, unused);
-            if (lane == 0) {
-#pragma unroll
-                for (int tt = 0; tt < MV_T; ++tt) ys[tt * QK + cl] = y[tt];
-            }
-        }
-        __syncthreads();
-        if (warp < MV_T) {
-            const int tt = warp;
-            if (orows[tt] >= 0) {
-                float v = ys[tt * QK + lane];
-                if (is_shared) v = oscale[tt] * v;
-                out[(size_t)orows[tt] * D + cb * QK + lane] = v;
-            }
+        switch (T) {
+        case 1: down_chunk<1>(a, cb, orows, oscale, hs, hds, ys); break;
+        case 2: down_chunk<2>(a, cb, orows, oscale, hs, hds, ys); break;
+        case 4: down_chunk<4>(a, cb, orows, oscale, hs, hds, ys); break;
+        default: down_chunk<8>(a, cb, orows, oscale, hs, hds, ys); break;
         }
     }
 }
