@@ -157,12 +157,17 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
             if (lane == 0) base[e] += chunk_count(e);
         __syncthreads();
     }
-    for (int e = tid; e < E; e += B_THREADS) a.cnt_g[(size_t)b * E + e] = base[e];
-    if (tid == 0) a.bad_g[b] = (int)*flag;
-    // 2. all ranges counted
-    if (!grid_barrier(a.bar_count, a.bar_gen, (unsigned)G, a.status)) return;
+    // 2. all ranges counted (a single range needs neither the count table nor the barrier)
     int bad = 0;
-    for (int i = tid; i < G; i += B_THREADS) bad |= __ldcg(a.bad_g + i);
+    if (G > 1) {
+        for (int e = tid; e < E; e += B_THREADS) a.cnt_g[(size_t)b * E + e] = base[e];
+        if (tid == 0) a.bad_g[b] = (int)*flag;
+        if (!grid_barrier(a.bar_count, a.bar_gen, (unsigned)G, a.status)) return;
+        for (int i = tid; i < G; i += B_THREADS) bad |= __ldcg(a.bad_g + i);
+    } else {
+        __syncthreads();
+        bad = (int)*flag;
+    }
     if (__syncthreads_or(bad)) {
         if (b == 0) {
             for (int e = tid; e <= E; e += B_THREADS) a.expStart[e] = 0;
@@ -183,12 +188,17 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     // for the plan, 16-row padded starts and TILE_N-row tile starts
     {
         int c = 0, before = 0;
-        if (tid < E)
-            for (int j = 0; j < G; ++j) {
-                const int v = __ldcg(a.cnt_g + (size_t)j * E + tid);
-                if (j < b) before += v;
-                c += v;
-            }
+        if (tid < E) {
+            if (G == 1)
+                c = base[tid];
+            else
+                for (int j = 0; j < G; ++j) {
+                    const int v = __ldcg(a.cnt_g + (size_t)j * E + tid);
+                    if (j < b) before += v;
+                    c += v;
+                }
+        }
+        __syncthreads();  // every count read before base[] is rewritten below
         const int pc = (c + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
         const int tc = (c + TILE_N - 1) / TILE_N;
         const int i0 = warp_incl_scan(c, lane), i1 = warp_incl_scan(pc, lane), i2 = warp_incl_scan(tc, lane);
@@ -376,6 +386,10 @@ int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *exp
         po.with_shared = with_shared ? 1 : 0;
         po.rows_max = L->rows_max;
         po.tiles_max = L->tiles_max;
+    }
+    if (G == 1) {  // one range: no grid barrier, so no cooperative launch either
+        bucket_kernel<<<1, B_THREADS, smem, s>>>(a, po);
+        return launch_status();
     }
     void *args[] = {(void *)&a, (void *)&po};
     return cuda_status(

@@ -3,11 +3,15 @@
 // mul_mat_id-style launch that gathers the selected experts' rows instead of
 // per-expert launches; lever 2: Q8_1 activations with int8 dp4a dots).
 //
-// Weight-stationary: a CTA owns 32 rows of one expert's matrix and streams
-// each row once per chunk of up to 8 tokens of the expert's CSR segment, so
+// Weight-stationary: a work item is 32 rows of one expert's matrix, whose
+// rows are streamed once per chunk of up to 8 tokens of the expert's CSR
+// segment, so
 // for decode batches (a few tokens per expert) every touched weight byte is
 // read once.  The chunk's arithmetic is specialised on its token count
-// (1, 2, 4 or 8 slots), so a one-token segment costs one token's work.
+// (1, 2, 4 or 8 slots), so a one-token segment costs one token's work.  The
+// grid is persistent (the GPU's resident CTAs) over the items of the experts
+// that received tokens, listed by every CTA from expStart, so an untouched
+// expert costs no CTA.
 // Each warp takes its rows two at a time (gate and up of one feature, or two
 // output columns); lane l owns the 32-wide blocks l, l + 32, ... of both rows
 // and loads all of them (2 x 16 contiguous bytes per block and row) before
@@ -24,6 +28,8 @@
 // down kernel: rows = output columns c, output partial rows (scattered to
 //   t*top_k + slot) or, for the shared expert, s_t * y to shared_out[t].
 #include "moe_internal.cuh"
+
+#include <algorithm>
 
 namespace moe {
 
@@ -69,6 +75,43 @@ __device__ __forceinline__ Seg segment_of(bool is_shared, int e, const int32_t *
     g.s1 = expStart[e + 1];
     g.ok = (g.s0 >= 0 && g.s1 >= g.s0 && g.s1 <= N * top_k);
     return g;
+}
+
+// List of the experts with a non-empty segment (the shared expert: {0}) in act[], count in
+// *n_act; a malformed CSR raises MOE_DEV_BAD_CSR and its expert counts as empty.  Whole CTA.
+__device__ __forceinline__ void active_experts(bool is_shared, int nexp, const int32_t *__restrict__ expStart, int N,
+                                               int top_k, int *act, int *n_act, unsigned *status) {
+    __shared__ int warp_cnt[MV_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (is_shared) {
+        if (threadIdx.x == 0) {
+            act[0] = 0;
+            *n_act = 1;
+        }
+        __syncthreads();
+        return;
+    }
+    int base = 0;
+    for (int e0 = 0; e0 < nexp; e0 += MV_WARPS * 32) {
+        const int e = e0 + threadIdx.x;
+        bool nonempty = false;
+        if (e < nexp) {
+            const int s0 = expStart[e], s1 = expStart[e + 1];
+            const bool ok = s0 >= 0 && s1 >= s0 && s1 <= N * top_k;
+            if (!ok) atomicOr(status, MOE_DEV_BAD_CSR);
+            nonempty = ok && s1 > s0;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, nonempty);
+        if (lane == 0) warp_cnt[warp] = __popc(m);
+        __syncthreads();
+        int before = base;
+        for (int w = 0; w < warp; ++w) before += warp_cnt[w];
+        if (nonempty) act[before + __popc(m & ((1u << lane) - 1))] = e;
+        for (int w = 0; w < MV_WARPS; ++w) base += warp_cnt[w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *n_act = base;
+    __syncthreads();
 }
 
 // Dots of two weight rows a, b (int8 [K], fp32 scales [K/32], fp32 mins or NULL) with T staged
@@ -218,11 +261,12 @@ __device__ __forceinline__ void gate_up_chunk(const GateUpArgs &a, int fb, const
     }
 }
 
-// grid (F/32, nexp); h_q/h_d rows: routed -> CSR entry j, shared -> token t.
+// Persistent grid over the work items (active expert, 32-feature block), expert-major;
+// h_q/h_d rows: routed -> CSR entry j, shared -> token t.
 __global__ void __launch_bounds__(MV_WARPS * 32)
 matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ gd, const float *__restrict__ gm,
                       const int8_t *__restrict__ uq, const float *__restrict__ ud, const float *__restrict__ um,
-                      int D, int F,
+                      int D, int F, int nexp,
                       bool is_shared, const int8_t *__restrict__ x_q, const float *__restrict__ x_d,
                       const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI, int N,
                       int top_k, int8_t *__restrict__ h_q, float *__restrict__ h_d,
@@ -233,12 +277,13 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
     float *hs = xds + MV_T * (D / QK);                                   // [MV_T][32]
     __shared__ int rows[MV_T];
     __shared__ int entries[MV_T];
-    const int fb = blockIdx.x, e = blockIdx.y;
-    Seg sg = segment_of(is_shared, e, expStart, N, top_k);
-    if (!sg.ok) {
-        if (threadIdx.x == 0) atomicOr(status, MOE_DEV_BAD_CSR);
-        return;
-    }
+    __shared__ int act[MAX_E];
+    __shared__ int n_act;
+    active_experts(is_shared, nexp, expStart, N, top_k, act, &n_act, status);
+    const int nfb = F / QK;
+    for (int item = blockIdx.x; item < n_act * nfb; item += gridDim.x) {
+    const int e = act[item / nfb], fb = item % nfb;
+    const Seg sg = segment_of(is_shared, e, expStart, N, top_k);
     GateUpArgs a{gq, uq, gd, gm, ud, um, D, F, (size_t)(is_shared ? 0 : e) * F, h_q, h_d, dbg_dots, dbg_block};
     for (int j0 = sg.s0; j0 < sg.s1; j0 += MV_T) {
         __syncthreads();  // previous chunk fully consumed
@@ -265,6 +310,8 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
         case 4: gate_up_chunk<4>(a, fb, rows, entries, xs, xds, hs); break;
         default: gate_up_chunk<8>(a, fb, rows, entries, xs, xds, hs); break;
         }
+    }
+    __syncthreads();  // the item's last chunk fully consumed before the next item stages
     }
 }
 
@@ -312,10 +359,10 @@ __device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int 
     }
 }
 
-// grid (D/32, nexp)
+// Persistent grid over the work items (active expert, 32-column block), expert-major.
 __global__ void __launch_bounds__(MV_WARPS * 32)
 matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, const float *__restrict__ dm,
-                   int D, int F,
+                   int D, int F, int nexp,
                    bool is_shared, const int8_t *__restrict__ h_q, const float *__restrict__ h_d,
                    const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI,
                    const int32_t *__restrict__ expTokK, int N, int top_k,
@@ -327,12 +374,13 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
     __shared__ int hrows[MV_T];
     __shared__ int orows[MV_T];
     __shared__ float oscale[MV_T];
-    const int cb = blockIdx.x, e = blockIdx.y;
-    Seg sg = segment_of(is_shared, e, expStart, N, top_k);
-    if (!sg.ok) {
-        if (threadIdx.x == 0) atomicOr(status, MOE_DEV_BAD_CSR);
-        return;
-    }
+    __shared__ int act[MAX_E];
+    __shared__ int n_act;
+    active_experts(is_shared, nexp, expStart, N, top_k, act, &n_act, status);
+    const int ncb = D / QK;
+    for (int item = blockIdx.x; item < n_act * ncb; item += gridDim.x) {
+    const int e = act[item / ncb], cb = item % ncb;
+    const Seg sg = segment_of(is_shared, e, expStart, N, top_k);
     DownArgs a{dq, dd, dm, D, F, (size_t)(is_shared ? 0 : e) * D, is_shared, out};
     for (int j0 = sg.s0; j0 < sg.s1; j0 += MV_T) {
         __syncthreads();
@@ -370,6 +418,28 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
         default: down_chunk<8>(a, cb, orows, oscale, hs, hds, ys); break;
         }
     }
+    __syncthreads();  // the item's last chunk fully consumed before the next item stages
+    }
+}
+
+// Persistent grid: the resident CTAs of the whole GPU, at most one per work item.  The
+// occupancy query is remembered for the last dynamic shared-memory size seen (per kernel).
+struct GridCache {
+    size_t smem = ~(size_t)0;
+    int resident = 0;
+};
+int persistent_grid(const void *kernel, size_t smem, int max_items, GridCache *cache) {
+    if (cache->smem != smem) {
+        int dev = 0, n = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0 ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, MV_WARPS * 32, smem) != cudaSuccess ||
+            per_sm <= 0)
+            return -1;
+        cache->resident = n * per_sm;
+        cache->smem = smem;
+    }
+    return std::max(1, std::min(cache->resident, max_items));
 }
 
 }  // namespace
@@ -383,9 +453,11 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_
     size_t smem = (size_t)MV_T * D + sizeof(float) * ((size_t)MV_T * (D / QK) + MV_T * QK);
     static int configured = 0;
     if (int rc = ensure_dynamic_smem((const void *)matvec_gate_up_kernel, smem, &configured)) return rc;
-    dim3 grid(F / QK, nexp);
+    static GridCache gc;
+    const int grid = persistent_grid((const void *)matvec_gate_up_kernel, smem, nexp * (F / QK), &gc);
+    if (grid < 0) return MOE_ERR_CUDA;
     matvec_gate_up_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.gate_q, set.gate_d, set.gate_m, set.up_q, set.up_d,
-                                                           set.up_m, D, F,
+                                                           set.up_m, D, F, nexp,
                                                            is_shared, x_q, x_d, expStart, expTokI, N, top_k,
                                                            h_q, h_d, dbg_dots, dbg_block, status);
     return launch_status();
@@ -400,8 +472,11 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_sha
     size_t smem = (size_t)MV_T * F + sizeof(float) * ((size_t)MV_T * (F / QK) + MV_T * QK);
     static int configured = 0;
     if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel, smem, &configured)) return rc;
-    dim3 grid(D / QK, nexp);
-    matvec_down_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, is_shared, h_q, h_d,
+    static GridCache gc;
+    const int grid = persistent_grid((const void *)matvec_down_kernel, smem, nexp * (D / QK), &gc);
+    if (grid < 0) return MOE_ERR_CUDA;
+    matvec_down_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, nexp, is_shared,
+                                                        h_q, h_d,
                                                         expStart, expTokI, expTokK, N, top_k, shexp_scale,
                                                         out, status);
     return launch_status();

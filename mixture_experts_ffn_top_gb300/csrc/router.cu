@@ -265,10 +265,12 @@ int launch_softmax(const float *part, int nsplit, int N, int E, int Eext, int to
 }  // namespace
 
 int router_nsplit(int N, int D, int E) {
-    // about four 8-warp CTAs per SM, each split at least 128 deep
+    // about four 8-warp CTAs per SM; each split at least 128 deep, or one K chunk (32) when
+    // the tiles are few (decode batches: one chunk per CTA, all of routerW read in one round)
     int tiles = ((N + RB_M - 1) / RB_M) * ((E + RB_N - 1) / RB_N);
     int want = (4 * 152 + tiles - 1) / tiles;
-    int maxs = D / 128 > 0 ? D / 128 : 1;
+    int depth = tiles <= 4 ? RB_K : 128;
+    int maxs = D / depth > 0 ? D / depth : 1;
     int s = want < 1 ? 1 : (want > maxs ? maxs : want);
     while (s > 1 && (D / QK) % s != 0) --s;  // equal splits on block boundaries
     return s;
