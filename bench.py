@@ -38,6 +38,7 @@ METRIC = "MoE-FFN prefill tokens/s/layer, OLMoE shape N=2048; % of int8 tensor p
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "olmoe"
 L2_FLUSH_BYTES = 512 << 20
+STAGE_STEPS = 50  # steps of the per-stage breakdown (moe_ffn_prefill_timed)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -62,6 +63,30 @@ def max_over_ranks(x: float, device) -> float:
 def job_throughput(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
     """Whole-job tokens/s: every rank's batch, over the slowest rank's step time."""
     return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
+def bind_near_gpu(ops):
+    """Move this thread onto the CPUs of the host NUMA node closest to the current GPU (the node
+    the device reports), so host memory it allocates and first touches is local to the GPU's
+    host link.  Returns (node or None, the previous CPU set or None)."""
+    try:
+        node = ops.moe_device_host_numa_node()
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            spec = f.read().strip()
+    except (OSError, RuntimeError, ValueError):
+        return None, None
+    if node < 0 or not spec:
+        return None, None
+    cpus = set()
+    for part in spec.split(","):
+        lo, _, hi = part.partition("-")
+        cpus.update(range(int(lo), int(hi or lo) + 1))
+    before = os.sched_getaffinity(0)
+    mine = cpus & before
+    if not mine:
+        return node, None
+    os.sched_setaffinity(0, mine)
+    return node, before
 
 
 def load_peaks():
@@ -266,7 +291,8 @@ def run_ours(args, rank, world, local_rank):
         resolved_path = ops.MOE_PATH_TENSOR if tensor else ops.MOE_PATH_MATVEC
     topk_idx = v["topk_idx"].cpu().numpy()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    # the timed steps: one plain moe_ffn_prefill call each, bracketed by two events
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     gpu_index = int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].strip().isdigit() else local_rank
     clocks = ClockSampler(gpu_index)
@@ -278,7 +304,9 @@ def run_ours(args, rank, world, local_rank):
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(1)  # before the step's events: every step starts with a cold L2
-        step(evs[i])
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
@@ -287,20 +315,36 @@ def run_ours(args, rank, world, local_rank):
     status = layer.status()
     if status:
         raise RuntimeError(f"device status {status} after the timed steps")
-    stage_ms = {s: [] for s in stages}
-    step_ms = []
-    for e in evs:
-        for j, s in enumerate(stages):
-            stage_ms[s].append(e[j].elapsed_time(e[j + 1]))
-        step_ms.append(e[0].elapsed_time(e[6]))
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms = max_over_ranks(statistics.mean(step_ms), device)
     value = job_throughput(world, N, ms)
+
+    # where the time goes: the same steps through moe_ffn_prefill_timed, which records events on
+    # the launching stream between its kernels (those events cost a few microseconds per stage,
+    # so this breakdown is not the headline)
+    n_stage_steps = min(args.steps, STAGE_STEPS)
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_stage_steps)]
+    for i in range(n_stage_steps):
+        flush.fill_(1)
+        step(sevs[i])
+    torch.cuda.synchronize()
+    if layer.status():
+        raise RuntimeError("device status set during the stage-timed steps")
+    stage_ms = {s: [] for s in stages}
+    for e in sevs:
+        for j, s in enumerate(stages):
+            stage_ms[s].append(e[j].elapsed_time(e[j + 1]))
+    stage_step_ms = statistics.mean(e[0].elapsed_time(e[6]) for e in sevs)
 
     # e2e: the public host-buffer call (moe_ffn_prefill_host) on pinned host memory; the hidden rows
     # come in and the output rows go out over the host link inside the timed region (the router
     # reads them and the combine writes them in place)
+    numa_node, cpus0 = bind_near_gpu(ops)  # pinned pages land on the node of the allocating CPU
     h_host = torch.from_numpy(inp["hidden"]).pin_memory()
     o_host = torch.empty((N, D), dtype=torch.float32).pin_memory()
+    o_host.zero_()
+    if cpus0 is not None:
+        os.sched_setaffinity(0, cpus0)
 
     def e2e_step():
         ops.moe_ffn_prefill_host(w, h_host, routerW, shg, k, wl.norm_topk_prob, ws, o_host, path=path)
@@ -383,15 +427,18 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "expert_path": {1: "matvec", 2: "tensor"}[resolved_path],
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write); expert weights exceed L2",
-                   "step": "one moe_ffn_prefill call; stage times from events it records between kernels"},
+                   "step": "one moe_ffn_prefill call between two events; stage times from "
+                           f"moe_ffn_prefill_timed over {n_stage_steps} further steps"},
         "stage_ms": {s: statistics.mean(vv) for s, vv in stage_ms.items()},
+        "stage_timed_ms_per_step": stage_step_ms,
         "layer_roofline_us": layer_roof_s * 1e6,
         "layer_roofline_frac": layer_roof_s / (ms / 1e3),
         "algorithmic": work,
         "roofline": roofline,
         "e2e": {"value": job_throughput(world, N, e2e_mean), "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
                 "d2h_bytes_per_step": N * D * 4, "ms_per_step": e2e_mean,
-                "api": "moe_ffn_prefill_host on pinned host buffers (read and written in place over the host link)"},
+                "api": "moe_ffn_prefill_host on pinned host buffers (read and written in place over the host link)",
+                "host_numa_node": numa_node},
         "with_residual": {"value": job_throughput(world, N, res_mean), "unit": UNIT, "ms_per_step": res_mean,
                           "api": "moe_ffn_prefill_residual (residual add fused into the combine)"},
         "gpu_launches": launches_per_step * args.steps,

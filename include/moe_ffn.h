@@ -154,7 +154,8 @@ int moe_weights_tensor_path(moe_weights_t w);
 /* ---------------------------------------------------------------------------
  * Workspace: one caller-owned device buffer per concurrent call chain.  The
  * first 256 bytes hold the device status word (and the bucketing kernel's
- * grid-barrier words).  moe_workspace_init zeroes those 256 bytes
+ * grid-barrier words and the small-batch routing's arrival counter, all zero
+ * between calls).  moe_workspace_init zeroes those 256 bytes
  * (asynchronously); moe_workspace_status synchronises the
  * stream, returns the status word (host int, MOE_DEV_* bits) and, when
  * clear != 0, zeroes it.  Two call chains must not share a workspace.
@@ -363,6 +364,12 @@ int moe_ffn_prefill_host(moe_weights_t w, const float *hidden_host, const float 
  * moe_ffn_prefill_host accepts), 0 otherwise (device or managed memory,
  * NULL, or pageable memory on a system without host page-table access). */
 int moe_host_memory_addressable(const void *p);
+/* The host NUMA node closest to the current device (where the host buffers of
+ * moe_ffn_prefill_host cross the fewest links: on a multi-socket host, memory
+ * of another socket is reached through the inter-socket link as well), or -1
+ * when the system reports no NUMA placement.  *node: host pointer.  Returns 0,
+ * MOE_ERR_INVALID_ARG for NULL, MOE_ERR_CUDA if the query fails. */
+int moe_device_host_numa_node(int *node);
 
 /* moe_ffn_prefill_ex that also records seven caller-created CUDA events on
  * `stream` around its stages, for measuring each kernel in place:

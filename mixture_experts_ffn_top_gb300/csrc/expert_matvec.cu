@@ -77,6 +77,16 @@ __device__ __forceinline__ Seg segment_of(bool is_shared, int e, const int32_t *
     return g;
 }
 
+// Asks L2 for [p, p + bytes) (16-byte aligned, a multiple of 16 bytes) in pieces of at most
+// 32 KB; a hint with no completion to wait for.
+__device__ __forceinline__ void l2_prefetch(const void *p, size_t bytes) {
+    const char *c = static_cast<const char *>(p);
+    for (size_t off = 0; off < bytes; off += 32768) {
+        const unsigned n = (unsigned)min((size_t)32768, bytes - off);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+    }
+}
+
 // List of the experts with a non-empty segment (the shared expert: {0}) in act[], count in
 // *n_act; a malformed CSR raises MOE_DEV_BAD_CSR and its expert counts as empty.  Whole CTA.
 __device__ __forceinline__ void active_experts(bool is_shared, int nexp, const int32_t *__restrict__ expStart, int N,
@@ -114,38 +124,37 @@ __device__ __forceinline__ void active_experts(bool is_shared, int nexp, const i
     __syncthreads();
 }
 
-// Dots of two weight rows a, b (int8 [K], fp32 scales [K/32], fp32 mins or NULL) with T staged
-// activation rows (xs [T][K] int8, xds [T][K/32] fp32).  Returns per-token fp32 sums, reduced
-// across the warp (valid in every lane).  The lane owning block dbg_block stores its isums.
-template <int T>
-__device__ __forceinline__ void two_rows_dot(const int8_t *__restrict__ wa, const float *__restrict__ da,
-                                             const float *__restrict__ ma, const int8_t *__restrict__ wb,
-                                             const float *__restrict__ db, const float *__restrict__ mb, int K,
-                                             const int8_t *xs, const float *xds, int lane, float (&acc_a)[T],
-                                             float (&acc_b)[T], int dbg_block, int (&dbg_a)[T], int (&dbg_b)[T]) {
+// Dots of R weight rows (int8 [K], fp32 scales [K/32], fp32 mins or NULL for every row) with T
+// staged activation rows (xs [T][K] int8, xds [T][K/32] fp32).  Lane l owns the 32-wide blocks
+// l, l + 32, ... and loads them for all R rows before any arithmetic.  Returns per-row, per-token
+// fp32 sums reduced across the warp (valid in every lane); the lane owning block dbg_block
+// stores its isums.
+template <int T, int R>
+__device__ __forceinline__ void rows_dot(const int8_t *const (&w)[R], const float *const (&d)[R],
+                                         const float *const (&m)[R], bool mins, int K, const int8_t *xs,
+                                         const float *xds, int lane, float (&acc)[R][T], int dbg_block,
+                                         int (&dbg)[R][T]) {
     const int nblk = K / QK;
 #pragma unroll
-    for (int tt = 0; tt < T; ++tt) acc_a[tt] = acc_b[tt] = 0.0f;
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) acc[i][tt] = 0.0f;
     for (int b0 = 0; b0 < nblk; b0 += 64) {
-        int4 qa[2][2], qb[2][2];
-        float sa[2], sb[2], na[2], nb[2];
+        int4 q[2][R][2];
+        float sc[2][R], mn[2][R];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int b = b0 + 32 * u + lane;
-            qa[u][0] = qa[u][1] = qb[u][0] = qb[u][1] = make_int4(0, 0, 0, 0);
-            sa[u] = sb[u] = na[u] = nb[u] = 0.0f;
-            if (b < nblk) {
-                const int4 *pa = reinterpret_cast<const int4 *>(wa + (size_t)b * QK);
-                const int4 *pb = reinterpret_cast<const int4 *>(wb + (size_t)b * QK);
-                qa[u][0] = __ldcs(pa);
-                qa[u][1] = __ldcs(pa + 1);
-                qb[u][0] = __ldcs(pb);
-                qb[u][1] = __ldcs(pb + 1);
-                sa[u] = __ldcs(da + b);
-                sb[u] = __ldcs(db + b);
-                if (ma != nullptr) {
-                    na[u] = __ldcs(ma + b);
-                    nb[u] = __ldcs(mb + b);
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                q[u][i][0] = q[u][i][1] = make_int4(0, 0, 0, 0);
+                sc[u][i] = mn[u][i] = 0.0f;
+                if (b < nblk) {
+                    const int4 *p = reinterpret_cast<const int4 *>(w[i] + (size_t)b * QK);
+                    q[u][i][0] = __ldcs(p);
+                    q[u][i][1] = __ldcs(p + 1);
+                    sc[u][i] = __ldcs(d[i] + b);
+                    if (mins) mn[u][i] = __ldcs(m[i] + b);
                 }
             }
         }
@@ -158,27 +167,29 @@ __device__ __forceinline__ void two_rows_dot(const int8_t *__restrict__ wa, cons
                 const int4 *px = reinterpret_cast<const int4 *>(xs + (size_t)tt * K + (size_t)b * QK);
                 const int4 x0 = px[0], x1 = px[1];
                 const float dx = xds[tt * nblk + b];
-                const int ia = dp4a32(qa[u], x0, x1), ib = dp4a32(qb[u], x0, x1);
-                acc_a[tt] = fmaf(sa[u] * dx, (float)ia, acc_a[tt]);
-                acc_b[tt] = fmaf(sb[u] * dx, (float)ib, acc_b[tt]);
-                if (ma != nullptr) {
-                    const float xsum = (float)codesum32(x0, x1);
-                    acc_a[tt] = fmaf(-(na[u] * dx), xsum, acc_a[tt]);
-                    acc_b[tt] = fmaf(-(nb[u] * dx), xsum, acc_b[tt]);
-                }
-                if (b == dbg_block) {
-                    dbg_a[tt] = ia;
-                    dbg_b[tt] = ib;
+                const float xsum = mins ? (float)codesum32(x0, x1) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const int is = dp4a32(q[u][i], x0, x1);
+                    acc[i][tt] = fmaf(sc[u][i] * dx, (float)is, acc[i][tt]);
+                    if (mins) acc[i][tt] = fmaf(-(mn[u][i] * dx), xsum, acc[i][tt]);
+                    if (b == dbg_block) dbg[i][tt] = is;
                 }
             }
         }
     }
 #pragma unroll
-    for (int tt = 0; tt < T; ++tt) {
-        acc_a[tt] = warp_sum(acc_a[tt]);
-        acc_b[tt] = warp_sum(acc_b[tt]);
-    }
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) acc[i][tt] = warp_sum(acc[i][tt]);
 }
+
+// Rows per rows_dot call for a kernel whose chunks have at most TMAX token slots: four when the
+// chunks are narrow (decode batches), two otherwise (register budget).
+template <int TMAX>
+struct RowsPerCall {
+    static constexpr int value = TMAX <= 2 ? 4 : 2;
+};
 
 // Stage T activation rows (int8 [K] + fp32 scales [K/32]) into shared memory; rows[tt] < 0
 // (no row) stages zeros.
@@ -212,38 +223,55 @@ struct GateUpArgs {
     int dbg_block;
 };
 
-// One chunk of T token slots of the gate/up kernel: every warp's 4 features, then the Q8_1
-// requantisation of the 32-feature block per token.
-template <int T>
+// One chunk of T token slots of the gate/up kernel: every warp's 4 features (R/2 per rows_dot
+// call: gate and up rows of each), then the Q8_1 requantisation of the 32-feature block per token.
+template <int T, int R>
 __device__ __forceinline__ void gate_up_chunk(const GateUpArgs &a, int fb, const int *rows, const int *entries,
                                               const int8_t *xs, const float *xds, float *hs) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = a.D;
-    for (int r = 0; r < MV_ROWS_PER_WARP; ++r) {
-        const int fl = warp * MV_ROWS_PER_WARP + r;  // feature within the 32-block
-        const int f = fb * QK + fl;
-        float g[T], u[T];
-        int dg[T], du[T];
+    constexpr int NF = R / 2;  // features per call
+    for (int r = 0; r < MV_ROWS_PER_WARP; r += NF) {
+        const int fl0 = warp * MV_ROWS_PER_WARP + r;  // first feature within the 32-block
+        const int8_t *wr[R];
+        const float *dr[R], *mr[R];
 #pragma unroll
-        for (int tt = 0; tt < T; ++tt) dg[tt] = du[tt] = 0;
-        const size_t so = (a.mat_off + f) * (D / QK);
-        two_rows_dot<T>(a.gq + (a.mat_off + f) * D, a.gd + so, a.gm ? a.gm + so : nullptr, a.uq + (a.mat_off + f) * D,
-                        a.ud + so, a.um ? a.um + so : nullptr, D, xs, xds, lane, g, u, a.dbg_block, dg, du);
-        if (a.dbg_dots != nullptr && a.dbg_block >= 0 && lane == (a.dbg_block & 31)) {
-#pragma unroll
-            for (int tt = 0; tt < T; ++tt) {
-                const int j = entries[tt];
-                if (j < 0 || rows[tt] < 0) continue;
-                a.dbg_dots[((size_t)j * 2 + 0) * a.F + f] = dg[tt];
-                a.dbg_dots[((size_t)j * 2 + 1) * a.F + f] = du[tt];
-            }
+        for (int i = 0; i < NF; ++i) {
+            const size_t f = a.mat_off + fb * QK + fl0 + i;
+            wr[2 * i] = a.gq + f * D;
+            wr[2 * i + 1] = a.uq + f * D;
+            dr[2 * i] = a.gd + f * (D / QK);
+            dr[2 * i + 1] = a.ud + f * (D / QK);
+            mr[2 * i] = a.gm ? a.gm + f * (D / QK) : nullptr;
+            mr[2 * i + 1] = a.um ? a.um + f * (D / QK) : nullptr;
         }
-        if (lane == 0) {
+        float acc[R][T];
+        int dbg[R][T];
 #pragma unroll
-            for (int tt = 0; tt < T; ++tt) {
-                const float gv = g[tt];
-                const float silu = gv / (1.0f + expf(-gv));
-                hs[tt * QK + fl] = silu * u[tt];
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) dbg[i][tt] = 0;
+        rows_dot<T, R>(wr, dr, mr, a.gm != nullptr, D, xs, xds, lane, acc, a.dbg_block, dbg);
+#pragma unroll
+        for (int i = 0; i < NF; ++i) {
+            const int fl = fl0 + i;
+            const int f = fb * QK + fl;
+            if (a.dbg_dots != nullptr && a.dbg_block >= 0 && lane == (a.dbg_block & 31)) {
+#pragma unroll
+                for (int tt = 0; tt < T; ++tt) {
+                    const int j = entries[tt];
+                    if (j < 0 || rows[tt] < 0) continue;
+                    a.dbg_dots[((size_t)j * 2 + 0) * a.F + f] = dbg[2 * i][tt];
+                    a.dbg_dots[((size_t)j * 2 + 1) * a.F + f] = dbg[2 * i + 1][tt];
+                }
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int tt = 0; tt < T; ++tt) {
+                    const float gv = acc[2 * i][tt];
+                    const float silu = gv / (1.0f + expf(-gv));
+                    hs[tt * QK + fl] = silu * acc[2 * i + 1][tt];
+                }
             }
         }
     }
@@ -262,7 +290,9 @@ __device__ __forceinline__ void gate_up_chunk(const GateUpArgs &a, int fb, const
 }
 
 // Persistent grid over the work items (active expert, 32-feature block), expert-major;
-// h_q/h_d rows: routed -> CSR entry j, shared -> token t.
+// h_q/h_d rows: routed -> CSR entry j, shared -> token t.  TMAX: the most token slots a chunk
+// can need (the launch's batch bounds every segment).
+template <int TMAX>
 __global__ void __launch_bounds__(MV_WARPS * 32)
 matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ gd, const float *__restrict__ gm,
                       const int8_t *__restrict__ uq, const float *__restrict__ ud, const float *__restrict__ um,
@@ -285,13 +315,13 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
     const int e = act[item / nfb], fb = item % nfb;
     const Seg sg = segment_of(is_shared, e, expStart, N, top_k);
     GateUpArgs a{gq, uq, gd, gm, ud, um, D, F, (size_t)(is_shared ? 0 : e) * F, h_q, h_d, dbg_dots, dbg_block};
-    for (int j0 = sg.s0; j0 < sg.s1; j0 += MV_T) {
+    for (int j0 = sg.s0; j0 < sg.s1; j0 += TMAX) {
         __syncthreads();  // previous chunk fully consumed
-        const int T = chunk_slots(min(MV_T, sg.s1 - j0));
+        const int T = chunk_slots(min(TMAX, sg.s1 - j0));
         if (threadIdx.x < MV_T) {
             int j = j0 + threadIdx.x;
             int t = -1;
-            if (j < sg.s1) {
+            if (threadIdx.x < TMAX && j < sg.s1) {
                 t = is_shared ? j : expTokI[j];
                 if ((unsigned)t >= (unsigned)N) {
                     atomicOr(status, MOE_DEV_BAD_CSR);
@@ -299,17 +329,16 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
                 }
             }
             rows[threadIdx.x] = t;
-            entries[threadIdx.x] = (j < sg.s1) ? j : -1;
+            entries[threadIdx.x] = (threadIdx.x < TMAX && j < sg.s1) ? j : -1;
         }
         __syncthreads();
         stage_rows(x_q, x_d, D, rows, T, xs, xds);
         __syncthreads();
-        switch (T) {
-        case 1: gate_up_chunk<1>(a, fb, rows, entries, xs, xds, hs); break;
-        case 2: gate_up_chunk<2>(a, fb, rows, entries, xs, xds, hs); break;
-        case 4: gate_up_chunk<4>(a, fb, rows, entries, xs, xds, hs); break;
-        default: gate_up_chunk<8>(a, fb, rows, entries, xs, xds, hs); break;
-        }
+        constexpr int R = RowsPerCall<TMAX>::value;
+        if (T == 1) gate_up_chunk<1, R>(a, fb, rows, entries, xs, xds, hs);
+        else if (TMAX >= 2 && T == 2) gate_up_chunk<(TMAX >= 2 ? 2 : 1), R>(a, fb, rows, entries, xs, xds, hs);
+        else if (TMAX >= 4 && T == 4) gate_up_chunk<(TMAX >= 4 ? 4 : 1), R>(a, fb, rows, entries, xs, xds, hs);
+        else if (TMAX >= 8) gate_up_chunk<(TMAX >= 8 ? 8 : 1), R>(a, fb, rows, entries, xs, xds, hs);
     }
     __syncthreads();  // the item's last chunk fully consumed before the next item stages
     }
@@ -324,28 +353,32 @@ struct DownArgs {
     float *out;
 };
 
-// One chunk of T token slots of the down kernel: every warp's 4 output columns (two pairs),
-// then the stores of the 32-column block per token.
-template <int T>
+// One chunk of T token slots of the down kernel: every warp's 4 output columns (R per rows_dot
+// call), then the stores of the 32-column block per token.
+template <int T, int R>
 __device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int *orows, const float *oscale,
                                            const int8_t *hs, const float *hds, float *ys) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int F = a.F;
-    for (int r = 0; r < MV_ROWS_PER_WARP; r += 2) {
-        const int cl = warp * MV_ROWS_PER_WARP + r;
-        const int c = cb * QK + cl;
-        float ya[T], yb[T];
-        int unused_a[T], unused_b[T];
-        const size_t so = (a.mat_off + c) * (F / QK), so1 = so + F / QK;
-        two_rows_dot<T>(a.dq + (a.mat_off + c) * F, a.dd + so, a.dm ? a.dm + so : nullptr,
-                        a.dq + (a.mat_off + c + 1) * F, a.dd + so1, a.dm ? a.dm + so1 : nullptr, F, hs, hds, lane,
-                        ya, yb, -1, unused_a, unused_b);
+    for (int r = 0; r < MV_ROWS_PER_WARP; r += R) {
+        const int cl0 = warp * MV_ROWS_PER_WARP + r;
+        const int8_t *wr[R];
+        const float *dr[R], *mr[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const size_t c = a.mat_off + cb * QK + cl0 + i;
+            wr[i] = a.dq + c * F;
+            dr[i] = a.dd + c * (F / QK);
+            mr[i] = a.dm ? a.dm + c * (F / QK) : nullptr;
+        }
+        float y[R][T];
+        int unused[R][T];
+        rows_dot<T, R>(wr, dr, mr, a.dm != nullptr, F, hs, hds, lane, y, -1, unused);
         if (lane == 0) {
 #pragma unroll
-            for (int tt = 0; tt < T; ++tt) {
-                ys[tt * QK + cl] = ya[tt];
-                ys[tt * QK + cl + 1] = yb[tt];
-            }
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+                for (int tt = 0; tt < T; ++tt) ys[tt * QK + cl0 + i] = y[i][tt];
         }
     }
     __syncthreads();
@@ -360,6 +393,7 @@ __device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int 
 }
 
 // Persistent grid over the work items (active expert, 32-column block), expert-major.
+template <int TMAX>
 __global__ void __launch_bounds__(MV_WARPS * 32)
 matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, const float *__restrict__ dm,
                    int D, int F, int nexp,
@@ -382,14 +416,20 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
     const int e = act[item / ncb], cb = item % ncb;
     const Seg sg = segment_of(is_shared, e, expStart, N, top_k);
     DownArgs a{dq, dd, dm, D, F, (size_t)(is_shared ? 0 : e) * D, is_shared, out};
-    for (int j0 = sg.s0; j0 < sg.s1; j0 += MV_T) {
+    if (threadIdx.x == 0) {
+        const size_t r0 = a.mat_off + (size_t)cb * QK, sbytes = (size_t)QK * (F / QK) * 4;
+        l2_prefetch(dq + r0 * F, (size_t)QK * F);
+        l2_prefetch(dd + r0 * (F / QK), sbytes);
+        if (dm != nullptr) l2_prefetch(dm + r0 * (F / QK), sbytes);
+    }
+    for (int j0 = sg.s0; j0 < sg.s1; j0 += TMAX) {
         __syncthreads();
-        const int T = chunk_slots(min(MV_T, sg.s1 - j0));
+        const int T = chunk_slots(min(TMAX, sg.s1 - j0));
         if (threadIdx.x < MV_T) {
             int j = j0 + threadIdx.x;
             int hr = -1, orow = -1;
             float sc = 1.0f;
-            if (j < sg.s1) {
+            if (threadIdx.x < TMAX && j < sg.s1) {
                 if (is_shared) {
                     hr = j;
                     orow = j;
@@ -411,12 +451,11 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
         __syncthreads();
         stage_rows(h_q, h_d, F, hrows, T, hs, hds);
         __syncthreads();
-        switch (T) {
-        case 1: down_chunk<1>(a, cb, orows, oscale, hs, hds, ys); break;
-        case 2: down_chunk<2>(a, cb, orows, oscale, hs, hds, ys); break;
-        case 4: down_chunk<4>(a, cb, orows, oscale, hs, hds, ys); break;
-        default: down_chunk<8>(a, cb, orows, oscale, hs, hds, ys); break;
-        }
+        constexpr int R = RowsPerCall<TMAX>::value;
+        if (T == 1) down_chunk<1, R>(a, cb, orows, oscale, hs, hds, ys);
+        else if (TMAX >= 2 && T == 2) down_chunk<(TMAX >= 2 ? 2 : 1), R>(a, cb, orows, oscale, hs, hds, ys);
+        else if (TMAX >= 4 && T == 4) down_chunk<(TMAX >= 4 ? 4 : 1), R>(a, cb, orows, oscale, hs, hds, ys);
+        else if (TMAX >= 8) down_chunk<(TMAX >= 8 ? 8 : 1), R>(a, cb, orows, oscale, hs, hds, ys);
     }
     __syncthreads();  // the item's last chunk fully consumed before the next item stages
     }
@@ -444,23 +483,67 @@ int persistent_grid(const void *kernel, size_t smem, int max_items, GridCache *c
 
 }  // namespace
 
+namespace {
+
+// Chunk width bound of a launch: no segment is longer than the batch (a token picks an expert
+// at most once; the shared expert's segment is the batch itself).
+int tmax_for(int N) { return N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : MV_T; }
+
+template <int TMAX>
+int gate_up_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *x_q, const float *x_d,
+                   const int32_t *expStart, const int32_t *expTokI, int N, int top_k, int8_t *h_q, float *h_d,
+                   int32_t *dbg_dots, int dbg_block, unsigned *status, cudaStream_t s) {
+    const size_t smem = (size_t)MV_T * D + sizeof(float) * ((size_t)MV_T * (D / QK) + MV_T * QK);
+    static int configured = 0;
+    if (int rc = ensure_dynamic_smem((const void *)matvec_gate_up_kernel<TMAX>, smem, &configured)) return rc;
+    static GridCache gc;
+    const int grid = persistent_grid((const void *)matvec_gate_up_kernel<TMAX>, smem, nexp * (F / QK), &gc);
+    if (grid < 0) return MOE_ERR_CUDA;
+    matvec_gate_up_kernel<TMAX><<<grid, MV_WARPS * 32, smem, s>>>(set.gate_q, set.gate_d, set.gate_m, set.up_q,
+                                                                 set.up_d, set.up_m, D, F, nexp, is_shared, x_q, x_d,
+                                                                 expStart, expTokI, N, top_k, h_q, h_d, dbg_dots,
+                                                                 dbg_block, status);
+    return launch_status();
+}
+
+template <int TMAX>
+int down_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *h_q, const float *h_d,
+                const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
+                const float *shexp_scale, float *out, unsigned *status, cudaStream_t s) {
+    const size_t smem = (size_t)MV_T * F + sizeof(float) * ((size_t)MV_T * (F / QK) + MV_T * QK);
+    static int configured = 0;
+    if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel<TMAX>, smem, &configured)) return rc;
+    static GridCache gc;
+    const int grid = persistent_grid((const void *)matvec_down_kernel<TMAX>, smem, nexp * (D / QK), &gc);
+    if (grid < 0) return MOE_ERR_CUDA;
+    matvec_down_kernel<TMAX><<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, nexp,
+                                                              is_shared, h_q, h_d, expStart, expTokI, expTokK, N,
+                                                              top_k, shexp_scale, out, status);
+    return launch_status();
+}
+
+}  // namespace
+
 int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_shared,
                           const int8_t *x_q, const float *x_d, const int32_t *expStart,
                           const int32_t *expTokI, int N, int top_k, int8_t *h_q, float *h_d,
                           int32_t *dbg_dots, int dbg_block, unsigned *status, cudaStream_t s) {
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
-    size_t smem = (size_t)MV_T * D + sizeof(float) * ((size_t)MV_T * (D / QK) + MV_T * QK);
-    static int configured = 0;
-    if (int rc = ensure_dynamic_smem((const void *)matvec_gate_up_kernel, smem, &configured)) return rc;
-    static GridCache gc;
-    const int grid = persistent_grid((const void *)matvec_gate_up_kernel, smem, nexp * (F / QK), &gc);
-    if (grid < 0) return MOE_ERR_CUDA;
-    matvec_gate_up_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.gate_q, set.gate_d, set.gate_m, set.up_q, set.up_d,
-                                                           set.up_m, D, F, nexp,
-                                                           is_shared, x_q, x_d, expStart, expTokI, N, top_k,
-                                                           h_q, h_d, dbg_dots, dbg_block, status);
-    return launch_status();
+    switch (tmax_for(N)) {
+    case 1:
+        return gate_up_launch<1>(set, D, F, nexp, is_shared, x_q, x_d, expStart, expTokI, N, top_k, h_q, h_d,
+                                 dbg_dots, dbg_block, status, s);
+    case 2:
+        return gate_up_launch<2>(set, D, F, nexp, is_shared, x_q, x_d, expStart, expTokI, N, top_k, h_q, h_d,
+                                 dbg_dots, dbg_block, status, s);
+    case 4:
+        return gate_up_launch<4>(set, D, F, nexp, is_shared, x_q, x_d, expStart, expTokI, N, top_k, h_q, h_d,
+                                 dbg_dots, dbg_block, status, s);
+    default:
+        return gate_up_launch<MV_T>(set, D, F, nexp, is_shared, x_q, x_d, expStart, expTokI, N, top_k, h_q, h_d,
+                                    dbg_dots, dbg_block, status, s);
+    }
 }
 
 int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_shared, const int8_t *h_q,
@@ -469,17 +552,20 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_sha
                        unsigned *status, cudaStream_t s) {
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
-    size_t smem = (size_t)MV_T * F + sizeof(float) * ((size_t)MV_T * (F / QK) + MV_T * QK);
-    static int configured = 0;
-    if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel, smem, &configured)) return rc;
-    static GridCache gc;
-    const int grid = persistent_grid((const void *)matvec_down_kernel, smem, nexp * (D / QK), &gc);
-    if (grid < 0) return MOE_ERR_CUDA;
-    matvec_down_kernel<<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, nexp, is_shared,
-                                                        h_q, h_d,
-                                                        expStart, expTokI, expTokK, N, top_k, shexp_scale,
-                                                        out, status);
-    return launch_status();
+    switch (tmax_for(N)) {
+    case 1:
+        return down_launch<1>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
+                              shexp_scale, out, status, s);
+    case 2:
+        return down_launch<2>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
+                              shexp_scale, out, status, s);
+    case 4:
+        return down_launch<4>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
+                              shexp_scale, out, status, s);
+    default:
+        return down_launch<MV_T>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
+                                 shexp_scale, out, status, s);
+    }
 }
 
 }  // namespace moe

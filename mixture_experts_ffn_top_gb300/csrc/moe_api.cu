@@ -424,14 +424,27 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
     float *part = ws_ptr<float>(ws, L.partials);
     float *shout = shexp_gate ? ws_ptr<float>(ws, L.shared_out) : nullptr;
     mark(0);
-    rc = launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh, xq, xd,
-                       nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream);
-    mark(1);
     // on the tensor path the bucketing kernel also writes the GEMMs' plan
     const bool tensor = (p == MOE_PATH_TENSOR);
-    if (!rc)
-        rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr);
-    mark(2);
+    // decode batches on the matvec path: routing and bucketing in one launch
+    int small = MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!tensor)
+        small = launch_route_small(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh,
+                                   xq, xd, ws_ptr<float>(ws, L.part_logits), es, ti, tk,
+                                   reinterpret_cast<unsigned *>(static_cast<char *>(ws) + ROUTE_COUNTER_OFFSET),
+                                   status_word(ws), stream);
+    if (small != MOE_ERR_UNSUPPORTED_SHAPE) {
+        rc = small;
+        mark(1);
+        mark(2);
+    } else {
+        rc = launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh, xq,
+                           xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream);
+        mark(1);
+        if (!rc)
+            rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr);
+        mark(2);
+    }
     if (tensor) {
         const bool with_shared = shout != nullptr;
         if (!rc) rc = launch_plan_and_gather(w, xq, xd, es, ti, tk, N, top_k, with_shared, ws, L, stream, true);
@@ -490,6 +503,16 @@ static const void *host_view(const void *p) {
 }
 
 int moe_host_memory_addressable(const void *p) { return p != nullptr && host_view(p) != nullptr ? 1 : 0; }
+
+int moe_device_host_numa_node(int *node) {
+    if (node == nullptr) return MOE_ERR_INVALID_ARG;
+    *node = -1;
+    int dev = 0, v = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrHostNumaId, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    *node = v < 0 ? -1 : v;
+    return MOE_OK;
+}
 
 int moe_ffn_prefill_host(moe_weights_t w, const float *hidden_host, const float *routerW, const float *shexp_gate,
                          int N, int top_k, int norm_topk_prob, float *out_host, int path, void *ws, size_t ws_bytes,

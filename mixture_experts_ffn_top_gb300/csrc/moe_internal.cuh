@@ -96,10 +96,19 @@ int launch_router(const float *hidden, const float *routerW, const float *shexp_
                   cudaStream_t s);
 int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,
                             float *w, cudaStream_t s);
+// router + softmax/top-k + bucketing of a batch of at most 8 tokens in one launch (counter: an
+// arrival word in the workspace's status block, ROUTE_COUNTER_OFFSET, zero between launches);
+// MOE_ERR_UNSUPPORTED_SHAPE when the batch is too large for it.
+constexpr size_t ROUTE_COUNTER_OFFSET = 192;
+int launch_route_small(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
+                       int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
+                       float *x_d, float *part_logits, int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
+                       unsigned *counter, unsigned *status, cudaStream_t s);
 int launch_quantize_q8_1(const float *x, int64_t nblk, int8_t *q, float *d, cudaStream_t s);
 // bucket.cu
 // ws: the workspace (status word at 0, the grid barrier's two words at BUCKET_BARRIER_OFFSET
-// and +64, the per-range count table at BUCKET_SCRATCH_OFFSET, bucket_scratch_bytes long).
+// and +64, the small-batch routing's arrival counter at ROUTE_COUNTER_OFFSET, the per-range
+// count table at BUCKET_SCRATCH_OFFSET, bucket_scratch_bytes long).
 // L non-null: also write the tensor path's plan into ws (layout L).
 constexpr size_t BUCKET_BARRIER_OFFSET = 64;
 constexpr size_t BUCKET_SCRATCH_OFFSET = 256;

@@ -3,7 +3,7 @@
 // #388: breakdown table "router" row -- matvec + softmax + top-k + shexp-gate,
 // per token -- and "Remaining levers" item 1, which moves it onto the GPU).
 //
-// Two kernels:
+// Two kernels (router_small_kernel replaces the first for batches of at most 8 tokens):
 //   router_logits_kernel: split-K fp32 SIMT GEMM  logits = hidden . routerW^T
 //     (routerW extended by the shared gate vector as row E).  The CTAs of
 //     expert tile 0 also quantise the hidden rows they stage (each 32-wide K
@@ -143,15 +143,71 @@ router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__
     }
 }
 
+// Small batches (N <= RS_MAX_N, decode): one CTA per expert row of routerW (row E: the
+// shared gate), its 8 warps splitting K, every thread holding the partial dots of all N tokens;
+// warp sums by a fixed butterfly, then the 8 warp sums in warp order, so the logits are
+// deterministic and need no split-K partials.  The N hidden rows' Q8_1 blocks are spread over
+// all warps of the grid.  Output: logits [N][Eext], read by softmax_topk_kernel as one split.
+constexpr int RS_THREADS = 256;
+constexpr int RS_MAX_N = 8;
+__device__ __forceinline__ void router_small_body(const float *__restrict__ hidden, const float *__restrict__ routerW,
+                                                  const float *__restrict__ shexp_gate, int N, int D, int E, int Eext,
+                                                  float *__restrict__ logits, int8_t *__restrict__ x_q,
+                                                  float *__restrict__ x_d) {
+    __shared__ float red[RS_THREADS / 32][RS_MAX_N];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e = blockIdx.x;
+    const float *w = e < E ? routerW + (size_t)e * D : shexp_gate;
+    float acc[RS_MAX_N];
+#pragma unroll
+    for (int t = 0; t < RS_MAX_N; ++t) acc[t] = 0.0f;
+#pragma unroll 2
+    for (int c = 4 * tid; c < D; c += 4 * RS_THREADS) {
+        const float4 wv = *reinterpret_cast<const float4 *>(w + c);
+#pragma unroll
+        for (int t = 0; t < RS_MAX_N; ++t)
+            if (t < N) {
+                const float4 xv = *reinterpret_cast<const float4 *>(hidden + (size_t)t * D + c);
+                acc[t] = fmaf(xv.x, wv.x, acc[t]);
+                acc[t] = fmaf(xv.y, wv.y, acc[t]);
+                acc[t] = fmaf(xv.z, wv.z, acc[t]);
+                acc[t] = fmaf(xv.w, wv.w, acc[t]);
+            }
+    }
+#pragma unroll
+    for (int t = 0; t < RS_MAX_N; ++t) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) red[warp][t] = v;
+    }
+    __syncthreads();
+    if (tid < N) {
+        float v = red[0][tid];
+        for (int w2 = 1; w2 < RS_THREADS / 32; ++w2) v = __fadd_rn(v, red[w2][tid]);
+        logits[(size_t)tid * Eext + e] = v;
+    }
+    // Q8_1 of the hidden rows: global warp g takes blocks g, g + (all warps), ...
+    const int nblk = N * (D / QK);
+    for (int b = blockIdx.x * (RS_THREADS / 32) + warp; b < nblk; b += gridDim.x * (RS_THREADS / 32)) {
+        float d16f;
+        const int q = q8_quantize_lane(hidden[(size_t)b * QK + lane], &d16f);
+        x_q[(size_t)b * QK + lane] = (int8_t)q;
+        if (lane == 0) x_d[b] = d16f;
+    }
+}
+
+__global__ void __launch_bounds__(RS_THREADS)
+router_small_kernel(const float *__restrict__ hidden, const float *__restrict__ routerW,
+                    const float *__restrict__ shexp_gate, int N, int D, int E, int Eext, float *__restrict__ logits,
+                    int8_t *__restrict__ x_q, float *__restrict__ x_d) {
+    router_small_body(hidden, routerW, shexp_gate, N, D, E, Eext, logits, x_q, x_d);
+}
+
 // One warp per token.  EPL = experts per lane (power of two, EPL*32 >= E).
 template <int EPL>
-__global__ void __launch_bounds__(256)
-softmax_topk_kernel(const float *__restrict__ part, int nsplit, int N, int E, int Eext, int top_k,
-                    int norm, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-                    float *__restrict__ shexp_scale, float *__restrict__ logits_out) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= N) return;
+__device__ __forceinline__ void softmax_topk_token(const float *__restrict__ part, int nsplit, int N, int E, int Eext,
+                                                   int top_k, int norm, int t, int lane, int32_t *__restrict__ topk_idx,
+                                                   float *__restrict__ topk_w, float *__restrict__ shexp_scale,
+                                                   float *__restrict__ logits_out) {
     float l[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
@@ -161,21 +217,21 @@ softmax_topk_kernel(const float *__restrict__ part, int nsplit, int N, int E, in
             // the split partials summed in split order; loads issued four at a time
             const float *pp = part + (size_t)t * Eext + e;
             const size_t stride = (size_t)N * Eext;
-            v = pp[0];
+            v = __ldcg(pp);
             int s = 1;
             for (; s + 4 <= nsplit; s += 4) {
-                const float a0 = pp[s * stride], a1 = pp[(s + 1) * stride], a2 = pp[(s + 2) * stride],
-                            a3 = pp[(s + 3) * stride];
+                const float a0 = __ldcg(pp + s * stride), a1 = __ldcg(pp + (s + 1) * stride),
+                            a2 = __ldcg(pp + (s + 2) * stride), a3 = __ldcg(pp + (s + 3) * stride);
                 v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a0), a1), a2), a3);
             }
-            for (; s < nsplit; ++s) v = __fadd_rn(v, pp[s * stride]);
+            for (; s < nsplit; ++s) v = __fadd_rn(v, __ldcg(pp + s * stride));
             if (logits_out) logits_out[(size_t)t * E + e] = v;
         }
         l[i] = v;
     }
     if (shexp_scale != nullptr && lane == 0) {
-        float g = part[(size_t)t * Eext + E];
-        for (int s = 1; s < nsplit; ++s) g = __fadd_rn(g, part[((size_t)s * N + t) * Eext + E]);
+        float g = __ldcg(part + (size_t)t * Eext + E);
+        for (int s = 1; s < nsplit; ++s) g = __fadd_rn(g, __ldcg(part + ((size_t)s * N + t) * Eext + E));
         shexp_scale[t] = __fdiv_rn(1.0f, 1.0f + expf(-g));
     }
     // softmax over all E experts
@@ -232,6 +288,119 @@ softmax_topk_kernel(const float *__restrict__ part, int nsplit, int N, int E, in
         topk_w[(size_t)t * top_k + lane] = norm ? __fdiv_rn(my_w, psel_sum) : my_w;
 }
 
+// One warp per token.
+template <int EPL>
+__global__ void __launch_bounds__(256)
+softmax_topk_kernel(const float *__restrict__ part, int nsplit, int N, int E, int Eext, int top_k,
+                    int norm, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                    float *__restrict__ shexp_scale, float *__restrict__ logits_out) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= N) return;
+    softmax_topk_token<EPL>(part, nsplit, N, E, Eext, top_k, norm, t, lane, topk_idx, topk_w, shexp_scale,
+                            logits_out);
+}
+
+// Counting sort of a small batch's N*top_k (<= RS_THREADS) routing entries by expert, stable in
+// t, into expStart/expTokI/expTokK -- the CSR the general bucketing kernel writes.  Whole CTA;
+// idx was written by this CTA (visible after the caller's __syncthreads).  An index outside
+// [0, E) raises MOE_DEV_BAD_ROUTING and leaves every segment empty.
+__device__ __forceinline__ void bucket_small(const int32_t *idx, int N, int k, int E, int32_t *expStart,
+                                             int32_t *expTokI, int32_t *expTokK, unsigned *status) {
+    __shared__ int ids[RS_THREADS];
+    __shared__ int st[MAX_E + 1];
+    __shared__ int wsum[RS_THREADS / 32];
+    __shared__ int bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int total = N * k;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    if (tid < total) {
+        const int e = idx[tid];
+        ids[tid] = e;
+        if (e < 0 || e >= E) bad = 1;
+    }
+    __syncthreads();
+    if (bad) {
+        for (int e = tid; e <= E; e += RS_THREADS) expStart[e] = 0;
+        if (tid == 0) atomicOr(status, MOE_DEV_BAD_ROUTING);
+        return;
+    }
+    // per-expert counts over a contiguous range of experts per thread, then a block scan
+    const int per = (E + RS_THREADS - 1) / RS_THREADS;
+    const int e0 = tid * per;
+    int cnt[(MAX_E + RS_THREADS - 1) / RS_THREADS];
+    int mine = 0;
+#pragma unroll
+    for (int i = 0; i < (MAX_E + RS_THREADS - 1) / RS_THREADS; ++i) {
+        cnt[i] = 0;
+        const int e = e0 + i;
+        if (i < per && e < E)
+            for (int j = 0; j < total; ++j) cnt[i] += ids[j] == e;
+        mine += cnt[i];
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = incl - mine;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+#pragma unroll
+    for (int i = 0; i < (MAX_E + RS_THREADS - 1) / RS_THREADS; ++i) {
+        const int e = e0 + i;
+        if (i < per && e < E) {
+            st[e] = before;
+            expStart[e] = before;
+            before += cnt[i];
+        }
+    }
+    if (tid == 0) expStart[E] = total;
+    __syncthreads();
+    // entry j = (t, s): its rank among the earlier entries of the same expert (earlier tokens:
+    // a token picks an expert once)
+    if (tid < total) {
+        const int e = ids[tid];
+        int rank = 0;
+        for (int j = 0; j < tid; ++j) rank += ids[j] == e;
+        const int pos = st[e] + rank;
+        expTokI[pos] = tid / k;
+        expTokK[pos] = tid % k;
+    }
+}
+
+// The whole routing of a small batch in one launch: every CTA computes one expert row's logits
+// (router_small_body); the last CTA to arrive (an arrival counter in the workspace, reset by that
+// CTA) runs softmax + top-k for the N tokens (warp t: token t) and the bucketing.  No CTA waits
+// for another.
+template <int EPL>
+__global__ void __launch_bounds__(RS_THREADS)
+route_small_kernel(const float *__restrict__ hidden, const float *__restrict__ routerW,
+                   const float *__restrict__ shexp_gate, int N, int D, int E, int Eext, int top_k, int norm,
+                   float *__restrict__ logits, int8_t *__restrict__ x_q, float *__restrict__ x_d,
+                   int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, float *__restrict__ shexp_scale,
+                   int32_t *__restrict__ expStart, int32_t *__restrict__ expTokI, int32_t *__restrict__ expTokK,
+                   unsigned *counter, unsigned *status) {
+    __shared__ int is_last;
+    router_small_body(hidden, routerW, shexp_gate, N, D, E, Eext, logits, x_q, x_d);
+    __threadfence();  // this CTA's logits are visible before it is counted
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) *counter = 0;  // every CTA has arrived: ready for the next launch
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < N)
+        softmax_topk_token<EPL>(logits, 1, N, E, Eext, top_k, norm, warp, lane, topk_idx, topk_w, shexp_scale,
+                                nullptr);
+    __syncthreads();
+    bucket_small(topk_idx, N, top_k, E, expStart, expTokI, expTokK, status);
+}
+
 __global__ void quantize_q8_1_kernel(const float *__restrict__ x, int64_t nblk, int8_t *__restrict__ q,
                                      float *__restrict__ d) {
     const int lane = threadIdx.x & 31;
@@ -281,6 +450,14 @@ int launch_router(const float *hidden, const float *routerW, const float *shexp_
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
                   cudaStream_t s) {
     int Eext = E + (shexp_gate ? 1 : 0);
+    if (N <= RS_MAX_N && D % 4 == 0) {
+        router_small_kernel<<<Eext, RS_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, part_logits, x_q,
+                                                        x_d);
+        int rc = launch_status();
+        if (rc) return rc;
+        return launch_softmax(part_logits, 1, N, E, Eext, top_k, norm, topk_idx, topk_w,
+                              shexp_gate ? shexp_scale : nullptr, logits_out, s);
+    }
     int ksplit = D / nsplit;
     dim3 grid((N + RB_M - 1) / RB_M, (Eext + RB_N - 1) / RB_N, nsplit);
     router_logits_kernel<<<grid, R_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, ksplit,
@@ -289,6 +466,28 @@ int launch_router(const float *hidden, const float *routerW, const float *shexp_
     if (rc) return rc;
     return launch_softmax(part_logits, nsplit, N, E, Eext, top_k, norm, topk_idx, topk_w,
                           shexp_gate ? shexp_scale : nullptr, logits_out, s);
+}
+
+int launch_route_small(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
+                       int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
+                       float *x_d, float *part_logits, int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
+                       unsigned *counter, unsigned *status, cudaStream_t s) {
+    if (N > RS_MAX_N || N * top_k > RS_THREADS || D % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int Eext = E + (shexp_gate ? 1 : 0);
+    const int epl = (E + 31) / 32;
+    float *sh = shexp_gate ? shexp_scale : nullptr;
+#define MOE_ROUTE_SMALL(EPLV)                                                                                   \
+    route_small_kernel<EPLV><<<Eext, RS_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, top_k, norm, \
+                                                         part_logits, x_q, x_d, topk_idx, topk_w, sh, expStart,  \
+                                                         expTokI, expTokK, counter, status)
+    if (epl <= 1) MOE_ROUTE_SMALL(1);
+    else if (epl <= 2) MOE_ROUTE_SMALL(2);
+    else if (epl <= 4) MOE_ROUTE_SMALL(4);
+    else if (epl <= 8) MOE_ROUTE_SMALL(8);
+    else if (epl <= 16) MOE_ROUTE_SMALL(16);
+    else MOE_ROUTE_SMALL(32);
+#undef MOE_ROUTE_SMALL
+    return launch_status();
 }
 
 int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,

@@ -56,6 +56,7 @@ _SIGS = {
     "moe_ffn_prefill_timed": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P, _P]),
     "moe_ffn_prefill_host": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_host_memory_addressable": (_I, [_P]),
+    "moe_device_host_numa_node": (_I, [_P]),
     "moe_combine_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill_residual": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
@@ -376,6 +377,13 @@ def _host(t: torch.Tensor, name: str):
     if not t.is_contiguous() or t.dtype != torch.float32:
         raise ValueError(f"{name} must be a contiguous float32 tensor")
     return _P(t.data_ptr())
+
+
+def moe_device_host_numa_node() -> int:
+    """Host NUMA node closest to the current device, or -1 (no NUMA placement reported)."""
+    node = ctypes.c_int(-1)
+    _check(lib().moe_device_host_numa_node(ctypes.byref(node)), "moe_device_host_numa_node")
+    return node.value
 
 
 def moe_host_memory_addressable(t: torch.Tensor) -> bool:

@@ -94,3 +94,5 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert lib.moe_weights_create(ctypes.byref(h), 8, 256, 128, None, None, None, 0, None, None, None, None) == -1
     lib.moe_ffn_prefill.argtypes = [V, V, V, V] + [ctypes.c_int] * 3 + [V, V, ctypes.c_size_t, V]
     assert lib.moe_ffn_prefill(None, None, None, None, 4, 2, 0, None, None, 0, None) == -1
+    lib.moe_device_host_numa_node.argtypes = [V]
+    assert lib.moe_device_host_numa_node(None) == -1

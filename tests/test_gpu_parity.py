@@ -426,6 +426,36 @@ def test_layer_parity(ops, name, path):
     assert clear.mean() > 0.95  # near-tied tokens are few (E=256 has the most)
 
 
+@pytest.mark.parametrize("name", ["decode_n1", "decode_n4", "decode_n8", "tiny"])
+@pytest.mark.parametrize("path", [1, 2])
+def test_layer_routing_state(ops, name, path):
+    """The routing a layer call leaves in its workspace (one fused launch for batches of at most
+    8 tokens on the matvec path, the general router and bucketing otherwise): indices, weights,
+    Q8_1 of x and the CSR equal the oracle's where the routing is decided."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=path)
+    assert layer.status() == 0
+    v = layer.views(wl.N)
+    clear = clear_tokens(ref["logits"], wl.top_k)
+    np.testing.assert_array_equal(v["topk_idx"].cpu().numpy()[clear], ref["topk_idx"][clear])
+    np.testing.assert_allclose(v["topk_w"].cpu().numpy()[clear], ref["topk_w"][clear], rtol=W_RTOL, atol=1e-7)
+    np.testing.assert_array_equal(v["x_q"].cpu().numpy(), ref["x_q"])
+    np.testing.assert_array_equal(v["x_d"].cpu().numpy(), O.halves(ref["x_d16"]))
+    if clear.all():
+        np.testing.assert_array_equal(v["expStart"].cpu().numpy(), ref["expStart"])
+        total = int(ref["expStart"][-1])
+        np.testing.assert_array_equal(v["expTokI"].cpu().numpy()[:total], ref["expTokI"])
+        np.testing.assert_array_equal(v["expTokK"].cpu().numpy()[:total], ref["expTokK"])
+    # a second call on the same workspace (the arrival counter is back at zero) gives the same state
+    idx1 = v["topk_idx"].cpu().numpy().copy()
+    es1 = v["expStart"].cpu().numpy().copy()
+    layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=path)
+    assert layer.status() == 0
+    np.testing.assert_array_equal(v["topk_idx"].cpu().numpy(), idx1)
+    np.testing.assert_array_equal(v["expStart"].cpu().numpy(), es1)
+
+
 def _random_layer(N, D, E, k, F, Fs, norm, seed):
     wl = Workload(f"rand{seed}", N=N, D=D, E=E, top_k=k, F=F, Fs=Fs, norm_topk_prob=norm, seed=seed)
     return wl, make_inputs(wl)
@@ -545,6 +575,15 @@ def test_q3_k_extreme_codes(ops, path):
     out = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=path)
     assert layer.status() == 0
     assert_out_close(out.cpu().numpy(), ref["out"], clear_tokens(ref["logits"], wl.top_k), what="q3_k extreme")
+
+
+def test_device_host_numa_node(ops):
+    """The host node the device reports exists on the host (or -1: no NUMA placement)."""
+    import os
+    node = ops.moe_device_host_numa_node()
+    assert node >= -1
+    if node >= 0 and os.path.isdir("/sys/devices/system/node"):
+        assert os.path.isdir(f"/sys/devices/system/node/node{node}")
 
 
 def test_zero_hidden_gives_zero(ops):
