@@ -156,11 +156,12 @@ void free_tensor_maps(moe_weights_s *w);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Raise a kernel's dynamic shared-memory limit when a launch needs more than the
-// default 48 KB; remembers the largest value set (per kernel, per process), so
-// repeated launches -- and launches under stream capture -- make no further call.
+// Raise a kernel's dynamic shared-memory limit to what a launch needs (the 48 KB that
+// needs no opt-in counts static shared memory too, so every size is set explicitly);
+// remembers the largest value set (per kernel, per process), so repeated launches --
+// and launches under stream capture -- make no further call.
 inline int ensure_dynamic_smem(const void *kernel, size_t bytes, int *configured) {
-    if (bytes <= 48 * 1024 || (int)bytes <= *configured) return MOE_OK;
+    if ((int)bytes <= *configured) return MOE_OK;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
         return MOE_ERR_CUDA;
     *configured = (int)bytes;
