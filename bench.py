@@ -39,6 +39,7 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "olmoe"
 L2_FLUSH_BYTES = 512 << 20
 STAGE_STEPS = 50  # steps of the per-stage breakdown (moe_ffn_prefill_timed)
+SMALL_BATCH = 8  # batches the library routes in one launch on the matvec path
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -415,10 +416,13 @@ def run_ours(args, rank, world, local_rank):
     roofline["peak_source"] = peak_src
     layer_roof_s = max(work["int8_ops"] / (peaks.get("bf16_tflops", 1900.0) * 1e12),
                        work["bytes"] / (peaks.get("hbm_gbs", 6800.0) * 1e9))
+    experts = 2 * (2 if Fs else 1)  # matvec: gate/up and down, routed (and shared)
     if resolved_path == ops.MOE_PATH_TENSOR:
         launches_per_step = 2 + 1 + 3 + 1  # router x2, bucketing(+plan), gather, gate/up, down, combine
+    elif N <= SMALL_BATCH:
+        launches_per_step = 1 + experts + 1  # routing in one launch, the expert matvecs, combine
     else:
-        launches_per_step = 2 + 1 + 2 * (2 if Fs else 1) + 1
+        launches_per_step = 2 + 1 + experts + 1
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
