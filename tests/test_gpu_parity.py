@@ -481,7 +481,7 @@ def test_layer_edge_shapes(ops, N, D, E, k, F, Fs, norm):
         assert_out_close(out.cpu().numpy(), ref["out"], clear, what=f"edge N={N} E={E} k={k}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "qwen3moe_shared"])
+@pytest.mark.parametrize("name", ["tiny", "qwen3moe_shared", "decode_n4"])
 def test_prefill_host_buffers_match_device_buffers(ops, name):
     """The host-buffer entry point reads hidden and writes out in place: same kernels, same bits."""
     wl, inp, ref = case(name)

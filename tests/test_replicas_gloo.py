@@ -82,3 +82,44 @@ def test_clock_summary_window_and_reasons():
     assert c["samples_in_window"] == 0 and c["samples"] == 2
     assert c["sm_mhz"] == 1770.0 and c["reasons"] == ["hw_slowdown"]
     assert bench.clock_summary([], 0.0, 1.0) is None
+
+
+class _FakeOps:
+    """Stands in for the binding's NUMA query (no GPU here)."""
+
+    def __init__(self, node=None, exc=None):
+        self.node, self.exc = node, exc
+
+    def moe_device_host_numa_node(self):
+        if self.exc is not None:
+            raise self.exc
+        return self.node
+
+
+def test_bind_near_gpu_moves_to_the_node_and_reports_the_old_set():
+    """The bench's pinned buffers are allocated from the CPUs of the node the device reports;
+    the previous CPU set is returned for restoring, and a node without CPUs we may use, no NUMA
+    placement, or a failed query leave the affinity alone."""
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    before = os.sched_getaffinity(0)
+    try:
+        nodes = sorted(int(d[4:]) for d in os.listdir("/sys/devices/system/node") if d.startswith("node")
+                       and d[4:].isdigit()) if os.path.isdir("/sys/devices/system/node") else []
+        if nodes:
+            node, prev = bench.bind_near_gpu(_FakeOps(nodes[0]))
+            assert node == nodes[0]
+            now = os.sched_getaffinity(0)
+            assert now <= before and now
+            if prev is not None:
+                assert prev == before
+                os.sched_setaffinity(0, prev)
+        assert bench.bind_near_gpu(_FakeOps(-1)) == (None, None)
+        assert bench.bind_near_gpu(_FakeOps(exc=RuntimeError("no device"))) == (None, None)
+        assert bench.bind_near_gpu(_FakeOps(10 ** 6)) == (None, None)  # no such node directory
+        assert os.sched_getaffinity(0) == before
+    finally:
+        os.sched_setaffinity(0, before)
