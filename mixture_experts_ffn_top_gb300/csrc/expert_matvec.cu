@@ -3,28 +3,28 @@
 // mul_mat_id-style launch that gathers the selected experts' rows instead of
 // per-expert launches; lever 2: Q8_1 activations with int8 dp4a dots).
 //
-// Weight-stationary: a work item is 32 rows of one expert's matrix, whose
-// rows are streamed once per chunk of up to 8 tokens of the expert's CSR
-// segment, so
-// for decode batches (a few tokens per expert) every touched weight byte is
-// read once.  The chunk's arithmetic is specialised on its token count
-// (1, 2, 4 or 8 slots), so a one-token segment costs one token's work.  The
-// grid is persistent (the GPU's resident CTAs) over the items of the experts
-// that received tokens, listed by every CTA from expStart, so an untouched
-// expert costs no CTA.
-// Each warp takes its rows two at a time (gate and up of one feature, or two
-// output columns); lane l owns the 32-wide blocks l, l + 32, ... of both rows
-// and loads all of them (2 x 16 contiguous bytes per block and row) before
-// any arithmetic, so the row pair's bytes are in flight together.  Per block
-// the lane forms the exact int32 dot isum_b (8 dp4a) with each staged token
-// and accumulates (d_w * d_x) * isum_b; the lanes' sums are reduced at the
-// end.  Q4_K weights (repacked to quants 0..15 with per-block scale d*sc and
-// min dmin*m) add the min term: the lane also sums the activation codes
-// (dp4a with ones) and accumulates -(m_w * d_x) * xsum_b.
+// Weight-stationary: a work item is 32 rows of one expert's matrix, streamed
+// once per chunk of up to TMAX tokens of the expert's CSR segment (TMAX from
+// the batch: 1, 2, 4 or 8), so for decode batches (a few tokens per expert)
+// every touched weight byte is read once.  The chunk's arithmetic is
+// specialised on its token count, so a one-token segment costs one token's
+// work.  The grid is persistent (the GPU's resident CTAs) over the items of
+// the experts that received tokens, listed by every CTA from expStart, so an
+// untouched expert costs no CTA.
+// Each warp takes its rows R at a time (R = 4 for chunks of at most 2 tokens,
+// else 2: gate and up of one or two features, or two or four output
+// columns); lane l owns the 32-wide blocks l, l + 32, ... of those rows and
+// loads all of them (2 x 16 contiguous bytes per block and row) before any
+// arithmetic, so their bytes are in flight together.  Per block the lane
+// forms the exact int32 dot isum_b (8 dp4a) with each staged token and
+// accumulates (d_w * d_x) * isum_b; the lanes' sums are reduced at the end.
+// Q4_K weights (repacked to quants 0..15 with per-block scale d*sc and min
+// dmin*m) add the min term: the lane also sums the activation codes (dp4a
+// with ones) and accumulates -(m_w * d_x) * xsum_b.
 //
 // gate/up kernel: rows = features f (gate and up), output h = SiLU(g) * u,
 //   requantised to Q8_1 per 32 features inside the CTA (the CTA owns exactly
-//   one 32-feature block).
+//   one 32-feature block per item).
 // down kernel: rows = output columns c, output partial rows (scattered to
 //   t*top_k + slot) or, for the shared expert, s_t * y to shared_out[t].
 #include "moe_internal.cuh"
