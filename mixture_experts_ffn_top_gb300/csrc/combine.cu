@@ -21,6 +21,8 @@ template <int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
                const float4 *__restrict__ shared, const float4 *residual, int N, int k, int D4, float4 *out) {
+    // launched early behind the down kernel: its partials are complete past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t total = (int64_t)N * D4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -73,7 +75,7 @@ combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
 }  // namespace
 
 int launch_combine(const float *partials, const float *topk_w, const float *shared, const float *residual, int N,
-                   int top_k, int D, float *out, cudaStream_t s) {
+                   int top_k, int D, float *out, cudaStream_t s, bool early) {
     const int D4 = D / 4;
     const int64_t total = (int64_t)N * D4;
     int64_t blocks = (total + 255) / 256;
@@ -85,15 +87,19 @@ int launch_combine(const float *partials, const float *topk_w, const float *shar
     const float4 *r4 = reinterpret_cast<const float4 *>(residual);
     float4 *o4 = reinterpret_cast<float4 *>(out);
     const unsigned g = (unsigned)blocks;
+    auto go = [&](auto kernel) {
+        if (early) return launch_early(kernel, dim3(g), dim3(256), 0, s, p4, topk_w, s4, r4, N, top_k, D4, o4);
+        kernel<<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4);
+        return launch_status();
+    };
     switch (top_k) {
-        case 1: combine_kernel<1><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
-        case 2: combine_kernel<2><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
-        case 4: combine_kernel<4><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
-        case 6: combine_kernel<6><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
-        case 8: combine_kernel<8><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
-        default: combine_kernel<0><<<g, 256, 0, s>>>(p4, topk_w, s4, r4, N, top_k, D4, o4); break;
+        case 1: return go(combine_kernel<1>);
+        case 2: return go(combine_kernel<2>);
+        case 4: return go(combine_kernel<4>);
+        case 6: return go(combine_kernel<6>);
+        case 8: return go(combine_kernel<8>);
+        default: return go(combine_kernel<0>);
     }
-    return launch_status();
 }
 
 }  // namespace moe

@@ -309,6 +309,8 @@ matvec_gate_up_kernel(const int8_t *__restrict__ gq, const float *__restrict__ g
     __shared__ int entries[MV_T];
     __shared__ int act[MAX_E];
     __shared__ int n_act;
+    // the down launch that follows may start now (it waits for this kernel's h_q itself)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     active_experts(is_shared, nexp, expStart, N, top_k, act, &n_act, status);
     const int nfb = F / QK;
     for (int item = blockIdx.x; item < n_act * nfb; item += gridDim.x) {
@@ -410,8 +412,19 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
     __shared__ float oscale[MV_T];
     __shared__ int act[MAX_E];
     __shared__ int n_act;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the CSR comes from a kernel before the gate/up launch; only h_q/h_d are that launch's output
     active_experts(is_shared, nexp, expStart, N, top_k, act, &n_act, status);
     const int ncb = D / QK;
+    if (threadIdx.x == 0 && (int)blockIdx.x < n_act * ncb) {
+        // launched early: start this CTA's first item's rows towards L2 while gate/up finishes
+        const int e = act[blockIdx.x / ncb], cb = blockIdx.x % ncb;
+        const size_t r0 = (size_t)(is_shared ? 0 : e) * D + (size_t)cb * QK, sbytes = (size_t)QK * (F / QK) * 4;
+        l2_prefetch(dq + r0 * F, (size_t)QK * F);
+        l2_prefetch(dd + r0 * (F / QK), sbytes);
+        if (dm != nullptr) l2_prefetch(dm + r0 * (F / QK), sbytes);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int item = blockIdx.x; item < n_act * ncb; item += gridDim.x) {
     const int e = act[item / ncb], cb = item % ncb;
     const Seg sg = segment_of(is_shared, e, expStart, N, top_k);
@@ -509,13 +522,17 @@ int gate_up_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared,
 template <int TMAX>
 int down_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *h_q, const float *h_d,
                 const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
-                const float *shexp_scale, float *out, unsigned *status, cudaStream_t s) {
+                const float *shexp_scale, float *out, unsigned *status, cudaStream_t s, bool early) {
     const size_t smem = (size_t)MV_T * F + sizeof(float) * ((size_t)MV_T * (F / QK) + MV_T * QK);
     static int configured = 0;
     if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel<TMAX>, smem, &configured)) return rc;
     static GridCache gc;
     const int grid = persistent_grid((const void *)matvec_down_kernel<TMAX>, smem, nexp * (D / QK), &gc);
     if (grid < 0) return MOE_ERR_CUDA;
+    if (early)
+        return launch_early(matvec_down_kernel<TMAX>, dim3(grid), dim3(MV_WARPS * 32), smem, s, set.down_q, set.down_d,
+                            set.down_m, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
+                            shexp_scale, out, status);
     matvec_down_kernel<TMAX><<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, nexp,
                                                               is_shared, h_q, h_d, expStart, expTokI, expTokK, N,
                                                               top_k, shexp_scale, out, status);
@@ -549,22 +566,22 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_
 int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_shared, const int8_t *h_q,
                        const float *h_d, const int32_t *expStart, const int32_t *expTokI,
                        const int32_t *expTokK, int N, int top_k, const float *shexp_scale, float *out,
-                       unsigned *status, cudaStream_t s) {
+                       unsigned *status, cudaStream_t s, bool early) {
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
     switch (tmax_for(N)) {
     case 1:
         return down_launch<1>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                              shexp_scale, out, status, s);
+                              shexp_scale, out, status, s, early);
     case 2:
         return down_launch<2>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                              shexp_scale, out, status, s);
+                              shexp_scale, out, status, s, early);
     case 4:
         return down_launch<4>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                              shexp_scale, out, status, s);
+                              shexp_scale, out, status, s, early);
     default:
         return down_launch<MV_T>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                                 shexp_scale, out, status, s);
+                                 shexp_scale, out, status, s, early);
     }
 }
 

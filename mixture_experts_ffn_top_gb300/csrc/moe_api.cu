@@ -466,14 +466,18 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
             rc = launch_matvec_gate_up(w, w->shared, true, xq, xd, nullptr, nullptr, N, top_k, hq + Nk * Fmax,
                                        hd + Nk * (Fmax / QK), nullptr, -1, st, stream);
         mark(4);
+        // without the stage events the down kernels and the combine start early, each behind the
+        // launch before it, and wait on the device for that launch's output
+        const bool early = ev == nullptr;
         if (!rc)
-            rc = launch_matvec_down(w, w->routed, false, hq, hd, es, ti, tk, N, top_k, nullptr, part, st, stream);
+            rc = launch_matvec_down(w, w->routed, false, hq, hd, es, ti, tk, N, top_k, nullptr, part, st, stream,
+                                    early);
         if (!rc && shout)
             rc = launch_matvec_down(w, w->shared, true, hq + Nk * Fmax, hd + Nk * (Fmax / QK), nullptr, nullptr,
-                                    nullptr, N, top_k, sh, shout, st, stream);
+                                    nullptr, N, top_k, sh, shout, st, stream, early);
         mark(5);
     }
-    if (!rc) rc = launch_combine(part, tw, shout, residual, N, top_k, D, out, stream);
+    if (!rc) rc = launch_combine(part, tw, shout, residual, N, top_k, D, out, stream, !tensor && ev == nullptr);
     mark(6);
     return rc;
 }

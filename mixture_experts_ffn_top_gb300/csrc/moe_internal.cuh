@@ -122,13 +122,18 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &ws, bool is_s
                           const int8_t *x_q, const float *x_d, const int32_t *expStart,
                           const int32_t *expTokI, int N, int top_k, int8_t *h_q, float *h_d,
                           int32_t *dbg_dots, int dbg_block, unsigned *status, cudaStream_t s);
+// early: launched to overlap the kernel before it (which must be a matvec gate/up launch of the
+// same call); the CSR must come from a kernel further back.
 int launch_matvec_down(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
                        const int8_t *h_q, const float *h_d, const int32_t *expStart,
                        const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
-                       const float *shexp_scale, float *out, unsigned *status, cudaStream_t s);
+                       const float *shexp_scale, float *out, unsigned *status, cudaStream_t s,
+                       bool early = false);
 // combine.cu
+// early: launched to overlap the kernel before it (see launch_early); topk_w must come from a
+// kernel further back.
 int launch_combine(const float *partials, const float *topk_w, const float *shared, const float *residual, int N,
-                   int top_k, int D, float *out, cudaStream_t s);
+                   int top_k, int D, float *out, cudaStream_t s, bool early = false);
 // weights.cu
 int repack_weights(moe_weights_s *w, const void *gate, const void *up, const void *down,
                    const void *sh_gate, const void *sh_up, const void *sh_down, cudaStream_t s);
@@ -168,6 +173,27 @@ inline int ensure_dynamic_smem(const void *kernel, size_t bytes, int *configured
     return MOE_OK;
 }
 inline int launch_status() { return cuda_status(cudaGetLastError()); }
+
+// Launches `kernel` so that it may start while the previous kernel on the stream is still
+// running (programmatic dependent launch: it is scheduled once every CTA of that kernel has
+// executed griddepcontrol.launch_dependents or exited).  The kernel must execute
+// griddepcontrol.wait before it reads anything that kernel writes; without this launch
+// attribute that wait returns at once.
+template <typename... KArgs, typename... Args>
+inline int launch_early(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
+}
 
 // ----------------------------------------------------- device helpers --
 __device__ __forceinline__ float warp_max(float v) {
