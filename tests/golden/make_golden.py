@@ -1,10 +1,12 @@
-"""Writes tests/golden/tiny_layer.json from the CPU oracle (and nothing else).
+"""Writes tests/golden/tiny_layer.json, tiny_q4k_layer.json and tiny_q3k_layer.json from the CPU
+oracle (and nothing else).
 
-The pages print no worked numeric example for this layer, so this fixture is a
-regression record of the pinned oracle on the seeded tiny workload (N=64,
-D=256, E=8, top_k=2, F=128, norm_topk_prob off, seed 0): it detects any later
-change of the oracle's results and any difference between the x86 and Arm
-builds.  Run: python tests/golden/make_golden.py
+The pages print no worked numeric example for this layer, so these fixtures are
+regression records of the pinned oracle on the seeded tiny workloads (N=64,
+D=256, E=8, top_k=2, norm_topk_prob off, seed 0; F=128 with Q8_0 expert
+weights, F=256 with Q4_K and with Q3_K): they detect any later change of the
+oracle's results and any difference between the x86 and Arm builds.
+Run: python tests/golden/make_golden.py
 """
 import json
 import os
@@ -19,8 +21,11 @@ import oracle  # noqa: E402
 from mixture_experts_ffn_top_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
 
 
-def main():
-    wl = WORKLOADS["tiny"]
+FIXTURES = {"tiny": "tiny_layer.json", "tiny_q4k": "tiny_q4k_layer.json", "tiny_q3k": "tiny_q3k_layer.json"}
+
+
+def write(name):
+    wl = WORKLOADS[name]
     r = oracle.moe_ffn_inputs(make_inputs(wl), wl.top_k, wl.norm_topk_prob)
     fx = {
         "workload": wl.describe(),
@@ -36,8 +41,13 @@ def main():
         "out_sum": float(r["out"].astype(np.float64).sum()),
         "out_l2": float(np.linalg.norm(r["out"].astype(np.float64))),
     }
-    with open(os.path.join(HERE, "tiny_layer.json"), "w") as f:
+    with open(os.path.join(HERE, FIXTURES[name]), "w") as f:
         f.write("{\n" + ",\n".join(f" {json.dumps(k)}: {json.dumps(v)}" for k, v in fx.items()) + "\n}\n")
+
+
+def main():
+    for name in FIXTURES:
+        write(name)
 
 
 if __name__ == "__main__":

@@ -67,8 +67,7 @@ MUTATIONS = [
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(tmp_path, name, old, new):
+def _scratch_copy(tmp_path):
     dst = tmp_path / "repo"
     (dst / "tests").mkdir(parents=True)
     shutil.copytree(os.path.join(ROOT, "oracle"), dst / "oracle", ignore=shutil.ignore_patterns("_build", "__pycache__"))
@@ -77,12 +76,31 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
     shutil.copy(os.path.join(ROOT, "mixture_experts_ffn_top_gb300", "workloads.py"), pkg / "workloads.py")
     for f in ("conftest.py", "test_oracle_pins.py"):
         shutil.copy(os.path.join(ROOT, "tests", f), dst / "tests" / f)
+    return dst
+
+
+def _run_pins(dst):
+    # the regression fixtures record this oracle's own results: they are left out, so a planted
+    # mistake counts as caught only when an independent pin fails
+    return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                           "-k", "not recorded_fixture", "tests/test_oracle_pins.py"], cwd=dst, capture_output=True,
+                          text=True, timeout=300)
+
+
+def test_unmodified_copy_passes_every_pin(tmp_path):
+    """Control: the scratch copy without a planted mistake passes, so a failure below is the mistake's."""
+    r = _run_pins(_scratch_copy(tmp_path))
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    dst = _scratch_copy(tmp_path)
     src = dst / "oracle" / "moe_oracle.c"
     text = src.read_text()
     assert old in text, f"mutation site for {name} not found"
     if name == "combine_shared_first":  # shared added first, and not again at the end
         text = text.replace("            if (S)\n                acc = acc + S[t * D + c];\n", "")
     src.write_text(text.replace(old, new, 1))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py"], cwd=dst, capture_output=True, text=True, timeout=300)
+    r = _run_pins(dst)
     assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -706,17 +706,20 @@ def test_combine_residual_added_after_the_shared_row():
 
 
 # ---------------------------------------------------- regression fixture ---
-def test_tiny_layer_matches_recorded_fixture():
-    """tests/golden/tiny_layer.json (written by tests/golden/make_golden.py from this oracle):
+@pytest.mark.parametrize("name,fixture", [("tiny", "tiny_layer.json"), ("tiny_q4k", "tiny_q4k_layer.json"),
+                                          ("tiny_q3k", "tiny_q3k_layer.json")])
+def test_tiny_layer_matches_recorded_fixture(name, fixture):
+    """tests/golden/<fixture> (written by tests/golden/make_golden.py from this oracle):
     routing, CSR and quant codes exactly; floats to 1e-6 relative."""
     import json
     import os
 
     from mixture_experts_ffn_top_gb300.workloads import WORKLOADS, make_inputs
 
-    with open(os.path.join(os.path.dirname(__file__), "golden", "tiny_layer.json")) as f:
+    with open(os.path.join(os.path.dirname(__file__), "golden", fixture)) as f:
         fx = json.load(f)
-    wl = WORKLOADS["tiny"]
+    wl = WORKLOADS[name]
+    assert fx["workload"] == wl.describe()
     r = O.moe_ffn_inputs(make_inputs(wl), wl.top_k, wl.norm_topk_prob)
     assert r["topk_idx"].tolist() == fx["topk_idx"]
     assert r["expStart"].tolist() == fx["expStart"]
