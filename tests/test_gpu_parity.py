@@ -586,6 +586,26 @@ def test_device_host_numa_node(ops):
         assert os.path.isdir(f"/sys/devices/system/node/node{node}")
 
 
+@pytest.mark.parametrize("wfmt", ["q4_k", "q3_k"])
+@pytest.mark.parametrize("N", [1, 3, 8])
+def test_kquant_decode_batches(ops, wfmt, N):
+    """K-quant weights at decode batch sizes (the matvec kernels' narrow-chunk variants, the
+    one-launch routing, the shared expert's single chunk): layer output and CSR against the oracle."""
+    wl = Workload(f"{wfmt}_dec{N}", N=N, D=512, E=16, top_k=4, F=256, Fs=256, norm_topk_prob=True, seed=70 + N,
+                  wfmt=wfmt)
+    inp = make_inputs(wl)
+    ref = O.moe_ffn_inputs(inp, wl.top_k, wl.norm_topk_prob)
+    layer = layer_for(ops, inp, wl)
+    clear = clear_tokens(ref["logits"], wl.top_k)
+    for path in (0, 1):
+        out = layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=path)
+        assert layer.status() == 0
+        assert_out_close(out.cpu().numpy(), ref["out"], clear, what=f"{wfmt} N={N} path {path}")
+        if clear.all():
+            v = layer.views(wl.N)
+            np.testing.assert_array_equal(v["expStart"].cpu().numpy(), ref["expStart"])
+
+
 def test_zero_hidden_gives_zero(ops):
     wl, inp = _random_layer(16, 256, 8, 2, 128, 64, False, seed=5)
     inp["hidden"][:] = 0.0
