@@ -195,9 +195,12 @@ int moe_router_topk(const float *hidden, const float *routerW, const float *shex
  * arguments and results as moe_router_topk, without the workspace: the router's
  * split-K partial logits go to a 16 MiB array inside the library (2^22 floats,
  * held on every GPU that loads the library until exit).  The problem must fit:
- * nsplit * N * (E + 1) <= 2^22 floats, nsplit being the router's split-K factor
- * (at most max(1, D/128)); otherwise MOE_ERR_WORKSPACE_TOO_SMALL and nothing
- * runs.  The first call on a device looks the array's device address up
+ * nsplit * N * (E + 1) <= 2^22 floats, nsplit being the router's split-K factor:
+ * 1 when N <= 8 and D % 4 == 0; otherwise, with tiles = ceil(N/64)*ceil(E/64)
+ * and SMs the current device's multiprocessor count, the largest s that
+ * divides D/32 with s <= min(ceil(4*SMs/tiles), D/depth), depth = 32 when
+ * tiles <= 4 and 128 otherwise (so at most min(4*SMs, D/32)).  A problem that
+ * does not fit returns MOE_ERR_WORKSPACE_TOO_SMALL and nothing runs.  The first call on a device looks the array's device address up
  * (cudaGetSymbolAddress, which may load the library's kernels onto that device)
  * and should therefore come before any stream capture.  All calls on a device
  * share the array, so calls that may overlap on the GPU race and must be
@@ -289,6 +292,33 @@ int moe_debug_gate_up_block_dots(moe_weights_t w, const int8_t *x_q, const float
                                  const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
                                  int block, int32_t *dots, int path, void *ws, size_t ws_bytes,
                                  cudaStream_t stream);
+
+/* Raw int32 block dot products of the down GEMM for one 32-block `block` of
+ * its reduction dimension (the intermediate size F), given requantised
+ * activations h_q [N*top_k][F] int8 and h_d [N*top_k][F/32] fp32 in segment
+ * order (as moe_expert_gate_up writes them): dots [N*top_k][D] int32, entry j
+ * in segment order, [j][c] = isum(W_d[e][c], h_j) over block `block`, as
+ * computed inside the selected path's kernel (stored weight codes, as for
+ * moe_debug_gate_up_block_dots).  expTokK is needed because the tensor path's
+ * plan (and its partial rows, written to the workspace) uses it.  Same errors
+ * as moe_expert_down; block outside [0, F/32) is MOE_ERR_UNSUPPORTED_SHAPE. */
+int moe_debug_down_block_dots(moe_weights_t w, const int8_t *h_q, const float *h_d,
+                              const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
+                              int N, int top_k, int block, int32_t *dots, int path, void *ws,
+                              size_t ws_bytes, cudaStream_t stream);
+
+/* Failure-detection check of the bucketing kernel's grid barrier: runs
+ * moe_bucket with the barrier waiting for one more arrival than there are
+ * CTAs, so it can never complete, and a wait limit of limit_ms (1..2000)
+ * instead of the normal 1 s.  Every CTA gives up after the limit, sets
+ * MOE_DEV_TIMEOUT in the workspace status word and returns without writing
+ * the CSR; the context stays usable.  The barrier's words are left mid-count:
+ * call moe_workspace_init before the workspace serves another call.  Needs a
+ * batch large enough for more than one token range (otherwise there is no
+ * barrier): MOE_ERR_UNSUPPORTED_SHAPE.  Same arguments as moe_bucket. */
+int moe_debug_bucket_barrier_timeout(const int32_t *topk_idx, int N, int top_k, int E,
+                                     int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
+                                     int limit_ms, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Failure-detection check of the tensor path: runs the gate/up grouped GEMM with
  * its TMA producer told to issue nothing, so the MMA's first wait can never be

@@ -24,6 +24,7 @@ namespace {
 constexpr int B_THREADS = 1024;
 constexpr int B_MIN_RANGE = 128;  // tokens per CTA at least
 constexpr unsigned long long B_BARRIER_NS = 1000000000ull;  // 1 s: a healthy barrier takes microseconds
+constexpr unsigned long long B_BARRIER_NS_MIN = 1000000ull;  // the shortest limit a caller may ask for (1 ms)
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
@@ -44,7 +45,8 @@ __device__ __forceinline__ unsigned long long gtimer() {
 // the workspace's status block, zero after moe_workspace_init and back to zero after every
 // completed barrier).  The wait is bounded; on expiry the CTA raises MOE_DEV_TIMEOUT and
 // reports failure (every CTA then returns without writing results).
-__device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned nblocks, unsigned *status) {
+__device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned nblocks, unsigned *status,
+                             unsigned long long limit_ns) {
     __shared__ int ok_s;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -58,7 +60,7 @@ __device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned nblocks, u
         } else {
             const unsigned long long t0 = gtimer();
             while (*reinterpret_cast<volatile unsigned *>(gen) == g0) {
-                if (gtimer() - t0 > B_BARRIER_NS) {
+                if (gtimer() - t0 > limit_ns) {
                     atomicOr(status, MOE_DEV_TIMEOUT);
                     ok_s = 0;
                     break;
@@ -72,7 +74,7 @@ __device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned nblocks, u
 }
 
 // Optional plan of the tensor path, derived from the CSR: padded segment starts
-// (16-row aligned), token tiles of <= TILE_N rows (routed experts first, then the
+// (16-row aligned), token tiles of <= tile_n rows (routed experts first, then the
 // shared expert's N rows) and, for every padded row, its source token, output row
 // and CSR entry.
 struct PlanOut {
@@ -81,6 +83,7 @@ struct PlanOut {
     TileDesc *tiles;
     int4 *rowinfo;
     int with_shared, rows_max, tiles_max;
+    int tile_n;  // token rows per tile
 };
 
 struct BucketArgs {
@@ -92,6 +95,8 @@ struct BucketArgs {
     int *bad_g;   // [G] per-range "bad routing" flags
     int range;    // tokens per CTA (multiple of 32)
     int chunk;    // tokens staged at a time (256, 512 or 1024)
+    unsigned long long barrier_ns;  // limit of the grid barrier's wait
+    int extra_arrivals;  // failure-detection check: arrivals the barrier waits for beyond the grid (0 normally)
 };
 
 __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a, const PlanOut po) {
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     if (G > 1) {
         for (int e = tid; e < E; e += B_THREADS) a.cnt_g[(size_t)b * E + e] = base[e];
         if (tid == 0) a.bad_g[b] = (int)*flag;
-        if (!grid_barrier(a.bar_count, a.bar_gen, (unsigned)G, a.status)) return;
+        if (!grid_barrier(a.bar_count, a.bar_gen, (unsigned)(G + a.extra_arrivals), a.status, a.barrier_ns)) return;
         for (int i = tid; i < G; i += B_THREADS) bad |= __ldcg(a.bad_g + i);
     } else {
         __syncthreads();
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     }
     // per expert: total over all ranges and the entries of the ranges before this one;
     // then exclusive scans over experts (one per thread, E <= 1024): segment starts and,
-    // for the plan, 16-row padded starts and TILE_N-row tile starts
+    // for the plan, 16-row padded starts and tile_n-row tile starts
     {
         int c = 0, before = 0;
         if (tid < E) {
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
         }
         __syncthreads();  // every count read before base[] is rewritten below
         const int pc = (c + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
-        const int tc = (c + TILE_N - 1) / TILE_N;
+        const int tc = (c + po.tile_n - 1) / po.tile_n;
         const int i0 = warp_incl_scan(c, lane), i1 = warp_incl_scan(pc, lane), i2 = warp_incl_scan(tc, lane);
         __shared__ int wt[3][32];
         if (lane == 31) {
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
             tst[E] = t;
             const int ns = po.with_shared ? N : 0;
             gst[E + 1] = g + (ns + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
-            tst[E + 1] = t + (ns + TILE_N - 1) / TILE_N;
+            tst[E + 1] = t + (ns + po.tile_n - 1) / po.tile_n;
         }
         __syncthreads();
     }
@@ -285,14 +290,14 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
         const int n = st0[e + 1] - st0[e];
         for (int r = gst[e] + n + lane; r < gst[e + 1] && r < po.rows_max; r += 32)
             po.rowinfo[r] = make_int4(-1, -1, -1, 0);
-        for (int i = lane; i * TILE_N < n; i += 32) {
+        for (int i = lane; i * po.tile_n < n; i += 32) {
             const int ti = tst[e] + i;
             if (ti >= po.tiles_max) break;
             TileDesc td;
-            td.row0 = gst[e] + i * TILE_N;
-            td.nrows = min(TILE_N, n - i * TILE_N);
+            td.row0 = gst[e] + i * po.tile_n;
+            td.nrows = min(po.tile_n, n - i * po.tile_n);
             td.expert = e;
-            td.entry0 = st0[e] + i * TILE_N;
+            td.entry0 = st0[e] + i * po.tile_n;
             po.tiles[ti] = td;
         }
     }
@@ -301,14 +306,14 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
         const int rend = (b == G - 1) ? gst[E + 1] - g : r1;  // the last range also takes the pad rows
         for (int i = r0 + tid; i < rend; i += B_THREADS)
             if (g + i < po.rows_max) po.rowinfo[g + i] = i < N ? make_int4(i, i, -1, 0) : make_int4(-1, -1, -1, 0);
-        for (int i = b + G * tid; i * TILE_N < N; i += G * B_THREADS) {
+        for (int i = b + G * tid; i * po.tile_n < N; i += G * B_THREADS) {
             const int ti = tst[E] + i;
             if (ti >= po.tiles_max) continue;
             TileDesc td;
-            td.row0 = g + i * TILE_N;
-            td.nrows = min(TILE_N, N - i * TILE_N);
+            td.row0 = g + i * po.tile_n;
+            td.nrows = min(po.tile_n, N - i * po.tile_n);
             td.expert = E;
-            td.entry0 = i * TILE_N;
+            td.entry0 = i * po.tile_n;
             po.tiles[ti] = td;
         }
     }
@@ -325,15 +330,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
 // Ranges: at least B_MIN_RANGE tokens per CTA, at most one CTA per SM, and a count table
 // of at most BUCKET_TABLE_MAX ints.
 int bucket_grid(int N, int E, int *range_out) {
-    static int num_sms = 0;
-    if (num_sms == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-            num_sms = n;
-        else
-            num_sms = 1;
-    }
+    const int num_sms = std::max(1, device_sm_count());
     const int gmax = std::min(num_sms, std::max(1, BUCKET_TABLE_MAX / std::max(E, 1)));
     int range = std::max(B_MIN_RANGE, (N + gmax - 1) / gmax);
     range = (range + 31) / 32 * 32;
@@ -347,7 +344,11 @@ size_t bucket_scratch_bytes(int N, int E) {
 }
 
 int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart, int32_t *expTokI,
-                  int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L, bool with_shared) {
+                  int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L, bool with_shared, int tile_rows,
+                  unsigned long long barrier_ns, int extra_arrivals) {
+    if (tile_rows < SEG_ALIGN || tile_rows % SEG_ALIGN) return MOE_ERR_INVALID_ARG;
+    if (barrier_ns == 0) barrier_ns = B_BARRIER_NS;
+    if (barrier_ns < B_BARRIER_NS_MIN || extra_arrivals < 0) return MOE_ERR_INVALID_ARG;
     int range = 0;
     const int G = bucket_grid(N, E, &range);
     // the largest token chunk (<= the range) whose bitmaps and staged ids fit in shared memory
@@ -359,7 +360,7 @@ int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *exp
     int chunk = 1024;
     while (chunk > 128 && (smem_for(chunk) > 200 * 1024 || chunk / 2 >= range)) chunk /= 2;
     const size_t smem = smem_for(chunk);
-    static int configured = 0;
+    static SmemOptIn configured;
     if (int rc = ensure_dynamic_smem((const void *)bucket_kernel, smem, &configured)) return rc;
     uint8_t *wb = static_cast<uint8_t *>(ws);
     BucketArgs a{};
@@ -377,7 +378,11 @@ int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *exp
     a.bad_g = a.cnt_g + (size_t)G * E;
     a.range = range;
     a.chunk = chunk;
+    a.barrier_ns = barrier_ns;
+    a.extra_arrivals = extra_arrivals;
+    if (extra_arrivals > 0 && G == 1) return MOE_ERR_UNSUPPORTED_SHAPE;  // no grid barrier to hold up
     PlanOut po{};
+    po.tile_n = tile_rows;
     if (L != nullptr) {
         po.hdr = ws_ptr<PlanHeader>(ws, L->plan);
         po.gstart = reinterpret_cast<int32_t *>(po.hdr + 1);

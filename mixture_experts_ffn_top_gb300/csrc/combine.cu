@@ -9,6 +9,8 @@
 // HBM-bound: each thread owns 4 consecutive columns (16-byte loads/stores); for the
 // usual top_k the slot loads are all issued before the fma chain; partial rows are
 // streamed once (evict-first loads), the output is written once.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -79,7 +81,7 @@ int launch_combine(const float *partials, const float *topk_w, const float *shar
     const int D4 = D / 4;
     const int64_t total = (int64_t)N * D4;
     int64_t blocks = (total + 255) / 256;
-    const int64_t cap = 152 * 8;  // 8 resident CTAs of 256 threads per SM
+    const int64_t cap = (int64_t)std::max(1, device_sm_count()) * 8;  // 8 resident CTAs of 256 threads per SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const float4 *p4 = reinterpret_cast<const float4 *>(partials);

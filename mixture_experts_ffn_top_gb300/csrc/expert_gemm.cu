@@ -22,8 +22,9 @@
 //               rows) into the 5-slot tile ring, both tiles' block scales into
 //               the 8-slot scale ring, one mbarrier per stage.
 //   warp 1      TMEM owner and MMA issuer: 2 x (M128 x N x K16) per block into
-//               one of 5 TMEM accumulators of 96 columns; a tile-ring slot is
-//               released by the commit of the MMAs that read it.  It starts a
+//               one of 5 TMEM accumulators of 96 columns; one commit per stage
+//               both releases the tile-ring slot and tells the drain the stage's
+//               accumulators are complete.  It starts a
 //               stage when the orchestrator's stage count (a shared word it
 //               polls) says so.
 //   warps 2-13  drain, 3 per SM sub-partition: warp w reads TMEM lanes
@@ -52,10 +53,15 @@
 #include <mutex>
 
 #include "moe_internal.cuh"
+#include "tc_glue.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 
 namespace {
+
+using namespace tc;
+using namespace gemm;
 
 constexpr int G_DRAIN_WARPS = 12;                 // 3 per SM sub-partition (128 registers each)
 constexpr int G_ORCH_WARP = 2 + G_DRAIN_WARPS;    // warp that tells the MMA warp when a stage may go
@@ -89,203 +95,11 @@ static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle a
 // used by stage L - G_SSTAGES, so G_SSTAGES >= G_STAGES + 3 keeps it unread by then.
 static_assert(G_SSTAGES >= G_STAGES + 3, "scale slots could be overwritten while still read");
 static_assert(G_TMEM_BUFS == 5, "the argument above assumes stage t's blocks reuse the slots of blocks 2t-5, 2t-4");
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s: any healthy wait is microseconds
-
-struct GemmMaps {
-    CUtensorMap a_r, sa_r, a_s, sa_s;  // weights + weight scales, routed / shared
-    CUtensorMap b[4], sb[4];           // tokens + token scales, box heights 16/32/64/96
-    CUtensorMap sm_r, sm_s;            // Q4_K: weight mins, routed / shared
-    CUtensorMap sx[4];                 // Q4_K: token code sums times scale, box heights as sb
-};
-
-struct GemmParams {
-    int K_r, K_s;      // reduction length of routed / shared tiles
-    int MT_r, MT_s;    // 128-row weight tiles per token tile, routed / shared
-    int rows_r, rows_s;  // weight rows per expert in the A tensor map (2F or D), routed / shared
-    int sblk_r, sblk_s;  // scale rows per expert in the SA map (K/32)
-    int E, D, F, Fs, Fmax, top_k, N, rows_max, tiles_max;
-    const PlanHeader *plan;
-    const TileDesc *tiles;
-    const int4 *rowinfo;
-    __half *h16;       // gate/up output (fp16 integer codes), row stride Fmax
-    float *h_dT;       // [Fmax/32][rows_max]
-    float *h_sT;       // Q4_K: [Fmax/32][rows_max] code sum of each h block times its scale
-    float *partials;
-    float *shared_out;
-    const float *shexp_scale;
-    int32_t *dbg_dots;
-    int dbg_block;
-    unsigned *status;
-    unsigned long long wait_ns;  // limit of every mbarrier wait
-    int starve;                  // failure-detection check: the producer issues no copy
-};
-
-// ------------------------------------------------------------- PTX glue ---
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase with the given parity.  Returns false (and raises
-// the CTA's abort flag and the device status bit) when the limit expires, or
-// as soon as another role of the CTA has aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned *status, unsigned long long limit_ns) {
-    if (mbar_try(bar, parity)) return true;
-    uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 63) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort_flag = 1;
-                atomicOr(status, MOE_DEV_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_shared(const int *p) {
-    int v;
-    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_shared(int *p, int v) {
-    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void st_evict_last(float *dst, float4 v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
-                 "f"(v.z), "f"(v.w), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
-// layout TMA writes (rows of 128 B, 8-row atoms of 1024 B).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
-    d |= (uint64_t)1 << 16;                          // leading byte offset (unused for this layout)
-    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8-row atom
-    d |= (uint64_t)1 << 46;                          // descriptor version (tcgen05)
-    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
-    return d;
-}
-// Instruction descriptor: D fp32, A and B fp16, both K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_f16(int n) {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// ------------------------------------------------------------ schedule ---
-struct Item {
-    int tile, mt, shared, K, nrows, row0, expert, entry0, nb, bi;
-};
-__device__ __forceinline__ int total_items(const GemmParams &p, int n_tiles, int n_rtiles) {
-    return n_rtiles * p.MT_r + (n_tiles - n_rtiles) * p.MT_s;
-}
-__device__ __forceinline__ Item item_at(const GemmParams &p, int it, int n_rtiles) {
-    Item x;
-    if (it < n_rtiles * p.MT_r) {
-        x.tile = it / p.MT_r;
-        x.mt = it - x.tile * p.MT_r;
-        x.shared = 0;
-        x.K = p.K_r;
-    } else {
-        int i2 = it - n_rtiles * p.MT_r;
-        x.tile = n_rtiles + i2 / p.MT_s;
-        x.mt = i2 % p.MT_s;
-        x.shared = 1;
-        x.K = p.K_s;
-    }
-    const TileDesc td = p.tiles[x.tile];
-    x.nrows = td.nrows;
-    x.row0 = td.row0;
-    x.expert = td.expert;
-    x.entry0 = td.entry0;
-    x.bi = x.nrows <= 16 ? 0 : x.nrows <= 32 ? 1 : x.nrows <= 64 ? 2 : 3;
-    x.nb = x.bi < 3 ? (16 << x.bi) : TILE_N;
-    return x;
-}
-
 // --------------------------------------------------------------- kernel ---
-// One warp reads 32 TMEM lanes x 32 consecutive fp32 columns.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr)
-        : "memory");
-}
-// Ties the registers a tcgen05.ld wrote to the tcgen05.wait::ld before it, so no use of
-// them can be scheduled above the wait.
-__device__ __forceinline__ void tmem_reg_fence32(uint32_t (&v)[32]) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 8)
-        asm volatile("" : "+r"(v[i]), "+r"(v[i + 1]), "+r"(v[i + 2]), "+r"(v[i + 3]), "+r"(v[i + 4]), "+r"(v[i + 5]),
-                     "+r"(v[i + 6]), "+r"(v[i + 7]));
-}
-// SiLU(g) * u with the fast exponential and division (the result is requantised to 8 bits)
-__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // MODE 0: gate/up (fused SiLU * up, Q8_1 requant); 1: down (scatter).
-// DUMP (gate/up only): also store the raw int32 block dots of block p.dbg_block
-// (the debug entry point; a separate instantiation keeps the hot loop lean).
+// DUMP: also store the raw int32 block dots of block p.dbg_block (the debug entry points; a
+// separate instantiation keeps the hot loop lean).
 // WF: weight format (0 Q8_0, 1 Q4_K: the weight is d*sc*q - dmin*m per 32-block, so each block
 // also subtracts (dmin*m) * (d_x * sum of the block's activation codes)).
 template <int MODE, bool DUMP, int WF>
@@ -310,7 +124,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
         return b;
     };
     const uint32_t full0 = next_bar(G_STAGES), empty0 = next_bar(G_STAGES);
-    const uint32_t tfull0 = next_bar(G_TMEM_BUFS), tempty0 = next_bar(G_TMEM_BUFS);
+    const uint32_t tempty0 = next_bar(G_TMEM_BUFS);
     const uint32_t hfull = next_bar(1), hempty = next_bar(1);
     const uint32_t done_bar = next_bar(1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * nb_);
@@ -321,12 +135,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);   // the copies' arrival (tiles and scales)
-            mbar_init(empty0 + 8 * s, 1);  // released by the MMA commit
+            mbar_init(empty0 + 8 * s, 1);  // the stage's MMAs are complete (one commit per stage)
         }
-        for (int b = 0; b < G_TMEM_BUFS; ++b) {
-            mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, G_DRAIN_WARPS);
-        }
+        for (int b = 0; b < G_TMEM_BUFS; ++b) mbar_init(tempty0 + 8 * b, G_DRAIN_WARPS);
         mbar_init(hfull, G_DRAIN_WARPS);  // every drain warp has stored its columns
         mbar_init(hempty, 1);             // the epilogue warp is done with the buffer
         mbar_init(done_bar, 1);
@@ -447,11 +258,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                             const uint32_t off = half * 64 + kk * 32;  // bytes along K inside the swizzle atom
                             mma_f16(d, smem_desc_sw128(a0 + off), smem_desc_sw128(b0 + off), idesc, kk);
                         }
-                        mma_commit(tfull0 + 8 * buf);
                         any = true;
                         if (++buf == G_TMEM_BUFS) buf = 0;
                     }
-                    mma_commit(empty0 + 8 * stage);  // the tile slot is free once these MMAs are done
+                    // one commit per stage: it tells the drain that both blocks' accumulators are
+                    // complete and the producer that the tile slot is free (a thread's commits are
+                    // retired at most about one per 330 cycles, so a commit per block would bound
+                    // the whole kernel)
+                    mma_commit(empty0 + 8 * stage);
                     if (++stage == G_STAGES) stage = 0;
                 }
             }
@@ -599,8 +413,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
         const int q = warp & 3;              // TMEM lane quarter (= SM sub-partition) of this warp
         const int grp = (warp - 2) >> 2;     // column group: token columns 32*grp + [0, 32)
         const int r = q * 32 + lane;         // row of the 128-row weight tile
-        int sstage = 0, buf = 0;
-        uint32_t tphase = 0, hphase = 0;
+        int sstage = 0, buf = 0, dstage = 0;
+        uint32_t tphase = 0, hphase = 0, dphase = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item x = item_at(p, it, n_rtiles);
@@ -611,10 +425,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) acc[m] = make_float2(0.0f, 0.0f);
             const uint32_t tlane = tmem_base + ((uint32_t)(q * 32) << 16) + c0;
-            // Per stage (two K blocks in two TMEM slots): one wait for the second slot's commit
-            // (it covers both blocks, and the MMA warp only issued them once the stage's tiles and
-            // scales had landed), both TMEM loads, then the slots go back before the math, which
-            // interleaves the two blocks.
+            // Per stage (two K blocks in two TMEM slots): one wait for the stage's commit (it covers
+            // both blocks, and the MMA warp only issued them once the stage's tiles and scales had
+            // landed), both TMEM loads, then the slots go back before the math, which interleaves
+            // the two blocks.  The drain never falls two phases behind a stage barrier: the MMAs of
+            // stage t + G_STAGES need TMEM slots it hands back only after stage t + 2.
             const int nst = x.K / 64;
             uint32_t v0[32], v1[32];
             for (int ks = 0; ks < nst && ok; ++ks) {
@@ -622,7 +437,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                 int s1 = buf + 1;
                 uint32_t ph1 = tphase;
                 if (s1 == G_TMEM_BUFS) s1 = 0, ph1 ^= 1;
-                ok = mbar_wait(tfull0 + 8 * s1, ph1, abort_flag, p.status, p.wait_ns);
+                ok = mbar_wait(empty0 + 8 * dstage, dphase, abort_flag, p.status, p.wait_ns);
+                if (++dstage == G_STAGES) dstage = 0, dphase ^= 1;
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -648,11 +464,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
                     const float *SA = reinterpret_cast<const float *>(sring + sstage * SSB);
                     const float *SB = SA + 256;
                     if (DUMP && x.shared == 0 && (2 * ks == p.dbg_block || 2 * ks + 1 == p.dbg_block)) {
-                        const int mat = r < 64 ? 0 : 1;
-                        const int f = x.mt * 64 + (r & 63);
                         const uint32_t *v = (2 * ks == p.dbg_block) ? v0 : v1;
-                        for (int j = 0; j < 32 && c0 + j < x.nrows; ++j)
-                            p.dbg_dots[((size_t)(x.entry0 + c0 + j) * 2 + mat) * p.F + f] = (int32_t)__uint_as_float(v[j]);
+                        for (int j = 0; j < 32 && c0 + j < x.nrows; ++j) {
+                            const size_t e = (size_t)(x.entry0 + c0 + j);
+                            if (MODE == 0)
+                                p.dbg_dots[(e * 2 + (r < 64 ? 0 : 1)) * p.F + x.mt * 64 + (r & 63)] =
+                                    (int32_t)__uint_as_float(v[j]);
+                            else
+                                p.dbg_dots[e * p.D + x.mt * 128 + r] = (int32_t)__uint_as_float(v[j]);
+                        }
                     }
                     const float dwa = SA[r], dwb = SA[128 + r];
                     const float2 dw2a = make_float2(dwa, dwa), dw2b = make_float2(dwb, dwb);
@@ -725,13 +545,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
 }
 
 // ------------------------------------------------ planning and gathering ---
-// One CTA: padded segment starts (16-row aligned), token tiles of <= TILE_N rows
+// One CTA: padded segment starts (16-row aligned), token tiles of <= tile_n rows
 // per segment (routed experts first, then the shared expert's N rows), and for
 // every padded row its source token, output row and CSR entry.
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI,
             const int32_t *__restrict__ expTokK, int N, int top_k, int E, int with_shared, int rows_max,
-            int tiles_max, PlanHeader *hdr, int32_t *gstart_out, TileDesc *tiles, int4 *rowinfo, unsigned *status) {
+            int tiles_max, int tile_n, PlanHeader *hdr, int32_t *gstart_out, TileDesc *tiles, int4 *rowinfo,
+            unsigned *status) {
     __shared__ int cnt[MAX_E + 1], gst[MAX_E + 2], tst[MAX_E + 2];
     __shared__ int bad;
     const int tid = threadIdx.x;
@@ -761,13 +582,13 @@ plan_kernel(const int32_t *__restrict__ expStart, const int32_t *__restrict__ ex
             gst[e] = g;
             tst[e] = t;
             g += (cnt[e] + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
-            t += (cnt[e] + TILE_N - 1) / TILE_N;
+            t += (cnt[e] + tile_n - 1) / tile_n;
         }
         gst[E] = g;
         tst[E] = t;
         const int ns = with_shared ? N : 0;
         gst[E + 1] = g + (ns + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;
-        tst[E + 1] = t + (ns + TILE_N - 1) / TILE_N;
+        tst[E + 1] = t + (ns + tile_n - 1) / tile_n;
         hdr->n_tiles = min(tst[E + 1], tiles_max);
         hdr->n_rows = min(gst[E + 1], rows_max);
         hdr->shared_row0 = with_shared ? g : -1;
@@ -780,14 +601,14 @@ plan_kernel(const int32_t *__restrict__ expStart, const int32_t *__restrict__ ex
         const bool sh = (e == E);
         if (sh && !with_shared) continue;
         const int n = sh ? N : cnt[e];
-        for (int i = 0; i * TILE_N < n; ++i) {
+        for (int i = 0; i * tile_n < n; ++i) {
             const int ti = tst[e] + i;
             if (ti >= tiles_max) break;
             TileDesc td;
-            td.row0 = gst[e] + i * TILE_N;
-            td.nrows = min(TILE_N, n - i * TILE_N);
+            td.row0 = gst[e] + i * tile_n;
+            td.nrows = min(tile_n, n - i * tile_n);
             td.expert = e;
-            td.entry0 = (sh ? 0 : expStart[e]) + i * TILE_N;
+            td.entry0 = (sh ? 0 : expStart[e]) + i * tile_n;
             tiles[ti] = td;
         }
     }
@@ -985,7 +806,7 @@ struct WeightMaps {
 // One instantiation per (mode, dump, weight format), each with its own dynamic shared memory size.
 template <int MODE, bool DUMP, int WF>
 int run_gemm(const GemmMaps &maps, const GemmParams &p, int num_sms, cudaStream_t s) {
-    static int configured = 0;
+    static SmemOptIn configured;
     if (int rc = ensure_dynamic_smem((const void *)grouped_gemm_kernel<MODE, DUMP, WF>, g_smem(WF), &configured))
         return rc;
     grouped_gemm_kernel<MODE, DUMP, WF><<<num_sms, G_THREADS, g_smem(WF), s>>>(maps, p);
@@ -1043,7 +864,7 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     void *bsum = mode == 0 ? (void *)ws_ptr<float>(ws, L.xg_sT) : (void *)ws_ptr<float>(ws, L.h_sT);
     const int kcols = mode == 0 ? D : Fmax;
     for (int i = 0; i < 4; ++i) {
-        const uint32_t nb = i < 3 ? (16u << i) : (uint32_t)TILE_N;
+        const uint32_t nb = i < 3 ? (16u << i) : (uint32_t)TILE_N;  // box heights 16/32/64/96
         if (!encode_2d(&maps.b[i], bdata, true, rows, kcols, 64, nb)) return MOE_ERR_CUDA;
         if (!encode_2d(&maps.sb[i], bscale, false, kcols / QK, rows, nb, 2)) return MOE_ERR_CUDA;
         if (wf && !encode_2d(&maps.sx[i], bsum, false, kcols / QK, rows, nb, 2)) return MOE_ERR_CUDA;
@@ -1072,18 +893,14 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
     p.wait_ns = wait_ns;
     p.starve = starve;
     (void)with_shared;
-    static int num_sms = 0;
-    if (num_sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
-    const bool dump = mode == 0 && dbg_dots != nullptr;
+    const bool dump = dbg_dots != nullptr;
+    const int num_sms = device_sm_count();
+    if (num_sms <= 0) return MOE_ERR_CUDA;
     if (mode == 0)
         return dump ? (wf ? run_gemm<0, true, 1>(maps, p, num_sms, s) : run_gemm<0, true, 0>(maps, p, num_sms, s))
                     : (wf ? run_gemm<0, false, 1>(maps, p, num_sms, s) : run_gemm<0, false, 0>(maps, p, num_sms, s));
-    return wf ? run_gemm<1, false, 1>(maps, p, num_sms, s) : run_gemm<1, false, 0>(maps, p, num_sms, s);
+    return dump ? (wf ? run_gemm<1, true, 1>(maps, p, num_sms, s) : run_gemm<1, true, 0>(maps, p, num_sms, s))
+                : (wf ? run_gemm<1, false, 1>(maps, p, num_sms, s) : run_gemm<1, false, 0>(maps, p, num_sms, s));
 }
 
 }  // namespace
@@ -1131,7 +948,7 @@ int launch_plan_and_gather(const moe_weights_s *w, const int8_t *x_q, const floa
     int rc = MOE_OK;
     if (!plan_ready) {
         plan_kernel<<<1, 1024, 0, s>>>(expStart, expTokI, expTokK, N, top_k, w->E, with_shared ? 1 : 0, L.rows_max,
-                                       L.tiles_max, hdr, gst, ws_ptr<TileDesc>(ws, L.tiles),
+                                       L.tiles_max, plan_tile_rows(w), hdr, gst, ws_ptr<TileDesc>(ws, L.tiles),
                                        ws_ptr<int4>(ws, L.rowinfo), reinterpret_cast<unsigned *>(ws));
         rc = launch_status();
     }
@@ -1153,8 +970,10 @@ int launch_gemm_gate_up_starved(const moe_weights_s *w, int N, int top_k, void *
 }
 
 int launch_gemm_down(const moe_weights_s *w, int N, int top_k, bool with_shared, const float *shexp_scale,
-                     float *partials, float *shared_out, void *ws, const WsLayout &L, cudaStream_t s) {
-    return launch_gemm(1, w, N, top_k, with_shared, ws, L, partials, shared_out, shexp_scale, nullptr, -1, s);
+                     float *partials, float *shared_out, void *ws, const WsLayout &L, cudaStream_t s,
+                     int32_t *dbg_dots, int dbg_block) {
+    return launch_gemm(1, w, N, top_k, with_shared, ws, L, partials, shared_out, shexp_scale, dbg_dots, dbg_block,
+                       s);
 }
 
 int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L, int8_t *h_q, float *h_d,

@@ -353,13 +353,15 @@ struct DownArgs {
     size_t mat_off;
     bool is_shared;
     float *out;
+    int32_t *dbg_dots;  // [entries][D] int32 dots of block dbg_block (the debug entry point), or NULL
+    int dbg_block;
 };
 
 // One chunk of T token slots of the down kernel: every warp's 4 output columns (R per rows_dot
 // call), then the stores of the 32-column block per token.
 template <int T, int R>
-__device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int *orows, const float *oscale,
-                                           const int8_t *hs, const float *hds, float *ys) {
+__device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int *hrows, const int *orows,
+                                           const float *oscale, const int8_t *hs, const float *hds, float *ys) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int F = a.F;
     for (int r = 0; r < MV_ROWS_PER_WARP; r += R) {
@@ -374,8 +376,15 @@ __device__ __forceinline__ void down_chunk(const DownArgs &a, int cb, const int 
             mr[i] = a.dm ? a.dm + c * (F / QK) : nullptr;
         }
         float y[R][T];
-        int unused[R][T];
-        rows_dot<T, R>(wr, dr, mr, a.dm != nullptr, F, hs, hds, lane, y, -1, unused);
+        int dbg[R][T];
+        rows_dot<T, R>(wr, dr, mr, a.dm != nullptr, F, hs, hds, lane, y, a.dbg_dots ? a.dbg_block : -1, dbg);
+        if (a.dbg_dots != nullptr && !a.is_shared && lane == (a.dbg_block & 31)) {
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+#pragma unroll
+                for (int tt = 0; tt < T; ++tt)
+                    if (hrows[tt] >= 0) a.dbg_dots[(size_t)hrows[tt] * a.D + cb * QK + cl0 + i] = dbg[i][tt];
+        }
         if (lane == 0) {
 #pragma unroll
             for (int i = 0; i < R; ++i)
@@ -402,7 +411,8 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
                    bool is_shared, const int8_t *__restrict__ h_q, const float *__restrict__ h_d,
                    const int32_t *__restrict__ expStart, const int32_t *__restrict__ expTokI,
                    const int32_t *__restrict__ expTokK, int N, int top_k,
-                   const float *__restrict__ shexp_scale, float *__restrict__ out, unsigned *status) {
+                   const float *__restrict__ shexp_scale, float *__restrict__ out, unsigned *status,
+                   int32_t *__restrict__ dbg_dots, int dbg_block) {
     extern __shared__ __align__(16) unsigned char smem[];
     int8_t *hs = reinterpret_cast<int8_t *>(smem);                      // [MV_T][F]
     float *hds = reinterpret_cast<float *>(smem + (size_t)MV_T * F);   // [MV_T][F/32]
@@ -428,7 +438,7 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
     for (int item = blockIdx.x; item < n_act * ncb; item += gridDim.x) {
     const int e = act[item / ncb], cb = item % ncb;
     const Seg sg = segment_of(is_shared, e, expStart, N, top_k);
-    DownArgs a{dq, dd, dm, D, F, (size_t)(is_shared ? 0 : e) * D, is_shared, out};
+    DownArgs a{dq, dd, dm, D, F, (size_t)(is_shared ? 0 : e) * D, is_shared, out, dbg_dots, dbg_block};
     if (threadIdx.x == 0) {
         const size_t r0 = a.mat_off + (size_t)cb * QK, sbytes = (size_t)QK * (F / QK) * 4;
         l2_prefetch(dq + r0 * F, (size_t)QK * F);
@@ -465,10 +475,10 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
         stage_rows(h_q, h_d, F, hrows, T, hs, hds);
         __syncthreads();
         constexpr int R = RowsPerCall<TMAX>::value;
-        if (T == 1) down_chunk<1, R>(a, cb, orows, oscale, hs, hds, ys);
-        else if (TMAX >= 2 && T == 2) down_chunk<(TMAX >= 2 ? 2 : 1), R>(a, cb, orows, oscale, hs, hds, ys);
-        else if (TMAX >= 4 && T == 4) down_chunk<(TMAX >= 4 ? 4 : 1), R>(a, cb, orows, oscale, hs, hds, ys);
-        else if (TMAX >= 8) down_chunk<(TMAX >= 8 ? 8 : 1), R>(a, cb, orows, oscale, hs, hds, ys);
+        if (T == 1) down_chunk<1, R>(a, cb, hrows, orows, oscale, hs, hds, ys);
+        else if (TMAX >= 2 && T == 2) down_chunk<(TMAX >= 2 ? 2 : 1), R>(a, cb, hrows, orows, oscale, hs, hds, ys);
+        else if (TMAX >= 4 && T == 4) down_chunk<(TMAX >= 4 ? 4 : 1), R>(a, cb, hrows, orows, oscale, hs, hds, ys);
+        else if (TMAX >= 8) down_chunk<(TMAX >= 8 ? 8 : 1), R>(a, cb, hrows, orows, oscale, hs, hds, ys);
     }
     __syncthreads();  // the item's last chunk fully consumed before the next item stages
     }
@@ -477,21 +487,25 @@ matvec_down_kernel(const int8_t *__restrict__ dq, const float *__restrict__ dd, 
 // Persistent grid: the resident CTAs of the whole GPU, at most one per work item.  The
 // occupancy query is remembered for the last dynamic shared-memory size seen (per kernel).
 struct GridCache {
-    size_t smem = ~(size_t)0;
-    int resident = 0;
+    size_t smem[MAX_DEVICES];
+    int resident[MAX_DEVICES] = {};
+    GridCache() {
+        for (auto &v : smem) v = ~(size_t)0;
+    }
 };
 int persistent_grid(const void *kernel, size_t smem, int max_items, GridCache *cache) {
-    if (cache->smem != smem) {
-        int dev = 0, n = 0, per_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0 ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, MV_WARPS * 32, smem) != cudaSuccess ||
+    const int dev = current_device();
+    if (dev < 0) return -1;
+    if (cache->smem[dev] != smem) {
+        const int n = device_sm_count();
+        int per_sm = 0;
+        if (n <= 0 || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, MV_WARPS * 32, smem) != cudaSuccess ||
             per_sm <= 0)
             return -1;
-        cache->resident = n * per_sm;
-        cache->smem = smem;
+        cache->resident[dev] = n * per_sm;
+        cache->smem[dev] = smem;
     }
-    return std::max(1, std::min(cache->resident, max_items));
+    return std::max(1, std::min(cache->resident[dev], max_items));
 }
 
 }  // namespace
@@ -507,7 +521,7 @@ int gate_up_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared,
                    const int32_t *expStart, const int32_t *expTokI, int N, int top_k, int8_t *h_q, float *h_d,
                    int32_t *dbg_dots, int dbg_block, unsigned *status, cudaStream_t s) {
     const size_t smem = (size_t)MV_T * D + sizeof(float) * ((size_t)MV_T * (D / QK) + MV_T * QK);
-    static int configured = 0;
+    static SmemOptIn configured;
     if (int rc = ensure_dynamic_smem((const void *)matvec_gate_up_kernel<TMAX>, smem, &configured)) return rc;
     static GridCache gc;
     const int grid = persistent_grid((const void *)matvec_gate_up_kernel<TMAX>, smem, nexp * (F / QK), &gc);
@@ -522,9 +536,10 @@ int gate_up_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared,
 template <int TMAX>
 int down_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *h_q, const float *h_d,
                 const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
-                const float *shexp_scale, float *out, unsigned *status, cudaStream_t s, bool early) {
+                const float *shexp_scale, float *out, unsigned *status, cudaStream_t s, bool early,
+                int32_t *dbg_dots, int dbg_block) {
     const size_t smem = (size_t)MV_T * F + sizeof(float) * ((size_t)MV_T * (F / QK) + MV_T * QK);
-    static int configured = 0;
+    static SmemOptIn configured;
     if (int rc = ensure_dynamic_smem((const void *)matvec_down_kernel<TMAX>, smem, &configured)) return rc;
     static GridCache gc;
     const int grid = persistent_grid((const void *)matvec_down_kernel<TMAX>, smem, nexp * (D / QK), &gc);
@@ -532,10 +547,10 @@ int down_launch(const WeightSet &set, int D, int F, int nexp, bool is_shared, co
     if (early)
         return launch_early(matvec_down_kernel<TMAX>, dim3(grid), dim3(MV_WARPS * 32), smem, s, set.down_q, set.down_d,
                             set.down_m, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                            shexp_scale, out, status);
+                            shexp_scale, out, status, dbg_dots, dbg_block);
     matvec_down_kernel<TMAX><<<grid, MV_WARPS * 32, smem, s>>>(set.down_q, set.down_d, set.down_m, D, F, nexp,
                                                               is_shared, h_q, h_d, expStart, expTokI, expTokK, N,
-                                                              top_k, shexp_scale, out, status);
+                                                              top_k, shexp_scale, out, status, dbg_dots, dbg_block);
     return launch_status();
 }
 
@@ -566,22 +581,22 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_
 int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_shared, const int8_t *h_q,
                        const float *h_d, const int32_t *expStart, const int32_t *expTokI,
                        const int32_t *expTokK, int N, int top_k, const float *shexp_scale, float *out,
-                       unsigned *status, cudaStream_t s, bool early) {
+                       unsigned *status, cudaStream_t s, bool early, int32_t *dbg_dots, int dbg_block) {
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
     switch (tmax_for(N)) {
     case 1:
         return down_launch<1>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                              shexp_scale, out, status, s, early);
+                              shexp_scale, out, status, s, early, dbg_dots, dbg_block);
     case 2:
         return down_launch<2>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                              shexp_scale, out, status, s, early);
+                              shexp_scale, out, status, s, early, dbg_dots, dbg_block);
     case 4:
         return down_launch<4>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                              shexp_scale, out, status, s, early);
+                              shexp_scale, out, status, s, early, dbg_dots, dbg_block);
     default:
         return down_launch<MV_T>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
-                                 shexp_scale, out, status, s, early);
+                                 shexp_scale, out, status, s, early, dbg_dots, dbg_block);
     }
 }
 

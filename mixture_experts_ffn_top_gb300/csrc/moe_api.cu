@@ -3,6 +3,7 @@
 // hot path allocates or synchronises; only moe_ffn_prefill_host's kernels touch
 // host memory (the caller's hidden and output rows, in place).
 #include <algorithm>
+#include <atomic>
 #include <new>
 
 #include "moe_internal.cuh"
@@ -11,9 +12,18 @@ using namespace moe;
 
 namespace moe {
 
-int router_nsplit(int N, int D, int E);
-
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int device_sm_count() {
+    static std::atomic<int> cached[MAX_DEVICES];
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 static bool tensor_shapes(int D, int F, int Fs) {
     return D % TILE_M == 0 && F % 64 == 0 && (Fs == 0 || Fs % 64 == 0);
@@ -66,16 +76,16 @@ WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs) {
     return L;
 }
 
-}  // namespace moe
-
-namespace {
-
 bool shape_ok(int N, int D, int E, int top_k) {
     if (N < 1 || D < QK || D % QK != 0 || E < 1 || E > MAX_E || top_k < 1 || top_k > E || top_k > 32)
         return false;
     if ((int64_t)N * top_k > (int64_t)0x7fffffff / 2) return false;
     return true;
 }
+
+}  // namespace moe
+
+namespace {
 
 int check_ws(const void *ws, size_t ws_bytes, const WsLayout &L) {
     if (ws == nullptr) return MOE_ERR_INVALID_ARG;
@@ -286,6 +296,18 @@ int moe_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expSta
     return launch_bucket(topk_idx, N, top_k, E, expStart, expTokI, expTokK, ws, stream);
 }
 
+int moe_debug_bucket_barrier_timeout(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart,
+                                     int32_t *expTokI, int32_t *expTokK, int limit_ms, void *ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+    if (!topk_idx || !expStart || !expTokI || !expTokK || !ws || limit_ms < 1 || limit_ms > 2000)
+        return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(N, QK, E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_bucket_workspace_size(N, top_k, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return launch_bucket(topk_idx, N, top_k, E, expStart, expTokI, expTokK, ws, stream, nullptr, false, TILE_N,
+                         (unsigned long long)limit_ms * 1000000ull, 1);
+}
+
 int moe_grouped_ffn_ex(moe_weights_t w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
                        const int32_t *expTokI, const int32_t *expTokK, int N, int top_k, const float *shexp_scale,
                        float *partials, float *shared_out, int path, void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -369,6 +391,27 @@ int moe_debug_gate_up_block_dots(moe_weights_t w, const int8_t *x_q, const float
                                  stream);
 }
 
+int moe_debug_down_block_dots(moe_weights_t w, const int8_t *h_q, const float *h_d, const int32_t *expStart,
+                              const int32_t *expTokI, const int32_t *expTokK, int N, int top_k, int block,
+                              int32_t *dots, int path, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!w || !h_q || !h_d || !expStart || !expTokI || !expTokK || !dots) return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(N, w->D, w->E, top_k) || block < 0 || block >= w->F / QK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const WsLayout L = ws_layout(N, w->D, w->E, w->F, top_k, w->Fs);
+    int rc = check_ws(ws, ws_bytes, L);
+    if (rc) return rc;
+    int p = pick_path(w, N, top_k, path);
+    if (p < 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    float *part = ws_ptr<float>(ws, L.partials);
+    if (p == MOE_PATH_TENSOR) {
+        rc = launch_plan_and_gather(w, nullptr, nullptr, expStart, expTokI, expTokK, N, top_k, false, ws, L, stream);
+        if (!rc) rc = launch_q8_to_h16(w, N, top_k, ws, L, h_q, h_d, stream);
+        if (!rc) rc = launch_gemm_down(w, N, top_k, false, nullptr, part, nullptr, ws, L, stream, dots, block);
+        return rc;
+    }
+    return launch_matvec_down(w, w->routed, false, h_q, h_d, expStart, expTokI, expTokK, N, top_k, nullptr, part,
+                              status_word(ws), stream, false, dots, block);
+}
+
 int moe_debug_expert_wait_timeout(moe_weights_t w, const int8_t *x_q, const float *x_d, const int32_t *expStart,
                                   const int32_t *expTokI, int N, int top_k, int limit_ms, void *ws, size_t ws_bytes,
                                   cudaStream_t stream) {
@@ -442,7 +485,8 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
                            xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream);
         mark(1);
         if (!rc)
-            rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr);
+            rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr,
+                               plan_tile_rows(w));
         mark(2);
     }
     if (tensor) {

@@ -72,6 +72,13 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(int N, int D, int E, int F, int top_k, int Fs);
+// The shape rules every entry point applies to (N, D, E, top_k) (moe_api.cu).
+bool shape_ok(int N, int D, int E, int top_k);
+// router.cu: the split-K factor of the router for a batch (workspace layout), and the split its
+// launch actually uses (1 for batches of at most 8 tokens with D % 4 == 0, which the one-pass
+// small-batch kernel routes); its partial-logit table holds split * N * (E + 1) floats.
+int router_nsplit(int N, int D, int E);
+int router_split_used(int N, int D, int E);
 
 template <typename T>
 inline T *ws_ptr(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
@@ -87,6 +94,10 @@ struct PlanHeader {
 struct TileDesc {
     int row0, nrows, expert, entry0;
 };
+
+// Token rows per tile in the tensor path's plan for these weights (the plan is written by the
+// bucketing kernel or plan_kernel and read by the grouped GEMM).
+inline int plan_tile_rows(const moe_weights_s *) { return TILE_N; }
 
 // ----------------------------------------------------------- launchers --
 // router.cu
@@ -116,7 +127,8 @@ constexpr int BUCKET_TABLE_MAX = 65536;  // ints in the ranges x experts count t
 int bucket_grid(int N, int E, int *range_out);
 size_t bucket_scratch_bytes(int N, int E);
 int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart, int32_t *expTokI,
-                  int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L = nullptr, bool with_shared = false);
+                  int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L = nullptr, bool with_shared = false,
+                  int tile_rows = TILE_N, unsigned long long barrier_ns = 0, int extra_arrivals = 0);
 // expert_matvec.cu
 int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
                           const int8_t *x_q, const float *x_d, const int32_t *expStart,
@@ -128,7 +140,7 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &ws, bool is_shar
                        const int8_t *h_q, const float *h_d, const int32_t *expStart,
                        const int32_t *expTokI, const int32_t *expTokK, int N, int top_k,
                        const float *shexp_scale, float *out, unsigned *status, cudaStream_t s,
-                       bool early = false);
+                       bool early = false, int32_t *dbg_dots = nullptr, int dbg_block = -1);
 // combine.cu
 // early: launched to overlap the kernel before it (see launch_early); topk_w must come from a
 // kernel further back.
@@ -151,25 +163,43 @@ int launch_gemm_gate_up_starved(const moe_weights_s *w, int N, int top_k, void *
                                 unsigned long long wait_ns, cudaStream_t s);
 int launch_gemm_down(const moe_weights_s *w, int N, int top_k, bool with_shared,
                      const float *shexp_scale, float *partials, float *shared_out, void *ws,
-                     const WsLayout &L, cudaStream_t s);
+                     const WsLayout &L, cudaStream_t s, int32_t *dbg_dots = nullptr, int dbg_block = -1);
 int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
                      int8_t *h_q, float *h_d, cudaStream_t s);
 int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
                      const int8_t *h_q, const float *h_d, cudaStream_t s);
 int prepare_tensor_maps(moe_weights_s *w);
+
 void free_tensor_maps(moe_weights_s *w);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Raise a kernel's dynamic shared-memory limit to what a launch needs (the 48 KB that
-// needs no opt-in counts static shared memory too, so every size is set explicitly);
-// remembers the largest value set (per kernel, per process), so repeated launches --
-// and launches under stream capture -- make no further call.
-inline int ensure_dynamic_smem(const void *kernel, size_t bytes, int *configured) {
-    if ((int)bytes <= *configured) return MOE_OK;
+constexpr int MAX_DEVICES = 64;  // device ordinals the per-device caches below cover
+
+// The current device's ordinal, or -1 when none can be queried.
+inline int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return -1;
+    return dev;
+}
+// The current device's multiprocessor count, queried once per device; 0 when there is no device.
+int device_sm_count();
+
+// Per-device record of the largest dynamic shared-memory size a kernel was opted into.
+struct SmemOptIn {
+    int bytes[MAX_DEVICES] = {};
+};
+// Raise a kernel's dynamic shared-memory limit to what a launch needs on the current device (the
+// 48 KB that needs no opt-in counts static shared memory too, so every size is set explicitly);
+// the attribute is per device, so the largest value set is remembered per kernel and device, and
+// repeated launches -- also launches under stream capture -- make no further call.
+inline int ensure_dynamic_smem(const void *kernel, size_t bytes, SmemOptIn *done) {
+    const int dev = current_device();
+    if (dev < 0) return MOE_ERR_CUDA;
+    if ((int)bytes <= done->bytes[dev]) return MOE_OK;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
         return MOE_ERR_CUDA;
-    *configured = (int)bytes;
+    done->bytes[dev] = (int)bytes;
     return MOE_OK;
 }
 inline int launch_status() { return cuda_status(cudaGetLastError()); }

@@ -435,15 +435,20 @@ int launch_softmax(const float *part, int nsplit, int N, int E, int Eext, int to
 
 int router_nsplit(int N, int D, int E) {
     // about four 8-warp CTAs per SM; each split at least 128 deep, or one K chunk (32) when
-    // the tiles are few (decode batches: one chunk per CTA, all of routerW read in one round)
+    // the tiles are few (decode batches: one chunk per CTA, all of routerW read in one round).
+    // The split sets the size of the workspace's partial-logit table, so a size query must run
+    // with the same device current as the calls (without a device it assumes one SM).
     int tiles = ((N + RB_M - 1) / RB_M) * ((E + RB_N - 1) / RB_N);
-    int want = (4 * 152 + tiles - 1) / tiles;
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    int want = (4 * sms + tiles - 1) / tiles;
     int depth = tiles <= 4 ? RB_K : 128;
     int maxs = D / depth > 0 ? D / depth : 1;
     int s = want < 1 ? 1 : (want > maxs ? maxs : want);
     while (s > 1 && (D / QK) % s != 0) --s;  // equal splits on block boundaries
     return s;
 }
+
+int router_split_used(int N, int D, int E) { return (N <= RS_MAX_N && D % 4 == 0) ? 1 : router_nsplit(N, D, E); }
 
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,

@@ -19,8 +19,6 @@
 
 namespace moe {
 
-int router_nsplit(int N, int D, int E);
-
 namespace {
 
 constexpr size_t kNoAllocScratchFloats = size_t(1) << 22;  // 16 MiB
@@ -60,10 +58,11 @@ extern "C" int moe_router_topk_noalloc(const float *hidden, const float *routerW
     using namespace moe;
     if (!hidden || !routerW || !topk_idx || !topk_w || !x_q || !x_d) return MOE_ERR_INVALID_ARG;
     if ((shexp_gate == nullptr) != (shexp_scale == nullptr)) return MOE_ERR_INVALID_ARG;
-    if (N < 1 || D < QK || D % QK != 0 || E < 1 || E > MAX_E || top_k < 1 || top_k > E || top_k > 32)
-        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!shape_ok(N, D, E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    // the split the router's launch uses decides how much of the array it writes
+    if ((size_t)router_split_used(N, D, E) * (size_t)N * (size_t)(E + 1) > kNoAllocScratchFloats)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
     const int nsplit = router_nsplit(N, D, E);
-    if ((size_t)nsplit * (size_t)N * (size_t)(E + 1) > kNoAllocScratchFloats) return MOE_ERR_WORKSPACE_TOO_SMALL;
     float *scratch = nullptr;
     int rc = scratch_for_current_device(&scratch);
     if (rc) return rc;

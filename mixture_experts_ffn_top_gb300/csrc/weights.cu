@@ -13,6 +13,8 @@
 //     (rows 0-63 gate f0..f0+63, rows 64-127 up f0..f0+63) so one MMA tile
 //     yields gate and up of the same 64 features; scales transposed to
 //     [K/32][rows] so a TMA box of 128 rows x 2 blocks is one copy.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 #include <vector>
@@ -173,7 +175,8 @@ int repack(int wfmt, const void *src, int nmat, int rows, int K, int8_t *q, floa
     int64_t total = (int64_t)nmat * rows * (K / QK);
     if (total == 0) return MOE_OK;
     int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    const int64_t cap = (int64_t)std::max(1, device_sm_count()) * 16;
+    if (blocks > cap) blocks = cap;
     if (wfmt == MOE_WFMT_Q4_K)
         repack_q4k_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
                                                            mn, h16, dT, mT, interleave, up_half);

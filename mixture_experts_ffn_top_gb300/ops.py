@@ -49,6 +49,8 @@ _SIGS = {
     "moe_expert_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_debug_gate_up_block_dots": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
+    "moe_debug_down_block_dots": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
+    "moe_debug_bucket_barrier_timeout": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_debug_expert_wait_timeout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -216,12 +218,14 @@ def moe_router_topk(hidden, routerW, shexp_gate, top_k, norm_topk_prob, ws, want
     return r
 
 
-def moe_router_topk_noalloc(hidden, routerW, shexp_gate, top_k, norm_topk_prob, want_logits=False, stream=None):
-    """moe_router_topk without a workspace (the library's fixed scratch); outputs as moe_router_topk."""
+def moe_router_topk_noalloc(hidden, routerW, shexp_gate, top_k, norm_topk_prob, want_logits=False, stream=None,
+                            outputs=None):
+    """moe_router_topk without a workspace (the library's fixed scratch); outputs as moe_router_topk
+    (written into `outputs`, a dict of those tensors, when given)."""
     N, D = hidden.shape
     E = routerW.shape[0]
     dev = hidden.device
-    r = dict(topk_idx=torch.empty((N, top_k), dtype=torch.int32, device=dev),
+    r = outputs if outputs is not None else dict(topk_idx=torch.empty((N, top_k), dtype=torch.int32, device=dev),
              topk_w=torch.empty((N, top_k), dtype=torch.float32, device=dev),
              shexp_scale=torch.empty(N, dtype=torch.float32, device=dev) if shexp_gate is not None else None,
              x_q=torch.empty((N, D), dtype=torch.int8, device=dev),
@@ -262,6 +266,20 @@ def moe_bucket(topk_idx, E, ws, stream=None):
     tk = torch.empty(N * k, dtype=torch.int32, device=dev)
     _check(lib().moe_bucket(_dev(topk_idx, torch.int32, "topk_idx"), N, k, E, _dev(es), _dev(ti), _dev(tk),
                             _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "moe_bucket")
+    return es, ti, tk
+
+
+def moe_debug_bucket_barrier_timeout(topk_idx, E, limit_ms, ws, stream=None):
+    """moe_bucket with a grid barrier that cannot complete (bounded by limit_ms); the outcome is
+    read with moe_workspace_status."""
+    N, k = topk_idx.shape
+    dev = topk_idx.device
+    es = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+    ti = torch.full((N * k,), -7, dtype=torch.int32, device=dev)
+    tk = torch.full((N * k,), -7, dtype=torch.int32, device=dev)
+    _check(lib().moe_debug_bucket_barrier_timeout(_dev(topk_idx, torch.int32, "topk_idx"), N, k, E, _dev(es),
+                                                  _dev(ti), _dev(tk), int(limit_ms), _dev(ws, torch.uint8, "ws"),
+                                                  ws.numel(), _stream(stream)), "moe_debug_bucket_barrier_timeout")
     return es, ti, tk
 
 
@@ -309,6 +327,19 @@ def moe_debug_gate_up_block_dots(w: MoeWeights, x_q, x_d, expStart, expTokI, top
                                             _dev(expStart, torch.int32), _dev(expTokI, torch.int32), N, top_k, block,
                                             _dev(dots), path, _dev(ws, torch.uint8), ws.numel(), _stream(stream))
     _check(rc, "moe_debug_gate_up_block_dots")
+    return dots
+
+
+def moe_debug_down_block_dots(w: MoeWeights, h_q, h_d, expStart, expTokI, expTokK, N, top_k, block, ws,
+                              path=MOE_PATH_AUTO, stream=None):
+    """int32 dots of the down GEMM's block `block` for every CSR entry and output column:
+    [N * top_k, D] (entries beyond expStart[E] stay zero)."""
+    dots = torch.zeros((N * top_k, w.D), dtype=torch.int32, device=h_q.device)
+    rc = lib().moe_debug_down_block_dots(w.handle, _dev(h_q, torch.int8), _dev(h_d, torch.float32),
+                                         _dev(expStart, torch.int32), _dev(expTokI, torch.int32),
+                                         _dev(expTokK, torch.int32), N, top_k, block, _dev(dots), path,
+                                         _dev(ws, torch.uint8), ws.numel(), _stream(stream))
+    _check(rc, "moe_debug_down_block_dots")
     return dots
 
 

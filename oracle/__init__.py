@@ -27,6 +27,7 @@ _lock = threading.Lock()
 _lib = None
 
 QK = 32
+Q8_0_BYTES = 34  # fp16 scale + 32 int8 quants
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _I = ctypes.c_int
@@ -150,6 +151,24 @@ def block_dots(w_row: np.ndarray, aq: np.ndarray) -> np.ndarray:
     nblk = aq.size // QK
     out = np.empty(nblk, np.int32)
     _L().oracle_block_dots(_p(w_row), _p(aq), _I(nblk), _p(out))
+    return out
+
+
+def block_dots_csr(W: np.ndarray, act: np.ndarray, expStart: np.ndarray, sel: np.ndarray | None,
+                   block: int) -> np.ndarray:
+    """int32 dots of one 32-wide block for every CSR entry and every weight row of its expert
+    (Q8_0 weights W [E][rows][K/32 blocks of 34 bytes]): out[j, r].  The activation row of entry
+    j is act[sel[j]] (token rows of x_q, sel = expTokI) or act[j] (h_q in entry order)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    act = np.ascontiguousarray(act, dtype=np.int8)
+    expStart = np.ascontiguousarray(expStart, dtype=np.int32)
+    E, rows = W.shape[0], W.shape[1]
+    K = act.shape[1]
+    assert W.shape[2] == K // QK * Q8_0_BYTES and 0 <= block < K // QK
+    n = int(expStart[E])
+    out = np.empty((n, rows), np.int32)
+    s = None if sel is None else np.ascontiguousarray(sel, dtype=np.int32)
+    _L().oracle_block_dots_csr(_p(W), _I(E), _I(rows), _I(K), _p(act), _p(expStart), _p(s), _I(block), _p(out))
     return out
 
 

@@ -289,6 +289,31 @@ void oracle_block_dots(const uint8_t *w_row, const int8_t *aq, int nblk, int32_t
         out[b] = block_isum((const int8_t *)(w_row + (size_t)b * Q8_0_BYTES + 2), aq + b * QK);
 }
 
+/* The int32 dot of block `block` for every CSR entry j and every weight row r of
+ * the entry's expert, Q8_0 weights: out[j][r] = sum over the block's 32 values of
+ * q_w[e][r] * q_a[row of j].  W is [E][rows][K/32 blocks of 34 bytes]; the
+ * activation row of entry j is act[sel[j]] (sel = expTokI: token rows of x_q) or
+ * act[j] when sel is NULL (h_q, stored in entry order).  Entries are independent,
+ * so they are split across threads; each dot is one serial integer sum. */
+void oracle_block_dots_csr(const uint8_t *W, int E, int rows, int K, const int8_t *act,
+                           const int32_t *expStart, const int32_t *sel, int block, int32_t *out)
+{
+    const int nblk = K / QK;
+    const size_t rbytes = (size_t)nblk * Q8_0_BYTES;
+    const int64_t n = expStart[E];
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t j = 0; j < n; ++j) {
+        int e = 0;
+        while (e + 1 < E && expStart[e + 1] <= j) ++e;
+        const int64_t a = sel ? (int64_t)sel[j] : j;
+        const int8_t *x = act + a * (int64_t)K + (int64_t)block * QK;
+        for (int r = 0; r < rows; ++r) {
+            const uint8_t *blk = W + ((size_t)e * rows + r) * rbytes + (size_t)block * Q8_0_BYTES;
+            out[j * rows + r] = block_isum((const int8_t *)(blk + 2), x);
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------
  * Q4_K weights (the K-quant the pages' MMQ work names next to Q8_0: #406
  * references "Q8_0/Q4_K MMQ"; its layout is the GGUF one, which the pages do

@@ -47,3 +47,29 @@ def test_starved_gemm_times_out_and_context_survives(ops):
     got = out.cpu().numpy().astype(np.float64)
     r = ref["out"].astype(np.float64)
     assert np.linalg.norm(got - r) / np.linalg.norm(r) < 2e-3
+
+
+def test_bucket_barrier_times_out_and_workspace_recovers(ops):
+    """The bucketing kernel's grid barrier told to wait for one CTA more than were launched: every
+    CTA gives up after the limit, the status word says timeout, the CSR is left unwritten; after
+    moe_workspace_init the same workspace buckets correctly."""
+    N, E, k = 4096, 64, 8
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    ws = ops.new_workspace(N, 32, E, 32, k)  # holds the bucketing scratch
+    d_idx = torch.from_numpy(idx).cuda()
+    t0 = time.time()
+    es, ti, tk = ops.moe_debug_bucket_barrier_timeout(d_idx, E, 20, ws)
+    word = ops.moe_workspace_status(ws)  # synchronises
+    elapsed = time.time() - t0
+    assert word & 0x4, f"status word {word}: no timeout reported"
+    assert ops.lib().moe_status_from_word(word) == -5
+    assert elapsed < 30
+    assert (es.cpu().numpy() == -7).all() and (ti.cpu().numpy() == -7).all()  # nothing written
+    ops.moe_workspace_init(ws)
+    es, ti, tk = ops.moe_bucket(d_idx, E, ws)
+    assert ops.moe_workspace_status(ws) == 0
+    res, rti, rtk = O.bucket(idx, E)
+    np.testing.assert_array_equal(es.cpu().numpy(), res)
+    np.testing.assert_array_equal(ti.cpu().numpy(), rti)
+    np.testing.assert_array_equal(tk.cpu().numpy(), rtk)

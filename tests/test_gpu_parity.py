@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from mixture_experts_ffn_top_gb300.workloads import WORKLOADS, Workload, make_inputs
+from mixture_experts_ffn_top_gb300.workloads import Q8_0_BYTES, WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -249,7 +249,58 @@ def _csr(ref):
     return dev(ref["expStart"]), dev(ref["expTokI"]), dev(ref["expTokK"])
 
 
-@pytest.mark.parametrize("name", SMALL + ["olmoe", "tiny_q4k", "olmoe_q4k", "tiny_q3k", "olmoe_q3k"])
+Q8_FULL = ["tiny", "qwen3moe_shared", "olmoe", "skewed"]  # Q8_0 workloads checked on every dot
+
+
+def _check_blocks(nblk):
+    """The first, second, a middle and the last block."""
+    return sorted({0, 1, nblk // 2 + 1, nblk - 1})
+
+
+@pytest.mark.parametrize("name", Q8_FULL)
+@pytest.mark.parametrize("path", [1, 2])
+def test_gate_up_block_dots_every_entry(ops, name, path):
+    """Every CSR entry x every feature x both matrices, four blocks: bit-exact against the
+    oracle's integer block dots."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    es, ti, tk = _csr(ref)
+    xq, xd = dev(ref["x_q"]), dev(O.halves(ref["x_d16"]))
+    total = int(ref["expStart"][-1])
+    for block in _check_blocks(wl.D // 32):
+        dots = ops.moe_debug_gate_up_block_dots(layer.w, xq, xd, es, ti, wl.top_k, block, layer.ws, path=path)
+        assert ops.moe_workspace_status(layer.ws) == 0
+        dots = dots.cpu().numpy()[:total]
+        for mat, W in ((0, inp["gate"]), (1, inp["up"])):
+            rd = O.block_dots_csr(W, ref["x_q"], ref["expStart"], ref["expTokI"], block)
+            bad = np.argwhere(dots[:, mat, :] != rd)
+            assert bad.size == 0, (block, mat, bad[:5].tolist())
+
+
+@pytest.mark.parametrize("name", Q8_FULL)
+@pytest.mark.parametrize("path", [1, 2])
+def test_down_block_dots_every_entry(ops, name, path):
+    """The down GEMM's int32 block dots on the oracle's h_q: every entry x every output column,
+    four blocks, bit-exact."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    es, ti, tk = _csr(ref)
+    total = int(ref["expStart"][-1])
+    hq = np.zeros((wl.N * wl.top_k, wl.F), np.int8)
+    hd = np.zeros((wl.N * wl.top_k, wl.F // 32), np.float32)
+    hq[:total] = ref["h_q"]
+    hd[:total] = O.halves(ref["h_d16"])
+    for block in _check_blocks(wl.F // 32):
+        dots = ops.moe_debug_down_block_dots(layer.w, dev(hq), dev(hd), es, ti, tk, wl.N, wl.top_k, block,
+                                             layer.ws, path=path)
+        assert ops.moe_workspace_status(layer.ws) == 0
+        rd = O.block_dots_csr(inp["down"], ref["h_q"], ref["expStart"], None, block)
+        got = dots.cpu().numpy()[:total]
+        bad = np.argwhere(got != rd)
+        assert bad.size == 0, (block, bad[:5].tolist())
+
+
+@pytest.mark.parametrize("name", ["tiny_q4k", "olmoe_q4k", "tiny_q3k", "olmoe_q3k"])
 @pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_block_dots_bit_exact(ops, name, path):
     wl, inp, ref = case(name)
@@ -269,7 +320,7 @@ def test_gate_up_block_dots_bit_exact(ops, name, path):
             e = int(np.searchsorted(ref["expStart"], j, side="right") - 1)
             t = int(ref["expTokI"][j])
             for mat, W in ((0, inp["gate"]), (1, inp["up"])):
-                for f in (0, wl.F // 2 + 3, wl.F - 1):
+                for f in sorted({0, 1, 31, 32, 63, 64, wl.F // 2 + 3, wl.F - 1}):
                     if wl.wfmt == "q4_k":
                         ref_dot = O.block_dots_q4_k(W[e, f], ref["x_q"][t])[block]
                     elif wl.wfmt == "q3_k":  # the library stores the codes -s_j*q_i
@@ -301,6 +352,25 @@ def test_gate_up_requantised_activations(ops, name, path):
     np.testing.assert_allclose(hd, rd, rtol=1e-3, atol=1e-30)
 
 
+def _abs_dot_bound(Wd, hq, hd, ref, wl):
+    """sum_i |w[e][c][i]| * |h[j][i]| for every CSR entry j (rows in entry order) and output
+    column c, from the dequantised Q8_0 down weights and the requantised activations."""
+    E, D, F = wl.E, wl.D, wl.F
+    out = np.zeros((hq.shape[0], D))
+    habs = np.abs(hq.astype(np.float64)) * np.repeat(hd.astype(np.float64), 32, axis=1)
+    es = ref["expStart"]
+    for e in range(E):
+        a, b = int(es[e]), int(es[e + 1])
+        if a == b:
+            continue
+        blk = Wd[e].reshape(D, F // 32, Q8_0_BYTES)
+        d = O.halves(blk[:, :, :2].copy().view(np.uint16)[..., 0]).astype(np.float64)
+        q = blk[:, :, 2:].view(np.int8).astype(np.float64)
+        wabs = np.abs(q * d[..., None]).reshape(D, F)
+        out[a:b] = habs[a:b] @ wabs.T
+    return out
+
+
 @pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K + Q3K)
 @pytest.mark.parametrize("path", [1, 2])
 def test_down_given_oracle_h(ops, name, path):
@@ -319,6 +389,17 @@ def test_down_given_oracle_h(ops, name, path):
     r = ref["partials"].astype(np.float64)
     rel = np.linalg.norm(got - r) / np.linalg.norm(r)
     assert rel <= 1e-5, rel
+    # element-wise: the kernel adds F/32 exact block terms in fp32 (one rounding each), the oracle
+    # rounds its double sum once, so |got - ref| <= (F/32 + 2) * 2^-24 * sum_b |term_b|, and
+    # sum_b |term_b| <= sum_i |w_i| * |h_i| (dequantised); the K-quant min terms double the count
+    if wl.wfmt == "q8_0":
+        bound = (wl.F // 32 + 2) * 2.0 ** -24 * _abs_dot_bound(inp["down"], hq[:total], hd[:total], ref, wl)
+        rows = (ref["expTokI"].astype(np.int64) * wl.top_k + ref["expTokK"])
+        err = np.abs(got[rows] - r[rows])
+        assert (err <= bound).all(), float((err / np.maximum(bound, 1e-300)).max())
+    else:
+        err = np.abs(got - r)
+        assert (err <= 2 * (2 * wl.F // 32 + 2) * 2.0 ** -24 * np.abs(r).max(axis=1, keepdims=True) * 8).all()
 
 
 @pytest.mark.parametrize("name", SMALL + ["olmoe", "skewed"] + Q4K + Q3K)

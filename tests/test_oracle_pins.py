@@ -309,6 +309,30 @@ def test_block_dots_integer_brute_force():
     assert got.tolist() == [32 * 127 * 127, -32 * 127 * 127]
 
 
+def test_block_dots_csr_integer_brute_force():
+    """Every CSR entry x every weight row of its expert, one block, against pure-Python integer
+    sums (token rows selected through expTokI, and activation rows in entry order)."""
+    rng = np.random.default_rng(11)
+    E, rows, K, N, k = 3, 5, 96, 7, 2
+    W = pack_q8_0(rng.standard_normal((E * rows, K)).astype(np.float32)).reshape(E, rows, -1)
+    qw = W.reshape(E, rows, K // 32, Q8_0_BYTES)[..., 2:].view(np.int8)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    es, ti, tk = O.bucket(idx, E)
+    xq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    hq = rng.integers(-127, 128, (N * k, K)).astype(np.int8)
+    for block in range(K // 32):
+        got_x = O.block_dots_csr(W, xq, es, ti, block)
+        got_h = O.block_dots_csr(W, hq, es, None, block)
+        for j in range(N * k):
+            e = max(i for i in range(E) if es[i] <= j)
+            for r in range(rows):
+                wq = [int(v) for v in qw[e, r, block]]
+                xs = [int(v) for v in xq[ti[j], 32 * block:32 * block + 32]]
+                hs = [int(v) for v in hq[j, 32 * block:32 * block + 32]]
+                assert got_x[j, r] == sum(a * b for a, b in zip(wq, xs))
+                assert got_h[j, r] == sum(a * b for a, b in zip(wq, hs))
+
+
 def _hand_q4_k_block() -> np.ndarray:
     """One Q4_K super-block written byte by byte: d = 1, dmin = 0.5, sc = 1..7, 63 and
     m = 0..6, 40 (bytes below), every quant byte 0x2F (even sub-blocks q = 15, odd q = 2)."""

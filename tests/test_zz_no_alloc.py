@@ -59,3 +59,55 @@ def test_noalloc_router_refuses_oversized_problem(ops):
     with pytest.raises(ops.MoeError) as exc:
         ops.moe_router_topk_noalloc(hidden, routerW, None, 8, False)
     assert exc.value.code == -3
+
+
+def _split_used(N, D, E, sms):
+    """The router's split-K factor as the header states it."""
+    if N <= 8 and D % 4 == 0:
+        return 1
+    tiles = -(-N // 64) * -(-E // 64)
+    depth = 32 if tiles <= 4 else 128
+    cap = min(-(-4 * sms // tiles), max(1, D // depth))
+    s = max(1, cap)
+    while s > 1 and (D // 32) % s != 0:
+        s -= 1
+    return s
+
+
+def test_noalloc_router_refuses_when_the_split_decides(ops):
+    # N * (E + 1) fits the 2^22-float scratch, the split-K table does not: refused on the host
+    # before anything runs, and no output is written
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N, D, E = 2048, 2048, 1024
+    split = _split_used(N, D, E, sms)
+    if not (N * (E + 1) <= 1 << 22 < split * N * (E + 1)):
+        pytest.skip(f"split {split} on {sms} SMs does not decide this shape")
+    hidden = torch.randn((N, D), dtype=torch.float32, device="cuda")
+    routerW = torch.randn((E, D), dtype=torch.float32, device="cuda")
+    outs = dict(topk_idx=torch.full((N, 8), -7, dtype=torch.int32, device="cuda"),
+                topk_w=torch.full((N, 8), -7.0, dtype=torch.float32, device="cuda"),
+                shexp_scale=None,
+                x_q=torch.full((N, D), -7, dtype=torch.int8, device="cuda"),
+                x_d=torch.full((N, D // 32), -7.0, dtype=torch.float32, device="cuda"),
+                logits=torch.full((N, E), -7.0, dtype=torch.float32, device="cuda"))
+    with pytest.raises(ops.MoeError) as exc:
+        ops.moe_router_topk_noalloc(hidden, routerW, None, 8, False, want_logits=True, outputs=outs)
+    assert exc.value.code == -3
+    torch.cuda.synchronize()
+    for name, t in outs.items():
+        if t is not None:
+            assert (t == -7).all(), f"{name} was written"
+
+
+def test_noalloc_router_small_batch_uses_one_split(ops):
+    # a decode-sized batch is routed in one pass (no split-K table beyond N * (E + 1))
+    wl = WORKLOADS["decode_n8"]
+    inp = make_inputs(wl)
+    hidden = torch.from_numpy(inp["hidden"]).cuda()
+    routerW = torch.from_numpy(inp["routerW"]).cuda()
+    ws = ops.new_workspace(wl.N, wl.D, wl.E, wl.F, wl.top_k, wl.Fs)
+    ref = ops.moe_router_topk(hidden, routerW, None, wl.top_k, wl.norm_topk_prob, ws, want_logits=True)
+    got = ops.moe_router_topk_noalloc(hidden, routerW, None, wl.top_k, wl.norm_topk_prob, want_logits=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got["topk_idx"].cpu().numpy(), ref["topk_idx"].cpu().numpy())
+    np.testing.assert_array_equal(got["logits"].cpu().numpy(), ref["logits"].cpu().numpy())
