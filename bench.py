@@ -12,8 +12,13 @@ device synchronise on both sides; every step is bracketed by CUDA events on
 the launching stream with events between the stages, and the L2 is flushed
 (a 512 MB write) between steps outside the events.  Under torchrun each rank
 runs its own token batch (replicas, weak scaling) and rank 0 prints the line
-with the maximum time over ranks.  --impl reference times the CPU oracle on
-the host cores on a bounded sample of the same workload.
+with the maximum time over ranks.  With one GPU the line also carries
+`configs`: the other workloads of the layer's survey (tiny, decode batches of
+1/4/8 tokens, the Qwen3-MoE-shaped layer with a shared expert, the Zipf-skewed
+long prefill), each timed the same way after the headline, with its tokens/s,
+layer roofline fraction, dominant kernel's fraction and stage times.
+--impl reference times the CPU oracle on the host cores on a bounded sample of
+the same workload.
 """
 from __future__ import annotations
 
@@ -244,6 +249,104 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+CONFIG_WORKLOADS = ["tiny", "decode_n1", "decode_n4", "decode_n8", "qwen3moe_shared", "skewed"]
+
+
+def resolve_path(ops, w, wl, path):
+    """The expert path a moe_ffn_prefill call takes (the library's auto rule)."""
+    if path != ops.MOE_PATH_AUTO:
+        return path
+    tensor = ops.moe_weights_tensor_path(w) and wl.N >= 64 and (wl.N * wl.top_k) // wl.E >= 8
+    return ops.MOE_PATH_TENSOR if tensor else ops.MOE_PATH_MATVEC
+
+
+def launches_per_step(ops, wl, resolved_path):
+    experts = 2 * (2 if wl.Fs else 1)  # matvec: gate/up and down, routed (and shared)
+    if resolved_path == ops.MOE_PATH_TENSOR:
+        return 2 + 1 + 3 + 1  # router x2, bucketing(+plan), gather, gate/up, down, combine
+    if wl.N <= SMALL_BATCH:
+        return 1 + experts + 1  # routing in one launch, the expert matvecs, combine
+    return 2 + 1 + experts + 1
+
+
+def measure(ops, wl, inp, hidden, steps, warmup, path, device, flush, peaks, world=1):
+    """One workload's layer: plain moe_ffn_prefill steps between two events (L2 flushed before
+    each), then the stage-timed variant; throughput, roofline fractions and stage times."""
+    import torch
+
+    layer = ops.MoeLayer.from_numpy(inp, device=device, top_k=wl.top_k, max_tokens=wl.N)
+    w, ws, stream = layer.w, layer.ws, torch.cuda.current_stream()
+    out = torch.empty((wl.N, wl.D), dtype=torch.float32, device=device)
+
+    def step(ev=None):
+        if ev is None:
+            ops.moe_ffn_prefill(w, hidden, layer.routerW, layer.shexp_gate, wl.top_k, wl.norm_topk_prob, ws,
+                                out=out, path=path)
+        else:
+            ops.moe_ffn_prefill_timed(w, hidden, layer.routerW, layer.shexp_gate, wl.top_k, wl.norm_topk_prob, ws,
+                                      ev, out=out, path=path)
+
+    for _ in range(warmup):
+        step()
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    if layer.status():
+        raise RuntimeError(f"{wl.name}: device status set during warm-up")
+    resolved = resolve_path(ops, w, wl, path)
+    topk_idx = layer.views(wl.N)["topk_idx"].cpu().numpy()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.fill_(1)  # before the step's events: every step starts with a cold L2
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if layer.status():
+        raise RuntimeError(f"{wl.name}: device status set during the timed steps")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    n_stage = min(steps, STAGE_STEPS)
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_stage)]
+    for i in range(n_stage):
+        flush.fill_(1)
+        step(sevs[i])
+    torch.cuda.synchronize()
+    if layer.status():
+        raise RuntimeError(f"{wl.name}: device status set during the stage-timed steps")
+    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in sevs) for j, s in enumerate(ops.PREFILL_STAGES)}
+    work = algorithmic_work(wl, topk_idx)
+    exp_ms = stage_ms["gate_up"] + stage_ms["down"]
+    if resolved == ops.MOE_PATH_TENSOR:
+        gu_ms = stage_ms["gate_up"]
+        tflops = work["int8_ops_gate_up"] / (gu_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                "kernel": "grouped_gemm_kernel gate/up launch (tcgen05 kind::f16 on exact fp16 integers)"}
+    else:
+        gbs = work["weight_bytes"] / (exp_ms / 1e3) / 1e9
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                "kernel": "grouped expert matvec: gate/up + down launches (dp4a)"}
+    layer_roof_s = max(work["int8_ops"] / (peaks.get("bf16_tflops", 1900.0) * 1e12),
+                       work["bytes"] / (peaks.get("hbm_gbs", 6800.0) * 1e9))
+    res = dict(layer=layer, out=out, step=step, ms=ms, t_wall=t_wall, value=job_throughput(world, wl.N, ms),
+               stage_ms=stage_ms, stage_step_ms=statistics.mean(e[0].elapsed_time(e[6]) for e in sevs),
+               work=work, roofline=roof, layer_roof_s=layer_roof_s, resolved=resolved, n_stage=n_stage,
+               launches=launches_per_step(ops, wl, resolved))
+    return res
+
+
+def config_entry(ops, wl, r):
+    """The per-workload record of the bench line."""
+    return {"workload": f"{wl.name}: {wl.describe()}", "tokens_per_s": r["value"], "ms_per_step": r["ms"],
+            "expert_path": {1: "matvec", 2: "tensor"}[r["resolved"]],
+            "layer_roofline_us": r["layer_roof_s"] * 1e6, "layer_roofline_frac": r["layer_roof_s"] / (r["ms"] / 1e3),
+            "dominant_kernel": {k: r["roofline"][k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac")},
+            "stage_ms": r["stage_ms"], "algorithmic": r["work"]}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -252,48 +355,16 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    peaks, peak_src = load_peaks()
     wl = WORKLOADS[args.workload]
     inp = make_inputs(wl)
     inp["hidden"] = rank_hidden(wl, inp["hidden"], rank, world)  # each rank its own token batch
-    layer = ops.MoeLayer.from_numpy(inp, device=device, top_k=wl.top_k, max_tokens=wl.N)
-    w = layer.w
-    stream = torch.cuda.current_stream()
     hidden = torch.from_numpy(inp["hidden"]).to(device)
-    routerW = layer.routerW
-    shg = layer.shexp_gate
-    out = torch.empty((wl.N, wl.D), dtype=torch.float32, device=device)
-    ws = layer.ws
-    N, D, E, F, k, Fs = wl.N, wl.D, wl.E, wl.F, wl.top_k, wl.Fs
-    path = args.path
-    resolved_path = path
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    v = layer.views(N)
-    # One step = one moe_ffn_prefill call (the layer as a user calls it); the timed variant
-    # records CUDA events on the launching stream between its stages, so each kernel's share
-    # is measured in place.  The L2 flush between steps also gives the host a head start.
-    stages = ops.PREFILL_STAGES
+    path = args.path
+    stream = torch.cuda.current_stream()
+    N, D, k = wl.N, wl.D, wl.top_k
 
-    def step(ev=None):
-        if ev is None:
-            ops.moe_ffn_prefill(w, hidden, routerW, shg, k, wl.norm_topk_prob, ws, out=out, path=path)
-        else:
-            ops.moe_ffn_prefill_timed(w, hidden, routerW, shg, k, wl.norm_topk_prob, ws, ev, out=out, path=path)
-
-    for _ in range(args.warmup):
-        step()
-        flush.fill_(1)
-    torch.cuda.synchronize()
-    status = layer.status()
-    if status:
-        raise RuntimeError(f"device status {status} after warm-up")
-    if path == ops.MOE_PATH_AUTO:
-        avg_rows = N * k // E
-        tensor = ops.moe_weights_tensor_path(w) and N >= 64 and avg_rows >= 8
-        resolved_path = ops.MOE_PATH_TENSOR if tensor else ops.MOE_PATH_MATVEC
-    topk_idx = v["topk_idx"].cpu().numpy()
-
-    # the timed steps: one plain moe_ffn_prefill call each, bracketed by two events
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     gpu_index = int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].strip().isdigit() else local_rank
     clocks = ClockSampler(gpu_index)
@@ -302,40 +373,23 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     clocks.wait_first()
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(1)  # before the step's events: every step starts with a cold L2
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
+    t_clk0 = time.perf_counter()
+    # the headline workload: its timed steps lie inside the clock sampler's window
+    head = measure(ops, wl, inp, hidden, args.steps, args.warmup, path, device, flush, peaks, world)
+    t_clk1 = time.perf_counter()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop(t_wall0, t_wall0 + t_wall)
-    status = layer.status()
-    if status:
-        raise RuntimeError(f"device status {status} after the timed steps")
-    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    ms = max_over_ranks(statistics.mean(step_ms), device)
+    clk = clocks.stop(t_clk0, t_clk1)
+    ms = max_over_ranks(head["ms"], device)
     value = job_throughput(world, N, ms)
-
-    # where the time goes: the same steps through moe_ffn_prefill_timed, which records events on
-    # the launching stream between its kernels (those events cost a few microseconds per stage,
-    # so this breakdown is not the headline)
-    n_stage_steps = min(args.steps, STAGE_STEPS)
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_stage_steps)]
-    for i in range(n_stage_steps):
-        flush.fill_(1)
-        step(sevs[i])
-    torch.cuda.synchronize()
-    if layer.status():
-        raise RuntimeError("device status set during the stage-timed steps")
-    stage_ms = {s: [] for s in stages}
-    for e in sevs:
-        for j, s in enumerate(stages):
-            stage_ms[s].append(e[j].elapsed_time(e[j + 1]))
-    stage_step_ms = statistics.mean(e[0].elapsed_time(e[6]) for e in sevs)
+    layer, w, ws = head["layer"], head["layer"].w, head["layer"].ws
+    routerW, shg = layer.routerW, layer.shexp_gate
+    stage_ms = head["stage_ms"]
+    roofline = dict(head["roofline"], peak_source=peak_src,
+                    traffic=measured_traffic("gate_up", wl.name) if head["resolved"] == ops.MOE_PATH_TENSOR
+                    else TRAFFIC.get(("experts", head["resolved"])))
+    head_path, head_work, layer_roof_s = head["resolved"], head["work"], head["layer_roof_s"]
+    head_launches, n_stage = head["launches"], head["n_stage"]
 
     # e2e: the public host-buffer call (moe_ffn_prefill_host) on pinned host memory; the hidden rows
     # come in and the output rows go out over the host link inside the timed region (the router
@@ -350,25 +404,27 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         ops.moe_ffn_prefill_host(w, h_host, routerW, shg, k, wl.norm_topk_prob, ws, o_host, path=path)
 
+    def timed(fn, n):
+        out = []
+        for _ in range(n):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            out.append(e0.elapsed_time(e1))
+        return statistics.mean(out)
+
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        e2e_step()
-        e1.record(stream)
-        e1.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e_mean = max_over_ranks(statistics.mean(e2e_ms), device)
+    e2e_mean = max_over_ranks(timed(e2e_step, args.steps), device)
     if layer.status():
         raise RuntimeError("device status set during the e2e steps")
 
-    # the same layer with the residual add fused into its combine (out = residual + FFN(hidden)),
-    # device buffers, timed like the main steps
+    # the same layer with the residual add fused into its combine (out = residual + FFN(hidden))
     residual = torch.randn((N, D), dtype=torch.float32, device=device, generator=None)
     res_out = torch.empty_like(residual)
 
@@ -378,66 +434,42 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(max(1, args.warmup)):
         res_step()
-    res_ms = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        res_step()
-        e1.record(stream)
-        e1.synchronize()
-        res_ms.append(e0.elapsed_time(e1))
-    res_mean = max_over_ranks(statistics.mean(res_ms), device)
+    res_mean = max_over_ranks(timed(res_step, args.steps), device)
     if layer.status():
         raise RuntimeError("device status set during the residual steps")
+    del head, layer, w, ws, routerW, shg
+    torch.cuda.empty_cache()
+
+    # the survey's other workloads, one after another on this GPU, each at the same steps/warm-up
+    configs = {}
+    if world == 1 and not args.no_configs:
+        for name in CONFIG_WORKLOADS:
+            if name == wl.name:
+                continue
+            cwl = WORKLOADS[name]
+            cinp = make_inputs(cwl)
+            r = measure(ops, cwl, cinp, torch.from_numpy(cinp["hidden"]).to(device), args.steps, args.warmup, path,
+                        device, flush, peaks)
+            configs[name] = config_entry(ops, cwl, r)
+            del r
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    peaks, peak_src = load_peaks()
-    work = algorithmic_work(wl, topk_idx)
-    exp_ms = statistics.mean(stage_ms["gate_up"]) + statistics.mean(stage_ms["down"])
-    if resolved_path == ops.MOE_PATH_TENSOR:
-        # the dominant kernel: the gate/up launch (2 of the 3 expert matrices), timed by the
-        # events around it inside moe_ffn_prefill_timed
-        gu_ms = statistics.mean(stage_ms["gate_up"])
-        tflops = work["int8_ops_gate_up"] / (gu_ms / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        roofline = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                    "traffic": measured_traffic("gate_up", wl.name)}
-        roof_kernel = "grouped_gemm_kernel gate/up launch (tcgen05 kind::f16 on exact fp16 integers)"
-    else:
-        gbs = work["weight_bytes"] / (exp_ms / 1e3) / 1e9
-        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-        roofline = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                    "traffic": TRAFFIC.get(("experts", resolved_path))}
-        roof_kernel = "grouped expert matvec: gate/up + down launches (dp4a)"
-    roofline["kernel"] = roof_kernel
-    roofline["peak_source"] = peak_src
-    layer_roof_s = max(work["int8_ops"] / (peaks.get("bf16_tflops", 1900.0) * 1e12),
-                       work["bytes"] / (peaks.get("hbm_gbs", 6800.0) * 1e9))
-    experts = 2 * (2 if Fs else 1)  # matvec: gate/up and down, routed (and shared)
-    if resolved_path == ops.MOE_PATH_TENSOR:
-        launches_per_step = 2 + 1 + 3 + 1  # router x2, bucketing(+plan), gather, gate/up, down, combine
-    elif N <= SMALL_BATCH:
-        launches_per_step = 1 + experts + 1  # routing in one launch, the expert matvecs, combine
-    else:
-        launches_per_step = 2 + 1 + experts + 1
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "i8", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {wl.describe()}", "tokens_per_rank": N,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "expert_path": {1: "matvec", 2: "tensor"}[resolved_path],
+                   "expert_path": {1: "matvec", 2: "tensor"}[head_path],
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write); expert weights exceed L2",
                    "step": "one moe_ffn_prefill call between two events; stage times from "
-                           f"moe_ffn_prefill_timed over {n_stage_steps} further steps"},
-        "stage_ms": {s: statistics.mean(vv) for s, vv in stage_ms.items()},
-        "stage_timed_ms_per_step": stage_step_ms,
+                           f"moe_ffn_prefill_timed over {n_stage} further steps"},
+        "stage_ms": stage_ms,
         "layer_roofline_us": layer_roof_s * 1e6,
         "layer_roofline_frac": layer_roof_s / (ms / 1e3),
-        "algorithmic": work,
+        "algorithmic": head_work,
         "roofline": roofline,
         "e2e": {"value": job_throughput(world, N, e2e_mean), "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
                 "d2h_bytes_per_step": N * D * 4, "ms_per_step": e2e_mean,
@@ -445,9 +477,9 @@ def run_ours(args, rank, world, local_rank):
                 "host_numa_node": numa_node},
         "with_residual": {"value": job_throughput(world, N, res_mean), "unit": UNIT, "ms_per_step": res_mean,
                           "api": "moe_ffn_prefill_residual (residual add fused into the combine)"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": head_launches * args.steps,
         "clocks": clk,
-        "wall_s_timed_region": t_wall,
+        "configs": configs,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
@@ -487,6 +519,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample (tokens per pass) for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle sample per step for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
