@@ -437,6 +437,37 @@ def run_ours(args, rank, world, local_rank):
     res_mean = max_over_ranks(timed(res_step, args.steps), device)
     if layer.status():
         raise RuntimeError("device status set during the residual steps")
+
+    # two chained layers (hidden <- hidden + FFN_l(hidden), l = 0, 1): the stack entry point, whose
+    # second router starts behind the first layer's combine, against two separate residual calls
+    from dataclasses import replace as _replace
+
+    inp2 = make_inputs(_replace(wl, seed=wl.seed + 100))
+    layer2 = ops.MoeLayer.from_numpy(inp2, device=device, top_k=k, max_tokens=N)
+    hs = hidden.clone()
+
+    def stack_step():
+        hs.copy_(hidden)
+        ops.moe_ffn_prefill_stack([w, layer2.w], [routerW, layer2.routerW], [shg, layer2.shexp_gate], hs, k,
+                                  wl.norm_topk_prob, ws, path=path)
+
+    h_a, h_b = hidden.clone(), torch.empty_like(hidden)
+
+    def two_calls_step():
+        h_a.copy_(hidden)
+        ops.moe_ffn_prefill_residual(w, h_a, routerW, shg, h_a, k, wl.norm_topk_prob, ws, out=h_b, path=path)
+        ops.moe_ffn_prefill_residual(layer2.w, h_b, layer2.routerW, layer2.shexp_gate, h_b, k, wl.norm_topk_prob, ws,
+                                     out=h_a, path=path)
+
+    for _ in range(max(1, args.warmup)):
+        stack_step()
+        two_calls_step()
+    stack_ms = max_over_ranks(timed(stack_step, args.steps), device)
+    two_ms = max_over_ranks(timed(two_calls_step, args.steps), device)
+    torch.cuda.synchronize()
+    if not torch.equal(hs, h_a):
+        raise RuntimeError("the layer stack and two separate calls disagree")
+    del layer2
     del head, layer, w, ws, routerW, shg
     torch.cuda.empty_cache()
 
@@ -477,6 +508,10 @@ def run_ours(args, rank, world, local_rank):
                 "host_numa_node": numa_node},
         "with_residual": {"value": job_throughput(world, N, res_mean), "unit": UNIT, "ms_per_step": res_mean,
                           "api": "moe_ffn_prefill_residual (residual add fused into the combine)"},
+        "layer_stack": {"layers": 2, "ms_per_step": stack_ms, "ms_two_separate_calls": two_ms,
+                        "tokens_per_s_per_layer": job_throughput(world, 2 * N, stack_ms),
+                        "api": "moe_ffn_prefill_stack (second router launched behind the first combine; "
+                               "the step includes one hidden-size device copy, as do the separate calls)"},
         "gpu_launches": head_launches * args.steps,
         "clocks": clk,
         "configs": configs,

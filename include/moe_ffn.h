@@ -401,6 +401,26 @@ int moe_host_memory_addressable(const void *p);
  * MOE_ERR_INVALID_ARG for NULL, MOE_ERR_CUDA if the query fails. */
 int moe_device_host_numa_node(int *node);
 
+/* A stack of routed-MoE FFN layers applied in place, one after another on
+ * `stream`: for l = 0..n_layers-1, hidden <- hidden + FFN_l(hidden), each
+ * layer exactly as moe_ffn_prefill_residual computes it with the residual
+ * and output both `hidden` (so the results equal n_layers such calls bit for
+ * bit).  Layer l uses weights w[l], routerW[l] and shexp_gate[l] (the array
+ * itself may be NULL when no layer has a shared expert; entries may be NULL
+ * per layer).  w, routerW and shexp_gate are HOST arrays of n_layers handles
+ * / device pointers.  Every layer shares N, top_k, norm_topk_prob, path and
+ * the workspace, which must be large enough for each layer's shapes (same D
+ * in every layer).  From the second layer on, the router is launched so that
+ * it may start while the previous layer's combine is still running
+ * (cross-layer overlap, #388 "Remaining levers" 2): it first pulls its own
+ * router weights into L2, then waits on the device for the previous layer's
+ * output before reading it.  Errors as moe_ffn_prefill; nothing is launched
+ * when an argument check fails. */
+int moe_ffn_prefill_stack(const moe_weights_t *w, const float *const *routerW,
+                          const float *const *shexp_gate, int n_layers, float *hidden, int N,
+                          int top_k, int norm_topk_prob, int path, void *ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
 /* moe_ffn_prefill_ex that also records seven caller-created CUDA events on
  * `stream` around its stages, for measuring each kernel in place:
  *   [0] start, [1] after the router (+softmax/top-k/Q8_1), [2] after bucketing

@@ -23,6 +23,8 @@ template <int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
                const float4 *__restrict__ shared, const float4 *residual, int N, int k, int D4, float4 *out) {
+    // the next layer's router may be scheduled now (it waits for this grid before reading out)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // launched early behind the down kernel: its partials are complete past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t total = (int64_t)N * D4;

@@ -442,7 +442,8 @@ int moe_combine(const float *partials, const float *topk_w, const float *shared,
 
 static int prefill_impl(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
                         int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
-                        cudaStream_t stream, cudaEvent_t *ev, const float *residual = nullptr) {
+                        cudaStream_t stream, cudaEvent_t *ev, const float *residual = nullptr,
+                        bool early_router = false) {
     if (!w || !hidden || !routerW || !out) return MOE_ERR_INVALID_ARG;
     if (residual && ((uintptr_t)residual % 16 || w->D % 4)) return MOE_ERR_INVALID_ARG;
     if (shexp_gate && w->Fs == 0) return MOE_ERR_INVALID_ARG;
@@ -475,14 +476,14 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
         small = launch_route_small(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh,
                                    xq, xd, ws_ptr<float>(ws, L.part_logits), es, ti, tk,
                                    reinterpret_cast<unsigned *>(static_cast<char *>(ws) + ROUTE_COUNTER_OFFSET),
-                                   status_word(ws), stream);
+                                   status_word(ws), stream, early_router && ev == nullptr);
     if (small != MOE_ERR_UNSUPPORTED_SHAPE) {
         rc = small;
         mark(1);
         mark(2);
     } else {
         rc = launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh, xq,
-                           xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream);
+                           xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream, early_router && ev == nullptr);
         mark(1);
         if (!rc)
             rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr,
@@ -579,6 +580,28 @@ int moe_ffn_prefill_residual(moe_weights_t w, const float *hidden, const float *
     if (!residual) return MOE_ERR_INVALID_ARG;
     return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
                         nullptr, residual);
+}
+
+int moe_ffn_prefill_stack(const moe_weights_t *w, const float *const *routerW, const float *const *shexp_gate,
+                          int n_layers, float *hidden, int N, int top_k, int norm_topk_prob, int path, void *ws,
+                          size_t ws_bytes, cudaStream_t stream) {
+    if (!w || !routerW || !hidden || n_layers < 1) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        if (!w[l] || !routerW[l]) return MOE_ERR_INVALID_ARG;
+        if (w[l]->D != w[0]->D || (reinterpret_cast<uintptr_t>(hidden) % 16) || w[0]->D % 4) return MOE_ERR_INVALID_ARG;
+        const WsLayout L = ws_layout(N, w[l]->D, w[l]->E, w[l]->F, top_k, w[l]->Fs);
+        if (!shape_ok(N, w[l]->D, w[l]->E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (int rc = check_ws(ws, ws_bytes, L)) return rc;
+    }
+    for (int l = 0; l < n_layers; ++l) {
+        // hidden <- hidden + FFN_l(hidden), in place; from the second layer on the router is
+        // launched behind the previous layer's combine (it waits on the device for its output)
+        const float *g = shexp_gate ? shexp_gate[l] : nullptr;
+        if (int rc = prefill_impl(w[l], hidden, routerW[l], g, N, top_k, norm_topk_prob, hidden, path, ws, ws_bytes,
+                                  stream, nullptr, hidden, l > 0))
+            return rc;
+    }
+    return MOE_OK;
 }
 
 int moe_ffn_prefill_timed(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,

@@ -104,9 +104,11 @@ inline int plan_tile_rows(const moe_weights_s *) { return TILE_N; }
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
-                  cudaStream_t s);
+                  cudaStream_t s, bool early = false);
 int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,
                             float *w, cudaStream_t s);
+// early (both routers): launched to overlap the kernel before it, the previous layer's combine (see
+// launch_early); the router kernels wait on the device before reading hidden.
 // router + softmax/top-k + bucketing of a batch of at most 8 tokens in one launch (counter: an
 // arrival word in the workspace's status block, ROUTE_COUNTER_OFFSET, zero between launches);
 // MOE_ERR_UNSUPPORTED_SHAPE when the batch is too large for it.
@@ -114,7 +116,7 @@ constexpr size_t ROUTE_COUNTER_OFFSET = 192;
 int launch_route_small(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
                        int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
                        float *x_d, float *part_logits, int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
-                       unsigned *counter, unsigned *status, cudaStream_t s);
+                       unsigned *counter, unsigned *status, cudaStream_t s, bool early = false);
 int launch_quantize_q8_1(const float *x, int64_t nblk, int8_t *q, float *d, cudaStream_t s);
 // bucket.cu
 // ws: the workspace (status word at 0, the grid barrier's two words at BUCKET_BARRIER_OFFSET

@@ -39,6 +39,15 @@ router_logits_kernel(const float *__restrict__ hidden, const float *__restrict__
     const int k_end = min(D, k_begin + ksplit);
     const bool quantise = (blockIdx.y == 0);
     const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4x4 outputs each
+    // Launched early behind the previous layer's combine (a chain of layers): this CTA's slice of
+    // routerW does not depend on it, so ask L2 for it first; hidden is the previous layer's output,
+    // read only after the wait (which returns at once without the launch attribute).
+    for (int i = tid; i < RB_N * ((k_end - k_begin + 31) / 32); i += R_THREADS) {
+        const int e = e0 + i / ((k_end - k_begin + 31) / 32), c = k_begin + 32 * (i % ((k_end - k_begin + 31) / 32));
+        const float *src = e < E ? routerW + (size_t)e * D + c : (e == E && shexp_gate ? shexp_gate + c : nullptr);
+        if (src != nullptr && c < k_end) asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -158,6 +167,9 @@ __device__ __forceinline__ void router_small_body(const float *__restrict__ hidd
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int e = blockIdx.x;
     const float *w = e < E ? routerW + (size_t)e * D : shexp_gate;
+    // launched early behind the previous layer's combine: the weight row first, hidden after the wait
+    for (int c = 32 * tid; c < D; c += 32 * RS_THREADS) asm volatile("prefetch.global.L2 [%0];" ::"l"(w + c));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float acc[RS_MAX_N];
 #pragma unroll
     for (int t = 0; t < RS_MAX_N; ++t) acc[t] = 0.0f;
@@ -453,21 +465,33 @@ int router_split_used(int N, int D, int E) { return (N <= RS_MAX_N && D % 4 == 0
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
-                  cudaStream_t s) {
+                  cudaStream_t s, bool early) {
     int Eext = E + (shexp_gate ? 1 : 0);
     if (N <= RS_MAX_N && D % 4 == 0) {
-        router_small_kernel<<<Eext, RS_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, part_logits, x_q,
-                                                        x_d);
-        int rc = launch_status();
+        int rc = MOE_OK;
+        if (early)
+            rc = launch_early(router_small_kernel, dim3(Eext), dim3(RS_THREADS), 0, s, hidden, routerW, shexp_gate, N, D,
+                              E, Eext, part_logits, x_q, x_d);
+        else {
+            router_small_kernel<<<Eext, RS_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, part_logits,
+                                                            x_q, x_d);
+            rc = launch_status();
+        }
         if (rc) return rc;
         return launch_softmax(part_logits, 1, N, E, Eext, top_k, norm, topk_idx, topk_w,
                               shexp_gate ? shexp_scale : nullptr, logits_out, s);
     }
     int ksplit = D / nsplit;
     dim3 grid((N + RB_M - 1) / RB_M, (Eext + RB_N - 1) / RB_N, nsplit);
-    router_logits_kernel<<<grid, R_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, ksplit,
-                                                   part_logits, x_q, x_d);
-    int rc = launch_status();
+    int rc = MOE_OK;
+    if (early)
+        rc = launch_early(router_logits_kernel, grid, dim3(R_THREADS), 0, s, hidden, routerW, shexp_gate, N, D, E, Eext,
+                          ksplit, part_logits, x_q, x_d);
+    else {
+        router_logits_kernel<<<grid, R_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, ksplit,
+                                                       part_logits, x_q, x_d);
+        rc = launch_status();
+    }
     if (rc) return rc;
     return launch_softmax(part_logits, nsplit, N, E, Eext, top_k, norm, topk_idx, topk_w,
                           shexp_gate ? shexp_scale : nullptr, logits_out, s);
@@ -476,23 +500,26 @@ int launch_router(const float *hidden, const float *routerW, const float *shexp_
 int launch_route_small(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
                        int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
                        float *x_d, float *part_logits, int32_t *expStart, int32_t *expTokI, int32_t *expTokK,
-                       unsigned *counter, unsigned *status, cudaStream_t s) {
+                       unsigned *counter, unsigned *status, cudaStream_t s, bool early) {
     if (N > RS_MAX_N || N * top_k > RS_THREADS || D % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     const int Eext = E + (shexp_gate ? 1 : 0);
     const int epl = (E + 31) / 32;
     float *sh = shexp_gate ? shexp_scale : nullptr;
-#define MOE_ROUTE_SMALL(EPLV)                                                                                   \
-    route_small_kernel<EPLV><<<Eext, RS_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, top_k, norm, \
-                                                         part_logits, x_q, x_d, topk_idx, topk_w, sh, expStart,  \
-                                                         expTokI, expTokK, counter, status)
-    if (epl <= 1) MOE_ROUTE_SMALL(1);
-    else if (epl <= 2) MOE_ROUTE_SMALL(2);
-    else if (epl <= 4) MOE_ROUTE_SMALL(4);
-    else if (epl <= 8) MOE_ROUTE_SMALL(8);
-    else if (epl <= 16) MOE_ROUTE_SMALL(16);
-    else MOE_ROUTE_SMALL(32);
-#undef MOE_ROUTE_SMALL
-    return launch_status();
+    auto go = [&](auto kernel) {
+        if (early)
+            return launch_early(kernel, dim3(Eext), dim3(RS_THREADS), 0, s, hidden, routerW, shexp_gate, N, D, E, Eext,
+                                top_k, norm, part_logits, x_q, x_d, topk_idx, topk_w, sh, expStart, expTokI, expTokK,
+                                counter, status);
+        kernel<<<Eext, RS_THREADS, 0, s>>>(hidden, routerW, shexp_gate, N, D, E, Eext, top_k, norm, part_logits, x_q,
+                                           x_d, topk_idx, topk_w, sh, expStart, expTokI, expTokK, counter, status);
+        return launch_status();
+    };
+    if (epl <= 1) return go(route_small_kernel<1>);
+    if (epl <= 2) return go(route_small_kernel<2>);
+    if (epl <= 4) return go(route_small_kernel<4>);
+    if (epl <= 8) return go(route_small_kernel<8>);
+    if (epl <= 16) return go(route_small_kernel<16>);
+    return go(route_small_kernel<32>);
 }
 
 int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,

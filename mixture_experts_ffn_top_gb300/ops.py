@@ -62,6 +62,7 @@ _SIGS = {
     "moe_combine_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill_residual": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
+    "moe_ffn_prefill_stack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _SZ, _P]),
 }
 
 
@@ -372,6 +373,25 @@ def moe_combine_residual(partials, topk_w, shared, residual, out=None, stream=No
                                       _dev(shared, torch.float32, "shared"), _dev(residual, torch.float32, "residual"),
                                       N, k, D, _dev(out, torch.float32, "out"), _stream(stream)), "moe_combine_residual")
     return out
+
+
+def moe_ffn_prefill_stack(weights, routerWs, shexp_gates, hidden, top_k, norm_topk_prob, ws, path=MOE_PATH_AUTO,
+                          stream=None):
+    """Layers applied in place, hidden <- hidden + FFN_l(hidden) for each layer l in order (weights,
+    routerWs, shexp_gates: one entry per layer; shexp_gates entries may be None)."""
+    n = len(weights)
+    assert len(routerWs) == n and len(shexp_gates) == n
+    N = hidden.shape[0]
+    wh = (_P * n)(*[w.handle for w in weights])
+    rw = (_P * n)(*[_dev(r, torch.float32, "routerW") for r in routerWs])
+    sg = None
+    if any(g is not None for g in shexp_gates):
+        sg = (_P * n)(*[_dev(g, torch.float32) for g in shexp_gates])
+    rc = lib().moe_ffn_prefill_stack(ctypes.cast(wh, _P), ctypes.cast(rw, _P), None if sg is None else ctypes.cast(sg, _P),
+                                     n, _dev(hidden, torch.float32, "hidden"), N, top_k, int(norm_topk_prob), path,
+                                     _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check(rc, "moe_ffn_prefill_stack")
+    return hidden
 
 
 def moe_ffn_prefill_residual(w: MoeWeights, hidden, routerW, shexp_gate, residual, top_k, norm_topk_prob, ws,

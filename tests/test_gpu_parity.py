@@ -694,3 +694,59 @@ def test_zero_hidden_gives_zero(ops):
     out = layer.prefill(dev(inp["hidden"]), 2, False)
     assert layer.status() == 0
     assert torch.count_nonzero(out).item() == 0
+
+
+# ---------------------------------------------------------- layer stacks ---
+def _stack_layers(ops, wl, n):
+    from dataclasses import replace
+
+    inps = [make_inputs(replace(wl, seed=wl.seed + 100 * l)) for l in range(n)]
+    layers = [layer_for(ops, inp, wl) for inp in inps]
+    return inps, layers
+
+
+@pytest.mark.parametrize("name,n", [("tiny", 3), ("olmoe", 2), ("qwen3moe_shared", 2), ("decode_n4", 3)])
+def test_layer_stack_equals_sequential_calls(ops, name, n):
+    """moe_ffn_prefill_stack (routers of later layers launched behind the previous combine) gives the
+    same bits as n separate moe_ffn_prefill_residual calls."""
+    wl = WORKLOADS[name]
+    inps, layers = _stack_layers(ops, wl, n)
+    h0 = dev(inps[0]["hidden"])
+    h = h0.clone()
+    for inp, lay in zip(inps, layers):
+        h = ops.moe_ffn_prefill_residual(lay.w, h, lay.routerW, lay.shexp_gate, h, wl.top_k, wl.norm_topk_prob,
+                                         lay.ws)
+    hs = h0.clone()
+    ops.moe_ffn_prefill_stack([l.w for l in layers], [l.routerW for l in layers], [l.shexp_gate for l in layers], hs,
+                              wl.top_k, wl.norm_topk_prob, layers[0].ws)
+    torch.cuda.synchronize()
+    assert all(l.status() == 0 for l in layers)
+    a, b = hs.cpu().numpy(), h.cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), float(np.abs(a - b).max())
+
+
+def test_layer_stack_against_oracle_chain(ops):
+    """Three tiny layers in place against the oracle applying the same layers one after another
+    (out = (routed + shared) + hidden per layer)."""
+    wl = WORKLOADS["tiny"]
+    inps, layers = _stack_layers(ops, wl, 3)
+    h = inps[0]["hidden"].copy()
+    for inp in inps:
+        step = dict(inp, hidden=h)
+        r = O.moe_ffn_inputs(step, wl.top_k, wl.norm_topk_prob)
+        h = O.combine(r["partials"], r["topk_w"], r.get("shared_out"), h)
+    hs = dev(inps[0]["hidden"])
+    ops.moe_ffn_prefill_stack([l.w for l in layers], [l.routerW for l in layers], [l.shexp_gate for l in layers], hs,
+                              wl.top_k, wl.norm_topk_prob, layers[0].ws)
+    got = hs.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - h) / np.linalg.norm(h)
+    assert rel <= 2e-3, rel
+
+
+def test_layer_stack_rejects_bad_arguments(ops):
+    wl = WORKLOADS["tiny"]
+    inps, layers = _stack_layers(ops, wl, 2)
+    h = dev(inps[0]["hidden"])
+    with pytest.raises(ops.MoeError):
+        ops.moe_ffn_prefill_stack([l.w for l in layers], [layers[0].routerW, layers[1].routerW], [None, None], h,
+                                  wl.top_k, wl.norm_topk_prob, layers[0].ws[:1024])
