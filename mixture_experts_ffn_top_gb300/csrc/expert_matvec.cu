@@ -562,6 +562,9 @@ int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &set, bool is_
                           int32_t *dbg_dots, int dbg_block, unsigned *status, cudaStream_t s) {
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
+    if (matvec_ring_eligible(N, D, F, N, nexp, is_shared ? N : N * top_k, set.gate_m != nullptr, x_q, x_d, set))
+        return launch_matvec_ring_gate_up(set, D, F, nexp, is_shared, x_q, x_d, expStart, expTokI, N, top_k, h_q, h_d,
+                                          dbg_dots, dbg_block, status, s);
     switch (tmax_for(N)) {
     case 1:
         return gate_up_launch<1>(set, D, F, nexp, is_shared, x_q, x_d, expStart, expTokI, N, top_k, h_q, h_d,
@@ -584,6 +587,10 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &set, bool is_sha
                        unsigned *status, cudaStream_t s, bool early, int32_t *dbg_dots, int dbg_block) {
     const int D = w->D, F = set.F;
     const int nexp = is_shared ? 1 : w->E;
+    const int rows = is_shared ? N : N * top_k;
+    if (matvec_ring_eligible(N, F, D, rows, nexp, rows, set.down_m != nullptr, h_q, h_d, set))
+        return launch_matvec_ring_down(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,
+                                       shexp_scale, out, status, s, early, dbg_dots, dbg_block);
     switch (tmax_for(N)) {
     case 1:
         return down_launch<1>(set, D, F, nexp, is_shared, h_q, h_d, expStart, expTokI, expTokK, N, top_k,

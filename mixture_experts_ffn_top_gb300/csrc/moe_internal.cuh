@@ -171,6 +171,19 @@ int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const W
 int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
                      const int8_t *h_q, const float *h_d, cudaStream_t s);
 int prepare_tensor_maps(moe_weights_s *w);
+// matvec_ring.cu: the matvecs of batches of at most 8 tokens with the weight rows streamed through
+// a shared-memory ring; eligible when the batch's activation rows and two stages fit on chip,
+// K % 128 == 0 and every operand is 16-byte aligned.  Same arguments and results as launch_matvec_gate_up / launch_matvec_down.
+bool matvec_ring_eligible(int N, int K, int rows_e, int n_xrows, int nexp, int entries, bool mins, const void *xq,
+                          const void *xd, const WeightSet &set);
+int launch_matvec_ring_gate_up(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *x_q,
+                               const float *x_d, const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
+                               int8_t *h_q, float *h_d, int32_t *dbg_dots, int dbg_block, unsigned *status,
+                               cudaStream_t s);
+int launch_matvec_ring_down(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *h_q,
+                            const float *h_d, const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
+                            int N, int top_k, const float *shexp_scale, float *out, unsigned *status, cudaStream_t s,
+                            bool early, int32_t *dbg_dots, int dbg_block);
 
 void free_tensor_maps(moe_weights_s *w);
 
