@@ -194,14 +194,27 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     {
         int c = 0, before = 0;
         if (tid < E) {
-            if (G == 1)
+            if (G == 1) {
                 c = base[tid];
-            else
-                for (int j = 0; j < G; ++j) {
+            } else {
+                // the column of expert tid, eight loads in flight at a time
+                int j = 0;
+                for (; j + 8 <= G; j += 8) {
+                    int v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = __ldcg(a.cnt_g + (size_t)(j + u) * E + tid);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (j + u < b) before += v[u];
+                        c += v[u];
+                    }
+                }
+                for (; j < G; ++j) {
                     const int v = __ldcg(a.cnt_g + (size_t)j * E + tid);
                     if (j < b) before += v;
                     c += v;
                 }
+            }
         }
         __syncthreads();  // every count read before base[] is rewritten below
         const int pc = (c + SEG_ALIGN - 1) / SEG_ALIGN * SEG_ALIGN;

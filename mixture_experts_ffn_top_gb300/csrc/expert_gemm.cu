@@ -907,6 +907,18 @@ int launch_gemm(int mode, const moe_weights_s *w, int N, int top_k, bool with_sh
 
 bool tensor_path_supported(const moe_weights_s *w) { return w && w->tensor_ok && w->tmaps != nullptr; }
 
+bool encode_fp32_sw128_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int prepare_tensor_maps(moe_weights_s *w) {
     if (!encode_fn()) return MOE_OK;  // no driver entry point: the tensor path stays off
     WeightMaps *m = new WeightMaps();

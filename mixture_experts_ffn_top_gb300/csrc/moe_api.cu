@@ -266,7 +266,7 @@ int moe_router_topk(const float *hidden, const float *routerW, const float *shex
     if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
     float *part = ws_ptr<float>(ws, 256);
     return launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, topk_idx, topk_w,
-                         shexp_scale, x_q, x_d, logits_out, part, nsplit, stream);
+                         shexp_scale, x_q, x_d, logits_out, part, nsplit, stream, false, status_word(ws));
 }
 
 int moe_topk_from_logits(const float *logits, int N, int E, int top_k, int norm_topk_prob, int32_t *topk_idx,
@@ -483,7 +483,8 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
         mark(2);
     } else {
         rc = launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh, xq,
-                           xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream, early_router && ev == nullptr);
+                           xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream, early_router && ev == nullptr,
+                           status_word(ws));
         mark(1);
         if (!rc)
             rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr,

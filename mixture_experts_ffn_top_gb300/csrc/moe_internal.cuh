@@ -1,6 +1,7 @@
 // moe_internal.cuh -- shared declarations of the CUDA library (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -101,10 +102,20 @@ inline int plan_tile_rows(const moe_weights_s *) { return TILE_N; }
 
 // ----------------------------------------------------------- launchers --
 // router.cu
+// status (nullable): the workspace's status word; with it, batches the tensor-core router can take
+// (router_tc_eligible) run there (part_logits unused), without it on the fp32 SIMT router.
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
-                  cudaStream_t s, bool early = false);
+                  cudaStream_t s, bool early = false, unsigned *status = nullptr);
+// router_tc.cu: logits on the tensor cores (split tf32, three MMAs per K step) with the Q8_1 of x
+// and the per-token softmax / top-k in one cluster launch; E % 16 == 0, E (+16 with the shared
+// gate) <= 128, N > 8, 16-byte-aligned hidden / routerW / gate.
+bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden, const float *routerW,
+                        const float *shexp_gate);
+int launch_router_tc(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
+                     int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
+                     float *x_d, float *logits_out, unsigned *status, cudaStream_t s, bool early);
 int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,
                             float *w, cudaStream_t s);
 // early (both routers): launched to overlap the kernel before it, the previous layer's combine (see
@@ -171,6 +182,9 @@ int launch_h16_to_q8(const moe_weights_s *w, int N, int top_k, void *ws, const W
 int launch_q8_to_h16(const moe_weights_s *w, int N, int top_k, void *ws, const WsLayout &L,
                      const int8_t *h_q, const float *h_d, cudaStream_t s);
 int prepare_tensor_maps(moe_weights_s *w);
+// Tensor map of a row-major fp32 matrix [rows][cols] read in 128-byte-swizzled boxes of 32
+// columns x box_rows rows (false when the driver entry point or the encoding fails).
+bool encode_fp32_sw128_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 // matvec_ring.cu: the matvecs of batches of at most 8 tokens with the weight rows streamed through
 // a shared-memory ring; eligible when the batch's activation rows and two stages fit on chip,
 // K % 128 == 0 and every operand is 16-byte aligned.  Same arguments and results as launch_matvec_gate_up / launch_matvec_down.

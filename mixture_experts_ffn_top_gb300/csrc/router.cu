@@ -12,6 +12,7 @@
 //     fixed order, softmax over all E, top-k by repeated warp argmax (ties to
 //     the lower expert index), weights, sigmoid gate.
 #include "moe_internal.cuh"
+#include "topk_token.cuh"
 
 namespace moe {
 
@@ -214,90 +215,32 @@ router_small_kernel(const float *__restrict__ hidden, const float *__restrict__ 
     router_small_body(hidden, routerW, shexp_gate, N, D, E, Eext, logits, x_q, x_d);
 }
 
-// One warp per token.  EPL = experts per lane (power of two, EPL*32 >= E).
+// One warp per token: the split-K partials summed in split order (loads issued four at a time),
+// then route_token.  EPL = experts per lane (power of two, EPL*32 >= E).
 template <int EPL>
 __device__ __forceinline__ void softmax_topk_token(const float *__restrict__ part, int nsplit, int N, int E, int Eext,
                                                    int top_k, int norm, int t, int lane, int32_t *__restrict__ topk_idx,
                                                    float *__restrict__ topk_w, float *__restrict__ shexp_scale,
                                                    float *__restrict__ logits_out) {
-    float l[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        int e = lane + 32 * i;
-        float v = -INFINITY;
-        if (e < E) {
-            // the split partials summed in split order; loads issued four at a time
-            const float *pp = part + (size_t)t * Eext + e;
-            const size_t stride = (size_t)N * Eext;
-            v = __ldcg(pp);
-            int s = 1;
-            for (; s + 4 <= nsplit; s += 4) {
-                const float a0 = __ldcg(pp + s * stride), a1 = __ldcg(pp + (s + 1) * stride),
-                            a2 = __ldcg(pp + (s + 2) * stride), a3 = __ldcg(pp + (s + 3) * stride);
-                v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a0), a1), a2), a3);
-            }
-            for (; s < nsplit; ++s) v = __fadd_rn(v, __ldcg(pp + s * stride));
-            if (logits_out) logits_out[(size_t)t * E + e] = v;
+    const size_t stride = (size_t)N * Eext;
+    auto logit = [&](int e) {
+        const float *pp = part + (size_t)t * Eext + e;
+        float v = __ldcg(pp);
+        int s = 1;
+        for (; s + 4 <= nsplit; s += 4) {
+            const float a0 = __ldcg(pp + s * stride), a1 = __ldcg(pp + (s + 1) * stride),
+                        a2 = __ldcg(pp + (s + 2) * stride), a3 = __ldcg(pp + (s + 3) * stride);
+            v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a0), a1), a2), a3);
         }
-        l[i] = v;
-    }
-    if (shexp_scale != nullptr && lane == 0) {
+        for (; s < nsplit; ++s) v = __fadd_rn(v, __ldcg(pp + s * stride));
+        return v;
+    };
+    auto gate = [&]() {
         float g = __ldcg(part + (size_t)t * Eext + E);
         for (int s = 1; s < nsplit; ++s) g = __fadd_rn(g, __ldcg(part + ((size_t)s * N + t) * Eext + E));
-        shexp_scale[t] = __fdiv_rn(1.0f, 1.0f + expf(-g));
-    }
-    // softmax over all E experts
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) m = fmaxf(m, l[i]);
-    m = warp_max(m);
-    float p[EPL];
-    float z = 0.0f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        p[i] = (lane + 32 * i < E) ? expf(l[i] - m) : 0.0f;
-        z += p[i];
-    }
-    z = warp_sum(z);
-    // top-k (top_k <= 32): repeated warp argmax on the logits, ties to the lower index;
-    // lane s keeps slot s's probability
-    float psel_sum = 0.0f;
-    float my_w = 0.0f;
-    for (int s = 0; s < top_k; ++s) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
-            bool cand = e < E && p[i] >= 0.0f;  // p = -1 marks a taken expert
-            if (cand && (bi == 0x7fffffff || l[i] > bv || (l[i] == bv && e < bi))) {
-                bv = l[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        float pw = 0.0f;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (lane + 32 * i == bi) {
-                pw = __fdiv_rn(p[i], z);
-                p[i] = -1.0f;
-            }
-        pw = __shfl_sync(0xffffffffu, pw, bi & 31);
-        psel_sum = __fadd_rn(psel_sum, pw);
-        if (lane == s) my_w = pw;
-        if (lane == 0) topk_idx[(size_t)t * top_k + s] = bi;
-    }
-    if (lane < top_k)
-        topk_w[(size_t)t * top_k + lane] = norm ? __fdiv_rn(my_w, psel_sum) : my_w;
+        return g;
+    };
+    route_token<EPL>(logit, gate, E, top_k, norm, t, lane, topk_idx, topk_w, shexp_scale, logits_out);
 }
 
 // One warp per token.
@@ -465,8 +408,13 @@ int router_split_used(int N, int D, int E) { return (N <= RS_MAX_N && D % 4 == 0
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
-                  cudaStream_t s, bool early) {
+                  cudaStream_t s, bool early, unsigned *status) {
     int Eext = E + (shexp_gate ? 1 : 0);
+    if (status != nullptr && router_tc_eligible(N, D, E, shexp_gate != nullptr, hidden, routerW, shexp_gate)) {
+        const int rc = launch_router_tc(hidden, routerW, shexp_gate, N, D, E, top_k, norm, topk_idx, topk_w,
+                                        shexp_scale, x_q, x_d, logits_out, status, s, early);
+        if (rc != MOE_ERR_UNSUPPORTED_SHAPE) return rc;  // else: no room for the cluster, the SIMT router
+    }
     if (N <= RS_MAX_N && D % 4 == 0) {
         int rc = MOE_OK;
         if (early)

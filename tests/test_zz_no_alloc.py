@@ -30,6 +30,9 @@ def ops():
 
 @pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared"])
 def test_noalloc_router_matches_workspace_router(ops, name):
+    """The no-alloc router (always the fp32 SIMT kernels) against moe_router_topk, which takes the
+    tensor-core router where it applies (OLMoE): identical quantised activations, logits within the
+    router's tolerance, identical routing on tokens whose k-th / (k+1)-th logit gap is clear."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl)
     hidden = torch.from_numpy(inp["hidden"]).cuda()
@@ -41,14 +44,20 @@ def test_noalloc_router_matches_workspace_router(ops, name):
     for _ in range(2):  # the shared scratch keeps the previous call's contents
         got = ops.moe_router_topk_noalloc(hidden, routerW, shg, wl.top_k, wl.norm_topk_prob, want_logits=True)
         torch.cuda.synchronize()
-        np.testing.assert_allclose(got["logits"].cpu().numpy(), ref["logits"].cpu().numpy(), rtol=1e-6, atol=1e-6)
-        np.testing.assert_array_equal(got["topk_idx"].cpu().numpy(), ref["topk_idx"].cpu().numpy())
-        np.testing.assert_allclose(got["topk_w"].cpu().numpy(), ref["topk_w"].cpu().numpy(), rtol=1e-6, atol=1e-7)
+        lg, lr = got["logits"].cpu().numpy(), ref["logits"].cpu().numpy()
+        scale = np.maximum(np.abs(lr).max(axis=1), np.sqrt((lr ** 2).mean(axis=1)))
+        assert (np.abs(lg - lr).max(axis=1) <= 2e-4 * scale).all()
+        srt = np.sort(lr, axis=1)[:, ::-1]
+        clear = (srt[:, wl.top_k - 1] - srt[:, wl.top_k]) > 4e-4 * scale
+        assert clear.mean() > 0.9
+        np.testing.assert_array_equal(got["topk_idx"].cpu().numpy()[clear], ref["topk_idx"].cpu().numpy()[clear])
+        np.testing.assert_allclose(got["topk_w"].cpu().numpy()[clear], ref["topk_w"].cpu().numpy()[clear],
+                                   rtol=2e-4, atol=1e-6)
         np.testing.assert_array_equal(got["x_q"].cpu().numpy(), ref["x_q"].cpu().numpy())
         np.testing.assert_array_equal(got["x_d"].cpu().numpy(), ref["x_d"].cpu().numpy())
         if shg is not None:
             np.testing.assert_allclose(got["shexp_scale"].cpu().numpy(), ref["shexp_scale"].cpu().numpy(),
-                                       rtol=1e-6, atol=1e-7)
+                                       rtol=1e-4, atol=1e-6)
 
 
 def test_noalloc_router_refuses_oversized_problem(ops):
