@@ -55,14 +55,14 @@ __device__ __forceinline__ void route_token(Logit logit, Gate gate, int E, int t
         for (int j = 0; j < EPL; ++j) {
 #pragma unroll
             for (int src = 0; src < 32; ++src) {
+                // straight-line code (no branch between the shuffles), so they issue back to back;
+                // experts past E hold -inf and count for no one (eo < E masks them)
                 const float o = __shfl_sync(0xffffffffu, l[j], src);
                 const int eo = src + 32 * j;
-                if (eo < E) {
 #pragma unroll
-                    for (int i = 0; i < EPL; ++i) {
-                        const int e = lane + 32 * i;
-                        rank[i] += (o > l[i] || (o == l[i] && eo < e)) ? 1 : 0;
-                    }
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = lane + 32 * i;
+                    rank[i] += (int)((eo < E) & ((o > l[i]) | ((o == l[i]) & (eo < e))));
                 }
             }
         }
