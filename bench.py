@@ -260,13 +260,20 @@ def resolve_path(ops, w, wl, path):
     return ops.MOE_PATH_TENSOR if tensor else ops.MOE_PATH_MATVEC
 
 
+def router_launches(wl):
+    """Launches of the routing of a batch of more than SMALL_BATCH tokens: one on the tensor cores
+    (E a multiple of 16, E + 16 rows for a shared gate <= 128), else the SIMT logits and softmax."""
+    rows = wl.E + (16 if wl.Fs else 0)
+    return 1 if (wl.E % 16 == 0 and rows <= 128) else 2
+
+
 def launches_per_step(ops, wl, resolved_path):
     experts = 2 * (2 if wl.Fs else 1)  # matvec: gate/up and down, routed (and shared)
     if resolved_path == ops.MOE_PATH_TENSOR:
-        return 2 + 1 + 3 + 1  # router x2, bucketing(+plan), gather, gate/up, down, combine
+        return router_launches(wl) + 1 + 3 + 1  # router, bucketing(+plan), gather, gate/up, down, combine
     if wl.N <= SMALL_BATCH:
         return 1 + experts + 1  # routing in one launch, the expert matvecs, combine
-    return 2 + 1 + experts + 1
+    return router_launches(wl) + 1 + experts + 1
 
 
 def measure(ops, wl, inp, hidden, steps, warmup, path, device, flush, peaks, world=1):
@@ -523,9 +530,9 @@ def run_ours(args, rank, world, local_rank):
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, keyed by
 # (stage, workload), with the sha256 prefix of the kernel source the counters were taken on
-# (profiles/grouped_gemm_olmoe.md); reported only while the source is unchanged.
-TRAFFIC = {("gate_up", "olmoe"): (679.342080e6, "mixture_experts_ffn_top_gb300/csrc/expert_gemm.cu",
-                                  "3eab63c9dc15455b")}
+# (profiles/launches_olmoe_layer.md); reported only while the source is unchanged.
+TRAFFIC = {("gate_up", "olmoe"): (674.3e6, "mixture_experts_ffn_top_gb300/csrc/expert_gemm.cu",
+                                  "031c18b8eae26e1d")}
 
 
 def measured_traffic(stage, workload):
