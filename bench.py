@@ -262,9 +262,8 @@ def resolve_path(ops, w, wl, path):
 
 def router_launches(wl):
     """Launches of the routing of a batch of more than SMALL_BATCH tokens: one on the tensor cores
-    (E a multiple of 16, E + 16 rows for a shared gate <= 128), else the SIMT logits and softmax."""
-    rows = wl.E + (16 if wl.Fs else 0)
-    return 1 if (wl.E % 16 == 0 and rows <= 128) else 2
+    (E a multiple of 16, 16 <= E <= 256), else the SIMT logits and softmax."""
+    return 1 if (wl.E % 16 == 0 and 16 <= wl.E <= 256) else 2
 
 
 def launches_per_step(ops, wl, resolved_path):

@@ -109,8 +109,8 @@ int launch_router(const float *hidden, const float *routerW, const float *shexp_
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
                   cudaStream_t s, bool early = false, unsigned *status = nullptr);
 // router_tc.cu: logits on the tensor cores (split tf32, three MMAs per K step) with the Q8_1 of x
-// and the per-token softmax / top-k in one cluster launch; E % 16 == 0, E (+16 with the shared
-// gate) <= 128, N > 8, 16-byte-aligned hidden / routerW / gate.
+// and the per-token softmax / top-k in one cluster launch; E % 16 == 0, 16 <= E <= 256, N > 8,
+// 16-byte-aligned hidden / routerW / gate.
 bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden, const float *routerW,
                         const float *shexp_gate);
 int launch_router_tc(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,

@@ -3,27 +3,31 @@
 // ("Carnice prefill toward llama.cpp 676 t/s", #388: breakdown table "router" row -- matvec +
 // softmax + top-k + shexp-gate -- and "Remaining levers" item 1, which moves it onto the GPU).
 //
-// logits = hidden . [routerW; w_sg]^T is a dense fp32 contraction (N x D by D x (E + 1)).  The
-// tensor cores read fp32 operands as tf32 (10 explicit mantissa bits), so every operand x is split
-// into hi = x with its low 13 mantissa bits cleared and lo = (x - hi) cut the same way (x - hi is
-// exact in fp32), and each K step issues three kind::tf32 MMAs, hi*hi + hi*lo + lo*hi, into one
-// fp32 accumulator in tensor memory: every product is exact and the dropped lo*lo term and the
-// cut of lo are below 2^-20 of |x*w|, so the logits carry fp32-level error (the fp32 SIMT router's
-// within its tolerance of the oracle).
+// logits = hidden . routerW^T is a dense fp32 contraction (N x D by D x E).  The tensor cores read
+// fp32 operands as tf32 (10 explicit mantissa bits), so every operand x is split into hi = x with
+// its low 13 mantissa bits cleared and lo = (x - hi) cut the same way (x - hi is exact in fp32), and
+// each K step issues three kind::tf32 MMAs, hi*hi + hi*lo + lo*hi, into one fp32 accumulator in
+// tensor memory (N = E <= 256): every product is exact and the dropped lo*lo term and the cut of lo
+// are below 2^-20 of |x*w|, so the logits carry fp32-level error (the fp32 SIMT router's within
+// its tolerance of the oracle).  The shared gate g_t = x_t . w_sg (one more column) is formed on
+// the CUDA cores by the threads that already hold x_t's values (fp32 fused multiply-adds).
 //
 // Grid: one thread-block cluster of KS CTAs per 128-token tile; CTA r of a cluster takes the K
-// range [r, r + 1) * D / KS.  Per 32-wide K block the producer loads the token tile [128 x 32]
-// and the router tile [E x 32] (and the shared-gate row) by TMA; eight converter warps quantise the
-// token rows (each 32-wide row is one Q8_1 block: the same rule as the SIMT router, so x_q and x_d
-// are identical) and split both tiles into hi / lo in place; one thread issues the MMAs.  At the
-// end every CTA leaves its partial logits [128 x (E + 1)] in shared memory, the cluster meets at a
-// barrier, and CTA r sums the KS partials of its 128 / KS tokens in split order through
+// range [r, r + 1) * D / KS.  Per 32-wide K block the producer loads the token tile [128 x 32] and
+// the router tile [E x 32] by TMA into a ring as deep as shared memory allows (stages of 48-96 KB);
+// two groups of eight converter warps take alternate K blocks: they quantise the token rows (each
+// 32-wide row is one Q8_1 block: the same rule as the SIMT router, so x_q and x_d are identical),
+// accumulate the gate dot and split both tiles into hi / lo in place; one thread issues the MMAs.
+// At the end every CTA leaves its partial logits [128 x (E + 1)] in shared memory, the cluster
+// meets at a barrier, and CTA r sums the KS partials of its 128 / KS tokens in split order through
 // distributed shared memory and routes them (route_token, the SIMT router's arithmetic).  No
 // partial leaves the chip and no second launch is needed.
 //
 // Every mbarrier wait is bounded (MOE_DEV_TIMEOUT; every role then drains out, waits bounded for
 // its copies and MMAs, and still meets the cluster barriers, which every thread reaches).
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "moe_internal.cuh"
 #include "tc_glue.cuh"
@@ -36,27 +40,37 @@ namespace {
 using namespace tc;
 
 constexpr int RT_M = 128;                        // tokens per tile (MMA M)
-constexpr int RT_MAX_N = 128;                    // router rows per tile (E, or E + 16 with the gate)
-constexpr int RT_STAGES = 3;
+constexpr int RT_MAX_N = 256;                    // router rows (experts) per tile: the MMA's N
+constexpr int RT_MAX_STAGES = 6;
 constexpr int RT_CONV_WARPS = 8;                 // per converter group: two threads per tile row
 constexpr int RT_THREADS = 32 * (2 + 2 * RT_CONV_WARPS);  // warp 0 TMA, warp 1 MMA + TMEM, 2-17 convert
                                                           // (two groups, alternate K blocks; 2-5 drain), all route
 constexpr int RT_A = RT_M * 128;                 // token tile: 128 rows x 32 fp32
-constexpr int RT_B = RT_MAX_N * 128;             // router tile
-constexpr int RT_STAGE = 2 * RT_A + 2 * RT_B;    // hi and lo of both: 64 KB
-constexpr int RT_SMEM = 1024 + RT_STAGES * RT_STAGE;
-constexpr int RT_TMEM_COLS = 128;
+constexpr int RT_SMEM_MAX = 220 * 1024;          // dynamic shared memory of one CTA at most (the
+                                                 // static barriers and gate partials fit beside it)
+constexpr int RT_TMEM_COLS = 256;
 constexpr int RT_MAX_KS = 8;
 constexpr unsigned long long RT_WAIT_NS = 2000000000ull;
-static_assert(RT_SMEM <= 227 * 1024, "shared memory budget");
-static_assert((RT_M * (RT_MAX_N + 1) + 32 + RT_M * (RT_MAX_N + 1)) * 4 <= RT_STAGES * RT_STAGE,
-              "partials and the summed logits fit in the stage ring");
+// Shared memory of a launch: the stage ring (stage = token tile hi + lo, router tile hi + lo, as many
+// stages as fit, at most RT_MAX_STAGES), reused after the main loop for the partial logits
+// [128][E + 1] and the summed logits of this CTA's tokens [128 / KS][E + 1]; the gate slice of the
+// CTA's K range stays apart.
+__host__ __device__ constexpr int rt_stage_bytes(int E) { return 2 * RT_A + 2 * E * 128; }
+__host__ __device__ constexpr int rt_gate_bytes(int D) { return D * 4; }
+__host__ __device__ inline int rt_stages(int E, int D) {
+    const int s = (RT_SMEM_MAX - 1024 - rt_gate_bytes(D)) / rt_stage_bytes(E);
+    return s < RT_MAX_STAGES ? s : RT_MAX_STAGES;
+}
+__host__ __device__ inline int rt_tail_bytes(int E, int ks) {
+    return (RT_M * (E + 1) + 32 + (RT_M / ks) * (E + 1)) * 4;
+}
 
 struct RtMaps {
-    CUtensorMap x, w, g;  // hidden [N][D], routerW [E][D], shared gate [1][D] (boxes of 32 fp32)
+    CUtensorMap x, w;  // hidden [N][D], routerW [E][D] (boxes of 32 fp32)
 };
 struct RtParams {
-    int N, D, E, nmma, ks, kb_per, top_k, norm, has_gate;
+    int N, D, E, ks, kb_per, top_k, norm, has_gate, stages;
+    const float *gate_w;  // the shared gate vector [D] (has_gate)
     int8_t *x_q;
     float *x_d;
     int32_t *topk_idx;
@@ -138,10 +152,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ __align__(8) uint64_t full_bar[RT_STAGES], conv_bar[RT_STAGES], empty_bar[RT_STAGES];
+    __shared__ __align__(8) uint64_t full_bar[RT_MAX_STAGES], conv_bar[RT_MAX_STAGES], empty_bar[RT_MAX_STAGES];
     __shared__ __align__(8) uint64_t acc_bar, done_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
+    __shared__ float gpart[2][RT_M][2];  // the shared gate's partial dots: [group][row][half]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)cluster_rank();
@@ -149,10 +164,13 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     const int t0 = tile * RT_M;
     const int kb0 = rank * p.kb_per;
     const int nblk = p.D / QK;
-    const int nrow_b = p.E + (p.has_gate ? 1 : 0);  // router rows loaded per stage
+    const int S = p.stages;
+    const int SB = rt_stage_bytes(p.E);      // stage: [A hi][A lo][B hi][B lo]
+    const int B_BYTES = p.E * 128;
+    float *gw = reinterpret_cast<float *>(smem + S * SB);  // gate weights of this K range
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < RT_STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&conv_bar[s]), RT_CONV_WARPS);
             mbar_init(smem_u32(&empty_bar[s]), 1);
@@ -162,18 +180,12 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // router rows past the loaded ones (the gate's 15 padding rows) stay zero in every stage, hi and lo
-    for (int i = threadIdx.x; i < RT_STAGES * 2 * (p.nmma - nrow_b) * 8; i += RT_THREADS) {
-        const int per = (p.nmma - nrow_b) * 8;
-        const int s = i / (2 * per), h = (i / per) & 1, rc = i % per;
-        *reinterpret_cast<uint4 *>(smem + s * RT_STAGE + 2 * RT_A + h * RT_B + (nrow_b + rc / 8) * 128 +
-                                   (rc % 8) * 16) = make_uint4(0, 0, 0, 0);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // the shared gate's slice of this K range (a weight: it does not depend on the previous launch)
+    if (p.has_gate)
+        for (int i = threadIdx.x; i < p.kb_per * QK; i += RT_THREADS) gw[i] = p.gate_w[kb0 * QK + i];
     if (warp == 0 && lane == 0) {
         prefetch_map(&maps.x);
         prefetch_map(&maps.w);
-        if (p.has_gate) prefetch_map(&maps.g);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
@@ -191,28 +203,23 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
         if (lane == 0) {
             // the router rows of this K range beyond the ring's first fill do not depend on the
             // previous launch: ask L2 for them (hidden may be that launch's output: a chain of layers)
-            for (int i = RT_STAGES; i < p.kb_per; ++i) {
-                tma_prefetch_2d(&maps.w, (kb0 + i) * QK, 0);
-                if (p.has_gate) tma_prefetch_2d(&maps.g, (kb0 + i) * QK, 0);
-            }
+            for (int i = S; i < p.kb_per; ++i) tma_prefetch_2d(&maps.w, (kb0 + i) * QK, 0);
             asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t issued = 0, last_par = 0;
             for (int i = 0; i < p.kb_per; ++i) {
-                const int s = i % RT_STAGES;
-                if (i >= RT_STAGES &&
-                    !mbar_wait(smem_u32(&empty_bar[s]), ((i / RT_STAGES) - 1) & 1, &abort_flag, p.status, RT_WAIT_NS))
+                const int s = i % S;
+                if (i >= S && !mbar_wait(smem_u32(&empty_bar[s]), ((i / S) - 1) & 1, &abort_flag, p.status, RT_WAIT_NS))
                     break;
-                uint8_t *st = smem + s * RT_STAGE;
+                uint8_t *st = smem + s * SB;
                 const uint32_t fb = smem_u32(&full_bar[s]);
                 const int k0 = (kb0 + i) * QK;
-                mbar_expect_tx(fb, RT_A + nrow_b * 128);
+                mbar_expect_tx(fb, RT_A + B_BYTES);
                 tma_load_2d(smem_u32(st), &maps.x, k0, t0, fb);
                 tma_load_2d(smem_u32(st + 2 * RT_A), &maps.w, k0, 0, fb);
-                if (p.has_gate) tma_load_2d(smem_u32(st + 2 * RT_A + p.E * 128), &maps.g, k0, 0, fb);
                 issued |= 1u << s;
-                last_par = (last_par & ~(1u << s)) | ((uint32_t)((i / RT_STAGES) & 1) << s);
+                last_par = (last_par & ~(1u << s)) | ((uint32_t)((i / S) & 1) << s);
             }
-            for (int s = 0; s < RT_STAGES; ++s)
+            for (int s = 0; s < S; ++s)
                 if (issued >> s & 1) {
                     const uint64_t tw = globaltimer();
                     while (!mbar_try(smem_u32(&full_bar[s]), last_par >> s & 1) && globaltimer() - tw < RT_WAIT_NS) {
@@ -222,18 +229,18 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA ---
         if (lane == 0) {
-            const uint32_t idesc = idesc_tf32(p.nmma);
+            const uint32_t idesc = idesc_tf32(p.E);
             bool ok = true;
             int i = 0;
             for (; i < p.kb_per; ++i) {
-                const int s = i % RT_STAGES;
-                ok = mbar_wait(smem_u32(&conv_bar[s]), (i / RT_STAGES) & 1, &abort_flag, p.status, RT_WAIT_NS);
+                const int s = i % S;
+                ok = mbar_wait(smem_u32(&conv_bar[s]), (i / S) & 1, &abort_flag, p.status, RT_WAIT_NS);
                 if (!ok) break;
                 tc_fence_after();
                 // descriptors of the four tiles; K step k starts 32 bytes further (2 in the
                 // descriptor's 16-byte address field)
-                const uint64_t ah = smem_desc_sw128(smem_u32(smem + s * RT_STAGE));
-                const uint64_t al = ah + (RT_A >> 4), bh = ah + ((2 * RT_A) >> 4), bl = bh + (RT_B >> 4);
+                const uint64_t ah = smem_desc_sw128(smem_u32(smem + s * SB));
+                const uint64_t al = ah + (RT_A >> 4), bh = ah + ((2 * RT_A) >> 4), bl = bh + (B_BYTES >> 4);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {  // K = 8 tf32 (32 bytes) per MMA
                     mma_tf32(tmem, ah + 2 * k, bh + 2 * k, idesc, (i | k) != 0);
@@ -253,20 +260,21 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     } else {
         // ------------------------------------------------- convert, then drain ---
         // two groups of eight warps take alternate K blocks; in a group, two threads per tile row:
-        // thread (r, h) takes the 16-byte chunks 4h .. 4h + 3 of token row r and of router row r
-        // (when r < E + gate)
+        // thread (r, h) takes the 16-byte chunks 4h .. 4h + 3 of token row r (its Q8_1, its hi / lo
+        // split, and its shared-gate dot on the CUDA cores) and of router rows r and r + 128 (< E)
         const int grp = (warp - 2) / RT_CONV_WARPS;
         const int ci = threadIdx.x - 64 - grp * RT_CONV_WARPS * 32;
         const int r = ci >> 1, h = ci & 1;
         const int t = t0 + r;
         const int sw = r & 7;  // 128-byte swizzle: chunk j of row r sits at chunk j ^ (r % 8)
+        float gacc = 0.0f;     // shared-gate dot of this row's half over this group's K blocks
         bool ok = true;
         for (int i = grp; i < p.kb_per; i += 2) {
-            const int s = i % RT_STAGES;
-            ok = mbar_wait(smem_u32(&full_bar[s]), (i / RT_STAGES) & 1, &abort_flag, p.status, RT_WAIT_NS);
+            const int s = i % S;
+            ok = mbar_wait(smem_u32(&full_bar[s]), (i / S) & 1, &abort_flag, p.status, RT_WAIT_NS);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            uint8_t *st = smem + s * RT_STAGE;
+            uint8_t *st = smem + s * SB;
             uint32_t qw[4];
             float d16;
             {
@@ -291,14 +299,27 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                             ((uint32_t)(q3 & 0xff) << 24);
                 }
                 d16 = __half2float(__float2half_rn(d));
+                if (p.has_gate) {
+                    // K positions 16h .. 16h + 15 of this block, in order
+                    const float *g = gw + i * QK + 16 * h;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        gacc = fmaf(v[j].x, g[4 * j + 0], gacc);
+                        gacc = fmaf(v[j].y, g[4 * j + 1], gacc);
+                        gacc = fmaf(v[j].z, g[4 * j + 2], gacc);
+                        gacc = fmaf(v[j].w, g[4 * j + 3], gacc);
+                    }
+                }
                 split_half(row, st + RT_A + r * 128, v, sw, h);
             }
-            if (r < nrow_b) {
-                uint8_t *row = st + 2 * RT_A + r * 128;
+#pragma unroll
+            for (int rb = r; rb < r + RT_M + 1; rb += RT_M) {  // router rows r and r + 128
+                if (rb >= p.E) break;
+                uint8_t *row = st + 2 * RT_A + rb * 128;
                 float4 v[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const float4 *>(row + (((4 * h + j) ^ sw) << 4));
-                split_half(row, st + 2 * RT_A + RT_B + r * 128, v, sw, h);
+                split_half(row, st + 2 * RT_A + B_BYTES + rb * 128, v, sw, h);
             }
             // the tensor core reads these through the async proxy
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -312,7 +333,9 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                 if (h == 0) p.x_d[(size_t)t * nblk + kb] = d16;
             }
         }
-        // partial logits of this K range: warps 2-5, one TMEM lane quarter each -> shared [128][nmma + 1]
+        gpart[grp][r][h] = gacc;
+        // partial logits of this K range: warps 2-5, one TMEM lane quarter each -> shared [128][E + 1],
+        // column E the shared gate's partial (the four partial dots of the row in a fixed order)
         if (warp < 6) {
             if (ok) ok = mbar_wait(smem_u32(&acc_bar), 0, &abort_flag, p.status, RT_WAIT_NS);
             ok = __all_sync(0xffffffffu, ok) && !abort_flag;
@@ -321,15 +344,21 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                 const int q = warp & 3;
                 const int rr = q * 32 + lane;
                 float *P = reinterpret_cast<float *>(smem);
-                for (int c0 = 0; c0 < p.nmma; c0 += 16) {
+                for (int c0 = 0; c0 < p.E; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) P[rr * (p.nmma + 1) + c0 + j] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) P[rr * (p.E + 1) + c0 + j] = __uint_as_float(v[j]);
                 }
             }
         }
+    }
+    __syncthreads();  // the gate partials of both groups are in place
+    if (warp >= 2 && warp < 6 && p.has_gate && !abort_flag) {
+        const int rr = (warp & 3) * 32 + lane;
+        reinterpret_cast<float *>(smem)[rr * (p.E + 1) + p.E] =
+            __fadd_rn(__fadd_rn(gpart[0][rr][0], gpart[0][rr][1]), __fadd_rn(gpart[1][rr][0], gpart[1][rr][1]));
     }
     tc_fence_before();
     __syncthreads();
@@ -340,8 +369,8 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     // token routes from there
     const int per = RT_M / p.ks;
     const int ext = p.E + (p.has_gate ? 1 : 0);
-    const int stride = p.nmma + 1;
-    float *S = reinterpret_cast<float *>(smem) + ((RT_M * stride + 31) & ~31);  // [per][ext]
+    const int stride = p.E + 1;
+    float *Lsum = reinterpret_cast<float *>(smem) + ((RT_M * stride + 31) & ~31);  // [per][ext]
     if (!abort_flag) {
         const uint32_t pbase = smem_u32(smem);
         for (int i = threadIdx.x; i < per * ext; i += RT_THREADS) {
@@ -354,7 +383,7 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
 #pragma unroll
             for (int q = 1; q < RT_MAX_KS; ++q)
                 if (q < p.ks) v = __fadd_rn(v, part[q]);
-            S[i] = v;
+            Lsum[i] = v;
         }
     }
     __syncthreads();
@@ -362,7 +391,7 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
         for (int tl = warp; tl < per; tl += RT_THREADS / 32) {
             const int t = t0 + rank * per + tl;
             if (t >= p.N) break;
-            const float *row = S + tl * ext;
+            const float *row = Lsum + tl * ext;
             auto logit = [&](int e) { return row[e]; };
             auto gate = [&]() { return row[p.E]; };
             route_token<EPL>(logit, gate, p.E, p.top_k, p.norm, t, lane, p.topk_idx, p.topk_w,
@@ -393,7 +422,7 @@ int pick_ks(int tiles, int D) {
             cudaLaunchConfig_t q{};
             q.gridDim = dim3(ks, 1);
             q.blockDim = dim3(RT_THREADS);
-            q.dynamicSmemBytes = RT_SMEM;
+            q.dynamicSmemBytes = RT_SMEM_MAX;  // every launch's size or less
             cudaLaunchAttribute ca[1];
             ca[0].id = cudaLaunchAttributeClusterDimension;
             ca[0].val.clusterDim.x = ks;
@@ -418,14 +447,18 @@ int pick_ks(int tiles, int D) {
 template <int EPL>
 int launch_tc(const RtMaps &maps, RtParams p, int tiles, cudaStream_t s, bool early) {
     static SmemOptIn configured;
-    if (int rc = ensure_dynamic_smem((const void *)router_tc_kernel<EPL>, RT_SMEM, &configured)) return rc;
+    if (int rc = ensure_dynamic_smem((const void *)router_tc_kernel<EPL>, RT_SMEM_MAX, &configured)) return rc;
     p.ks = pick_ks<EPL>(tiles, p.D);
     if (p.ks == 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     p.kb_per = p.D / QK / p.ks;
+    p.stages = rt_stages(p.E, p.D);
+    const size_t ring = (size_t)p.stages * rt_stage_bytes(p.E) + rt_gate_bytes(p.D);
+    const size_t smem = 1024 + std::max(ring, (size_t)rt_tail_bytes(p.E, p.ks));
+    if (p.stages < 2 || smem > (size_t)RT_SMEM_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ks, tiles);
     cfg.blockDim = dim3(RT_THREADS);
-    cfg.dynamicSmemBytes = RT_SMEM;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -443,23 +476,21 @@ int launch_tc(const RtMaps &maps, RtParams p, int tiles, cudaStream_t s, bool ea
 
 bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden, const float *routerW,
                         const float *shexp_gate) {
-    const int nmma = E + (has_gate ? 16 : 0);
     const uintptr_t al = reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(routerW) |
                          (has_gate ? reinterpret_cast<uintptr_t>(shexp_gate) : 0);
-    return N > 8 && E % 16 == 0 && E >= 16 && nmma <= RT_MAX_N && D % QK == 0 && al % 16 == 0;
+    return N > 8 && E % 16 == 0 && E >= 16 && E <= RT_MAX_N && D % QK == 0 && al % 16 == 0 && rt_stages(E, D) >= 2;
 }
 
 int launch_router_tc(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
-                            int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
-                            int8_t *x_q, float *x_d, float *logits_out, unsigned *status, cudaStream_t s,
-                            bool early) {
+                     int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
+                     float *x_d, float *logits_out, unsigned *status, cudaStream_t s, bool early) {
     RtMaps maps;
     RtParams p{};
     p.N = N;
     p.D = D;
     p.E = E;
     p.has_gate = shexp_gate != nullptr;
-    p.nmma = E + (p.has_gate ? 16 : 0);
+    p.gate_w = shexp_gate;
     p.top_k = top_k;
     p.norm = norm;
     p.x_q = x_q;
@@ -471,15 +502,11 @@ int launch_router_tc(const float *hidden, const float *routerW, const float *she
     p.status = status;
     if (!encode_fp32_sw128_2d(&maps.x, hidden, N, D, RT_M) || !encode_fp32_sw128_2d(&maps.w, routerW, E, D, E))
         return MOE_ERR_CUDA;
-    if (p.has_gate) {
-        if (!encode_fp32_sw128_2d(&maps.g, shexp_gate, 1, D, 1)) return MOE_ERR_CUDA;
-    } else {
-        maps.g = maps.w;
-    }
     const int tiles = (N + RT_M - 1) / RT_M;
     if (E <= 32) return launch_tc<1>(maps, p, tiles, s, early);
     if (E <= 64) return launch_tc<2>(maps, p, tiles, s, early);
-    return launch_tc<4>(maps, p, tiles, s, early);
+    if (E <= 128) return launch_tc<4>(maps, p, tiles, s, early);
+    return launch_tc<8>(maps, p, tiles, s, early);
 }
 
 }  // namespace moe
