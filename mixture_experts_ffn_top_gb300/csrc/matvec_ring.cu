@@ -242,43 +242,40 @@ __device__ __forceinline__ void consume_stage(const RingArgs &a, const uint8_t *
     }
 }
 
-template <int MODE, bool DBG>
-__global__ void __launch_bounds__(RG_THREADS, 2)
-matvec_ring_kernel(const RingArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full_bar[RG_MAX_STAGES], empty_bar[RG_MAX_STAGES];
-    __shared__ int warp_cnt[RG_CW];
-    __shared__ int n_pairs;
-    __shared__ int item_done[RG_HBUF];
-    __shared__ __align__(8) uint64_t x_bar;  // the staged activation rows have landed
-    __shared__ volatile int abort_flag;
-
+// The bulk copies of stage s of a work item whose first weight row is erow: gate/up 8 gate + 8 up
+// rows (with scales, Q4_K mins), down 16 rows, completing on the mbarrier fb.
+template <int MODE>
+__device__ __forceinline__ void issue_stage(const RingArgs &a, size_t erow, int s, uint32_t dst, uint32_t fb) {
     const int K = a.K, nblk = K / QK;
-    const int S = a.stages;
-    uint8_t *ring = smem;
-    int8_t *xs = reinterpret_cast<int8_t *>(smem + (size_t)S * a.stage_bytes);
-    float *xds = reinterpret_cast<float *>(xs + (size_t)a.n_xrows * K);
-    float *hbuf = xds + (size_t)a.n_xrows * nblk;        // [RG_HBUF][RG_CHUNK][32]
-    int *act = reinterpret_cast<int *>(hbuf + RG_HBUF * RG_CHUNK * QK);               // [pairs_max]
-    int4 *slot_tab = reinterpret_cast<int4 *>(act + ((a.pairs_max + 3) & ~3));         // [pairs_max][8]
-    int *pair_cnt = reinterpret_cast<int *>(slot_tab + (size_t)a.pairs_max * RG_CHUNK);  // [pairs_max]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // the launch that follows (down after gate/up, the combine after down) may be scheduled now:
-    // it waits on the device for this one's output before reading it
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), RG_CW);
+    const bool mins = a.m0 != nullptr;
+    const uint32_t sbytes = (uint32_t)(nblk * 4);
+    if (MODE == 0) {
+        const size_t r0 = erow + (size_t)s * 8;
+        const uint32_t qb = (uint32_t)(8 * K), db = 8 * sbytes;
+        mbar_expect_tx(fb, 2 * qb + 2 * db * (mins ? 2 : 1));
+        bulk_load(dst, a.q0 + r0 * K, qb, fb);
+        bulk_load(dst + qb, a.q1 + r0 * K, qb, fb);
+        bulk_load(dst + 2 * qb, a.d0 + r0 * nblk, db, fb);
+        bulk_load(dst + 2 * qb + db, a.d1 + r0 * nblk, db, fb);
+        if (mins) {
+            bulk_load(dst + 2 * qb + 2 * db, a.m0 + r0 * nblk, db, fb);
+            bulk_load(dst + 2 * qb + 3 * db, a.m1 + r0 * nblk, db, fb);
         }
-        mbar_init(smem_u32(&x_bar), 1);
-        for (int i = 0; i < RG_HBUF; ++i) item_done[i] = 0;
-        abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    } else {
+        const size_t r0 = erow + (size_t)s * 16;
+        const uint32_t qb = (uint32_t)(16 * K), db = 16 * sbytes;
+        mbar_expect_tx(fb, qb + db * (mins ? 2 : 1));
+        bulk_load(dst, a.q0 + r0 * K, qb, fb);
+        bulk_load(dst + qb, a.d0 + r0 * nblk, db, fb);
+        if (mins) bulk_load(dst + qb + db, a.m0 + r0 * nblk, db, fb);
     }
-    // work list: (expert, chunk of 8 CSR entries) for every non-empty segment; the expert list
-    // comes from a launch before the previous one, so it is complete without the dependency wait
+}
+
+// Work list: (expert, chunk of 8 CSR entries) for every non-empty segment, in act[] (count in
+// *n_pairs); the expert list comes from a launch before the previous one, so it is complete without
+// the dependency wait.  Whole CTA (the consumer threads count the experts).
+__device__ __forceinline__ void build_work_list(const RingArgs &a, int *act, int *warp_cnt, int *n_pairs) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     {
         int base = 0;
         const int ct = threadIdx.x - 32;  // consumer threads count the experts
@@ -317,9 +314,101 @@ matvec_ring_kernel(const RingArgs a) {
         }
         if (threadIdx.x == 0) {
             if (base > a.pairs_max) atomicOr(a.status, MOE_DEV_BAD_CSR);  // overlapping segments
-            n_pairs = min(base, a.pairs_max);
+            *n_pairs = min(base, a.pairs_max);
         }
     }
+}
+
+// One work item of a consumer warp: its stages from the ring (stage counter k over the CTA's run),
+// then on gate/up the requantisation by the warp that completes the item.  Returns false when a
+// wait gave up.
+template <int MODE, bool DBG>
+__device__ __forceinline__ bool consume_item(const RingArgs &a, int it, int ii, int &k, int S, int slot_bytes,
+                                             const uint8_t *ring, uint64_t *full_bar, uint64_t *empty_bar,
+                                             volatile int *abort_flag, const int4 *slot_tab, const int *pair_cnt,
+                                             int *item_done, const int8_t *xs, const float *xds, float *hbuf, int cw,
+                                             int lane) {
+    const int nob = a.rows_e / QK;
+    const int spi = MODE == 0 ? QK / 8 : QK / 16;  // stages per item
+    const int ob = it % nob;
+    const Slot sl = load_slot(slot_tab, pair_cnt, it / nob, lane);
+    const int T = sl.cnt <= 1 ? 1 : sl.cnt <= 2 ? 2 : sl.cnt <= 4 ? 4 : 8;
+    float *hb = hbuf + (ii % RG_HBUF) * RG_CHUNK * QK;
+    for (int s = 0; s < spi; ++s, ++k) {
+        const int slot = k % S;
+        bool ok = mbar_wait(smem_u32(&full_bar[slot]), (k / S) & 1, abort_flag, a.status, RG_WAIT_NS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        const uint8_t *st = ring + (size_t)slot * slot_bytes;
+        if (T == 1) consume_stage<MODE, 1, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        else if (T == 2) consume_stage<MODE, 2, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        else if (T == 4) consume_stage<MODE, 4, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        else consume_stage<MODE, 8, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        __syncwarp();
+        if (MODE == 0 && s == spi - 1) {
+            // the warp that completes the item requantises its 32 features per slot (the buffer is
+            // reused three items later, after every warp has moved past this one)
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&item_done[ii % RG_HBUF], 1) == RG_CW - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence_block();
+                if (lane == 0) item_done[ii % RG_HBUF] = 0;
+                for (int tt = 0; tt < sl.cnt; ++tt) {
+                    float d16f;
+                    const int q = q8_quantize_lane(hb[tt * QK + lane], &d16f);
+                    const int j = __shfl_sync(0xffffffffu, sl.ent, tt);
+                    if (j >= 0) {
+                        a.h_q[(size_t)j * a.rows_e + ob * QK + lane] = (int8_t)q;
+                        if (lane == 0) a.h_d[(size_t)j * (a.rows_e / QK) + ob] = d16f;
+                    }
+                }
+            }
+        }
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+    }
+    return true;
+}
+
+template <int MODE, bool DBG>
+__global__ void __launch_bounds__(RG_THREADS, 2)
+matvec_ring_kernel(const RingArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[RG_MAX_STAGES], empty_bar[RG_MAX_STAGES];
+    __shared__ int warp_cnt[RG_CW];
+    __shared__ int n_pairs;
+    __shared__ int item_done[RG_HBUF];
+    __shared__ __align__(8) uint64_t x_bar;  // the staged activation rows have landed
+    __shared__ volatile int abort_flag;
+
+    const int K = a.K, nblk = K / QK;
+    const int S = a.stages;
+    uint8_t *ring = smem;
+    int8_t *xs = reinterpret_cast<int8_t *>(smem + (size_t)S * a.stage_bytes);
+    float *xds = reinterpret_cast<float *>(xs + (size_t)a.n_xrows * K);
+    float *hbuf = xds + (size_t)a.n_xrows * nblk;        // [RG_HBUF][RG_CHUNK][32]
+    int *act = reinterpret_cast<int *>(hbuf + RG_HBUF * RG_CHUNK * QK);               // [pairs_max]
+    int4 *slot_tab = reinterpret_cast<int4 *>(act + ((a.pairs_max + 3) & ~3));         // [pairs_max][8]
+    int *pair_cnt = reinterpret_cast<int *>(slot_tab + (size_t)a.pairs_max * RG_CHUNK);  // [pairs_max]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the launch that follows (down after gate/up, the combine after down) may be scheduled now:
+    // it waits on the device for this one's output before reading it
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), RG_CW);
+        }
+        mbar_init(smem_u32(&x_bar), 1);
+        for (int i = 0; i < RG_HBUF; ++i) item_done[i] = 0;
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    build_work_list(a, act, warp_cnt, &n_pairs);
     __syncthreads();
     const int nob = a.rows_e / QK;                    // 32-row output blocks per expert
     const int spi = MODE == 0 ? QK / 8 : QK / 16;     // stages per item
@@ -331,7 +420,6 @@ matvec_ring_kernel(const RingArgs a) {
             uint32_t issued = 0, last_par = 0;
             int k = 0;
             bool ok = true, staged = false;
-            const bool mins = a.m0 != nullptr;
             // the batch's activation rows, once the ring is full: for the down launch they are the
             // previous launch's output, so the weights stream first
             auto stage_x = [&]() {
@@ -353,29 +441,8 @@ matvec_ring_kernel(const RingArgs a) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full_bar[slot]);
-                    const uint32_t dst = smem_u32(ring + (size_t)slot * a.stage_bytes);
-                    const uint32_t sbytes = (uint32_t)(nblk * 4);
-                    if (MODE == 0) {
-                        const size_t r0 = erow + (size_t)s * 8;
-                        const uint32_t qb = (uint32_t)(8 * K), db = 8 * sbytes;
-                        mbar_expect_tx(fb, 2 * qb + 2 * db * (mins ? 2 : 1));
-                        bulk_load(dst, a.q0 + r0 * K, qb, fb);
-                        bulk_load(dst + qb, a.q1 + r0 * K, qb, fb);
-                        bulk_load(dst + 2 * qb, a.d0 + r0 * nblk, db, fb);
-                        bulk_load(dst + 2 * qb + db, a.d1 + r0 * nblk, db, fb);
-                        if (mins) {
-                            bulk_load(dst + 2 * qb + 2 * db, a.m0 + r0 * nblk, db, fb);
-                            bulk_load(dst + 2 * qb + 3 * db, a.m1 + r0 * nblk, db, fb);
-                        }
-                    } else {
-                        const size_t r0 = erow + (size_t)s * 16;
-                        const uint32_t qb = (uint32_t)(16 * K), db = 16 * sbytes;
-                        mbar_expect_tx(fb, qb + db * (mins ? 2 : 1));
-                        bulk_load(dst, a.q0 + r0 * K, qb, fb);
-                        bulk_load(dst + qb, a.d0 + r0 * nblk, db, fb);
-                        if (mins) bulk_load(dst + qb + db, a.m0 + r0 * nblk, db, fb);
-                    }
+                    issue_stage<MODE>(a, erow, s, smem_u32(ring + (size_t)slot * a.stage_bytes),
+                                      smem_u32(&full_bar[slot]));
                     issued |= 1u << slot;
                     last_par = (last_par & ~(1u << slot)) | ((uint32_t)((k / S) & 1) << slot);
                 }
@@ -415,51 +482,13 @@ matvec_ring_kernel(const RingArgs a) {
             ok = mbar_wait(smem_u32(&x_bar), 0, &abort_flag, a.status, RG_WAIT_NS);
             ok = __all_sync(0xffffffffu, ok);
         }
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ii) {
-            const int ob = it % nob;
-            const Slot sl = load_slot(slot_tab, pair_cnt, it / nob, lane);
-            const int T = sl.cnt <= 1 ? 1 : sl.cnt <= 2 ? 2 : sl.cnt <= 4 ? 4 : 8;
-            float *hb = hbuf + (ii % RG_HBUF) * RG_CHUNK * QK;
-            for (int s = 0; s < spi; ++s, ++k) {
-                const int slot = k % S;
-                ok = mbar_wait(smem_u32(&full_bar[slot]), (k / S) & 1, &abort_flag, a.status, RG_WAIT_NS);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                const uint8_t *st = ring + (size_t)slot * a.stage_bytes;
-                if (T == 1) consume_stage<MODE, 1, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-                else if (T == 2) consume_stage<MODE, 2, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-                else if (T == 4) consume_stage<MODE, 4, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-                else consume_stage<MODE, 8, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-                __syncwarp();
-                if (MODE == 0 && s == spi - 1) {
-                    // the warp that completes the item requantises its 32 features per slot (the
-                    // buffer is reused three items later, after every warp has moved past this one)
-                    int last = 0;
-                    if (lane == 0) {
-                        __threadfence_block();
-                        last = atomicAdd(&item_done[ii % RG_HBUF], 1) == RG_CW - 1;
-                    }
-                    last = __shfl_sync(0xffffffffu, last, 0);
-                    if (last) {
-                        __threadfence_block();
-                        if (lane == 0) item_done[ii % RG_HBUF] = 0;
-                        for (int tt = 0; tt < sl.cnt; ++tt) {
-                            float d16f;
-                            const int q = q8_quantize_lane(hb[tt * QK + lane], &d16f);
-                            const int j = __shfl_sync(0xffffffffu, sl.ent, tt);
-                            if (j >= 0) {
-                                a.h_q[(size_t)j * a.rows_e + ob * QK + lane] = (int8_t)q;
-                                if (lane == 0) a.h_d[(size_t)j * (a.rows_e / QK) + ob] = d16f;
-                            }
-                        }
-                    }
-                }
-                if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-            }
-        }
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ii)
+            ok = consume_item<MODE, DBG>(a, it, ii, k, S, a.stage_bytes, ring, full_bar, empty_bar, &abort_flag,
+                                         slot_tab, pair_cnt, item_done, xs, xds, hbuf, cw, lane);
     }
     __syncthreads();
 }
+
 
 }  // namespace
 
@@ -593,5 +622,6 @@ int launch_matvec_ring_down(const WeightSet &set, int D, int F, int nexp, bool i
     return dbg_dots ? run_ring<1, true>(a, pl, pl.pairs_max * (D / QK), s, early)
                     : run_ring<1, false>(a, pl, pl.pairs_max * (D / QK), s, early);
 }
+
 
 }  // namespace moe
