@@ -97,6 +97,8 @@ struct BucketArgs {
     int chunk;    // tokens staged at a time (256, 512 or 1024)
     unsigned long long barrier_ns;  // limit of the grid barrier's wait
     int extra_arrivals;  // failure-detection check: arrivals the barrier waits for beyond the grid (0 normally)
+    int counts_ready;    // the count table (and zero bad flags) already written by the router launch, whose
+                         // 128-token tiles are these ranges: no histogram pass, no grid barrier
 };
 
 __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a, const PlanOut po) {
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
         return (int)wpre[e * B_WORDS + B_WORDS - 1] + __popc(bm[e * B_WORDS + B_WORDS - 1]);
     };
     // 1. histogram of this range
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = 0; c < nchunks && !a.counts_ready; ++c) {
         build(r0 + c * a.chunk, true);
         for (int e = warp; e < E; e += B_THREADS / 32)
             if (lane == 0) base[e] += chunk_count(e);
@@ -164,7 +166,9 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     }
     // 2. all ranges counted (a single range needs neither the count table nor the barrier)
     int bad = 0;
-    if (G > 1) {
+    if (a.counts_ready) {
+        __syncthreads();
+    } else if (G > 1) {
         for (int e = tid; e < E; e += B_THREADS) a.cnt_g[(size_t)b * E + e] = base[e];
         if (tid == 0) a.bad_g[b] = (int)*flag;
         if (!grid_barrier(a.bar_count, a.bar_gen, (unsigned)(G + a.extra_arrivals), a.status, a.barrier_ns)) return;
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     {
         int c = 0, before = 0;
         if (tid < E) {
-            if (G == 1) {
+            if (G == 1 && !a.counts_ready) {
                 c = base[tid];
             } else {
                 // the column of expert tid, eight loads in flight at a time
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
     // of e in this chunk) + (earlier bits of its word) -- ascending in t
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = r0 + c * a.chunk;
-        if (nchunks > 1) build(t0, false);  // a single chunk is still in place from the count pass
+        if (nchunks > 1 || a.counts_ready) build(t0, false);  // a single chunk stays in place from the count pass
         // one warp per expert; lane r writes the expert's r-th entry of the chunk, so the
         // CSR and row-map stores of a warp go to consecutive addresses
         for (int e = warp; e < E; e += B_THREADS / 32) {
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(B_THREADS, 1) bucket_kernel(const BucketArgs a
                     if (my[s] == e) slot = s;
                 const int t = t0 + tl;
                 const int pos = eb + r;
+                if (pos >= total) continue;  // a count table that disagrees with the routing
                 a.expTokI[pos] = t;
                 a.expTokK[pos] = slot;
                 if (plan) {
@@ -358,7 +363,7 @@ size_t bucket_scratch_bytes(int N, int E) {
 
 int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart, int32_t *expTokI,
                   int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L, bool with_shared, int tile_rows,
-                  unsigned long long barrier_ns, int extra_arrivals) {
+                  unsigned long long barrier_ns, int extra_arrivals, bool counts_ready) {
     if (tile_rows < SEG_ALIGN || tile_rows % SEG_ALIGN) return MOE_ERR_INVALID_ARG;
     if (barrier_ns == 0) barrier_ns = B_BARRIER_NS;
     if (barrier_ns < B_BARRIER_NS_MIN || extra_arrivals < 0) return MOE_ERR_INVALID_ARG;
@@ -393,7 +398,8 @@ int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *exp
     a.chunk = chunk;
     a.barrier_ns = barrier_ns;
     a.extra_arrivals = extra_arrivals;
-    if (extra_arrivals > 0 && G == 1) return MOE_ERR_UNSUPPORTED_SHAPE;  // no grid barrier to hold up
+    a.counts_ready = counts_ready ? 1 : 0;
+    if (extra_arrivals > 0 && (G == 1 || counts_ready)) return MOE_ERR_UNSUPPORTED_SHAPE;  // no grid barrier
     PlanOut po{};
     po.tile_n = tile_rows;
     if (L != nullptr) {
@@ -405,8 +411,8 @@ int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *exp
         po.rows_max = L->rows_max;
         po.tiles_max = L->tiles_max;
     }
-    if (G == 1) {  // one range: no grid barrier, so no cooperative launch either
-        bucket_kernel<<<1, B_THREADS, smem, s>>>(a, po);
+    if (G == 1 || counts_ready) {  // no grid barrier, so no cooperative launch either
+        bucket_kernel<<<G, B_THREADS, smem, s>>>(a, po);
         return launch_status();
     }
     void *args[] = {(void *)&a, (void *)&po};

@@ -482,13 +482,21 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
         mark(1);
         mark(2);
     } else {
+        // when the bucketing's token ranges are the tensor-core router's 128-token tiles, the
+        // router also writes the bucketing's count table (its scratch, unused by that router)
+        int range = 0;
+        const int G = bucket_grid(N, E, &range);
+        int *tile_counts = (range == 128 && (size_t)G * (E + 1) * 4 <= bucket_scratch_bytes(N, E))
+                               ? reinterpret_cast<int *>(static_cast<char *>(ws) + BUCKET_SCRATCH_OFFSET)
+                               : nullptr;
+        bool counted = false;
         rc = launch_router(hidden, routerW, shexp_gate, N, D, E, top_k, norm_topk_prob ? 1 : 0, idx, tw, sh, xq,
                            xd, nullptr, ws_ptr<float>(ws, L.part_logits), L.nsplit, stream, early_router && ev == nullptr,
-                           status_word(ws));
+                           status_word(ws), tile_counts, &counted);
         mark(1);
         if (!rc)
             rc = launch_bucket(idx, N, top_k, E, es, ti, tk, ws, stream, tensor ? &L : nullptr, shout != nullptr,
-                               plan_tile_rows(w));
+                               plan_tile_rows(w), 0, 0, counted);
         mark(2);
     }
     if (tensor) {

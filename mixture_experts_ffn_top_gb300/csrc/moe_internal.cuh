@@ -104,10 +104,13 @@ inline int plan_tile_rows(const moe_weights_s *) { return TILE_N; }
 // router.cu
 // status (nullable): the workspace's status word; with it, batches the tensor-core router can take
 // (router_tc_eligible) run there (part_logits unused), without it on the fp32 SIMT router.
+// tile_counts (nullable; with status): ask the tensor-core router for the bucketing kernel's count
+// table of 128-token ranges; *counted tells whether it wrote it.
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
-                  cudaStream_t s, bool early = false, unsigned *status = nullptr);
+                  cudaStream_t s, bool early = false, unsigned *status = nullptr, int *tile_counts = nullptr,
+                  bool *counted = nullptr);
 // router_tc.cu: logits on the tensor cores (split tf32, three MMAs per K step) with the Q8_1 of x
 // and the per-token softmax / top-k in one cluster launch; E % 16 == 0, 16 <= E <= 256, N > 8,
 // 16-byte-aligned hidden / routerW / gate.
@@ -115,7 +118,8 @@ bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden,
                         const float *shexp_gate);
 int launch_router_tc(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
                      int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
-                     float *x_d, float *logits_out, unsigned *status, cudaStream_t s, bool early);
+                     float *x_d, float *logits_out, unsigned *status, cudaStream_t s, bool early,
+                     int *tile_counts = nullptr);
 int launch_topk_from_logits(const float *logits, int N, int E, int top_k, int norm, int32_t *idx,
                             float *w, cudaStream_t s);
 // early (both routers): launched to overlap the kernel before it, the previous layer's combine (see
@@ -141,7 +145,8 @@ int bucket_grid(int N, int E, int *range_out);
 size_t bucket_scratch_bytes(int N, int E);
 int launch_bucket(const int32_t *topk_idx, int N, int top_k, int E, int32_t *expStart, int32_t *expTokI,
                   int32_t *expTokK, void *ws, cudaStream_t s, const WsLayout *L = nullptr, bool with_shared = false,
-                  int tile_rows = TILE_N, unsigned long long barrier_ns = 0, int extra_arrivals = 0);
+                  int tile_rows = TILE_N, unsigned long long barrier_ns = 0, int extra_arrivals = 0,
+                  bool counts_ready = false);
 // expert_matvec.cu
 int launch_matvec_gate_up(const moe_weights_s *w, const WeightSet &ws, bool is_shared,
                           const int8_t *x_q, const float *x_d, const int32_t *expStart,

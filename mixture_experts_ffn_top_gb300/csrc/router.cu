@@ -408,11 +408,13 @@ int router_split_used(int N, int D, int E) { return (N <= RS_MAX_N && D % 4 == 0
 int launch_router(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D,
                   int E, int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale,
                   int8_t *x_q, float *x_d, float *logits_out, float *part_logits, int nsplit,
-                  cudaStream_t s, bool early, unsigned *status) {
+                  cudaStream_t s, bool early, unsigned *status, int *tile_counts, bool *counted) {
     int Eext = E + (shexp_gate ? 1 : 0);
+    if (counted) *counted = false;
     if (status != nullptr && router_tc_eligible(N, D, E, shexp_gate != nullptr, hidden, routerW, shexp_gate)) {
         const int rc = launch_router_tc(hidden, routerW, shexp_gate, N, D, E, top_k, norm, topk_idx, topk_w,
-                                        shexp_scale, x_q, x_d, logits_out, status, s, early);
+                                        shexp_scale, x_q, x_d, logits_out, status, s, early, tile_counts);
+        if (rc == MOE_OK && counted) *counted = tile_counts != nullptr;
         if (rc != MOE_ERR_UNSUPPORTED_SHAPE) return rc;  // else: no room for the cluster, the SIMT router
     }
     if (N <= RS_MAX_N && D % 4 == 0) {

@@ -62,7 +62,7 @@ __host__ __device__ inline int rt_stages(int E, int D) {
     return s < RT_MAX_STAGES ? s : RT_MAX_STAGES;
 }
 __host__ __device__ inline int rt_tail_bytes(int E, int ks) {
-    return (RT_M * (E + 1) + 32 + (RT_M / ks) * (E + 1)) * 4;
+    return (RT_M * (E + 1) + 32 + (RT_M / ks) * (E + 1) + 32 + E) * 4;
 }
 
 struct RtMaps {
@@ -71,6 +71,8 @@ struct RtMaps {
 struct RtParams {
     int N, D, E, ks, kb_per, top_k, norm, has_gate, stages;
     const float *gate_w;  // the shared gate vector [D] (has_gate)
+    int *tile_counts;     // nullable: per token tile, how many of its routing entries chose each expert
+                          // ([tiles][E], then [tiles] zero flags: the bucketing kernel's count table)
     int8_t *x_q;
     float *x_d;
     int32_t *topk_idx;
@@ -398,7 +400,32 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                              p.has_gate ? p.shexp_scale : nullptr, p.logits_out);
         }
     }
-    cluster_sync();  // no CTA leaves while another still reads its partials
+    if (p.tile_counts != nullptr) {
+        // this tile's expert histogram (the bucketing kernel's count table row): every CTA counts
+        // the entries of its own tokens, CTA 0 of the cluster adds the KS counts
+        int *hist = reinterpret_cast<int *>(Lsum + ((per * ext + 31) & ~31));
+        for (int e = threadIdx.x; e < p.E; e += RT_THREADS) hist[e] = 0;
+        __syncthreads();  // the routing's stores (this CTA's) are visible to it past the barrier
+        const int tb = t0 + rank * per, te = min(p.N, tb + per);
+        for (int i = threadIdx.x; i < (te - tb) * p.top_k; i += RT_THREADS) {
+            const int e = p.topk_idx[(size_t)tb * p.top_k + i];
+            if ((unsigned)e < (unsigned)p.E) atomicAdd(&hist[e], 1);
+        }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its partials (or its counts)
+    if (p.tile_counts != nullptr) {
+        if (rank == 0) {
+            int *hist = reinterpret_cast<int *>(Lsum + ((per * ext + 31) & ~31));
+            const uint32_t hb = smem_u32(hist);
+            for (int e = threadIdx.x; e < p.E; e += RT_THREADS) {
+                int c = 0;
+                for (int q = 0; q < p.ks; ++q) c += __float_as_int(ld_cluster(hb + 4 * e, q));
+                p.tile_counts[(size_t)tile * p.E + e] = c;
+            }
+            if (threadIdx.x == 0) p.tile_counts[(size_t)gridDim.y * p.E + tile] = 0;  // no bad entries
+        }
+        cluster_sync();  // CTA 0 has read every CTA's counts
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(RT_TMEM_COLS)
@@ -483,7 +510,7 @@ bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden,
 
 int launch_router_tc(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
                      int top_k, int norm, int32_t *topk_idx, float *topk_w, float *shexp_scale, int8_t *x_q,
-                     float *x_d, float *logits_out, unsigned *status, cudaStream_t s, bool early) {
+                     float *x_d, float *logits_out, unsigned *status, cudaStream_t s, bool early, int *tile_counts) {
     RtMaps maps;
     RtParams p{};
     p.N = N;
@@ -500,6 +527,7 @@ int launch_router_tc(const float *hidden, const float *routerW, const float *she
     p.shexp_scale = shexp_scale;
     p.logits_out = logits_out;
     p.status = status;
+    p.tile_counts = tile_counts;
     if (!encode_fp32_sw128_2d(&maps.x, hidden, N, D, RT_M) || !encode_fp32_sw128_2d(&maps.w, routerW, E, D, E))
         return MOE_ERR_CUDA;
     const int tiles = (N + RT_M - 1) / RT_M;
