@@ -537,6 +537,25 @@ def test_layer_routing_state(ops, name, path):
     np.testing.assert_array_equal(v["expStart"].cpu().numpy(), es1)
 
 
+@pytest.mark.parametrize("name", ["olmoe", "qwen3moe_shared", "skewed", "tiny"])
+def test_layer_csr_equals_bucketing_of_its_routing(ops, name):
+    """The CSR a tensor-path layer call leaves (for these shapes the router writes the bucketing's
+    count table and the bucketing runs without its histogram pass): bit-exact against the oracle's
+    counting sort of the routing the same call produced (integer work, every token)."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    layer.prefill(dev(inp["hidden"]), wl.top_k, wl.norm_topk_prob, path=2)
+    assert layer.status() == 0
+    v = layer.views(wl.N)
+    idx = v["topk_idx"].cpu().numpy().astype(np.int32)
+    es, ti, tk = O.bucket(idx, wl.E)
+    total = int(es[-1])
+    assert total == wl.N * wl.top_k
+    np.testing.assert_array_equal(v["expStart"].cpu().numpy(), es)
+    np.testing.assert_array_equal(v["expTokI"].cpu().numpy()[:total], ti)
+    np.testing.assert_array_equal(v["expTokK"].cpu().numpy()[:total], tk)
+
+
 def _random_layer(N, D, E, k, F, Fs, norm, seed):
     wl = Workload(f"rand{seed}", N=N, D=D, E=E, top_k=k, F=F, Fs=Fs, norm_topk_prob=norm, seed=seed)
     return wl, make_inputs(wl)
