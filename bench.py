@@ -249,7 +249,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-CONFIG_WORKLOADS = ["tiny", "decode_n1", "decode_n4", "decode_n8", "qwen3moe_shared", "skewed"]
+CONFIG_WORKLOADS = ["tiny", "decode_n1", "decode_n4", "decode_n8", "decode_n8_q4k", "qwen3moe_shared", "skewed"]
 
 
 def resolve_path(ops, w, wl, path):

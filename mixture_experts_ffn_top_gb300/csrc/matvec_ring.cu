@@ -21,6 +21,10 @@
 // item last requantises its 32 features per token (Q8_1).  down: unweighted partial rows to
 // t * top_k + slot, or s_t * y for the shared expert.
 //
+// Q4_K weights stream in their nibble-packed copy (16 bytes per 32-block, byte j = q[j] | q[j+16] << 4):
+// half the quant bytes; each lane unpacks its block into the same two 16-code halves, so the int32
+// dots, and with them the results, are the same bits.
+//
 // Every wait is bounded (MOE_DEV_TIMEOUT, then every role drains out; the producer waits, bounded,
 // for its copies in flight before the CTA exits).
 #include "moe_internal.cuh"
@@ -74,10 +78,11 @@ __device__ __forceinline__ int dp4a4(int4 a, int4 b) {
     return __dp4a(a.w, b.w, s);
 }
 
-// Per-lane dots of two weight rows (quants w0/w1 [K], scales s0/s1 [K/32], mins n0/n1 or NULL)
-// with T staged activation rows tok[0..T-1] (xs [rows][K], xds [rows][K/32]); returns the
-// warp-reduced sums in every lane.  DBG: the lane owning block dbg_block keeps its isums in dbg.
-template <int T, bool DBG>
+// Per-lane dots of two weight rows (quants w0/w1 [K], or [K/2] nibble-packed with PK; scales s0/s1
+// [K/32], mins n0/n1 or NULL) with T staged activation rows tok[0..T-1] (xs [rows][K], xds
+// [rows][K/32]); returns the warp-reduced sums in every lane.  DBG: the lane owning block
+// dbg_block keeps its isums in dbg.
+template <int T, bool DBG, bool PK>
 __device__ __forceinline__ void ring_dot(const int8_t *w0, const int8_t *w1, const float *s0, const float *s1,
                                          const float *n0, const float *n1, int K, const int8_t *xs, const float *xds,
                                          const int (&tok)[T], int lane, float (&acc)[2][T], int dbg_block,
@@ -92,8 +97,28 @@ __device__ __forceinline__ void ring_dot(const int8_t *w0, const int8_t *w1, con
     const int h = (lane >> 2) & 1;
 #pragma unroll UNR
     for (int b = lane; b < nblk; b += 32) {
-        const int4 *p0 = reinterpret_cast<const int4 *>(w0 + b * QK), *p1 = reinterpret_cast<const int4 *>(w1 + b * QK);
-        const int4 q0a = p0[h], q0b = p0[h ^ 1], q1a = p1[h], q1b = p1[h ^ 1];
+        int4 q0a, q0b, q1a, q1b;  // codes of the halves h and h ^ 1 of the block
+        if (PK) {
+            // one 16-byte load per row: low nibbles are codes 0-15, high nibbles codes 16-31
+            const int4 v0 = reinterpret_cast<const int4 *>(w0)[b], v1 = reinterpret_cast<const int4 *>(w1)[b];
+            const int4 l0 = make_int4(v0.x & 0x0F0F0F0F, v0.y & 0x0F0F0F0F, v0.z & 0x0F0F0F0F, v0.w & 0x0F0F0F0F);
+            const int4 u0 = make_int4((v0.x >> 4) & 0x0F0F0F0F, (v0.y >> 4) & 0x0F0F0F0F, (v0.z >> 4) & 0x0F0F0F0F,
+                                      (v0.w >> 4) & 0x0F0F0F0F);
+            const int4 l1 = make_int4(v1.x & 0x0F0F0F0F, v1.y & 0x0F0F0F0F, v1.z & 0x0F0F0F0F, v1.w & 0x0F0F0F0F);
+            const int4 u1 = make_int4((v1.x >> 4) & 0x0F0F0F0F, (v1.y >> 4) & 0x0F0F0F0F, (v1.z >> 4) & 0x0F0F0F0F,
+                                      (v1.w >> 4) & 0x0F0F0F0F);
+            q0a = h ? u0 : l0;
+            q0b = h ? l0 : u0;
+            q1a = h ? u1 : l1;
+            q1b = h ? l1 : u1;
+        } else {
+            const int4 *p0 = reinterpret_cast<const int4 *>(w0 + b * QK),
+                       *p1 = reinterpret_cast<const int4 *>(w1 + b * QK);
+            q0a = p0[h];
+            q0b = p0[h ^ 1];
+            q1a = p1[h];
+            q1b = p1[h ^ 1];
+        }
         const float sc0 = s0[b], sc1 = s1[b];
         const float mn0 = mins ? n0[b] : 0.0f, mn1 = mins ? n1[b] : 0.0f;
 #pragma unroll
@@ -178,16 +203,17 @@ __device__ __forceinline__ Slot load_slot(const int4 *slot_tab, const int *pair_
 }
 
 // One stage of one consumer warp: rows cw and cw + 8 of the stage against the item's T slots.
-template <int MODE, int T, bool DBG>
+template <int MODE, int T, bool DBG, bool PK>
 __device__ __forceinline__ void consume_stage(const RingArgs &a, const uint8_t *st, int cw, int lane, int ob, int s,
                                               const Slot &sl, const int8_t *xs, const float *xds, float *hbuf) {
     const int K = a.K, nblk = K / QK;
     const bool mins = a.m0 != nullptr;
-    // stage: rows [16 x K] (gate/up: 8 gate rows then 8 up rows), scales [16 x nblk], mins [16 x nblk];
-    // this warp's rows are cw and cw + 8
-    const int8_t *w0 = reinterpret_cast<const int8_t *>(st) + (size_t)cw * K;
-    const int8_t *w1 = w0 + (size_t)8 * K;
-    const float *sc = reinterpret_cast<const float *>(st + (size_t)16 * K);
+    // stage: rows [16 x rb] (gate/up: 8 gate rows then 8 up rows; rb = K, or K/2 packed), scales
+    // [16 x nblk], mins [16 x nblk]; this warp's rows are cw and cw + 8
+    const int rb = PK ? K / 2 : K;
+    const int8_t *w0 = reinterpret_cast<const int8_t *>(st) + (size_t)cw * rb;
+    const int8_t *w1 = w0 + (size_t)8 * rb;
+    const float *sc = reinterpret_cast<const float *>(st + (size_t)16 * rb);
     const float *s0 = sc + cw * nblk, *s1 = s0 + 8 * nblk;
     const float *n0 = mins ? s0 + 16 * nblk : nullptr, *n1 = mins ? s1 + 16 * nblk : nullptr;
     int tok[T];
@@ -195,7 +221,7 @@ __device__ __forceinline__ void consume_stage(const RingArgs &a, const uint8_t *
     for (int tt = 0; tt < T; ++tt) tok[tt] = __shfl_sync(0xffffffffu, sl.row, tt);
     float acc[2][T];
     int dbg[2][T];
-    ring_dot<T, DBG>(w0, w1, s0, s1, n0, n1, K, xs, xds, tok, lane, acc, a.dbg_block, dbg);
+    ring_dot<T, DBG, PK>(w0, w1, s0, s1, n0, n1, K, xs, xds, tok, lane, acc, a.dbg_block, dbg);
     // slot tt's values go out through lane tt (which holds the slot's rows)
     float v0 = 0.0f, v1 = 0.0f;
     int d0 = 0, d1 = 0;
@@ -243,10 +269,12 @@ __device__ __forceinline__ void consume_stage(const RingArgs &a, const uint8_t *
 }
 
 // The bulk copies of stage s of a work item whose first weight row is erow: gate/up 8 gate + 8 up
-// rows (with scales, Q4_K mins), down 16 rows, completing on the mbarrier fb.
-template <int MODE>
+// rows (with scales, Q4_K mins), down 16 rows, completing on the mbarrier fb.  PK: rows of K/2
+// packed bytes.
+template <int MODE, bool PK>
 __device__ __forceinline__ void issue_stage(const RingArgs &a, size_t erow, int s, uint32_t dst, uint32_t fb) {
-    const int K = a.K, nblk = K / QK;
+    const int nblk = a.K / QK;
+    const int K = PK ? a.K / 2 : a.K;  // bytes per weight row
     const bool mins = a.m0 != nullptr;
     const uint32_t sbytes = (uint32_t)(nblk * 4);
     if (MODE == 0) {
@@ -322,7 +350,7 @@ __device__ __forceinline__ void build_work_list(const RingArgs &a, int *act, int
 // One work item of a consumer warp: its stages from the ring (stage counter k over the CTA's run),
 // then on gate/up the requantisation by the warp that completes the item.  Returns false when a
 // wait gave up.
-template <int MODE, bool DBG>
+template <int MODE, bool DBG, bool PK>
 __device__ __forceinline__ bool consume_item(const RingArgs &a, int it, int ii, int &k, int S, int slot_bytes,
                                              const uint8_t *ring, uint64_t *full_bar, uint64_t *empty_bar,
                                              volatile int *abort_flag, const int4 *slot_tab, const int *pair_cnt,
@@ -340,10 +368,10 @@ __device__ __forceinline__ bool consume_item(const RingArgs &a, int it, int ii, 
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) return false;
         const uint8_t *st = ring + (size_t)slot * slot_bytes;
-        if (T == 1) consume_stage<MODE, 1, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-        else if (T == 2) consume_stage<MODE, 2, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-        else if (T == 4) consume_stage<MODE, 4, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
-        else consume_stage<MODE, 8, DBG>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        if (T == 1) consume_stage<MODE, 1, DBG, PK>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        else if (T == 2) consume_stage<MODE, 2, DBG, PK>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        else if (T == 4) consume_stage<MODE, 4, DBG, PK>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
+        else consume_stage<MODE, 8, DBG, PK>(a, st, cw, lane, ob, s, sl, xs, xds, hb);
         __syncwarp();
         if (MODE == 0 && s == spi - 1) {
             // the warp that completes the item requantises its 32 features per slot (the buffer is
@@ -373,7 +401,7 @@ __device__ __forceinline__ bool consume_item(const RingArgs &a, int it, int ii, 
     return true;
 }
 
-template <int MODE, bool DBG>
+template <int MODE, bool DBG, bool PK>
 __global__ void __launch_bounds__(RG_THREADS, 2)
 matvec_ring_kernel(const RingArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -441,7 +469,7 @@ matvec_ring_kernel(const RingArgs a) {
                         ok = false;
                         break;
                     }
-                    issue_stage<MODE>(a, erow, s, smem_u32(ring + (size_t)slot * a.stage_bytes),
+                    issue_stage<MODE, PK>(a, erow, s, smem_u32(ring + (size_t)slot * a.stage_bytes),
                                       smem_u32(&full_bar[slot]));
                     issued |= 1u << slot;
                     last_par = (last_par & ~(1u << slot)) | ((uint32_t)((k / S) & 1) << slot);
@@ -483,7 +511,7 @@ matvec_ring_kernel(const RingArgs a) {
             ok = __all_sync(0xffffffffu, ok);
         }
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ii)
-            ok = consume_item<MODE, DBG>(a, it, ii, k, S, a.stage_bytes, ring, full_bar, empty_bar, &abort_flag,
+            ok = consume_item<MODE, DBG, PK>(a, it, ii, k, S, a.stage_bytes, ring, full_bar, empty_bar, &abort_flag,
                                          slot_tab, pair_cnt, item_done, xs, xds, hbuf, cw, lane);
     }
     __syncthreads();
@@ -500,12 +528,12 @@ struct RingPlan {
     int stages, stage_bytes, pairs_max;
     size_t smem;
 };
-static RingPlan ring_plan(int mode, int K, int rows_e, int n_xrows, int nexp, int entries, bool mins) {
+static RingPlan ring_plan(int mode, int K, int rows_e, int n_xrows, int nexp, int entries, bool mins, bool pk) {
     RingPlan p{};
     if (K % 128 != 0 || rows_e % QK != 0 || nexp >= (1 << RG_PAIR_SHIFT)) return p;
     const int nblk = K / QK;
     const int srows = mode == 0 ? 16 : 16;  // rows per stage (gate/up: 8 of each matrix)
-    p.stage_bytes = srows * K + srows * nblk * 4 * (mins ? 2 : 1);
+    p.stage_bytes = srows * (pk ? K / 2 : K) + srows * nblk * 4 * (mins ? 2 : 1);
     p.pairs_max = nexp + (entries + RG_CHUNK - 1) / RG_CHUNK;
     const size_t fixed = (size_t)n_xrows * K + (size_t)n_xrows * nblk * 4 + RG_HBUF * RG_CHUNK * QK * 4 +
                          (size_t)((p.pairs_max + 3) & ~3) * 4 + (size_t)p.pairs_max * (RG_CHUNK * 16 + 4) + 128;
@@ -527,37 +555,48 @@ static int ring_grid(const void *kernel, size_t smem, int max_items) {
     return std::max(1, std::min(n * per_sm, max_items));
 }
 
-template <int MODE, bool DBG>
-static int run_ring(const RingArgs &a, const RingPlan &pl, int max_items, cudaStream_t s, bool early) {
+template <int MODE, bool DBG, bool PK>
+static int run_ring_k(const RingArgs &a, const RingPlan &pl, int max_items, cudaStream_t s, bool early) {
     static SmemOptIn configured;
-    if (int rc = ensure_dynamic_smem((const void *)matvec_ring_kernel<MODE, DBG>, pl.smem, &configured)) return rc;
-    const int grid = ring_grid((const void *)matvec_ring_kernel<MODE, DBG>, pl.smem, max_items);
+    const void *k = (const void *)matvec_ring_kernel<MODE, DBG, PK>;
+    if (int rc = ensure_dynamic_smem(k, pl.smem, &configured)) return rc;
+    const int grid = ring_grid(k, pl.smem, max_items);
     if (grid < 0) return MOE_ERR_CUDA;
-    if (early) return launch_early(matvec_ring_kernel<MODE, DBG>, dim3(grid), dim3(RG_THREADS), pl.smem, s, a);
-    matvec_ring_kernel<MODE, DBG><<<grid, RG_THREADS, pl.smem, s>>>(a);
+    if (early) return launch_early(matvec_ring_kernel<MODE, DBG, PK>, dim3(grid), dim3(RG_THREADS), pl.smem, s, a);
+    matvec_ring_kernel<MODE, DBG, PK><<<grid, RG_THREADS, pl.smem, s>>>(a);
     return launch_status();
+}
+
+template <int MODE>
+static int run_ring(const RingArgs &a, const RingPlan &pl, int max_items, cudaStream_t s, bool early, bool dbg,
+                    bool pk) {
+    if (pk)
+        return dbg ? run_ring_k<MODE, true, true>(a, pl, max_items, s, early)
+                   : run_ring_k<MODE, false, true>(a, pl, max_items, s, early);
+    return dbg ? run_ring_k<MODE, true, false>(a, pl, max_items, s, early)
+               : run_ring_k<MODE, false, false>(a, pl, max_items, s, early);
 }
 
 bool matvec_ring_eligible(int N, int K, int rows_e, int n_xrows, int nexp, int entries, bool mins, const void *xq,
                           const void *xd, const WeightSet &set) {
     // bulk copies: 16-byte aligned addresses (the spans' sizes are multiples of 16 once K % 128 == 0)
     const void *ptrs[] = {xq, xd, set.gate_q, set.up_q, set.down_q, set.gate_d, set.up_d, set.down_d,
-                          set.gate_m, set.up_m, set.down_m};
+                          set.gate_m, set.up_m, set.down_m, set.gate_p, set.up_p, set.down_p};
     for (const void *q : ptrs)
         if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return false;
-    return N <= RG_CHUNK && ring_plan(0, K, rows_e, n_xrows, nexp, entries, mins).ok;
+    return N <= RG_CHUNK && ring_plan(0, K, rows_e, n_xrows, nexp, entries, mins, set.gate_p != nullptr).ok;
 }
 
 int launch_matvec_ring_gate_up(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *x_q,
                                const float *x_d, const int32_t *expStart, const int32_t *expTokI, int N, int top_k,
                                int8_t *h_q, float *h_d, int32_t *dbg_dots, int dbg_block, unsigned *status,
                                cudaStream_t s) {
-    const bool mins = set.gate_m != nullptr;
-    const RingPlan pl = ring_plan(0, D, F, N, nexp, is_shared ? N : N * top_k, mins);
+    const bool mins = set.gate_m != nullptr, pk = set.gate_p != nullptr;
+    const RingPlan pl = ring_plan(0, D, F, N, nexp, is_shared ? N : N * top_k, mins, pk);
     if (!pl.ok) return MOE_ERR_UNSUPPORTED_SHAPE;
     RingArgs a{};
-    a.q0 = set.gate_q;
-    a.q1 = set.up_q;
+    a.q0 = pk ? reinterpret_cast<const int8_t *>(set.gate_p) : set.gate_q;
+    a.q1 = pk ? reinterpret_cast<const int8_t *>(set.up_p) : set.up_q;
     a.d0 = set.gate_d;
     a.d1 = set.up_d;
     a.m0 = set.gate_m;
@@ -582,20 +621,19 @@ int launch_matvec_ring_gate_up(const WeightSet &set, int D, int F, int nexp, boo
     a.stages = pl.stages;
     a.stage_bytes = pl.stage_bytes;
     a.pairs_max = pl.pairs_max;
-    return dbg_dots ? run_ring<0, true>(a, pl, pl.pairs_max * (F / QK), s, false)
-                    : run_ring<0, false>(a, pl, pl.pairs_max * (F / QK), s, false);
+    return run_ring<0>(a, pl, pl.pairs_max * (F / QK), s, false, dbg_dots != nullptr, pk);
 }
 
 int launch_matvec_ring_down(const WeightSet &set, int D, int F, int nexp, bool is_shared, const int8_t *h_q,
                             const float *h_d, const int32_t *expStart, const int32_t *expTokI, const int32_t *expTokK,
                             int N, int top_k, const float *shexp_scale, float *out, unsigned *status, cudaStream_t s,
                             bool early, int32_t *dbg_dots, int dbg_block) {
-    const bool mins = set.down_m != nullptr;
+    const bool mins = set.down_m != nullptr, pk = set.down_p != nullptr;
     const int rows = is_shared ? N : N * top_k;
-    const RingPlan pl = ring_plan(1, F, D, rows, nexp, rows, mins);
+    const RingPlan pl = ring_plan(1, F, D, rows, nexp, rows, mins, pk);
     if (!pl.ok) return MOE_ERR_UNSUPPORTED_SHAPE;
     RingArgs a{};
-    a.q0 = set.down_q;
+    a.q0 = pk ? reinterpret_cast<const int8_t *>(set.down_p) : set.down_q;
     a.d0 = set.down_d;
     a.m0 = set.down_m;
     a.K = F;
@@ -619,8 +657,7 @@ int launch_matvec_ring_down(const WeightSet &set, int D, int F, int nexp, bool i
     a.stages = pl.stages;
     a.stage_bytes = pl.stage_bytes;
     a.pairs_max = pl.pairs_max;
-    return dbg_dots ? run_ring<1, true>(a, pl, pl.pairs_max * (D / QK), s, early)
-                    : run_ring<1, false>(a, pl, pl.pairs_max * (D / QK), s, early);
+    return run_ring<1>(a, pl, pl.pairs_max * (D / QK), s, early, dbg_dots != nullptr, pk);
 }
 
 

@@ -33,6 +33,10 @@ struct WeightSet {
     float *down_d = nullptr;                    // [nexp][D][F/32]
     // Q4_K only: per-32-block mins dmin*m (the weight is d*sc*q - dmin*m, quants 0..15 above)
     float *gate_m = nullptr, *up_m = nullptr, *down_m = nullptr;  // same shapes as the scales
+    // Q4_K only: the quants packed two per byte, 16 bytes per 32-block: byte j of a block holds
+    // q[j] in its low and q[j + 16] in its high nibble (the decode ring's stream: half the bytes)
+    uint8_t *gate_p = nullptr, *up_p = nullptr;  // [nexp][F][D/2]
+    uint8_t *down_p = nullptr;                   // [nexp][D][F/2]
     // tensor path: exact fp16 integers in tile-interleaved order + transposed scales
     __half *gu16 = nullptr;   // [nexp][2F][D]: 128-row tile mt = 64 gate rows then 64 up rows
     float *gu_dT = nullptr;   // [nexp][D/32][2F] (same row order)

@@ -91,7 +91,7 @@ __global__ void repack_kernel(const uint8_t *__restrict__ src, int nmat, int row
 __global__ void repack_q4k_kernel(const uint8_t *__restrict__ src, int nmat, int rows, int nblk,
                                   int8_t *__restrict__ q, float *__restrict__ d, float *__restrict__ mn,
                                   __half *__restrict__ h16, float *__restrict__ dT, float *__restrict__ mT,
-                                  int interleave_gu, int up_half) {
+                                  int interleave_gu, int up_half, uint8_t *__restrict__ packed) {
     const int64_t total = (int64_t)nmat * rows * nblk;
     const int64_t row_bytes = (int64_t)(nblk / 8) * Q4_K_BYTES;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -120,6 +120,12 @@ __global__ void repack_q4k_kernel(const uint8_t *__restrict__ src, int nmat, int
         for (int l = 0; l < QK; ++l) vals[l] = (int8_t)((j & 1) ? (qs[l] >> 4) : (qs[l] & 15));
         store_block(vals, scale, mr, b, m, r, rows, nblk, q, d, h16, dT, interleave_gu, up_half);
         if (q != nullptr) mn[mr * nblk + b] = minv;
+        if (packed != nullptr) {  // byte l: q[l] low nibble, q[l + 16] high nibble
+            alignas(16) uint8_t pk[16];
+#pragma unroll
+            for (int l = 0; l < 16; ++l) pk[l] = (uint8_t)(vals[l] | (vals[l + 16] << 4));
+            *reinterpret_cast<int4 *>(packed + (mr * nblk + b) * 16) = *reinterpret_cast<const int4 *>(pk);
+        }
         if (h16 != nullptr) mT[dT_index(m, b, r, rows, nblk, interleave_gu, up_half)] = minv;
     }
 }
@@ -171,7 +177,7 @@ __global__ void repack_q3k_kernel(const uint8_t *__restrict__ src, int nmat, int
 }
 
 int repack(int wfmt, const void *src, int nmat, int rows, int K, int8_t *q, float *d, float *mn, __half *h16,
-           float *dT, float *mT, int interleave, int up_half, cudaStream_t s) {
+           float *dT, float *mT, uint8_t *packed, int interleave, int up_half, cudaStream_t s) {
     int64_t total = (int64_t)nmat * rows * (K / QK);
     if (total == 0) return MOE_OK;
     int64_t blocks = (total + 255) / 256;
@@ -179,7 +185,7 @@ int repack(int wfmt, const void *src, int nmat, int rows, int K, int8_t *q, floa
     if (blocks > cap) blocks = cap;
     if (wfmt == MOE_WFMT_Q4_K)
         repack_q4k_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
-                                                           mn, h16, dT, mT, interleave, up_half);
+                                                           mn, h16, dT, mT, interleave, up_half, packed);
     else if (wfmt == MOE_WFMT_Q3_K)
         repack_q3k_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), nmat, rows, K / QK, q, d,
                                                            h16, dT, interleave, up_half);
@@ -215,6 +221,9 @@ static size_t layout_set(WeightSet &ws, int nexp, int D, int F, bool tensor, int
         ws.gate_m = (float *)take(gu / QK * sizeof(float));
         ws.up_m = (float *)take(gu / QK * sizeof(float));
         ws.down_m = (float *)take(dn / QK * sizeof(float));
+        ws.gate_p = (uint8_t *)take(gu / 2);
+        ws.up_p = (uint8_t *)take(gu / 2);
+        ws.down_p = (uint8_t *)take(dn / 2);
     }
     if (tensor) {
         ws.gu16 = (__half *)take(2 * gu * sizeof(__half));
@@ -244,10 +253,13 @@ int repack_weights(moe_weights_s *w, const void *gate, const void *up, const voi
     // the arena start doubles as the handle's allocation
     w->routed_arena_ = arena;
     auto sets = [&](WeightSet &ws, int nexp, int Fx, const void *g, const void *u, const void *dn) {
-        int rc = repack(wf, g, nexp, Fx, D, ws.gate_q, ws.gate_d, ws.gate_m, ws.gu16, ws.gu_dT, ws.gu_mT, 1, 0, s);
-        if (!rc) rc = repack(wf, u, nexp, Fx, D, ws.up_q, ws.up_d, ws.up_m, ws.gu16, ws.gu_dT, ws.gu_mT, 1, 1, s);
+        int rc = repack(wf, g, nexp, Fx, D, ws.gate_q, ws.gate_d, ws.gate_m, ws.gu16, ws.gu_dT, ws.gu_mT, ws.gate_p, 1,
+                        0, s);
         if (!rc)
-            rc = repack(wf, dn, nexp, D, Fx, ws.down_q, ws.down_d, ws.down_m, ws.dn16, ws.dn_dT, ws.dn_mT, 0, 0, s);
+            rc = repack(wf, u, nexp, Fx, D, ws.up_q, ws.up_d, ws.up_m, ws.gu16, ws.gu_dT, ws.gu_mT, ws.up_p, 1, 1, s);
+        if (!rc)
+            rc = repack(wf, dn, nexp, D, Fx, ws.down_q, ws.down_d, ws.down_m, ws.dn16, ws.dn_dT, ws.dn_mT, ws.down_p, 0,
+                        0, s);
         return rc;
     };
     int rc = sets(w->routed, E, F, gate, up, down);

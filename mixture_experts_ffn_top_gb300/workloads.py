@@ -122,6 +122,8 @@ WORKLOADS = {
                            seed=5, wfmt="q4_k"),
     "olmoe_q4k": Workload("olmoe_q4k", N=2048, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False,
                           seed=1, wfmt="q4_k"),
+    "decode_n8_q4k": Workload("decode_n8_q4k", N=8, D=2048, E=64, top_k=8, F=1024, Fs=0, norm_topk_prob=False,
+                              seed=2, wfmt="q4_k"),
     # and with Q3_K expert weights
     "tiny_q3k": Workload("tiny_q3k", N=64, D=256, E=8, top_k=2, F=256, Fs=0, norm_topk_prob=False, seed=0,
                          wfmt="q3_k"),

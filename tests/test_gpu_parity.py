@@ -300,6 +300,61 @@ def test_down_block_dots_every_entry(ops, name, path):
         assert bad.size == 0, (block, bad[:5].tolist())
 
 
+def _decode_case(name):
+    """Decode batches (at most 8 tokens: the matvec path streams the weights through its ring):
+    the OLMoE-shaped Q8_0 workloads, and K-quant layers of the same batch sizes."""
+    if name in WORKLOADS:
+        return case(name)
+    wfmt, n = name.split("_n")
+    wl = Workload(name, N=int(n), D=512, E=16, top_k=4, F=256, Fs=256, norm_topk_prob=True, seed=80 + int(n),
+                  wfmt=wfmt)
+    inp = make_inputs(wl)
+    return wl, inp, O.moe_ffn_inputs(inp, wl.top_k, wl.norm_topk_prob)
+
+
+def _row_dots(wfmt, w_row, act_row):
+    if wfmt == "q4_k":
+        return O.block_dots_q4_k(w_row, act_row)
+    if wfmt == "q3_k":  # the library stores the codes -s_j*q_i
+        return -O.block_dots_q3_k(w_row, act_row)
+    return O.block_dots(w_row, act_row)
+
+
+@pytest.mark.parametrize("name", ["decode_n1", "decode_n8", "q4_k_n1", "q4_k_n8", "q3_k_n8"])
+def test_decode_block_dots_every_entry(ops, name):
+    """The decode matvecs (Q4_K from its nibble-packed copy): every CSR entry x every row of
+    gate, up and down, three blocks, bit-exact against the oracle's integer block dots."""
+    wl, inp, ref = _decode_case(name)
+    layer = layer_for(ops, inp, wl)
+    es, ti, tk = _csr(ref)
+    total = int(ref["expStart"][-1])
+    xq, xd = dev(ref["x_q"]), dev(O.halves(ref["x_d16"]))
+    ent_e = np.searchsorted(ref["expStart"], np.arange(total), side="right") - 1
+    gu_blocks = sorted({0, wl.D // 64 + 1, wl.D // 32 - 1})
+    gu = {b: ops.moe_debug_gate_up_block_dots(layer.w, xq, xd, es, ti, wl.top_k, b, layer.ws, path=1)
+          .cpu().numpy()[:total] for b in gu_blocks}
+    assert ops.moe_workspace_status(layer.ws) == 0
+    hq = np.zeros((wl.N * wl.top_k, wl.F), np.int8)
+    hd = np.zeros((wl.N * wl.top_k, wl.F // 32), np.float32)
+    hq[:total] = ref["h_q"]
+    hd[:total] = O.halves(ref["h_d16"])
+    dn_blocks = sorted({0, wl.F // 64 + 1, wl.F // 32 - 1})
+    dn = {b: ops.moe_debug_down_block_dots(layer.w, dev(hq), dev(hd), es, ti, tk, wl.N, wl.top_k, b, layer.ws,
+                                           path=1).cpu().numpy()[:total] for b in dn_blocks}
+    assert ops.moe_workspace_status(layer.ws) == 0
+    for j in range(total):
+        e, t = int(ent_e[j]), int(ref["expTokI"][j])
+        for mat, W in ((0, inp["gate"]), (1, inp["up"])):
+            want = np.stack([_row_dots(wl.wfmt, W[e, f], ref["x_q"][t]) for f in range(wl.F)])
+            for b in gu_blocks:
+                bad = np.argwhere(gu[b][j, mat] != want[:, b])
+                assert bad.size == 0, (j, mat, b, bad[:5].tolist())
+        want = np.stack([_row_dots(wl.wfmt, inp["down"][e, c], ref["h_q"][j]) for c in range(wl.D)])
+        for b in dn_blocks:
+            bad = np.argwhere(dn[b][j] != want[:, b])
+            assert bad.size == 0, (j, b, bad[:5].tolist())
+
+
 @pytest.mark.parametrize("name", ["tiny_q4k", "olmoe_q4k", "tiny_q3k", "olmoe_q3k"])
 @pytest.mark.parametrize("path", [1, 2])
 def test_gate_up_block_dots_bit_exact(ops, name, path):
