@@ -293,6 +293,25 @@ def combine(partials, w, S=None, R=None):
     return out
 
 
+def combine_residual_rmsnorm(partials, w, S, R, gamma, eps: float):
+    """The combine with residual R, then RMSNorm of that row with weight gamma [D] and eps (the
+    next layer's input): returns (out, normed)."""
+    partials = _f32(partials)
+    w = _f32(w)
+    N, k = w.shape
+    D = partials.shape[1]
+    assert partials.shape[0] == N * k
+    R = _f32(R)
+    gamma = _f32(gamma)
+    assert R.shape == (N, D) and gamma.shape == (D,)
+    out = np.empty((N, D), np.float32)
+    normed = np.empty((N, D), np.float32)
+    Sp = _p(None if S is None else _f32(S))
+    _L().oracle_combine_residual_rmsnorm(_p(partials), _p(w), Sp, _p(R), _p(gamma), ctypes.c_double(eps), _I64(N),
+                                         _I(k), _I(D), _p(out), _p(normed))
+    return out, normed
+
+
 # ---------------------------------------------------------- whole layer ---
 def moe_ffn(hidden, routerW, gate, up, down, top_k: int, norm_topk_prob: bool,
             shexp_gate=None, sh_gate=None, sh_up=None, sh_down=None, keep: bool = True, fmt: str = "q8_0") -> dict:

@@ -682,6 +682,37 @@ void oracle_combine_residual(const float *partials, const float *w, const float 
         }
 }
 
+/* ------------------------------------------------------------------------
+ * The combine with the residual, then the next layer's input norm.  The pages
+ * feed the router a normalised activation ("Carnice prefill toward llama.cpp
+ * 676 t/s", #388, "Remaining levers" item 1: norm[N x embDim] x routerW) and
+ * chain the layers through the residual stream (item 2: layer L+1's trunk
+ * starts with its norm of layer L's combine output); they do not spell the
+ * norm out.  Read as RMSNorm with a per-column weight gamma and an epsilon
+ * (the norm of the OLMoE and Qwen3-MoE layer families the pages run): per
+ * token row t,
+ *   out[t,c]    = the combine with residual above (fp32, fixed order);
+ *   ms          = (sum over c of out[t,c]^2) / D                  (double)
+ *   normed[t,c] = out[t,c] * (1 / sqrt(ms + eps)) * gamma[c]       (double,
+ *                 rounded to fp32 once).
+ * ---------------------------------------------------------------------- */
+void oracle_combine_residual_rmsnorm(const float *partials, const float *w, const float *S, const float *R,
+                                     const float *gamma, double eps, int64_t N, int k, int D, float *out,
+                                     float *normed)
+{
+    oracle_combine_residual(partials, w, S, R, N, k, D, out);
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < N; ++t) {
+        const float *o = out + t * D;
+        double ss = 0.0;
+        for (int c = 0; c < D; ++c)
+            ss += (double)o[c] * (double)o[c];
+        double r = 1.0 / sqrt(ss / (double)D + eps);
+        for (int c = 0; c < D; ++c)
+            normed[t * D + c] = (float)((double)o[c] * r * (double)gamma[c]);
+    }
+}
+
 /* Threads the OpenMP runtime will use (reported beside oracle timings). */
 int oracle_num_threads(void)
 {

@@ -64,6 +64,11 @@ MUTATIONS = [
     ("combine_residual_dropped", "            acc = acc + R[t * D + c];\n", ""),
     ("combine_shared_first", "            float acc = 0.0f;\n            for (int s = 0; s < k; ++s)",
      "            float acc = S ? S[t * D + c] : 0.0f;\n            if (S) S = S + 0 * c;\n            for (int s = 0; s < k; ++s)"),
+    ("rmsnorm_without_epsilon", "double r = 1.0 / sqrt(ss / (double)D + eps);", "double r = 1.0 / sqrt(ss / (double)D);"),
+    ("rmsnorm_sum_not_mean", "double r = 1.0 / sqrt(ss / (double)D + eps);", "double r = 1.0 / sqrt(ss + eps);"),
+    ("rmsnorm_gamma_by_row", "* r * (double)gamma[c]);", "* r * (double)gamma[t % D]);"),
+    ("rmsnorm_scale_from_the_routed_sum", "            ss += (double)o[c] * (double)o[c];",
+     "            ss += ((double)o[c] - R[t * D + c]) * ((double)o[c] - R[t * D + c]);"),
 ]
 
 

@@ -729,6 +729,75 @@ def test_combine_residual_added_after_the_shared_row():
     assert float(O.combine(p, w, S, R)[0, 0]) == 1.0 + 2.0 ** -23
 
 
+def _single_slot(rows):
+    """k = 1, w = 1, zero residual, no shared row: the combine's out is `rows` itself."""
+    rows = np.asarray(rows, np.float32)
+    return rows, np.ones((rows.shape[0], 1), np.float32), np.zeros_like(rows)
+
+
+def test_rmsnorm_constant_rows_give_gamma():
+    """A row of one value c (any sign, any size) has RMS |c|: with eps = 0 every normed value is
+    sign(c) * gamma[c], exactly (c^2 and its square root are exact in double)."""
+    rng = np.random.default_rng(17)
+    D = 40
+    rows = np.array([[3.0] * D, [-0.375] * D, [2.0 ** -60] * D, [1.5e30] * D], np.float32)
+    gamma = (rng.standard_normal(D) * 3.0).astype(np.float32)
+    p, w, R = _single_slot(rows)
+    out, normed = O.combine_residual_rmsnorm(p, w, None, R, gamma, 0.0)
+    np.testing.assert_array_equal(out, rows)
+    np.testing.assert_array_equal(normed, np.sign(rows) * gamma[None, :])
+
+
+def test_rmsnorm_epsilon_closed_form():
+    """A constant row c with eps = 3 c^2: c / sqrt(c^2 + 3 c^2) = 1/2 exactly."""
+    for c in (2.0, 0.25, -6.0):
+        p, w, R = _single_slot(np.full((1, 24), c))
+        _, normed = O.combine_residual_rmsnorm(p, w, None, R, np.ones(24, np.float32), 3.0 * c * c)
+        np.testing.assert_array_equal(normed, np.full((1, 24), 0.5 * np.sign(c), np.float32))
+
+
+def test_rmsnorm_rows_have_unit_rms():
+    """gamma = 1, eps = 0: every normed row has mean square 1 (to fp32 rounding), whatever its scale."""
+    rng = np.random.default_rng(18)
+    rows = (rng.standard_normal((8, 256)) * 10.0 ** rng.integers(-8, 8, (8, 1))).astype(np.float32)
+    p, w, R = _single_slot(rows)
+    _, normed = O.combine_residual_rmsnorm(p, w, None, R, np.ones(256, np.float32), 0.0)
+    ms = (normed.astype(np.float64) ** 2).mean(axis=1)
+    np.testing.assert_allclose(ms, 1.0, rtol=2e-7)
+
+
+def test_rmsnorm_power_of_two_scale_invariance_and_gamma_linearity():
+    """With eps = 0, scaling a row by 2^j changes nothing (every step scales exactly), and doubling
+    gamma doubles every normed value exactly."""
+    rng = np.random.default_rng(19)
+    rows = rng.standard_normal((5, 64)).astype(np.float32)
+    gamma = rng.standard_normal(64).astype(np.float32)
+    p, w, R = _single_slot(rows)
+    _, n1 = O.combine_residual_rmsnorm(p, w, None, R, gamma, 0.0)
+    p8, _, R8 = _single_slot(rows * np.float32(8.0))
+    _, n8 = O.combine_residual_rmsnorm(p8, w, None, R8, gamma, 0.0)
+    np.testing.assert_array_equal(n1, n8)
+    _, n2 = O.combine_residual_rmsnorm(p, w, None, R, gamma * np.float32(2.0), 0.0)
+    np.testing.assert_array_equal(n2, n1 * np.float32(2.0))
+
+
+def test_rmsnorm_normalises_the_residual_combine_output():
+    """out is the combine with residual bit for bit, and the norm is taken of out (not of the
+    routed sum alone): each normed row is out * r * gamma with one r per row."""
+    rng = np.random.default_rng(20)
+    N, k, D = 4, 3, 48
+    p = rng.standard_normal((N * k, D)).astype(np.float32)
+    w = rng.random((N, k)).astype(np.float32)
+    S = rng.standard_normal((N, D)).astype(np.float32)
+    R = (rng.standard_normal((N, D)) * 4.0).astype(np.float32)
+    gamma = (rng.random(D) + 0.5).astype(np.float32)
+    out, normed = O.combine_residual_rmsnorm(p, w, S, R, gamma, 1e-6)
+    np.testing.assert_array_equal(out, O.combine(p, w, S, R))
+    ratio = normed.astype(np.float64) / (out.astype(np.float64) * gamma.astype(np.float64))
+    want = 1.0 / np.sqrt((out.astype(np.float64) ** 2).mean(axis=1) + 1e-6)
+    np.testing.assert_allclose(ratio, np.broadcast_to(want[:, None], ratio.shape), rtol=2e-7)
+
+
 # ---------------------------------------------------- regression fixture ---
 @pytest.mark.parametrize("name,fixture", [("tiny", "tiny_layer.json"), ("tiny_q4k", "tiny_q4k_layer.json"),
                                           ("tiny_q3k", "tiny_q3k_layer.json")])
