@@ -444,6 +444,20 @@ def run_ours(args, rank, world, local_rank):
     if layer.status():
         raise RuntimeError("device status set during the residual steps")
 
+    # ... and with the next layer's RMSNorm of that output fused in as well (a second output row)
+    gamma = torch.ones(D, dtype=torch.float32, device=device)
+    normed = torch.empty_like(residual)
+
+    def norm_step():
+        ops.moe_ffn_prefill_residual_rmsnorm(w, hidden, routerW, shg, residual, gamma, 1e-6, k, wl.norm_topk_prob, ws,
+                                             out=res_out, normed=normed, path=path)
+
+    for _ in range(max(1, args.warmup)):
+        norm_step()
+    norm_mean = max_over_ranks(timed(norm_step, args.steps), device)
+    if layer.status():
+        raise RuntimeError("device status set during the residual + norm steps")
+
     # two chained layers (hidden <- hidden + FFN_l(hidden), l = 0, 1): the stack entry point, whose
     # second router starts behind the first layer's combine, against two separate residual calls
     from dataclasses import replace as _replace
@@ -514,6 +528,9 @@ def run_ours(args, rank, world, local_rank):
                 "host_numa_node": numa_node},
         "with_residual": {"value": job_throughput(world, N, res_mean), "unit": UNIT, "ms_per_step": res_mean,
                           "api": "moe_ffn_prefill_residual (residual add fused into the combine)"},
+        "with_residual_rmsnorm": {"value": job_throughput(world, N, norm_mean), "unit": UNIT, "ms_per_step": norm_mean,
+                                  "api": "moe_ffn_prefill_residual_rmsnorm (residual add and the next layer's "
+                                         "RMSNorm fused into the combine)"},
         "layer_stack": {"layers": 2, "ms_per_step": stack_ms, "ms_two_separate_calls": two_ms,
                         "tokens_per_s_per_layer": job_throughput(world, 2 * N, stack_ms),
                         "api": "moe_ffn_prefill_stack (second router launched behind the first combine; "

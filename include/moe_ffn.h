@@ -352,6 +352,24 @@ int moe_combine(const float *partials, const float *topk_w, const float *shared,
 int moe_combine_residual(const float *partials, const float *topk_w, const float *shared,
                          const float *residual, int N, int top_k, int D, float *out,
                          cudaStream_t stream);
+/* moe_combine_residual, then the next layer's input norm of every output row.
+ * The pages feed the router a normalised activation ("Carnice prefill toward
+ * llama.cpp 676 t/s", #388, "Remaining levers" item 1: norm[N x embDim] x
+ * routerW) and chain the layers through this residual stream (item 2); the
+ * norm is read as RMSNorm with a per-column weight:
+ *   out[t][c]    = moe_combine_residual's value (bit for bit);
+ *   normed[t][c] = (out[t][c] * r_t) * gamma[c],
+ *   r_t          = 1 / sqrt(sum_c out[t][c]^2 / D + eps)   (fp32; the row sum in a
+ *                  fixed order: each thread's columns, then a warp butterfly,
+ *                  then the warps in order; 128 threads per row, or 512 when N
+ *                  is below 8 times the SM count, so its grouping, and the last
+ *                  bits of normed, depend on N).
+ * residual [N][D] fp32, non-NULL (it may be `out`); gamma [D] fp32, device;
+ * eps > 0 and finite; normed [N][D] fp32, overlapping neither out nor any
+ * input; gamma and normed 16-byte aligned.  MOE_ERR_INVALID_ARG otherwise. */
+int moe_combine_residual_rmsnorm(const float *partials, const float *topk_w, const float *shared,
+                                 const float *residual, const float *gamma, float eps, int N,
+                                 int top_k, int D, float *out, float *normed, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_ffn_prefill -- the whole layer in one call (all of the above, on one
@@ -374,6 +392,14 @@ int moe_ffn_prefill_residual(moe_weights_t w, const float *hidden, const float *
                              const float *shexp_gate, const float *residual, int N, int top_k,
                              int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
                              cudaStream_t stream);
+/* moe_ffn_prefill_residual whose combine also writes the next layer's normalised
+ * input (moe_combine_residual_rmsnorm): out = residual + FFN(hidden), normed =
+ * RMSNorm(out) * gamma.  Arguments as there and as moe_combine_residual_rmsnorm. */
+int moe_ffn_prefill_residual_rmsnorm(moe_weights_t w, const float *hidden, const float *routerW,
+                                     const float *shexp_gate, const float *residual,
+                                     const float *gamma, float eps, int N, int top_k,
+                                     int norm_topk_prob, float *out, float *normed, int path,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* moe_ffn_prefill_ex with hidden and out in HOST memory (the layer as a host
  * program calls it).  No staging copies: the router reads the hidden rows and

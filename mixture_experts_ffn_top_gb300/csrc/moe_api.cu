@@ -435,6 +435,23 @@ int moe_combine_residual(const float *partials, const float *topk_w, const float
     return launch_combine(partials, topk_w, shared, residual, N, top_k, D, out, stream);
 }
 
+// eps of the fused norm: positive and finite
+static bool norm_args_ok(const float *gamma, float eps, const float *normed, const float *out, const float *residual) {
+    return gamma && normed && eps > 0.0f && eps <= 3.0e38f && normed != out && normed != residual &&
+           ((uintptr_t)gamma | (uintptr_t)normed) % 16 == 0;
+}
+
+int moe_combine_residual_rmsnorm(const float *partials, const float *topk_w, const float *shared,
+                                 const float *residual, const float *gamma, float eps, int N, int top_k, int D,
+                                 float *out, float *normed, cudaStream_t stream) {
+    if (!partials || !topk_w || !out || !residual) return MOE_ERR_INVALID_ARG;
+    if (!norm_args_ok(gamma, eps, normed, out, residual)) return MOE_ERR_INVALID_ARG;
+    if (N < 1 || top_k < 1 || D < 4 || D % 4) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (((uintptr_t)partials | (uintptr_t)out | (uintptr_t)shared | (uintptr_t)residual) % 16)
+        return MOE_ERR_INVALID_ARG;
+    return launch_combine_rmsnorm(partials, topk_w, shared, residual, gamma, eps, N, top_k, D, out, normed, stream);
+}
+
 int moe_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k, int D, float *out,
                 cudaStream_t stream) {
     return moe_combine_residual(partials, topk_w, shared, nullptr, N, top_k, D, out, stream);
@@ -443,7 +460,8 @@ int moe_combine(const float *partials, const float *topk_w, const float *shared,
 static int prefill_impl(moe_weights_t w, const float *hidden, const float *routerW, const float *shexp_gate, int N,
                         int top_k, int norm_topk_prob, float *out, int path, void *ws, size_t ws_bytes,
                         cudaStream_t stream, cudaEvent_t *ev, const float *residual = nullptr,
-                        bool early_router = false) {
+                        bool early_router = false, const float *gamma = nullptr, float eps = 0.0f,
+                        float *normed = nullptr) {
     if (!w || !hidden || !routerW || !out) return MOE_ERR_INVALID_ARG;
     if (residual && ((uintptr_t)residual % 16 || w->D % 4)) return MOE_ERR_INVALID_ARG;
     if (shexp_gate && w->Fs == 0) return MOE_ERR_INVALID_ARG;
@@ -531,7 +549,10 @@ static int prefill_impl(moe_weights_t w, const float *hidden, const float *route
                                     nullptr, N, top_k, sh, shout, st, stream, early);
         mark(5);
     }
-    if (!rc) rc = launch_combine(part, tw, shout, residual, N, top_k, D, out, stream, !tensor && ev == nullptr);
+    if (!rc)
+        rc = gamma ? launch_combine_rmsnorm(part, tw, shout, residual, gamma, eps, N, top_k, D, out, normed, stream,
+                                            !tensor && ev == nullptr)
+                   : launch_combine(part, tw, shout, residual, N, top_k, D, out, stream, !tensor && ev == nullptr);
     mark(6);
     return rc;
 }
@@ -589,6 +610,16 @@ int moe_ffn_prefill_residual(moe_weights_t w, const float *hidden, const float *
     if (!residual) return MOE_ERR_INVALID_ARG;
     return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
                         nullptr, residual);
+}
+
+int moe_ffn_prefill_residual_rmsnorm(moe_weights_t w, const float *hidden, const float *routerW,
+                                     const float *shexp_gate, const float *residual, const float *gamma, float eps,
+                                     int N, int top_k, int norm_topk_prob, float *out, float *normed, int path,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!residual || !out) return MOE_ERR_INVALID_ARG;
+    if (!norm_args_ok(gamma, eps, normed, out, residual)) return MOE_ERR_INVALID_ARG;
+    return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
+                        nullptr, residual, false, gamma, eps, normed);
 }
 
 int moe_ffn_prefill_stack(const moe_weights_t *w, const float *const *routerW, const float *const *shexp_gate,

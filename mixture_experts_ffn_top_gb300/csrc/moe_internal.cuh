@@ -168,6 +168,10 @@ int launch_matvec_down(const moe_weights_s *w, const WeightSet &ws, bool is_shar
 // kernel further back.
 int launch_combine(const float *partials, const float *topk_w, const float *shared, const float *residual, int N,
                    int top_k, int D, float *out, cudaStream_t s, bool early = false);
+// launch_combine with a residual, then RMSNorm of each output row into normed (gamma [D], eps > 0).
+int launch_combine_rmsnorm(const float *partials, const float *topk_w, const float *shared, const float *residual,
+                           const float *gamma, float eps, int N, int top_k, int D, float *out, float *normed,
+                           cudaStream_t s, bool early = false);
 // weights.cu
 int repack_weights(moe_weights_s *w, const void *gate, const void *up, const void *down,
                    const void *sh_gate, const void *sh_up, const void *sh_down, cudaStream_t s);

@@ -61,6 +61,9 @@ _SIGS = {
     "moe_device_host_numa_node": (_I, [_P]),
     "moe_combine_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill_residual": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
+    "moe_combine_residual_rmsnorm": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P]),
+    "moe_ffn_prefill_residual_rmsnorm": (_I, [_P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _I, _P,
+                                               _SZ, _P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
     "moe_ffn_prefill_stack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _SZ, _P]),
 }
@@ -375,6 +378,25 @@ def moe_combine_residual(partials, topk_w, shared, residual, out=None, stream=No
     return out
 
 
+def moe_combine_residual_rmsnorm(partials, topk_w, shared, residual, gamma, eps, out=None, normed=None,
+                                 stream=None):
+    """moe_combine_residual, then RMSNorm of each output row with weight gamma and eps (the next
+    layer's input).  Returns (out, normed); out may be residual."""
+    N, k = topk_w.shape
+    D = partials.shape[1]
+    if out is None:
+        out = torch.empty((N, D), dtype=torch.float32, device=partials.device)
+    if normed is None:
+        normed = torch.empty((N, D), dtype=torch.float32, device=partials.device)
+    _check(lib().moe_combine_residual_rmsnorm(_dev(partials, torch.float32, "partials"),
+                                              _dev(topk_w, torch.float32, "topk_w"), _dev(shared, torch.float32, "shared"),
+                                              _dev(residual, torch.float32, "residual"),
+                                              _dev(gamma, torch.float32, "gamma"), float(eps), N, k, D,
+                                              _dev(out, torch.float32, "out"), _dev(normed, torch.float32, "normed"),
+                                              _stream(stream)), "moe_combine_residual_rmsnorm")
+    return out, normed
+
+
 def moe_ffn_prefill_stack(weights, routerWs, shexp_gates, hidden, top_k, norm_topk_prob, ws, path=MOE_PATH_AUTO,
                           stream=None):
     """Layers applied in place, hidden <- hidden + FFN_l(hidden) for each layer l in order (weights,
@@ -407,6 +429,26 @@ def moe_ffn_prefill_residual(w: MoeWeights, hidden, routerW, shexp_gate, residua
                                         _stream(stream))
     _check(rc, "moe_ffn_prefill_residual")
     return out
+
+
+def moe_ffn_prefill_residual_rmsnorm(w: MoeWeights, hidden, routerW, shexp_gate, residual, gamma, eps, top_k,
+                                     norm_topk_prob, ws, out=None, normed=None, path=MOE_PATH_AUTO, stream=None):
+    """The layer with the residual add and the next layer's RMSNorm fused into its combine:
+    out = residual + FFN(hidden), normed = RMSNorm(out) * gamma.  Returns (out, normed)."""
+    N = hidden.shape[0]
+    if out is None:
+        out = torch.empty((N, w.D), dtype=torch.float32, device=hidden.device)
+    if normed is None:
+        normed = torch.empty((N, w.D), dtype=torch.float32, device=hidden.device)
+    rc = lib().moe_ffn_prefill_residual_rmsnorm(w.handle, _dev(hidden, torch.float32, "hidden"),
+                                                _dev(routerW, torch.float32, "routerW"), _dev(shexp_gate, torch.float32),
+                                                _dev(residual, torch.float32, "residual"),
+                                                _dev(gamma, torch.float32, "gamma"), float(eps), N, top_k,
+                                                int(norm_topk_prob), _dev(out, torch.float32, "out"),
+                                                _dev(normed, torch.float32, "normed"), path, _dev(ws, torch.uint8, "ws"),
+                                                ws.numel(), _stream(stream))
+    _check(rc, "moe_ffn_prefill_residual_rmsnorm")
+    return out, normed
 
 
 def moe_ffn_prefill(w: MoeWeights, hidden, routerW, shexp_gate, top_k, norm_topk_prob, ws, out=None,

@@ -546,6 +546,114 @@ def test_layer_with_residual(ops, name):
     np.testing.assert_array_equal(R.cpu().numpy(), want)
 
 
+# RMSNorm of the combined row: out is bit-exact, and only the row's factor r = 1/sqrt(ms + eps) carries
+# rounding.  The kernel sums the squares in fp32: D/128 terms per thread (128 threads per row; D/512
+# with 512), a 5-level warp butterfly, at most 16 warps in order, so the sum is within
+# 2^-24 * (D/128 + 21) relative, r within half that plus 3 ulps (/D, + eps, square root, divide), and
+# normed two products more: |normed - ref| <= 2e-6 * |ref| elementwise for D <= 4096 against the
+# oracle's double evaluation.
+NORM_RTOL = 2e-6
+
+
+def _gamma(D, seed):
+    return (1.0 + 0.25 * np.random.default_rng(seed).standard_normal(D)).astype(np.float32)
+
+
+def _assert_normed(got, want):
+    err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    bound = NORM_RTOL * np.abs(want.astype(np.float64))
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (bad[:5].tolist(), float((err / np.maximum(np.abs(want), 1e-30)).max()))
+
+
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared"])
+def test_combine_residual_rmsnorm_against_oracle(ops, name):
+    """The combine with residual (bit-exact) and the next layer's RMSNorm of it (within NORM_RTOL of
+    the oracle's double evaluation), out of place and in place (out = residual)."""
+    wl, inp, ref = case(name)
+    R = np.random.default_rng(33).standard_normal((wl.N, wl.D)).astype(np.float32)
+    gamma = _gamma(wl.D, 34)
+    S_np = ref["shared_out"] if wl.has_shared else None
+    want_out, want_norm = O.combine_residual_rmsnorm(ref["partials"], ref["topk_w"], S_np, R, gamma, 1e-6)
+    S = dev(S_np) if wl.has_shared else None
+    out, normed = ops.moe_combine_residual_rmsnorm(dev(ref["partials"]), dev(ref["topk_w"]), S, dev(R), dev(gamma),
+                                                   1e-6)
+    np.testing.assert_array_equal(out.cpu().numpy(), want_out)
+    _assert_normed(normed.cpu().numpy(), want_norm)
+    r_dev = dev(R)
+    _, normed2 = ops.moe_combine_residual_rmsnorm(dev(ref["partials"]), dev(ref["topk_w"]), S, r_dev, dev(gamma),
+                                                  1e-6, out=r_dev)
+    np.testing.assert_array_equal(r_dev.cpu().numpy(), want_out)
+    np.testing.assert_array_equal(normed2.cpu().numpy(), normed.cpu().numpy())
+
+
+def test_combine_rmsnorm_edge_rows(ops):
+    """Constant rows (normed = sign * gamma up to the factor's rounding), a zero row (normed = 0,
+    eps keeps it finite), a huge and a tiny row (no overflow or underflow in the sum of squares at
+    these magnitudes), a ragged width (D = 260: 65 float4 columns over 128 threads), top_k = 3 (the
+    generic slot loop)."""
+    D, k = 260, 3
+    rows = np.zeros((5, D), np.float32)
+    rows[0] = 3.0
+    rows[1] = -0.5
+    rows[3] = np.random.default_rng(35).standard_normal(D).astype(np.float32) * 1e15
+    rows[4] = np.random.default_rng(36).standard_normal(D).astype(np.float32) * 1e-15
+    p = np.zeros((5 * k, D), np.float32)
+    p[0::k] = rows  # slot 0 carries the row, weight 1; slots 1, 2 weight 0
+    w = np.zeros((5, k), np.float32)
+    w[:, 0] = 1.0
+    R = np.zeros((5, D), np.float32)
+    gamma = _gamma(D, 37)
+    want_out, want_norm = O.combine_residual_rmsnorm(p, w, None, R, gamma, 1e-12)
+    out, normed = ops.moe_combine_residual_rmsnorm(dev(p), dev(w), None, dev(R), dev(gamma), 1e-12)
+    np.testing.assert_array_equal(out.cpu().numpy(), want_out)
+    got = normed.cpu().numpy()
+    _assert_normed(got, want_norm)
+    assert not np.any(got[2])  # the zero row
+    assert np.all(np.isfinite(got))
+
+
+def test_combine_rmsnorm_rejects_bad_arguments(ops):
+    p = dev(np.ones((4, 8), np.float32))
+    w = dev(np.ones((4, 1), np.float32))
+    R = dev(np.zeros((4, 8), np.float32))
+    g = dev(np.ones(8, np.float32))
+    for eps in (0.0, -1e-6, float("inf"), float("nan")):
+        with pytest.raises(ops.MoeError):
+            ops.moe_combine_residual_rmsnorm(p, w, None, R, g, eps)
+    out = torch.empty((4, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(ops.MoeError):
+        ops.moe_combine_residual_rmsnorm(p, w, None, R, g, 1e-6, out=out, normed=out)
+    with pytest.raises(ops.MoeError):
+        ops.moe_combine_residual_rmsnorm(p, w, None, R, g, 1e-6, normed=R)
+
+
+@pytest.mark.parametrize("name,path", [("tiny", 0), ("olmoe", 0), ("qwen3moe_shared", 0), ("decode_n4", 0),
+                                       ("tiny", 2)])
+def test_layer_with_residual_rmsnorm(ops, name, path):
+    """moe_ffn_prefill_residual_rmsnorm: out equals moe_ffn_prefill_residual's bit for bit (also in
+    place), and normed is the RMSNorm of that out within NORM_RTOL of the oracle."""
+    wl, inp, ref = case(name)
+    layer = layer_for(ops, inp, wl)
+    R = np.random.default_rng(38).standard_normal((wl.N, wl.D)).astype(np.float32)
+    gamma = _gamma(wl.D, 39)
+    want = ops.moe_ffn_prefill_residual(layer.w, dev(inp["hidden"]), layer.routerW, layer.shexp_gate, dev(R),
+                                        wl.top_k, wl.norm_topk_prob, layer.ws, path=path).cpu().numpy()
+    out, normed = ops.moe_ffn_prefill_residual_rmsnorm(layer.w, dev(inp["hidden"]), layer.routerW, layer.shexp_gate,
+                                                       dev(R), dev(gamma), 1e-5, wl.top_k, wl.norm_topk_prob,
+                                                       layer.ws, path=path)
+    assert layer.status() == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), want)
+    ones = np.ones((wl.N, 1), np.float32)
+    _, want_norm = O.combine_residual_rmsnorm(want, ones, None, np.zeros_like(want), gamma, 1e-5)
+    _assert_normed(normed.cpu().numpy(), want_norm)
+    r_dev = dev(R)
+    ops.moe_ffn_prefill_residual_rmsnorm(layer.w, dev(inp["hidden"]), layer.routerW, layer.shexp_gate, r_dev,
+                                         dev(gamma), 1e-5, wl.top_k, wl.norm_topk_prob, layer.ws, out=r_dev, path=path)
+    assert layer.status() == 0
+    np.testing.assert_array_equal(r_dev.cpu().numpy(), want)
+
+
 # ---------------------------------------------------------- whole layer ---
 @pytest.mark.parametrize("name", CONFIGS + Q4K + Q3K)
 @pytest.mark.parametrize("path", [0, 1, 2])
