@@ -80,8 +80,8 @@ __device__ __forceinline__ int dp4a4(int4 a, int4 b) {
 
 // Per-lane dots of two weight rows (quants w0/w1 [K], or [K/2] nibble-packed with PK; scales s0/s1
 // [K/32], mins n0/n1 or NULL) with T staged activation rows tok[0..T-1] (xs [rows][K], xds
-// [rows][K/32]); returns the warp-reduced sums in every lane.  DBG: the lane owning block
-// dbg_block keeps its isums in dbg.
+// [rows][K/32]); returns each lane's partial sums over its blocks (reduce_lanes adds them across
+// the warp).  DBG: the lane owning block dbg_block keeps its isums in dbg.
 template <int T, bool DBG, bool PK>
 __device__ __forceinline__ void ring_dot(const int8_t *w0, const int8_t *w1, const float *s0, const float *s1,
                                          const float *n0, const float *n1, int K, const int8_t *xs, const float *xds,
@@ -141,11 +141,40 @@ __device__ __forceinline__ void ring_dot(const int8_t *w0, const int8_t *w1, con
             }
         }
     }
+}
+
+// The warp sums of NV values (a power of two, 2..32) per lane, with the additions of warp_sum: at
+// offset o every lane adds its own partial and lane (l ^ o)'s, so each sum is warp_sum's bit for
+// bit.  At each of the first log2(NV) offsets (16, 8, ...) a lane keeps only half of its values
+// (the lower half where bit o of its index is clear, the upper where set) and sends the other half,
+// so NV - 1 shuffles do what NV warp_sums do with 5 NV.  Returns the full sum of value
+// lane / (32 / NV), held by the 32 / NV lanes that share that quotient.
+// One offset O of reduce_lanes with N values still per lane (compile-time throughout, so the
+// values stay in registers).
+template <int N, int O>
+__device__ __forceinline__ void reduce_lanes_step(float *v, int lane) {
+    if constexpr (O > 0) {
+        if constexpr (N > 1) {
+            const bool upper = (lane & O) != 0;
 #pragma unroll
-    for (int tt = 0; tt < T; ++tt) {
-        acc[0][tt] = warp_sum(acc[0][tt]);
-        acc[1][tt] = warp_sum(acc[1][tt]);
+            for (int i = 0; i < N / 2; ++i) {
+                const float keep = upper ? v[i + N / 2] : v[i];
+                const float send = upper ? v[i] : v[i + N / 2];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            reduce_lanes_step<N / 2, O / 2>(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            reduce_lanes_step<1, O / 2>(v, lane);
+        }
     }
+}
+
+template <int NV>
+__device__ __forceinline__ float reduce_lanes(float (&v)[NV], int lane) {
+    static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "a power of two");
+    reduce_lanes_step<NV, 16>(v, lane);
+    return v[0];
 }
 
 // The CSR entries of one work item, one slot per lane (lanes 0-7; other lanes hold dead slots):
@@ -222,49 +251,54 @@ __device__ __forceinline__ void consume_stage(const RingArgs &a, const uint8_t *
     float acc[2][T];
     int dbg[2][T];
     ring_dot<T, DBG, PK>(w0, w1, s0, s1, n0, n1, K, xs, xds, tok, lane, acc, a.dbg_block, dbg);
-    // slot tt's values go out through lane tt (which holds the slot's rows)
-    float v0 = 0.0f, v1 = 0.0f;
-    int d0 = 0, d1 = 0;
+    // the 2T sums (row m, slot tt) at index m * T + tt: lane l holds the sum of index l / (16 / T)
+    float v[2 * T];
 #pragma unroll
     for (int tt = 0; tt < T; ++tt) {
-        if (lane == tt) {
-            v0 = acc[0][tt];
-            v1 = acc[1][tt];
-        }
-        if (DBG) {
-            const int src = a.dbg_block & 31;  // the lane that owned block dbg_block
-            const int g0 = __shfl_sync(0xffffffffu, dbg[0][tt], src), g1 = __shfl_sync(0xffffffffu, dbg[1][tt], src);
-            if (lane == tt) {
+        v[tt] = acc[0][tt];
+        v[T + tt] = acc[1][tt];
+    }
+    const float mine = reduce_lanes<2 * T>(v, lane);
+    const int idx = lane / (16 / T);
+    const int m = idx / T, tt = idx % T;         // m = lane's bit 4
+    const bool first = (lane % (16 / T)) == 0;   // one lane of those holding the same sum
+    // DBG: slot tt's two isums of block dbg_block, from the lane that owned the block
+    int d0 = 0, d1 = 0;
+    if (DBG) {
+        const int src = a.dbg_block & 31;
+#pragma unroll
+        for (int u = 0; u < T; ++u) {
+            const int g0 = __shfl_sync(0xffffffffu, dbg[0][u], src), g1 = __shfl_sync(0xffffffffu, dbg[1][u], src);
+            if (lane == u) {
                 d0 = g0;
                 d1 = g1;
             }
         }
     }
-    const bool live = lane < T && lane < sl.cnt && sl.ent >= 0;
+    const bool live_own = lane < T && lane < sl.cnt && sl.ent >= 0;  // slot `lane`, for the DBG writes
     if (MODE == 0) {
         const int f = ob * QK + s * 8 + cw;  // feature within the expert
-        if (DBG && live && a.dbg_block >= 0) {
+        if (DBG && live_own && a.dbg_block >= 0) {
             a.dbg_dots[((size_t)sl.ent * 2 + 0) * a.rows_e + f] = d0;
             a.dbg_dots[((size_t)sl.ent * 2 + 1) * a.rows_e + f] = d1;
         }
-        if (lane < T) {
-            const float silu = v0 / (1.0f + expf(-v0));
-            hbuf[lane * QK + s * 8 + cw] = silu * v1;
+        const float up = __shfl_xor_sync(0xffffffffu, mine, 16);  // the same slot's up row sum
+        if (m == 0 && first) {
+            const float silu = mine / (1.0f + expf(-mine));
+            hbuf[tt * QK + s * 8 + cw] = silu * up;
         }
     } else {
         const int c0 = ob * QK + s * 16 + cw;  // output columns c0 and c0 + 8
-        if (DBG && live && !a.is_shared && a.dbg_block >= 0) {
+        if (DBG && live_own && !a.is_shared && a.dbg_block >= 0) {
             a.dbg_dots[(size_t)sl.ent * a.D + c0] = d0;
             a.dbg_dots[(size_t)sl.ent * a.D + c0 + 8] = d1;
         }
-        if (live && sl.orow >= 0) {
-            if (a.is_shared) {
-                v0 = sl.osc * v0;
-                v1 = sl.osc * v1;
-            }
-            a.out[(size_t)sl.orow * a.D + c0] = v0;
-            a.out[(size_t)sl.orow * a.D + c0 + 8] = v1;
-        }
+        // slot tt's output row, scale and liveness come from lane tt, which holds that slot
+        const int orow = __shfl_sync(0xffffffffu, sl.orow, tt);
+        const int ent = __shfl_sync(0xffffffffu, sl.ent, tt);
+        const float osc = __shfl_sync(0xffffffffu, sl.osc, tt);
+        if (first && tt < sl.cnt && ent >= 0 && orow >= 0)
+            a.out[(size_t)orow * a.D + c0 + 8 * m] = a.is_shared ? osc * mine : mine;
     }
 }
 
