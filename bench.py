@@ -13,9 +13,10 @@ the launching stream with events between the stages, and the L2 is flushed
 (a 512 MB write) between steps outside the events.  Under torchrun each rank
 runs its own token batch (replicas, weak scaling) and rank 0 prints the line
 with the maximum time over ranks.  With one GPU the line also carries
-`configs`: the other workloads of the layer's survey (tiny, decode batches of
-1/4/8 tokens, the Qwen3-MoE-shaped layer with a shared expert, the Zipf-skewed
-long prefill), each timed the same way after the headline, with its tokens/s,
+`configs`: the layer's other workloads (tiny, decode batches of 1/4/8 tokens
+with Q8_0 and of 8 tokens with Q4_K weights, the Qwen3-MoE-shaped layer with a
+shared expert, the Zipf-skewed long prefill), each timed the same way after
+the headline, with its tokens/s,
 layer roofline fraction, dominant kernel's fraction and stage times.
 --impl reference times the CPU oracle on the host cores on a bounded sample of
 the same workload.
@@ -491,7 +492,7 @@ def run_ours(args, rank, world, local_rank):
     del head, layer, w, ws, routerW, shg
     torch.cuda.empty_cache()
 
-    # the survey's other workloads, one after another on this GPU, each at the same steps/warm-up
+    # the other workloads, one after another on this GPU, each at the same steps/warm-up
     configs = {}
     if world == 1 and not args.no_configs:
         for name in CONFIG_WORKLOADS:
