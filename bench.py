@@ -488,6 +488,20 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if not torch.equal(hs, h_a):
         raise RuntimeError("the layer stack and two separate calls disagree")
+
+    # the same two layers pre-normed (normed = RMSNorm_0(h); h += FFN_l(normed); the next norm fused
+    # into each combine, a final norm after the last layer)
+    gam = [gamma, gamma, gamma]
+    nrm = torch.empty_like(hidden)
+
+    def stack_norm_step():
+        hs.copy_(hidden)
+        ops.moe_ffn_prefill_stack_rmsnorm([w, layer2.w], [routerW, layer2.routerW], [shg, layer2.shexp_gate], gam,
+                                          1e-6, hs, k, wl.norm_topk_prob, ws, normed=nrm, path=path)
+
+    for _ in range(max(1, args.warmup)):
+        stack_norm_step()
+    stack_norm_ms = max_over_ranks(timed(stack_norm_step, args.steps), device)
     del layer2
     del head, layer, w, ws, routerW, shg
     torch.cuda.empty_cache()
@@ -536,6 +550,10 @@ def run_ours(args, rank, world, local_rank):
                         "tokens_per_s_per_layer": job_throughput(world, 2 * N, stack_ms),
                         "api": "moe_ffn_prefill_stack (second router launched behind the first combine; "
                                "the step includes one hidden-size device copy, as do the separate calls)"},
+        "layer_stack_rmsnorm": {"layers": 2, "ms_per_step": stack_norm_ms,
+                                "tokens_per_s_per_layer": job_throughput(world, 2 * N, stack_norm_ms),
+                                "api": "moe_ffn_prefill_stack_rmsnorm (an input norm before each layer, the later "
+                                       "ones and a final one fused into the combines; one hidden-size copy)"},
         "gpu_launches": head_launches * args.steps,
         "clocks": clk,
         "configs": configs,

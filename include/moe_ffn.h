@@ -370,6 +370,12 @@ int moe_combine_residual(const float *partials, const float *topk_w, const float
 int moe_combine_residual_rmsnorm(const float *partials, const float *topk_w, const float *shared,
                                  const float *residual, const float *gamma, float eps, int N,
                                  int top_k, int D, float *out, float *normed, cudaStream_t stream);
+/* The same norm of rows x alone: normed[t][c] = (x[t][c] * r_t) * gamma[c],
+ * r_t = 1 / sqrt(sum_c x[t][c]^2 / D + eps), summed as above (the input norm of
+ * a stack's first layer).  x [N][D], gamma [D], normed [N][D] (not x): fp32,
+ * device, 16-byte aligned; eps > 0 and finite. */
+int moe_rmsnorm(const float *x, const float *gamma, float eps, int N, int D, float *normed,
+                cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_ffn_prefill -- the whole layer in one call (all of the above, on one
@@ -394,7 +400,8 @@ int moe_ffn_prefill_residual(moe_weights_t w, const float *hidden, const float *
                              cudaStream_t stream);
 /* moe_ffn_prefill_residual whose combine also writes the next layer's normalised
  * input (moe_combine_residual_rmsnorm): out = residual + FFN(hidden), normed =
- * RMSNorm(out) * gamma.  Arguments as there and as moe_combine_residual_rmsnorm. */
+ * RMSNorm(out) * gamma.  Arguments as there and as moe_combine_residual_rmsnorm;
+ * normed may be `hidden` itself (the router has read it before the combine writes). */
 int moe_ffn_prefill_residual_rmsnorm(moe_weights_t w, const float *hidden, const float *routerW,
                                      const float *shexp_gate, const float *residual,
                                      const float *gamma, float eps, int N, int top_k,
@@ -446,6 +453,21 @@ int moe_ffn_prefill_stack(const moe_weights_t *w, const float *const *routerW,
                           const float *const *shexp_gate, int n_layers, float *hidden, int N,
                           int top_k, int norm_topk_prob, int path, void *ws, size_t ws_bytes,
                           cudaStream_t stream);
+/* moe_ffn_prefill_stack with an input norm before every layer (the pre-norm
+ * chain the pages' router input implies, #388 "Remaining levers" items 1-2):
+ *   normed = RMSNorm_0(hidden);  for l: hidden = hidden + FFN_l(normed),
+ *   normed = RMSNorm_{l+1}(hidden) (fused into layer l's combine; after the last
+ *   layer only when gamma[n_layers] is not NULL).
+ * gamma: host array of n_layers + 1 device pointers to [D] fp32 weights (the
+ * last may be NULL); normed [N][D] fp32 device (not hidden), holds the last
+ * norm on return; eps > 0 and finite.  Every router after the first norm is
+ * launched behind the kernel that writes its input.  Errors as
+ * moe_ffn_prefill_stack. */
+int moe_ffn_prefill_stack_rmsnorm(const moe_weights_t *w, const float *const *routerW,
+                                  const float *const *shexp_gate, const float *const *gamma,
+                                  float eps, int n_layers, float *hidden, float *normed, int N,
+                                  int top_k, int norm_topk_prob, int path, void *ws,
+                                  size_t ws_bytes, cudaStream_t stream);
 
 /* moe_ffn_prefill_ex that also records seven caller-created CUDA events on
  * `stream` around its stages, for measuring each kernel in place:

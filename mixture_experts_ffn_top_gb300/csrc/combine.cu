@@ -89,7 +89,8 @@ combine_kernel(const float4 *__restrict__ partials, const float *__restrict__ w,
 }
 
 // The combine with residual, then the next layer's input norm read as RMSNorm: one CTA per token
-// row at a time (the grid strides over rows).  Each element is combine4's value (out, bit for bit
+// row at a time (the grid strides over rows).  With k = 0 and no out it is the norm of the
+// residual rows alone (the first layer's input norm of a stack).  Each element is combine4's value (out, bit for bit
 // the plain combine's); the row's sum of squares is accumulated in fp32 per thread (its columns in
 // order), then over the warp (butterfly) and the warps (in order), and
 //   normed = (out * r) * gamma,  r = 1 / sqrt(sum / D + eps)  (IEEE divide and square root).
@@ -109,7 +110,7 @@ combine_rmsnorm_kernel(const float4 *__restrict__ partials, const float *__restr
         float ss = 0.0f;
         for (int c = threadIdx.x; c < D4; c += CN_THREADS) {
             const float4 v = combine4<KMAX>(partials, w, shared, residual, t, c, k, D4);
-            out[t * D4 + c] = v;
+            if (out != nullptr) out[t * D4 + c] = v;
             ss = __fmaf_rn(v.x, v.x, ss);
             ss = __fmaf_rn(v.y, v.y, ss);
             ss = __fmaf_rn(v.z, v.z, ss);
@@ -127,7 +128,9 @@ combine_rmsnorm_kernel(const float4 *__restrict__ partials, const float *__restr
         __syncthreads();
         const float r = r_row;
         for (int c = threadIdx.x; c < D4; c += CN_THREADS) {
-            const float4 o = out[t * D4 + c];  // this thread's own store above
+            // this thread's own store above, or (no out: the norm of the residual rows alone) the
+            // value again
+            const float4 o = out != nullptr ? out[t * D4 + c] : combine4<KMAX>(partials, w, shared, residual, t, c, k, D4);
             const float4 g = gamma[c];
             normed[t * D4 + c] = make_float4(__fmul_rn(__fmul_rn(o.x, r), g.x), __fmul_rn(__fmul_rn(o.y, r), g.y),
                                              __fmul_rn(__fmul_rn(o.z, r), g.z), __fmul_rn(__fmul_rn(o.w, r), g.w));
@@ -198,6 +201,10 @@ int launch_combine_rmsnorm(const float *partials, const float *topk_w, const flo
         case 8: return go(combine_rmsnorm_kernel<8, 128>, combine_rmsnorm_kernel<8, 512>);
         default: return go(combine_rmsnorm_kernel<0, 128>, combine_rmsnorm_kernel<0, 512>);
     }
+}
+
+int launch_rmsnorm(const float *x, const float *gamma, float eps, int N, int D, float *normed, cudaStream_t s) {
+    return launch_combine_rmsnorm(nullptr, nullptr, nullptr, x, gamma, eps, N, 0, D, nullptr, normed, s, false);
 }
 
 }  // namespace moe

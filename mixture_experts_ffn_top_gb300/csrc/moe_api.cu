@@ -452,6 +452,12 @@ int moe_combine_residual_rmsnorm(const float *partials, const float *topk_w, con
     return launch_combine_rmsnorm(partials, topk_w, shared, residual, gamma, eps, N, top_k, D, out, normed, stream);
 }
 
+int moe_rmsnorm(const float *x, const float *gamma, float eps, int N, int D, float *normed, cudaStream_t stream) {
+    if (!x || !norm_args_ok(gamma, eps, normed, nullptr, x) || (uintptr_t)x % 16) return MOE_ERR_INVALID_ARG;
+    if (N < 1 || D < 4 || D % 4) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return launch_rmsnorm(x, gamma, eps, N, D, normed, stream);
+}
+
 int moe_combine(const float *partials, const float *topk_w, const float *shared, int N, int top_k, int D, float *out,
                 cudaStream_t stream) {
     return moe_combine_residual(partials, topk_w, shared, nullptr, N, top_k, D, out, stream);
@@ -620,6 +626,33 @@ int moe_ffn_prefill_residual_rmsnorm(moe_weights_t w, const float *hidden, const
     if (!norm_args_ok(gamma, eps, normed, out, residual)) return MOE_ERR_INVALID_ARG;
     return prefill_impl(w, hidden, routerW, shexp_gate, N, top_k, norm_topk_prob, out, path, ws, ws_bytes, stream,
                         nullptr, residual, false, gamma, eps, normed);
+}
+
+int moe_ffn_prefill_stack_rmsnorm(const moe_weights_t *w, const float *const *routerW,
+                                  const float *const *shexp_gate, const float *const *gamma, float eps, int n_layers,
+                                  float *hidden, float *normed, int N, int top_k, int norm_topk_prob, int path,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!w || !routerW || !hidden || !gamma || n_layers < 1) return MOE_ERR_INVALID_ARG;
+    if (!norm_args_ok(gamma[0], eps, normed, hidden, hidden)) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        if (!w[l] || !routerW[l] || !gamma[l] || (uintptr_t)gamma[l] % 16) return MOE_ERR_INVALID_ARG;
+        if (w[l]->D != w[0]->D || (reinterpret_cast<uintptr_t>(hidden) % 16) || w[0]->D % 4) return MOE_ERR_INVALID_ARG;
+        const WsLayout L = ws_layout(N, w[l]->D, w[l]->E, w[l]->F, top_k, w[l]->Fs);
+        if (!shape_ok(N, w[l]->D, w[l]->E, top_k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (int rc = check_ws(ws, ws_bytes, L)) return rc;
+    }
+    if (gamma[n_layers] && (uintptr_t)gamma[n_layers] % 16) return MOE_ERR_INVALID_ARG;
+    // the first layer's input norm; afterwards every layer's combine writes both the residual stream
+    // and the next layer's normalised input, and the next router is launched behind that combine
+    if (int rc = launch_rmsnorm(hidden, gamma[0], eps, N, w[0]->D, normed, stream)) return rc;
+    for (int l = 0; l < n_layers; ++l) {
+        const float *g = shexp_gate ? shexp_gate[l] : nullptr;
+        const float *gn = gamma[l + 1];  // NULL after the last layer: no final norm
+        if (int rc = prefill_impl(w[l], normed, routerW[l], g, N, top_k, norm_topk_prob, hidden, path, ws, ws_bytes,
+                                  stream, nullptr, hidden, true, gn, eps, gn ? normed : nullptr))
+            return rc;
+    }
+    return MOE_OK;
 }
 
 int moe_ffn_prefill_stack(const moe_weights_t *w, const float *const *routerW, const float *const *shexp_gate,

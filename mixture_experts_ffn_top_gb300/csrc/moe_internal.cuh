@@ -172,6 +172,8 @@ int launch_combine(const float *partials, const float *topk_w, const float *shar
 int launch_combine_rmsnorm(const float *partials, const float *topk_w, const float *shared, const float *residual,
                            const float *gamma, float eps, int N, int top_k, int D, float *out, float *normed,
                            cudaStream_t s, bool early = false);
+// normed = RMSNorm(x) * gamma alone (launch_combine_rmsnorm with no slots and no out).
+int launch_rmsnorm(const float *x, const float *gamma, float eps, int N, int D, float *normed, cudaStream_t s);
 // weights.cu
 int repack_weights(moe_weights_s *w, const void *gate, const void *up, const void *down,
                    const void *sh_gate, const void *sh_up, const void *sh_down, cudaStream_t s);

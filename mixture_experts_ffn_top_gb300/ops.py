@@ -62,6 +62,8 @@ _SIGS = {
     "moe_combine_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_ffn_prefill_residual": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _SZ, _P]),
     "moe_combine_residual_rmsnorm": (_I, [_P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P]),
+    "moe_rmsnorm": (_I, [_P, _P, ctypes.c_float, _I, _I, _P, _P]),
+    "moe_ffn_prefill_stack_rmsnorm": (_I, [_P, _P, _P, _P, ctypes.c_float, _I, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_ffn_prefill_residual_rmsnorm": (_I, [_P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _I, _P,
                                                _SZ, _P]),
     "moe_workspace_views": (_I, [_P, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_P)] * 10),
@@ -395,6 +397,41 @@ def moe_combine_residual_rmsnorm(partials, topk_w, shared, residual, gamma, eps,
                                               _dev(out, torch.float32, "out"), _dev(normed, torch.float32, "normed"),
                                               _stream(stream)), "moe_combine_residual_rmsnorm")
     return out, normed
+
+
+def moe_rmsnorm(x, gamma, eps, normed=None, stream=None):
+    """normed = RMSNorm(x) * gamma (rows of x, weight gamma [D], eps)."""
+    N, D = x.shape
+    if normed is None:
+        normed = torch.empty((N, D), dtype=torch.float32, device=x.device)
+    _check(lib().moe_rmsnorm(_dev(x, torch.float32, "x"), _dev(gamma, torch.float32, "gamma"), float(eps), N, D,
+                             _dev(normed, torch.float32, "normed"), _stream(stream)), "moe_rmsnorm")
+    return normed
+
+
+def moe_ffn_prefill_stack_rmsnorm(weights, routerWs, shexp_gates, gammas, eps, hidden, top_k, norm_topk_prob, ws,
+                                  normed=None, path=MOE_PATH_AUTO, stream=None):
+    """Pre-norm layers in place: normed = RMSNorm_0(hidden); per layer l hidden += FFN_l(normed) and
+    normed = RMSNorm_{l+1}(hidden) (gammas: n + 1 entries, the last may be None).  Returns
+    (hidden, normed)."""
+    n = len(weights)
+    assert len(routerWs) == n and len(shexp_gates) == n and len(gammas) == n + 1
+    N, D = hidden.shape
+    if normed is None:
+        normed = torch.empty((N, D), dtype=torch.float32, device=hidden.device)
+    wh = (_P * n)(*[w.handle for w in weights])
+    rw = (_P * n)(*[_dev(r, torch.float32, "routerW") for r in routerWs])
+    sg = None
+    if any(g is not None for g in shexp_gates):
+        sg = (_P * n)(*[_dev(g, torch.float32) for g in shexp_gates])
+    gm = (_P * (n + 1))(*[_dev(g, torch.float32) for g in gammas])
+    rc = lib().moe_ffn_prefill_stack_rmsnorm(ctypes.cast(wh, _P), ctypes.cast(rw, _P),
+                                             None if sg is None else ctypes.cast(sg, _P), ctypes.cast(gm, _P),
+                                             float(eps), n, _dev(hidden, torch.float32, "hidden"),
+                                             _dev(normed, torch.float32, "normed"), N, top_k, int(norm_topk_prob), path,
+                                             _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check(rc, "moe_ffn_prefill_stack_rmsnorm")
+    return hidden, normed
 
 
 def moe_ffn_prefill_stack(weights, routerWs, shexp_gates, hidden, top_k, norm_topk_prob, ws, path=MOE_PATH_AUTO,

@@ -312,6 +312,16 @@ def combine_residual_rmsnorm(partials, w, S, R, gamma, eps: float):
     return out, normed
 
 
+def rmsnorm(x, gamma, eps: float):
+    """RMSNorm of rows x with weight gamma: the residual combine's norm with no routed slot
+    (one slot of weight 0 contributes +0, then the row x is added)."""
+    x = _f32(x)
+    N, D = x.shape
+    _, normed = combine_residual_rmsnorm(np.zeros((N, D), np.float32), np.zeros((N, 1), np.float32), None, x, gamma,
+                                         eps)
+    return normed
+
+
 # ---------------------------------------------------------- whole layer ---
 def moe_ffn(hidden, routerW, gate, up, down, top_k: int, norm_topk_prob: bool,
             shexp_gate=None, sh_gate=None, sh_up=None, sh_down=None, keep: bool = True, fmt: str = "q8_0") -> dict:

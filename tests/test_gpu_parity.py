@@ -925,6 +925,74 @@ def test_layer_stack_against_oracle_chain(ops):
     assert rel <= 2e-3, rel
 
 
+@pytest.mark.parametrize("name", ["tiny", "olmoe"])
+def test_rmsnorm_alone_against_oracle(ops, name):
+    wl = WORKLOADS[name]
+    x = (np.random.default_rng(40).standard_normal((wl.N, wl.D)) * 3.0).astype(np.float32)
+    gamma = _gamma(wl.D, 41)
+    got = ops.moe_rmsnorm(dev(x), dev(gamma), 1e-6).cpu().numpy()
+    _assert_normed(got, O.rmsnorm(x, gamma, 1e-6))
+    with pytest.raises(ops.MoeError):
+        xd = dev(x)
+        ops.moe_rmsnorm(xd, dev(gamma), 1e-6, normed=xd)
+
+
+def _gammas(wl, n, final):
+    gs = [dev(_gamma(wl.D, 50 + l)) for l in range(n)]
+    return gs + [dev(_gamma(wl.D, 50 + n)) if final else None]
+
+
+@pytest.mark.parametrize("name,n,final", [("tiny", 3, True), ("olmoe", 2, True), ("qwen3moe_shared", 2, False),
+                                          ("decode_n4", 3, True)])
+def test_layer_stack_rmsnorm_equals_sequential_calls(ops, name, n, final):
+    """moe_ffn_prefill_stack_rmsnorm (the first norm alone, every later one fused into the previous
+    layer's combine, each router launched behind the kernel that writes its input) gives the same
+    bits as the public calls one after another."""
+    wl = WORKLOADS[name]
+    inps, layers = _stack_layers(ops, wl, n)
+    gammas = _gammas(wl, n, final)
+    h = dev(inps[0]["hidden"])
+    normed = ops.moe_rmsnorm(h, gammas[0], 1e-5)
+    for l, lay in enumerate(layers):
+        if gammas[l + 1] is not None:
+            ops.moe_ffn_prefill_residual_rmsnorm(lay.w, normed, lay.routerW, lay.shexp_gate, h, gammas[l + 1], 1e-5,
+                                                 wl.top_k, wl.norm_topk_prob, lay.ws, out=h, normed=normed)
+        else:
+            ops.moe_ffn_prefill_residual(lay.w, normed, lay.routerW, lay.shexp_gate, h, wl.top_k, wl.norm_topk_prob,
+                                         lay.ws, out=h)
+    hs = dev(inps[0]["hidden"])
+    _, ns = ops.moe_ffn_prefill_stack_rmsnorm([l.w for l in layers], [l.routerW for l in layers],
+                                              [l.shexp_gate for l in layers], gammas, 1e-5, hs, wl.top_k,
+                                              wl.norm_topk_prob, layers[0].ws)
+    torch.cuda.synchronize()
+    assert all(l.status() == 0 for l in layers)
+    for a, b in ((hs, h), (ns, normed)):
+        a, b = a.cpu().numpy(), b.cpu().numpy()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), float(np.abs(a - b).max())
+
+
+def test_layer_stack_rmsnorm_against_oracle_chain(ops):
+    """Three tiny pre-norm layers against the oracle chain: normed = RMSNorm_l(h), h = (routed +
+    shared) + h per layer, within the layer's output bar."""
+    wl = WORKLOADS["tiny"]
+    inps, layers = _stack_layers(ops, wl, 3)
+    gam = [_gamma(wl.D, 50 + l) for l in range(4)]
+    h = inps[0]["hidden"].copy()
+    for l, inp in enumerate(inps):
+        x = O.rmsnorm(h, gam[l], 1e-5)
+        r = O.moe_ffn_inputs(dict(inp, hidden=x), wl.top_k, wl.norm_topk_prob)
+        h = O.combine(r["partials"], r["topk_w"], r.get("shared_out"), h)
+    want_norm = O.rmsnorm(h, gam[3], 1e-5)
+    hs = dev(inps[0]["hidden"])
+    _, ns = ops.moe_ffn_prefill_stack_rmsnorm([l.w for l in layers], [l.routerW for l in layers],
+                                              [l.shexp_gate for l in layers], [dev(g) for g in gam], 1e-5, hs,
+                                              wl.top_k, wl.norm_topk_prob, layers[0].ws)
+    got = hs.cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(got - h) / np.linalg.norm(h) <= 2e-3
+    gn = ns.cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(gn - want_norm) / np.linalg.norm(want_norm) <= 2e-3
+
+
 def test_layer_stack_rejects_bad_arguments(ops):
     wl = WORKLOADS["tiny"]
     inps, layers = _stack_layers(ops, wl, 2)

@@ -798,6 +798,13 @@ def test_rmsnorm_normalises_the_residual_combine_output():
     np.testing.assert_allclose(ratio, np.broadcast_to(want[:, None], ratio.shape), rtol=2e-7)
 
 
+def test_rmsnorm_alone_constant_rows():
+    """The norm of rows alone (no routed slot): a constant row c gives sign(c) * gamma exactly."""
+    gamma = np.linspace(-2.0, 3.0, 16).astype(np.float32)
+    x = np.array([[5.0] * 16, [-0.125] * 16], np.float32)
+    np.testing.assert_array_equal(O.rmsnorm(x, gamma, 0.0), np.sign(x) * gamma[None, :])
+
+
 # ---------------------------------------------------- regression fixture ---
 @pytest.mark.parametrize("name,fixture", [("tiny", "tiny_layer.json"), ("tiny_q4k", "tiny_q4k_layer.json"),
                                           ("tiny_q3k", "tiny_q3k_layer.json")])
