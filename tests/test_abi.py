@@ -96,3 +96,24 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert lib.moe_ffn_prefill(None, None, None, None, 4, 2, 0, None, None, 0, None) == -1
     lib.moe_device_host_numa_node.argtypes = [V]
     assert lib.moe_device_host_numa_node(None) == -1
+
+
+def test_norm_entry_points_reject_bad_arguments_before_any_cuda_call(lib):
+    """Null pointers, a non-positive or non-finite eps and a normed buffer that is the output are
+    refused (MOE_ERR_INVALID_ARG) by the host-side checks; the pointers below are never dereferenced."""
+    V, F, I = ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+    a, b, c, d = V(0x1000), V(0x2000), V(0x3000), V(0x4000)
+    lib.moe_rmsnorm.argtypes = [V, V, F, I, I, V, V]
+    assert lib.moe_rmsnorm(None, b, 1e-6, 4, 64, c, None) == -1
+    for eps in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.moe_rmsnorm(a, b, eps, 4, 64, c, None) == -1
+    assert lib.moe_rmsnorm(a, b, 1e-6, 4, 64, a, None) == -1          # normed is x
+    lib.moe_combine_residual_rmsnorm.argtypes = [V, V, V, V, V, F, I, I, I, V, V, V]
+    assert lib.moe_combine_residual_rmsnorm(a, b, None, None, c, 1e-6, 4, 2, 64, d, V(0x5000), None) == -1
+    assert lib.moe_combine_residual_rmsnorm(a, b, None, c, d, 1e-6, 4, 2, 64, V(0x5000), V(0x5000), None) == -1
+    assert lib.moe_combine_residual_rmsnorm(a, b, None, c, d, 0.0, 4, 2, 64, V(0x5000), V(0x6000), None) == -1
+    lib.moe_ffn_prefill_residual_rmsnorm.argtypes = [V, V, V, V, V, V, F, I, I, I, V, V, I, V, ctypes.c_size_t, V]
+    assert lib.moe_ffn_prefill_residual_rmsnorm(None, a, b, None, c, d, 1e-6, 4, 2, 0, V(0x5000), V(0x5000), 0,
+                                                None, 0, None) == -1
+    lib.moe_ffn_prefill_stack_rmsnorm.argtypes = [V, V, V, V, F, I, V, V, I, I, I, I, V, ctypes.c_size_t, V]
+    assert lib.moe_ffn_prefill_stack_rmsnorm(None, None, None, None, 1e-6, 1, a, b, 4, 2, 0, 0, None, 0, None) == -1
