@@ -263,8 +263,8 @@ def resolve_path(ops, w, wl, path):
 
 def router_launches(wl):
     """Launches of the routing of a batch of more than SMALL_BATCH tokens: one on the tensor cores
-    (E a multiple of 16, 16 <= E <= 256), else the SIMT logits and softmax."""
-    return 1 if (wl.E % 16 == 0 and 16 <= wl.E <= 256) else 2
+    (E a multiple of 8, 8 <= E <= 256), else the SIMT logits and softmax."""
+    return 1 if (wl.E % 8 == 0 and 8 <= wl.E <= 256) else 2
 
 
 def launches_per_step(ops, wl, resolved_path):

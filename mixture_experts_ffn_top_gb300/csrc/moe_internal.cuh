@@ -116,7 +116,7 @@ int launch_router(const float *hidden, const float *routerW, const float *shexp_
                   cudaStream_t s, bool early = false, unsigned *status = nullptr, int *tile_counts = nullptr,
                   bool *counted = nullptr);
 // router_tc.cu: logits on the tensor cores (split tf32, three MMAs per K step) with the Q8_1 of x
-// and the per-token softmax / top-k in one cluster launch; E % 16 == 0, 16 <= E <= 256, N > 8,
+// and the per-token softmax / top-k in one cluster launch; E % 8 == 0, 8 <= E <= 256, N > 8,
 // 16-byte-aligned hidden / routerW / gate.
 bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden, const float *routerW,
                         const float *shexp_gate);

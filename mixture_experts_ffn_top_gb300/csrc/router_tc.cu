@@ -55,7 +55,9 @@ constexpr unsigned long long RT_WAIT_NS = 2000000000ull;
 // stages as fit, at most RT_MAX_STAGES), reused after the main loop for the partial logits
 // [128][E + 1] and the summed logits of this CTA's tokens [128 / KS][E + 1]; the gate slice of the
 // CTA's K range stays apart.
-__host__ __device__ constexpr int rt_stage_bytes(int E) { return 2 * RT_A + 2 * E * 128; }
+// The MMA's N: E rounded up to a multiple of 16 (the router tile's extra rows are zero).
+__host__ __device__ constexpr int rt_nmma(int E) { return (E + 15) & ~15; }
+__host__ __device__ constexpr int rt_stage_bytes(int E) { return 2 * RT_A + 2 * rt_nmma(E) * 128; }
 __host__ __device__ constexpr int rt_gate_bytes(int D) { return D * 4; }
 __host__ __device__ inline int rt_stages(int E, int D) {
     const int s = (RT_SMEM_MAX - 1024 - rt_gate_bytes(D)) / rt_stage_bytes(E);
@@ -168,7 +170,8 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     const int nblk = p.D / QK;
     const int S = p.stages;
     const int SB = rt_stage_bytes(p.E);      // stage: [A hi][A lo][B hi][B lo]
-    const int B_BYTES = p.E * 128;
+    const int NM = rt_nmma(p.E);
+    const int B_BYTES = NM * 128;  // a router tile on chip: NM rows of 32 fp32, E of them loaded
     float *gw = reinterpret_cast<float *>(smem + S * SB);  // gate weights of this K range
 
     if (threadIdx.x == 0) {
@@ -195,6 +198,17 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (p.E < NM) {
+        // the router tile's rows E .. NM-1 (hi and lo) are zero in every stage: no copy writes them
+        for (int st = 0; st < S; ++st) {
+            float *bh = reinterpret_cast<float *>(smem + st * SB + 2 * RT_A);
+            for (int i = threadIdx.x; i < (NM - p.E) * 32; i += RT_THREADS) {
+                bh[p.E * 32 + i] = 0.0f;
+                bh[NM * 32 + p.E * 32 + i] = 0.0f;
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tensor core reads them
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -215,7 +229,7 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                 uint8_t *st = smem + s * SB;
                 const uint32_t fb = smem_u32(&full_bar[s]);
                 const int k0 = (kb0 + i) * QK;
-                mbar_expect_tx(fb, RT_A + B_BYTES);
+                mbar_expect_tx(fb, RT_A + p.E * 128);
                 tma_load_2d(smem_u32(st), &maps.x, k0, t0, fb);
                 tma_load_2d(smem_u32(st + 2 * RT_A), &maps.w, k0, 0, fb);
                 issued |= 1u << s;
@@ -231,7 +245,7 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA ---
         if (lane == 0) {
-            const uint32_t idesc = idesc_tf32(p.E);
+            const uint32_t idesc = idesc_tf32(NM);
             bool ok = true;
             int i = 0;
             for (; i < p.kb_per; ++i) {
@@ -351,7 +365,8 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, const RtParams p) {
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) P[rr * (p.E + 1) + c0 + j] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < p.E) P[rr * (p.E + 1) + c0 + j] = __uint_as_float(v[j]);
                 }
             }
         }
@@ -505,7 +520,7 @@ bool router_tc_eligible(int N, int D, int E, bool has_gate, const float *hidden,
                         const float *shexp_gate) {
     const uintptr_t al = reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(routerW) |
                          (has_gate ? reinterpret_cast<uintptr_t>(shexp_gate) : 0);
-    return N > 8 && E % 16 == 0 && E >= 16 && E <= RT_MAX_N && D % QK == 0 && al % 16 == 0 && rt_stages(E, D) >= 2;
+    return N > 8 && E % 8 == 0 && E >= 8 && E <= RT_MAX_N && D % QK == 0 && al % 16 == 0 && rt_stages(E, D) >= 2;
 }
 
 int launch_router_tc(const float *hidden, const float *routerW, const float *shexp_gate, int N, int D, int E,
