@@ -224,6 +224,40 @@ def test_bucket_flags_bad_routing(ops, bad):
     assert ops.moe_workspace_status(ws) == 0  # cleared
 
 
+def test_decode_ring_flags_malformed_csr(ops):
+    """The decode matvecs check every CSR-derived index before using it: a token index past N, a
+    segment outside [0, N * top_k] or a slot past top_k raises MOE_DEV_BAD_CSR (the entry or the
+    segment is skipped, nothing is read out of bounds), and the same workspace gives the right
+    results again once the status is read."""
+    wl, inp, ref = case("decode_n4")
+    layer = layer_for(ops, inp, wl)
+    xq, xd = dev(ref["x_q"]), dev(O.halves(ref["x_d16"]))
+    es, ti, tk = ref["expStart"], ref["expTokI"], ref["expTokK"]
+    want_hq, _ = ops.moe_expert_gate_up(layer.w, xq, xd, dev(es), dev(ti), wl.top_k, layer.ws, path=1)
+    assert ops.moe_workspace_status(layer.ws) == 0
+    ti_bad = ti.copy()
+    ti_bad[0] = wl.N + 1000
+    ops.moe_expert_gate_up(layer.w, xq, xd, dev(es), dev(ti_bad), wl.top_k, layer.ws, path=1)
+    assert ops.moe_workspace_status(layer.ws) & 0x2
+    es_bad = es.copy()
+    es_bad[1] = -1
+    ops.moe_expert_gate_up(layer.w, xq, xd, dev(es_bad), dev(ti), wl.top_k, layer.ws, path=1)
+    assert ops.moe_workspace_status(layer.ws) & 0x2
+    total = int(es[-1])
+    hq = np.zeros((wl.N * wl.top_k, wl.F), np.int8)
+    hd = np.zeros((wl.N * wl.top_k, wl.F // 32), np.float32)
+    hq[:total] = ref["h_q"]
+    hd[:total] = O.halves(ref["h_d16"])
+    tk_bad = tk.copy()
+    tk_bad[0] = wl.top_k + 3
+    ops.moe_expert_down(layer.w, dev(hq), dev(hd), dev(es), dev(ti), dev(tk_bad), wl.N, wl.top_k, layer.ws, path=1)
+    assert ops.moe_workspace_status(layer.ws) & 0x2
+    # the workspace is still good
+    got_hq, _ = ops.moe_expert_gate_up(layer.w, xq, xd, dev(es), dev(ti), wl.top_k, layer.ws, path=1)
+    assert ops.moe_workspace_status(layer.ws) == 0
+    np.testing.assert_array_equal(got_hq.cpu().numpy(), want_hq.cpu().numpy())
+
+
 def test_bucket_flags_bad_routing_in_a_late_range(ops):
     # many CTAs: the bad entry sits in the last token range, far from CTA 0
     N, E, k = 5000, 64, 8
