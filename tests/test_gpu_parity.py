@@ -122,6 +122,9 @@ def test_router_parity(ops, name):
     (1100, 512, 48, 6, 32, True),    # ragged last token tile, shared gate row
     (1024, 2048, 64, 8, 0, False),   # one full expert tile
     (1040, 256, 33, 3, 0, True),     # one expert past a 32-wide lane group
+    (300, 256, 8, 2, 32, True),      # 8 experts: the tensor-core router's N padded to 16, shared gate row
+    (520, 512, 24, 4, 0, False),     # 24 experts: N padded to 32 (8 zero router rows on chip)
+    (130, 1024, 40, 8, 0, True),     # 40 experts, two token tiles (one of 2 rows)
 ])
 def test_router_ragged_shapes(ops, N, D, E, k, Fs, norm):
     """Router, routing and Q8_1 of x on shapes with ragged token and expert tiles."""
