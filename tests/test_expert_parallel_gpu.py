@@ -33,7 +33,9 @@ def group():
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared", "decode_n8"])
+# decode_n8_q4k: the single-GPU layer streams the nibble-packed Q4_K copy through the decode ring,
+# the expert owner (64 single-slot rows) runs the register-loading matvecs on the int8 repack
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "qwen3moe_shared", "decode_n8", "decode_n8_q4k", "olmoe_q4k"])
 def test_device_expert_parallel_matches_prefill(group, name):
     from mixture_experts_ffn_top_gb300 import ops
     from mixture_experts_ffn_top_gb300.expert_parallel import DeviceBackend, expert_parallel_forward
