@@ -15,8 +15,8 @@ runs its own token batch (replicas, weak scaling) and rank 0 prints the line
 with the maximum time over ranks.  With one GPU the line also carries
 `configs`: the layer's other workloads (tiny, decode batches of 1/4/8 tokens
 with Q8_0 and of 8 tokens with Q4_K weights, the Qwen3-MoE-shaped layer with a
-shared expert, the Zipf-skewed long prefill), each timed the same way after
-the headline, with its tokens/s,
+shared expert, the Zipf-skewed long prefill, the OLMoE layer with Q4_K and with
+Q3_K experts), each timed the same way after the headline, with its tokens/s,
 layer roofline fraction, dominant kernel's fraction and stage times.
 --impl reference times the CPU oracle on the host cores on a bounded sample of
 the same workload.
@@ -250,7 +250,8 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-CONFIG_WORKLOADS = ["tiny", "decode_n1", "decode_n4", "decode_n8", "decode_n8_q4k", "qwen3moe_shared", "skewed"]
+CONFIG_WORKLOADS = ["tiny", "decode_n1", "decode_n4", "decode_n8", "decode_n8_q4k", "qwen3moe_shared", "skewed",
+                    "olmoe_q4k", "olmoe_q3k"]
 
 
 def resolve_path(ops, w, wl, path):
